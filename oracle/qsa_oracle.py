@@ -1,0 +1,245 @@
+"""fp64 CPU oracle for the QSA decode step.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+the CPU-baseline leg of the benchmark may import this module.  The product
+path (the CUDA library and its Python binding) never calls it, and it shares
+no code with that path: it decodes the byte formats itself, from their
+published definitions, and computes everything in float64 with plain numpy.
+
+What it computes, step by step (one decode unit = one request at one QSA
+layer):
+
+1. Index score per cached token t (the resident indexer over compact keys:
+   "Оффлоадинг KV-кэша Qwen3.8-Flash-Next в RAM через vLLM без потери скорости
+   декодирования", section "Механизм гибридного разреженного оффлоадинга"):
+       S_t = sum_h w_h * relu( sum_d q_{h,d} * k_{t,d} ),   k_{t,d} = sc_t * e4m3(code_{t,d})
+   with 8 index heads of 64 dims.  The dequantised key is code times scale,
+   which is this library's reading of "64 FP8 values plus one fp16 scale".
+2. C4 block score: the maximum of the (up to) four token scores of each
+   group of four adjacent tokens ("双卡RTX4090跑通Qwen3-Next：8并发满血长上下文实测",
+   the opening explanation of QSA and its C4 blocks).
+3. Selection: the K = min(budget/4, #blocks) blocks that rank highest under
+   the total order (score descending, block id ascending), returned in
+   ascending block id.  Each layer selects on its own (same page, same part:
+   the 12 sparse layers choose independently).
+4. Gather through the logical-token -> physical-slot table: slot >= 0 reads
+   row `slot` of the HBM pool, slot == -1 reads the token's row in the host
+   store (same page, section "显存账本：热缓存卸载省下约84%": logical token
+   addresses are kept apart from physical cache slots; missing blocks come
+   back from pinned host memory on demand).
+5. GQA decode attention over the gathered rows: query head h uses KV head
+   h // 4, logits = scale * q_h . K_i, softmax over the selected tokens,
+   output = sum_i p_i V_i, plus lse_h = log sum_i exp(logit_i).
+
+Every function below names the passage it follows.  Pins that tie this
+oracle to facts outside itself live in tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+INDEX_HEADS = 8
+INDEX_DIM = 64
+KV_HEADS = 4
+HEAD_DIM = 128
+Q_HEADS = 16
+GQA_GROUP = Q_HEADS // KV_HEADS
+ROW_BYTES = 2048
+
+
+# ------------------------------------------------------------------ formats
+
+def e4m3_value(code: int) -> float:
+    """Value of one FP8 E4M3 code (OCP 8-bit floating point specification,
+    E4M3 variant): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+    exponent field 0 encodes subnormals m/8 * 2^-6; S.1111.111 is NaN; there
+    is no infinity, so S.1111.110 = 448 is the largest finite value."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** (1 - 7)
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def decode_fp16(bits) -> np.ndarray:
+    """IEEE 754 binary16 from raw bits: 1 sign, 5 exponent (bias 15), 10
+    mantissa; exponent 0 = subnormal m * 2^-24; exponent 31 = inf/NaN."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    s = np.where(b & 0x8000, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    m = (b & 0x3FF).astype(np.float64)
+    sub = m * 2.0 ** -24
+    nrm = (1.0 + m / 1024.0) * np.exp2(e.astype(np.float64) - 15.0)
+    special = np.where(m == 0, np.inf, np.nan)
+    v = np.where(e == 0, sub, np.where(e == 31, special, nrm))
+    return s * v
+
+
+def decode_bf16(bits) -> np.ndarray:
+    """bfloat16 from raw bits: the upper 16 bits of an IEEE binary32
+    (1 sign, 8 exponent with bias 127, 7 mantissa)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    s = np.where(b & 0x8000, -1.0, 1.0)
+    e = (b >> 7) & 0xFF
+    m = (b & 0x7F).astype(np.float64)
+    sub = m * 2.0 ** (-126 - 7)
+    nrm = (1.0 + m / 128.0) * np.exp2(e.astype(np.float64) - 127.0)
+    special = np.where(m == 0, np.inf, np.nan)
+    v = np.where(e == 0, sub, np.where(e == 255, special, nrm))
+    return s * v
+
+
+# ------------------------------------------------------------ 1. index score
+
+def token_scores(codes, scale_bits, q_idx, w) -> np.ndarray:
+    """S_t for every token (step 1 above; resident indexer of the offload
+    digest, section "Механизм гибридного разреженного оффлоадинга").
+
+    codes: uint8 [n][64] e4m3; scale_bits: uint16 [n] fp16 bits;
+    q_idx: [8][64] float; w: [8] float.  Returns float64 [n].
+    """
+    k = decode_e4m3(codes) * decode_fp16(scale_bits)[:, None]          # [n][64]
+    dots = k @ np.asarray(q_idx, dtype=np.float64).T                     # [n][8]
+    return np.maximum(dots, 0.0) @ np.asarray(w, dtype=np.float64)      # [n]
+
+
+# ----------------------------------------------------------- 2. C4 blocks
+
+def c4_block_scores(S) -> np.ndarray:
+    """Block b covers tokens 4b..4b+3 (fewer in a ragged last block); its
+    score is the maximum of its tokens' scores (C4 grouping, RTX4090 port
+    page, opening explanation of QSA)."""
+    S = np.asarray(S, dtype=np.float64)
+    n = S.shape[0]
+    nb = (n + 3) // 4
+    out = np.empty(nb, dtype=np.float64)
+    for b in range(nb):
+        out[b] = S[4 * b:min(n, 4 * b + 4)].max()
+    return out
+
+
+# -------------------------------------------------------------- 3. top-k
+
+def select_blocks(blk, budget_tokens: int) -> np.ndarray:
+    """The K = min(budget_tokens // 4, #blocks) highest-ranking blocks under
+    (score descending, block id ascending), sorted by block id (per-layer
+    independent selection within indexer_budget: offload digest lead and
+    section "Механизм гибридного разреженного оффлоадинга"; RTX4090 port page,
+    opening explanation of QSA)."""
+    blk = np.asarray(blk, dtype=np.float64)
+    nb = blk.shape[0]
+    k = min(budget_tokens // 4, nb)
+    ids = np.arange(nb)
+    order = np.lexsort((ids, -blk))      # primary: -score, secondary: id
+    return np.sort(order[:k]).astype(np.int64)
+
+
+def selected_tokens(sel_blocks, n: int) -> np.ndarray:
+    """Token positions covered by the selected blocks, ascending, without the
+    positions past the end of the context."""
+    toks = [t for b in np.asarray(sel_blocks, dtype=np.int64)
+            for t in range(4 * int(b), min(n, 4 * int(b) + 4))]
+    return np.asarray(toks, dtype=np.int64)
+
+
+# ------------------------------------------------ 4. slot-table gather
+
+def ring_slot_row(ctx_len: int, layer: int, base_row: int, ring_tokens: int) -> np.ndarray:
+    """Slot-table row of one layer of a host-offloaded request: the newest
+    ring_tokens tokens live in the request's tail ring (token t in ring row
+    t mod ring_tokens of that layer's ring), every older token is cold
+    (-1, served from pinned host memory).  RTX4090 port page, section
+    "显存账本：热缓存卸载省下约84%" (tail ring buffer; full history in pinned
+    host memory; logical addresses separate from physical slots)."""
+    t = np.arange(ctx_len, dtype=np.int64)
+    hot = t >= ctx_len - ring_tokens
+    slots = base_row + layer * ring_tokens + (t % ring_tokens)
+    return np.where(hot, slots, -1).astype(np.int32)
+
+
+def resident_slot_row(ctx_len: int, layer: int, base_row: int) -> np.ndarray:
+    """Slot-table row of one layer of a fully HBM-resident request: token t
+    of layer l sits in row base_row + l * ctx_len + t."""
+    return (base_row + layer * ctx_len + np.arange(ctx_len, dtype=np.int64)).astype(np.int32)
+
+
+def gather_rows(tokens, slot_row, hbm_pool_rows, host_rows) -> np.ndarray:
+    """Bytes of the rows of the given logical tokens: pool row slot_row[t]
+    when it is >= 0, else host row t (step 4 above).  Returns uint8 [m][2048].
+    hbm_pool_rows / host_rows: anything indexable by row giving 2048 bytes."""
+    out = np.empty((len(tokens), ROW_BYTES), dtype=np.uint8)
+    for i, t in enumerate(tokens):
+        s = int(slot_row[int(t)])
+        out[i] = hbm_pool_rows[s] if s >= 0 else host_rows[int(t)]
+    return out
+
+
+# ----------------------------------------------------------- 5. attention
+
+def split_kv(rows_u8) -> tuple[np.ndarray, np.ndarray]:
+    """A 2048-byte row holds K[4][128] bf16 then V[4][128] bf16."""
+    r = np.ascontiguousarray(rows_u8, dtype=np.uint8).view(np.uint16).reshape(-1, 2, KV_HEADS, HEAD_DIM)
+    return decode_bf16(r[:, 0]), decode_bf16(r[:, 1])          # [m][4][128] each
+
+
+def decode_attention(q_bits, rows_u8, softmax_scale: float):
+    """GQA decode attention over the gathered rows (step 5 above; sparse
+    attention over the selected rows only, offload digest section
+    "Механизм гибридного разреженного оффлоадинга").
+
+    q_bits: uint16 [16][128] bf16 bits.  Returns (out float64 [16][128],
+    lse float64 [16]); with no rows, out = 0 and lse = -inf.
+    """
+    q = decode_bf16(q_bits).reshape(Q_HEADS, HEAD_DIM)
+    out = np.zeros((Q_HEADS, HEAD_DIM))
+    lse = np.full(Q_HEADS, -np.inf)
+    if len(rows_u8) == 0:
+        return out, lse
+    K, V = split_kv(rows_u8)
+    for h in range(Q_HEADS):
+        g = h // GQA_GROUP
+        logits = softmax_scale * (K[:, g, :] @ q[h])               # [m]
+        m = logits.max()
+        p = np.exp(logits - m)
+        l = p.sum()
+        out[h] = (p @ V[:, g, :]) / l
+        lse[h] = m + np.log(l)
+    return out, lse
+
+
+# ------------------------------------------------------- whole layer-step
+
+def layer_step(codes, scale_bits, q_idx, w, q_bits, slot_row, hbm_pool_rows,
+               host_rows, budget_tokens: int, softmax_scale: float):
+    """One decode unit end to end: steps 1-5 in the order the pages give
+    them (score every cached token, pick at most indexer_budget tokens by C4
+    blocks, bring only those rows, attend over them)."""
+    n = np.asarray(codes).shape[0]
+    S = token_scores(codes, scale_bits, q_idx, w)
+    blk = c4_block_scores(S)
+    sel = select_blocks(blk, budget_tokens)
+    toks = selected_tokens(sel, n)
+    rows = gather_rows(toks, slot_row, hbm_pool_rows, host_rows)
+    out, lse = decode_attention(q_bits, rows, softmax_scale)
+    return dict(scores=S, blk=blk, sel=sel, tokens=toks, out=out, lse=lse)
+
+
+def boundary_gap(blk, budget_tokens: int) -> float:
+    """Score gap between the last selected block and the best unselected one
+    (inf when every block is selected)."""
+    blk = np.asarray(blk, dtype=np.float64)
+    k = min(budget_tokens // 4, blk.shape[0])
+    if k >= blk.shape[0]:
+        return float("inf")
+    s = np.sort(blk)[::-1]
+    return float(s[k - 1] - s[k])

@@ -1,0 +1,166 @@
+"""Plant plausible slips in the oracle (on the CPU, in this process only) and
+check that the pins in test_oracle_pins.py catch every one of them."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import qsa_oracle as O
+from tests import test_oracle_pins as P
+
+
+def _table(bias=7, subnormals=True):
+    vals = []
+    for c in range(256):
+        s = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 7
+        if e == 15 and m == 7:
+            vals.append(float("nan"))
+        elif e == 0 and subnormals:
+            vals.append(s * m / 8 * 2.0 ** (1 - bias))
+        else:
+            vals.append(s * (1 + m / 8) * 2.0 ** (e - bias))
+    return np.array(vals)
+
+
+def _scores_no_relu(codes, sc, q, w):
+    k = O.decode_e4m3(codes) * O.decode_fp16(sc)[:, None]
+    return (k @ np.asarray(q, float).T) @ np.asarray(w, float)
+
+
+def _scores_no_scale(codes, sc, q, w):
+    k = O.decode_e4m3(codes)
+    return np.maximum(k @ np.asarray(q, float).T, 0) @ np.asarray(w, float)
+
+
+def _scores_q_rows_swapped(codes, sc, q, w):
+    k = O.decode_e4m3(codes) * O.decode_fp16(sc)[:, None]
+    q = np.asarray(q, float)[::-1]
+    return np.maximum(k @ q.T, 0) @ np.asarray(w, float)
+
+
+def _blk_mean(S):
+    S = np.asarray(S, float)
+    return np.array([S[4 * b:4 * b + 4].mean() for b in range((len(S) + 3) // 4)])
+
+
+def _blk_shifted(S):
+    S = np.asarray(S, float)
+    return np.array([S[max(0, 4 * b - 1):4 * b + 3].max() for b in range((len(S) + 3) // 4)])
+
+
+def _select_tie_high(blk, budget):
+    blk = np.asarray(blk, float)
+    k = min(budget // 4, len(blk))
+    order = np.lexsort((-np.arange(len(blk)), -blk))
+    return np.sort(order[:k])
+
+
+def _select_tokens_not_blocks(blk, budget):
+    blk = np.asarray(blk, float)
+    k = min(budget, len(blk))
+    return np.sort(np.lexsort((np.arange(len(blk)), -blk))[:k])
+
+
+def _select_unsorted(blk, budget):
+    blk = np.asarray(blk, float)
+    k = min(budget // 4, len(blk))
+    return np.lexsort((np.arange(len(blk)), -blk))[:k]
+
+
+def _tokens_unclipped(sel, n):
+    return np.asarray([t for b in sel for t in range(4 * int(b), 4 * int(b) + 4)], dtype=np.int64)
+
+
+def _ring_offset(ctx, layer, base, ring):
+    t = np.arange(ctx)
+    hot = t >= ctx - ring
+    return np.where(hot, base + layer * ring + (t - (ctx - ring)), -1).astype(np.int32)
+
+
+def _gather_host_only(tokens, slot, pool, host):
+    return np.stack([host[int(t)] for t in tokens]) if len(tokens) else np.zeros((0, 2048), np.uint8)
+
+
+def _attn_wrong_group(q_bits, rows, scale):
+    q = O.decode_bf16(q_bits).reshape(16, 128)
+    out = np.zeros((16, 128)); lse = np.full(16, -np.inf)
+    if len(rows) == 0:
+        return out, lse
+    K, V = O.split_kv(rows)
+    for h in range(16):
+        g = h % 4
+        lg = scale * (K[:, g] @ q[h]); m = lg.max(); p = np.exp(lg - m)
+        out[h] = p @ V[:, g] / p.sum(); lse[h] = m + np.log(p.sum())
+    return out, lse
+
+
+def _attn_no_scale(q_bits, rows, scale):
+    return O.__dict__["_orig_attn"](q_bits, rows, 1.0)
+
+
+def _attn_lse_drops_max(q_bits, rows, scale):
+    out, lse = O.__dict__["_orig_attn"](q_bits, rows, scale)
+    if len(rows) == 0:
+        return out, lse
+    K, _ = O.split_kv(rows)
+    q = O.decode_bf16(q_bits).reshape(16, 128)
+    for h in range(16):
+        lg = scale * (K[:, h // 4] @ q[h])
+        lse[h] = np.log(np.exp(lg - lg.max()).sum())
+    return out, lse
+
+
+def _fp16_bias16(bits):
+    return O.__dict__["_orig_fp16"](bits) * 0.5
+
+
+def _bf16_drop_subnormal(bits):
+    v = O.__dict__["_orig_bf16"](bits)
+    b = np.asarray(bits, dtype=np.uint16)
+    return np.where(((b >> 7) & 0xFF) == 0, 0.0, v)
+
+
+MUTATIONS = {
+    "e4m3 bias 8": {"E4M3_TABLE": _table(bias=8)},
+    "e4m3 no subnormals": {"E4M3_TABLE": _table(subnormals=False)},
+    "fp16 wrong bias": {"decode_fp16": _fp16_bias16},
+    "bf16 subnormals flushed": {"decode_bf16": _bf16_drop_subnormal},
+    "score without relu": {"token_scores": _scores_no_relu},
+    "score without scale": {"token_scores": _scores_no_scale},
+    "score with head rows swapped": {"token_scores": _scores_q_rows_swapped},
+    "block mean instead of max": {"c4_block_scores": _blk_mean},
+    "blocks shifted by one token": {"c4_block_scores": _blk_shifted},
+    "tie rule reversed": {"select_blocks": _select_tie_high},
+    "budget read as blocks": {"select_blocks": _select_tokens_not_blocks},
+    "selection not sorted": {"select_blocks": _select_unsorted},
+    "ragged tail not clipped": {"selected_tokens": _tokens_unclipped},
+    "ring slot offset instead of modulo": {"ring_slot_row": _ring_offset},
+    "gather ignores slot table": {"gather_rows": _gather_host_only},
+    "GQA group h % 4": {"decode_attention": _attn_wrong_group},
+    "softmax scale dropped": {"decode_attention": _attn_no_scale},
+    "lse without the max term": {"decode_attention": _attn_lse_drops_max},
+}
+
+
+def _all_pins():
+    pins = [getattr(P, n) for n in dir(P) if n.startswith("test_") and n != "test_c4_topk_hand_worked"]
+    cases = P._load("c4_topk_hand.json")["cases"]
+    pins += [(lambda c=c: P.test_c4_topk_hand_worked(c)) for c in cases]
+    return pins
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, monkeypatch):
+    monkeypatch.setattr(O, "_orig_attn", O.decode_attention, raising=False)
+    monkeypatch.setattr(O, "_orig_fp16", O.decode_fp16, raising=False)
+    monkeypatch.setattr(O, "_orig_bf16", O.decode_bf16, raising=False)
+    for attr, val in MUTATIONS[name].items():
+        monkeypatch.setattr(O, attr, val)
+    caught = 0
+    for pin in _all_pins():
+        try:
+            pin()
+        except Exception:
+            caught += 1
+    assert caught > 0, f"no pin catches: {name}"

@@ -1,0 +1,333 @@
+"""Pins that tie the fp64 oracle to facts outside itself.
+
+Each test checks the oracle against something it does not compute: values
+fixed by a format specification or worked by hand (tests/golden/), library
+routines for special cases (numpy / torch decoders, torch's fp64 softmax
+attention), closed forms, or invariants that any correct implementation must
+satisfy.  They are chosen so that a plausible slip in the oracle (a dropped
+term, a wrong sign or index, a transposed operand) makes one of them fail;
+tests/test_oracle_mutations.py checks that claim by planting such slips.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import qsa_oracle as O
+from sparse_attention_decode_qsa_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ----------------------------------------------------------------- formats
+
+def test_e4m3_spec_values():
+    for code_s, val, _ in _load("e4m3_spec_values.json")["values"]:
+        got = O.decode_e4m3(np.array([int(code_s, 16)], dtype=np.uint8))[0]
+        if val == "nan":
+            assert math.isnan(got), code_s
+        else:
+            assert got == val and math.copysign(1, got) == math.copysign(1, val), code_s
+
+
+def test_e4m3_matches_torch_for_all_codes():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.decode_e4m3(codes.numpy())
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_fp16_matches_numpy_for_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = O.decode_fp16(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_bf16_matches_torch_for_all_bit_patterns():
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    got = O.decode_bf16(bits.numpy().view(np.uint16))
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ------------------------------------------------------------- index score
+
+def _hand_score_inputs():
+    codes = np.zeros((6, 64), dtype=np.uint8)
+    codes[0, :] = 0x38
+    codes[1, :] = 0xB8
+    codes[2, 0] = 0x40
+    codes[3, :] = 0x7E
+    codes[4, :] = 0x01
+    codes[5, :32] = 0x7E
+    codes[5, 32:] = 0xFE
+    scales = np.array([0x3C00, 0x3C00, 0x3800, 0x0000, 0x4400, 0x2000], dtype=np.uint16)
+    q = np.zeros((8, 64))
+    q[0, :] = 1.0
+    q[1, :] = -1.0
+    q[2, 0] = 2.0
+    g = _load("index_score_hand.json")
+    w = np.array(g["w"])
+    return codes, scales, q, w, g
+
+
+def test_index_score_hand_worked():
+    codes, scales, q, w, g = _hand_score_inputs()
+    S = O.token_scores(codes, scales, q, w)
+    assert S.tolist() == [t["S"] for t in g["tokens"]]
+    assert O.c4_block_scores(S).tolist() == g["blocks"]["scores"]
+
+
+def test_index_score_one_hot_picks_single_element():
+    """q = e_d in head h only, w = e_h: S_t = relu(scale_t * e4m3(code[t][d])).
+    Checked against torch's fp8 decoding and numpy's fp16 decoding, for every
+    (h, d) on a few positions, which pins the index order of q, w and keys."""
+    rng = np.random.default_rng(7)
+    n = 32
+    codes = rng.integers(0, 256, size=(n, 64), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x30          # no NaN codes
+    scales = (rng.random(n) * 4).astype(np.float16).view(np.uint16)
+    ref_k = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy() * \
+        scales.view(np.float16).astype(np.float64)[:, None]
+    for h in (0, 3, 7):
+        for d in (0, 1, 17, 63):
+            q = np.zeros((8, 64)); q[h, d] = 1.0
+            w = np.zeros(8); w[h] = 1.0
+            S = O.token_scores(codes, scales, q, w)
+            assert np.array_equal(S, np.maximum(ref_k[:, d], 0.0))
+
+
+def test_index_score_invariants():
+    u = synth.unit_inputs(256, seed=11, planted_blocks=[], device="cpu")
+    codes = u.codes.numpy(); sc = u.scales.view(torch.int16).numpy().view(np.uint16)
+    q = u.q_idx.double().numpy(); w = u.w.double().numpy()
+    S = O.token_scores(codes, sc, q, w)
+    assert (S >= 0).all()
+    # linear in w (c > 0), and positively homogeneous in q
+    assert np.allclose(O.token_scores(codes, sc, q, 3.0 * w), 3.0 * S, rtol=1e-14, atol=0)
+    assert np.allclose(O.token_scores(codes, sc, 2.0 * q, w), 2.0 * S, rtol=1e-14, atol=0)
+    # permuting tokens permutes scores
+    p = np.random.default_rng(3).permutation(256)
+    assert np.array_equal(O.token_scores(codes[p], sc[p], q, w), S[p])
+    # zero scale -> zero score
+    sc0 = sc.copy(); sc0[5] = 0
+    assert O.token_scores(codes, sc0, q, w)[5] == 0.0
+    # relu: negating every key of a token swaps which heads contribute
+    neg = codes.copy(); neg[9] ^= 0x80
+    a = O.token_scores(codes[9:10], sc[9:10], q, w)[0]
+    b = O.token_scores(neg[9:10], sc[9:10], q, w)[0]
+    k = O.decode_e4m3(codes[9]) * O.decode_fp16(sc[9:10])[0]
+    dots = q @ k
+    assert np.isclose(a, (np.maximum(dots, 0) * w).sum(), rtol=1e-14)
+    assert np.isclose(b, (np.maximum(-dots, 0) * w).sum(), rtol=1e-14)
+    assert np.isclose(a - b, (dots * w).sum(), rtol=1e-12)   # relu(x) - relu(-x) = x
+
+
+# ----------------------------------------------------------- C4 and top-k
+
+@pytest.mark.parametrize("case", _load("c4_topk_hand.json")["cases"], ids=lambda c: c["name"])
+def test_c4_topk_hand_worked(case):
+    blk = O.c4_block_scores(np.array(case["token_scores"], dtype=np.float64))
+    assert blk.tolist() == case["blocks"]
+    assert O.select_blocks(blk, case["budget"]).tolist() == case["selected"]
+
+
+def _is_top_k(blk, sel, k):
+    """Definition of the selection: |sel| = k, and every selected block ranks
+    strictly above every unselected one under (score desc, id asc)."""
+    sel = set(int(b) for b in sel)
+    if len(sel) != k:
+        return False
+    rank = lambda b: (-blk[b], b)
+    worst_in = max(rank(b) for b in sel)
+    return all(rank(b) > worst_in for b in range(len(blk)) if b not in sel)
+
+
+def test_topk_definition_on_random_inputs_with_ties():
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        nb = int(rng.integers(1, 300))
+        blk = rng.integers(0, 6, size=nb).astype(np.float64)   # many ties
+        budget = 4 * int(rng.integers(1, 80))
+        sel = O.select_blocks(blk, budget)
+        k = min(budget // 4, nb)
+        assert list(sel) == sorted(sel)
+        assert _is_top_k(blk, sel, k)
+
+
+def test_topk_permutation_invariance():
+    rng = np.random.default_rng(9)
+    blk = rng.standard_normal(1000)
+    sel = set(O.select_blocks(blk, 400).tolist())
+    p = rng.permutation(1000)          # new block i holds old block p[i]
+    sel_p = O.select_blocks(blk[p], 400)
+    assert set(int(p[i]) for i in sel_p) == sel
+
+
+def test_planted_set_is_selected():
+    """A config-0 sized unit: the 512 planted blocks are exactly the top 512,
+    with a boundary gap far above 1e-3."""
+    n = 8192
+    planted = synth.planted_uniform(n // 4, 512, seed=1)
+    u = synth.unit_inputs(n, seed=2, planted_blocks=planted, device="cpu")
+    S = O.token_scores(u.codes.numpy(), u.scales.view(torch.int16).numpy().view(np.uint16),
+                       u.q_idx.numpy(), u.w.numpy())
+    blk = O.c4_block_scores(S)
+    sel = O.select_blocks(blk, 2048)
+    assert sel.tolist() == planted.tolist()
+    assert O.boundary_gap(blk, 2048) > 1.0
+
+
+def test_selected_tokens_ragged_tail():
+    assert O.selected_tokens([0, 2], 10).tolist() == [0, 1, 2, 3, 8, 9]
+    assert O.selected_tokens([], 10).tolist() == []
+
+
+# --------------------------------------------------------- slot table
+
+def test_ring_slot_row_hand_worked():
+    g = _load("ring_slots_hand.json")
+    got = O.ring_slot_row(g["ctx_len"], g["layer"], g["base_row"], g["ring_tokens"])
+    assert got.tolist() == g["slots"]
+
+
+def test_gather_through_remapped_slots_is_identical():
+    rng = np.random.default_rng(1)
+    n = 64
+    host = rng.integers(0, 256, size=(n, 2048), dtype=np.uint8)
+    pool = np.zeros((200, 2048), dtype=np.uint8)
+    slot = np.full(n, -1, dtype=np.int32)
+    # move a few tokens into arbitrary pool rows holding the same bytes
+    for t, s in [(3, 17), (40, 199), (63, 0), (10, 5)]:
+        pool[s] = host[t]
+        slot[t] = s
+    toks = np.arange(n)
+    a = O.gather_rows(toks, slot, pool, host)
+    assert np.array_equal(a, host)
+    # a slot pointing at a row with other bytes is visible
+    slot[3] = 1
+    assert not np.array_equal(O.gather_rows(toks, slot, pool, host), host)
+
+
+# ---------------------------------------------------------- attention
+
+def _rows_from(K, V):
+    """Pack float K, V [m][4][128] as bf16 rows (K then V)."""
+    kb = torch.from_numpy(K).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    vb = torch.from_numpy(V).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return np.concatenate([kb.reshape(len(K), -1), vb.reshape(len(V), -1)], axis=1).view(np.uint8)
+
+
+def _q_bits(q):
+    return torch.from_numpy(q).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_attention_dense_matches_torch_sdpa():
+    """Budget >= context: the whole path is dense attention, which torch's
+    fp64 scaled_dot_product_attention computes independently (GQA expanded by
+    repeating each KV head for its 4 query heads)."""
+    n = 37
+    u = synth.unit_inputs(n, seed=4, planted_blocks=[], device="cpu")
+    rows = synth.kv_rows(n, seed=5).numpy()
+    qb = u.q.view(torch.int16).numpy().view(np.uint16)
+    slot = np.full(n, -1, dtype=np.int32)
+    res = O.layer_step(u.codes.numpy(), u.scales.view(torch.int16).numpy().view(np.uint16),
+                       u.q_idx.numpy(), u.w.numpy(), qb, slot, None, rows, 2048, 1 / math.sqrt(128))
+    assert res["tokens"].tolist() == list(range(n))
+    rt = torch.from_numpy(rows).view(torch.bfloat16).reshape(n, 2, 4, 128).double()
+    K = rt[:, 0].permute(1, 0, 2).repeat_interleave(4, dim=0)      # [16][n][128]
+    V = rt[:, 1].permute(1, 0, 2).repeat_interleave(4, dim=0)
+    q = u.q.double().reshape(16, 1, 128)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, K, V, scale=1 / math.sqrt(128))
+    assert np.allclose(res["out"], ref.reshape(16, 128).numpy(), rtol=0, atol=1e-12)
+    logits = torch.einsum("hd,hnd->hn", u.q.double(), K) / math.sqrt(128)
+    assert np.allclose(res["lse"], torch.logsumexp(logits, dim=1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((16, 128))
+    # one row: output = V, lse = its logit
+    K = rng.standard_normal((1, 4, 128)); V = rng.standard_normal((1, 4, 128))
+    rows = _rows_from(K, V)
+    Kd, Vd = O.split_kv(rows)
+    out, lse = O.decode_attention(_q_bits(q), rows, 0.5)
+    qd = O.decode_bf16(_q_bits(q))
+    for h in range(16):
+        assert np.array_equal(out[h], Vd[0, h // 4])
+        assert np.isclose(lse[h], 0.5 * qd[h] @ Kd[0, h // 4], rtol=1e-15)
+    # identical keys: uniform weights, output = mean of V, lse = logit + log m
+    m = 9
+    K = np.repeat(rng.standard_normal((1, 4, 128)), m, axis=0)
+    V = rng.standard_normal((m, 4, 128))
+    rows = _rows_from(K, V)
+    Kd, Vd = O.split_kv(rows)
+    out, lse = O.decode_attention(_q_bits(q), rows, 0.25)
+    for h in range(16):
+        g = h // 4
+        assert np.allclose(out[h], Vd[:, g].mean(axis=0), rtol=0, atol=1e-13)
+        assert np.isclose(lse[h], 0.25 * qd[h] @ Kd[0, g] + math.log(m), rtol=1e-14)
+    # no rows: zeros and -inf
+    out, lse = O.decode_attention(_q_bits(q), np.zeros((0, 2048), np.uint8), 0.25)
+    assert (out == 0).all() and np.isneginf(lse).all()
+
+
+def test_attention_split_merge_and_permutation():
+    """Attention over A u B equals the log-sum-exp merge of A and B
+    (o = (e^{lse_A} o_A + e^{lse_B} o_B) / (e^{lse_A} + e^{lse_B}),
+    lse = log(e^{lse_A} + e^{lse_B})), and row order does not matter."""
+    rng = np.random.default_rng(8)
+    rows = synth.kv_rows(50, seed=9).numpy()
+    qb = _q_bits(rng.standard_normal((16, 128)))
+    o, l = O.decode_attention(qb, rows, 0.1)
+    oa, la = O.decode_attention(qb, rows[:20], 0.1)
+    ob, lb = O.decode_attention(qb, rows[20:], 0.1)
+    M = np.maximum(la, lb)
+    wa, wb = np.exp(la - M), np.exp(lb - M)
+    om = (wa[:, None] * oa + wb[:, None] * ob) / (wa + wb)[:, None]
+    assert np.allclose(o, om, rtol=0, atol=1e-13)
+    assert np.allclose(l, M + np.log(wa + wb), rtol=0, atol=1e-13)
+    p = rng.permutation(50)
+    op, lp = O.decode_attention(qb, rows[p], 0.1)
+    assert np.allclose(o, op, rtol=0, atol=1e-13) and np.allclose(l, lp, rtol=0, atol=1e-13)
+
+
+def test_gqa_grouping_uses_contiguous_heads():
+    """Changing KV head g's keys moves only query heads 4g..4g+3."""
+    rows = synth.kv_rows(12, seed=3).numpy().copy()
+    qb = _q_bits(np.random.default_rng(0).standard_normal((16, 128)))
+    o1, _ = O.decode_attention(qb, rows, 0.1)
+    r2 = rows.copy().view(np.uint16).reshape(12, 2, 4, 128)
+    r2[:, 0, 2, :] ^= 0x8000                 # flip the sign of K of KV head 2
+    o2, _ = O.decode_attention(qb, r2.reshape(12, -1).view(np.uint8), 0.1)
+    changed = [h for h in range(16) if not np.array_equal(o1[h], o2[h])]
+    assert changed == [8, 9, 10, 11]
+
+
+# ------------------------------------------------------ byte accounting
+
+def test_page_byte_accounting():
+    g = _load("page_sizes.json")
+    assert O.ROW_BYTES == g["kv_bytes_per_token_per_layer"]["value"]
+    assert O.INDEX_DIM + 2 == g["index_key_bytes_per_token_per_layer"]["value"]
+    n = 262144
+    blk = np.arange(n // 4, dtype=np.float64)
+    toks = O.selected_tokens(O.select_blocks(blk, g["indexer_budget_tokens"]["value"]), n)
+    assert len(toks) == g["indexer_budget_tokens"]["value"]
+    assert len(toks) * O.ROW_BYTES * g["qsa_layers"]["value"] == g["bytes_moved_per_decode_step"]["value"]
+    assert 4 * len(O.select_blocks(blk, 2048)) == 2048 and g["c4_block_tokens"]["value"] == 4
