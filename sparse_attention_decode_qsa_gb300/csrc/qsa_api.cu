@@ -1,0 +1,470 @@
+// C ABI of the QSA decode-step library and its host-side cache manager.
+//
+// The cache manager follows "双卡RTX4090跑通Qwen3-Next：8并发满血长上下文实测",
+// section "显存账本：热缓存卸载省下约84%": the full KV history of a long
+// request stays in pinned host memory, the GPU keeps a hot tail ring per
+// request plus a shared staging area, logical token addresses are kept apart
+// from physical cache slots (the slot table), and requests hold leases with
+// generation tags so that a finished or cancelled request gives its capacity
+// and slots back and a new request can reuse them safely.
+//
+// Host state: one lease per request slot and a first-fit free list of HBM
+// pool row ranges.  Device state (all caller-allocated): the pool, the index
+// keys, the slot table and the workspace (error word + split-K partials).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <iterator>
+#include <map>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "qsa_internal.cuh"
+
+using namespace qsa;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+qsa_status_t fail(qsa_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+qsa_status_t fail(qsa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+qsa_status_t ok() {
+  g_last_error.clear();
+  return QSA_OK;
+}
+
+qsa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(QSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct Lease {
+  uint32_t generation = 0;
+  bool active = false;
+  int64_t ctx_len = 0;
+  int32_t placement = 0;
+  int32_t layer_rows = 0;
+  int64_t row_base = 0;
+  int64_t rows = 0;
+  const uint8_t* host_rows = nullptr;  // device-usable address
+};
+
+int64_t splits_max_of(const qsa_cache_config& c) {
+  const int64_t kmax = c.budget_tokens / 4;
+  return (kmax + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit;
+}
+
+bool config_sizes_ok(const qsa_cache_config* c) {
+  return c && c->n_layers > 0 && c->max_requests > 0 && c->ctx_capacity > 0 &&
+         c->ctx_capacity <= 0x7FFFFFFFll && c->budget_tokens >= 4 &&
+         c->budget_tokens % 4 == 0 && c->budget_tokens <= QSA_MAX_BUDGET_TOKENS &&
+         c->ring_tokens > 0 && c->staging_rows >= 0 && c->hbm_pool_rows >= 0 &&
+         c->hbm_pool_rows <= 0x7FFFFFFFll;
+}
+
+}  // namespace
+
+struct qsa_cache {
+  qsa_cache_config cfg;
+  bool has_device = false;
+  int64_t staging_total = 0;
+  int64_t splits_max = 0;
+  std::vector<Lease> leases;
+  std::map<int64_t, int64_t> free_rows;  // start -> length
+
+  ErrorWord* err() const { return reinterpret_cast<ErrorWord*>(cfg.workspace); }
+  float* partials() const {
+    return reinterpret_cast<float*>(static_cast<uint8_t*>(cfg.workspace) + kErrBytes);
+  }
+
+  bool alloc_rows(int64_t n, int64_t* base) {
+    for (auto it = free_rows.begin(); it != free_rows.end(); ++it) {
+      if (it->second >= n) {
+        *base = it->first;
+        const int64_t rest = it->second - n, start = it->first + n;
+        free_rows.erase(it);
+        if (rest > 0) free_rows[start] = rest;
+        return true;
+      }
+    }
+    return false;
+  }
+
+  void release_rows(int64_t base, int64_t n) {
+    if (n <= 0) return;
+    auto next = free_rows.lower_bound(base);
+    if (next != free_rows.end() && base + n == next->first) {
+      n += next->second;
+      next = free_rows.erase(next);
+    }
+    if (next != free_rows.begin()) {
+      auto prev = std::prev(next);
+      if (prev->first + prev->second == base) {
+        prev->second += n;
+        return;
+      }
+    }
+    free_rows[base] = n;
+  }
+
+  qsa_status_t check_handle(qsa_handle h, const Lease** out) const {
+    if (h.index >= leases.size())
+      return fail(QSA_ERR_STALE_HANDLE, "request index %u out of range", h.index);
+    const Lease& l = leases[h.index];
+    if (!l.active || l.generation != h.generation)
+      return fail(QSA_ERR_STALE_HANDLE, "stale handle {%u, %u} (live generation %u, %s)", h.index,
+                  h.generation, l.generation, l.active ? "active" : "free");
+    *out = &l;
+    return QSA_OK;
+  }
+
+  // Validate a batch and describe its units for the kernels.
+  qsa_status_t build_batch(const qsa_batch* b, BatchDesc* d) const {
+    if (!has_device) return fail(QSA_ERR_NO_DEVICE, "cache has no device storage");
+    if (!b || !b->requests) return fail(QSA_ERR_INVALID_ARG, "null batch");
+    if (b->n_req <= 0 || b->n_layers <= 0 || b->layer0 < 0 ||
+        (int64_t)b->layer0 + b->n_layers > cfg.n_layers)
+      return fail(QSA_ERR_INVALID_ARG, "bad batch shape n_req=%d layer0=%d n_layers=%d",
+                  b->n_req, b->layer0, b->n_layers);
+    if ((int64_t)b->n_req * b->n_layers > kMaxUnits)
+      return fail(QSA_ERR_INVALID_ARG, "batch has %lld units, limit %d",
+                  (long long)b->n_req * b->n_layers, kMaxUnits);
+    d->n_units = b->n_req * b->n_layers;
+    d->n_layers = cfg.n_layers;
+    d->ctx_cap = cfg.ctx_capacity;
+    d->pool_rows = cfg.hbm_pool_rows;
+    d->index_keys = cfg.index_keys;
+    d->index_scales = cfg.index_scales;
+    d->slot_table = cfg.slot_table;
+    d->pool = static_cast<uint8_t*>(cfg.hbm_pool);
+    d->err = err();
+    d->partials = partials();
+    d->splits_max = (int32_t)splits_max;
+    d->pad0 = 0;
+    for (int i = 0; i < b->n_req; ++i) {
+      const Lease* l;
+      if (qsa_status_t st = check_handle(b->requests[i], &l)) return st;
+      for (int k = 0; k < i; ++k)
+        if (b->requests[k].index == b->requests[i].index)
+          return fail(QSA_ERR_INVALID_ARG, "request %u appears twice in the batch",
+                      b->requests[i].index);
+      for (int li = 0; li < b->n_layers; ++li) {
+        UnitDesc& u = d->u[li * b->n_req + i];
+        u.req = (int32_t)b->requests[i].index;
+        u.layer = b->layer0 + li;
+        u.n = l->ctx_len;
+        u.host_rows = l->host_rows ? l->host_rows + (int64_t)u.layer * l->ctx_len * kRowBytes
+                                   : nullptr;
+      }
+    }
+    return QSA_OK;
+  }
+};
+
+extern "C" {
+
+int32_t qsa_abi_version(void) { return QSA_ABI_VERSION; }
+
+const char* qsa_last_error_string(void) { return g_last_error.c_str(); }
+
+int64_t qsa_workspace_bytes(const qsa_cache_config* c) {
+  if (!config_sizes_ok(c)) return -1;
+  return kErrBytes + (int64_t)c->max_requests * c->n_layers * splits_max_of(*c) * kPartFloats *
+                         (int64_t)sizeof(float);
+}
+
+qsa_status_t qsa_cache_create(const qsa_cache_config* c, qsa_cache** out) {
+  if (!out) return fail(QSA_ERR_INVALID_ARG, "null output pointer");
+  *out = nullptr;
+  if (!config_sizes_ok(c)) return fail(QSA_ERR_INVALID_ARG, "bad cache config sizes");
+  const bool any = c->hbm_pool || c->index_keys || c->index_scales || c->slot_table || c->workspace;
+  const bool all = c->hbm_pool && c->index_keys && c->index_scales && c->slot_table && c->workspace;
+  if (any && !all)
+    return fail(QSA_ERR_INVALID_ARG, "device storage must be given completely or not at all");
+  if (all) {
+    if (c->workspace_bytes < qsa_workspace_bytes(c))
+      return fail(QSA_ERR_INVALID_ARG, "workspace has %lld bytes, needs %lld",
+                  (long long)c->workspace_bytes, (long long)qsa_workspace_bytes(c));
+    const void* ptrs[] = {c->hbm_pool, c->index_keys, c->index_scales, c->slot_table, c->workspace};
+    for (const void* p : ptrs)
+      if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+        return fail(QSA_ERR_INVALID_ARG, "device buffers must be 16-byte aligned");
+  }
+  const int64_t staging = (int64_t)c->n_layers * c->staging_rows;
+  if (staging > c->hbm_pool_rows)
+    return fail(QSA_ERR_CAPACITY, "staging (%lld rows) does not fit the pool (%lld rows)",
+                (long long)staging, (long long)c->hbm_pool_rows);
+
+  qsa_cache* cache = new (std::nothrow) qsa_cache();
+  if (!cache) return fail(QSA_ERR_INVALID_ARG, "out of host memory");
+  cache->cfg = *c;
+  cache->has_device = all;
+  cache->staging_total = staging;
+  cache->splits_max = splits_max_of(*c);
+  cache->leases.resize(c->max_requests);
+  if (c->hbm_pool_rows > staging) cache->free_rows[staging] = c->hbm_pool_rows - staging;
+
+  if (all) {
+    cudaError_t e = cudaMemset(c->workspace, 0, (size_t)c->workspace_bytes);
+    if (e == cudaSuccess)
+      e = cudaMemset(c->slot_table, 0xFF,
+                     (size_t)c->max_requests * c->n_layers * c->ctx_capacity * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      delete cache;
+      return cuda_fail(e, "initialising workspace and slot table");
+    }
+  }
+  *out = cache;
+  return ok();
+}
+
+qsa_status_t qsa_cache_destroy(qsa_cache* cache) {
+  delete cache;
+  return ok();
+}
+
+qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void* stream,
+                               qsa_handle* out) {
+  if (!c || !desc || !out) return fail(QSA_ERR_INVALID_ARG, "null argument");
+  if (desc->ctx_len < 1) return fail(QSA_ERR_INVALID_ARG, "ctx_len must be >= 1");
+  if (desc->ctx_len > c->cfg.ctx_capacity)
+    return fail(QSA_ERR_CAPACITY, "ctx_len %lld exceeds capacity %lld", (long long)desc->ctx_len,
+                (long long)c->cfg.ctx_capacity);
+  if (desc->placement != QSA_KV_HBM && desc->placement != QSA_KV_HOST_RING)
+    return fail(QSA_ERR_INVALID_ARG, "unknown placement %d", desc->placement);
+  if (desc->placement == QSA_KV_HOST_RING && !desc->host_rows)
+    return fail(QSA_ERR_INVALID_ARG, "host-ring placement needs host_rows");
+  if (desc->placement == QSA_KV_HBM && desc->host_rows)
+    return fail(QSA_ERR_INVALID_ARG, "HBM placement takes no host_rows");
+
+  int slot = -1;
+  for (size_t i = 0; i < c->leases.size(); ++i)
+    if (!c->leases[i].active) { slot = (int)i; break; }
+  if (slot < 0) return fail(QSA_ERR_OUT_OF_SLOTS, "all %d request slots are leased", c->cfg.max_requests);
+
+  const int32_t layer_rows = desc->placement == QSA_KV_HBM ? (int32_t)desc->ctx_len : c->cfg.ring_tokens;
+  const int64_t rows = (int64_t)layer_rows * c->cfg.n_layers;
+
+  const uint8_t* host_dev = nullptr;
+  if (desc->placement == QSA_KV_HOST_RING) {
+    if (c->has_device) {
+      void* dptr = nullptr;
+      cudaError_t e = cudaHostGetDevicePointer(&dptr, const_cast<void*>(desc->host_rows), 0);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(QSA_ERR_INVALID_ARG, "host_rows is not pinned, mapped host memory: %s",
+                    cudaGetErrorString(e));
+      }
+      host_dev = static_cast<const uint8_t*>(dptr);
+    } else {
+      host_dev = static_cast<const uint8_t*>(desc->host_rows);
+    }
+    if (reinterpret_cast<uintptr_t>(host_dev) % 16 != 0)
+      return fail(QSA_ERR_INVALID_ARG, "host_rows must be 16-byte aligned");
+  }
+
+  int64_t base = 0;
+  if (!c->alloc_rows(rows, &base))
+    return fail(QSA_ERR_CAPACITY, "no free pool range of %lld rows", (long long)rows);
+
+  if (c->has_device) {
+    int32_t* st = c->cfg.slot_table + (int64_t)slot * c->cfg.n_layers * c->cfg.ctx_capacity;
+    cudaError_t e = launch_slot_fill(st, c->cfg.n_layers, c->cfg.ctx_capacity, desc->ctx_len,
+                                     desc->placement, base, layer_rows,
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+      c->release_rows(base, rows);
+      return cuda_fail(e, "slot-table fill");
+    }
+  }
+
+  Lease& l = c->leases[slot];
+  l.generation += 1;
+  l.active = true;
+  l.ctx_len = desc->ctx_len;
+  l.placement = desc->placement;
+  l.layer_rows = layer_rows;
+  l.row_base = base;
+  l.rows = rows;
+  l.host_rows = host_dev;
+  out->index = (uint32_t)slot;
+  out->generation = l.generation;
+  return ok();
+}
+
+qsa_status_t qsa_request_end(qsa_cache* c, qsa_handle h) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  const Lease* cl;
+  if (qsa_status_t st = c->check_handle(h, &cl)) return st;
+  Lease& l = c->leases[h.index];
+  c->release_rows(l.row_base, l.rows);
+  l.active = false;
+  l.ctx_len = 0;
+  l.rows = 0;
+  l.host_rows = nullptr;
+  return ok();
+}
+
+qsa_status_t qsa_request_info_get(qsa_cache* c, qsa_handle h, qsa_request_info* out) {
+  if (!c || !out) return fail(QSA_ERR_INVALID_ARG, "null argument");
+  const Lease* l;
+  if (qsa_status_t st = c->check_handle(h, &l)) return st;
+  out->ctx_len = l->ctx_len;
+  out->placement = l->placement;
+  out->layer_rows = l->layer_rows;
+  out->hbm_row_base = l->row_base;
+  out->host_rows = l->host_rows;
+  return ok();
+}
+
+qsa_status_t qsa_cache_stats(const qsa_cache* c, qsa_stats* out) {
+  if (!c || !out) return fail(QSA_ERR_INVALID_ARG, "null argument");
+  std::memset(out, 0, sizeof *out);
+  out->max_requests = c->cfg.max_requests;
+  int64_t leased = 0;
+  for (const Lease& l : c->leases) {
+    if (l.active) { out->active_requests++; leased += l.rows; }
+  }
+  out->free_request_slots = c->cfg.max_requests - out->active_requests;
+  out->free_ranges = (int32_t)c->free_rows.size();
+  out->hbm_pool_rows = c->cfg.hbm_pool_rows;
+  for (const auto& kv : c->free_rows) {
+    out->free_hbm_rows += kv.second;
+    if (kv.second > out->largest_free_rows) out->largest_free_rows = kv.second;
+  }
+  out->staging_rows_total = c->staging_total;
+  out->hbm_kv_bytes_in_use = leased * kRowBytes;
+  return ok();
+}
+
+qsa_status_t qsa_slot_table_ptr(qsa_cache* c, qsa_handle h, int32_t layer, int32_t** out) {
+  if (!c || !out) return fail(QSA_ERR_INVALID_ARG, "null argument");
+  if (!c->has_device) return fail(QSA_ERR_NO_DEVICE, "cache has no device storage");
+  const Lease* l;
+  if (qsa_status_t st = c->check_handle(h, &l)) return st;
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(QSA_ERR_INVALID_ARG, "bad layer %d", layer);
+  *out = c->cfg.slot_table + ((int64_t)h.index * c->cfg.n_layers + layer) * c->cfg.ctx_capacity;
+  return ok();
+}
+
+qsa_status_t qsa_slot_table_set(qsa_cache* c, qsa_handle h, int32_t layer, const int64_t* tokens,
+                                const int32_t* slots, int32_t n, void* stream) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  int32_t* row = nullptr;
+  if (qsa_status_t st = qsa_slot_table_ptr(c, h, layer, &row)) return st;
+  if (n < 0 || (n > 0 && (!tokens || !slots))) return fail(QSA_ERR_INVALID_ARG, "bad token/slot arrays");
+  cudaError_t e = launch_slot_set(row, c->leases[h.index].ctx_len, c->cfg.hbm_pool_rows, tokens,
+                                  slots, n, c->err(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "slot-table set");
+  return ok();
+}
+
+qsa_status_t qsa_staging_ptr(qsa_cache* c, int32_t layer, void** out) {
+  if (!c || !out) return fail(QSA_ERR_INVALID_ARG, "null argument");
+  if (!c->has_device) return fail(QSA_ERR_NO_DEVICE, "cache has no device storage");
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(QSA_ERR_INVALID_ARG, "bad layer %d", layer);
+  *out = static_cast<uint8_t*>(c->cfg.hbm_pool) + (int64_t)layer * c->cfg.staging_rows * kRowBytes;
+  return ok();
+}
+
+qsa_status_t qsa_poll_error(qsa_cache* c, void* stream, int32_t* dev_status, int64_t* detail) {
+  if (!c || !dev_status) return fail(QSA_ERR_INVALID_ARG, "null argument");
+  if (!c->has_device) return fail(QSA_ERR_NO_DEVICE, "cache has no device storage");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ErrorWord host{};
+  cudaError_t e = cudaMemcpyAsync(&host, c->err(), sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->err(), 0, sizeof host, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *dev_status = host.status;
+  if (detail) *detail = host.detail;
+  return ok();
+}
+
+qsa_status_t qsa_index_score(qsa_cache* c, const qsa_batch* batch, const float* q_idx,
+                             const float* w, float* blk_scores, int64_t blk_stride, void* stream) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  BatchDesc d;
+  if (qsa_status_t st = c->build_batch(batch, &d)) return st;
+  if (!q_idx || !w || !blk_scores) return fail(QSA_ERR_INVALID_ARG, "null q_idx, w or blk_scores");
+  for (int u = 0; u < d.n_units; ++u)
+    if (blk_stride < (d.u[u].n + 3) / 4)
+      return fail(QSA_ERR_INVALID_ARG, "blk_stride %lld < %lld blocks of unit %d",
+                  (long long)blk_stride, (long long)((d.u[u].n + 3) / 4), u);
+  cudaError_t e = launch_index_score(d, q_idx, w, blk_scores, blk_stride,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "index-score launch");
+  return ok();
+}
+
+qsa_status_t qsa_select_c4_topk(qsa_cache* c, const qsa_batch* batch, const float* blk_scores,
+                                int64_t blk_stride, int32_t budget_tokens, int32_t* sel_blocks,
+                                int32_t* n_sel, void* stream) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  BatchDesc d;
+  if (qsa_status_t st = c->build_batch(batch, &d)) return st;
+  if (!blk_scores || !sel_blocks || !n_sel) return fail(QSA_ERR_INVALID_ARG, "null array");
+  if (budget_tokens < 4 || budget_tokens % 4 || budget_tokens > c->cfg.budget_tokens)
+    return fail(QSA_ERR_INVALID_ARG, "budget_tokens %d must be a multiple of 4 in [4, %d]",
+                budget_tokens, c->cfg.budget_tokens);
+  for (int u = 0; u < d.n_units; ++u)
+    if (blk_stride < (d.u[u].n + 3) / 4)
+      return fail(QSA_ERR_INVALID_ARG, "blk_stride too small for unit %d", u);
+  cudaError_t e = launch_select_topk(d, blk_scores, blk_stride, budget_tokens / 4, sel_blocks,
+                                     n_sel, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  return ok();
+}
+
+qsa_status_t qsa_gather_rows(qsa_cache* c, const qsa_batch* batch, const int32_t* sel_blocks,
+                             const int32_t* n_sel, int32_t budget_tokens, void* rows_out,
+                             int32_t* n_rows, void* stream) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  BatchDesc d;
+  if (qsa_status_t st = c->build_batch(batch, &d)) return st;
+  if (!sel_blocks || !n_sel || !rows_out) return fail(QSA_ERR_INVALID_ARG, "null array");
+  if (budget_tokens < 4 || budget_tokens % 4 || budget_tokens > c->cfg.budget_tokens)
+    return fail(QSA_ERR_INVALID_ARG, "bad budget_tokens %d", budget_tokens);
+  if (reinterpret_cast<uintptr_t>(rows_out) % 16)
+    return fail(QSA_ERR_INVALID_ARG, "rows_out must be 16-byte aligned");
+  cudaError_t e = launch_gather_rows(d, sel_blocks, n_sel, budget_tokens,
+                                     static_cast<uint8_t*>(rows_out), n_rows,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  return ok();
+}
+
+qsa_status_t qsa_sparse_decode_attn(qsa_cache* c, const qsa_batch* batch, const uint16_t* q,
+                                    const int32_t* sel_blocks, const int32_t* n_sel,
+                                    int32_t budget_tokens, const void* gathered,
+                                    float softmax_scale, float* out, float* lse, void* stream) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  BatchDesc d;
+  if (qsa_status_t st = c->build_batch(batch, &d)) return st;
+  if (!q || !sel_blocks || !n_sel || !out) return fail(QSA_ERR_INVALID_ARG, "null array");
+  if (budget_tokens < 4 || budget_tokens % 4 || budget_tokens > c->cfg.budget_tokens)
+    return fail(QSA_ERR_INVALID_ARG, "bad budget_tokens %d", budget_tokens);
+  if (reinterpret_cast<uintptr_t>(gathered) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
+    return fail(QSA_ERR_INVALID_ARG, "q and gathered must be 16-byte aligned");
+  if (!(softmax_scale == softmax_scale)) return fail(QSA_ERR_INVALID_ARG, "softmax_scale is NaN");
+  cudaError_t e = launch_sparse_attn(d, q, sel_blocks, n_sel, budget_tokens,
+                                     static_cast<const uint8_t*>(gathered), softmax_scale, out,
+                                     lse, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// Internal declarations shared by the kernels and the C-ABI layer of the
+// QSA decode-step library.  Not part of the public interface (include/qsa.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qsa.h"
+
+namespace qsa {
+
+constexpr int kIndexHeads = QSA_INDEX_HEADS;  // 8
+constexpr int kIndexDim = QSA_INDEX_DIM;      // 64
+constexpr int kKvHeads = QSA_KV_HEADS;        // 4
+constexpr int kHeadDim = QSA_HEAD_DIM;        // 128
+constexpr int kQHeads = QSA_Q_HEADS;          // 16
+constexpr int kGroup = kQHeads / kKvHeads;    // 4 query heads per KV head
+constexpr int kRowBytes = QSA_ROW_BYTES;      // 2048
+constexpr int kMaxUnits = QSA_MAX_UNITS;
+
+// Split-K granularity of the attention: one CTA covers this many selected
+// C4 blocks (32 tokens, 64 KiB of rows).
+constexpr int kAttnBlocksPerSplit = 8;
+constexpr int kAttnTokensPerSplit = kAttnBlocksPerSplit * 4;
+// One split-K partial: running max m[16] and sum l[16] (base-2 logits), then
+// the unnormalised accumulator acc[16][128].
+constexpr int kPartFloats = kQHeads + kQHeads + kQHeads * kHeadDim;  // 2080
+// Bytes at the start of the workspace reserved for the device error word.
+constexpr int64_t kErrBytes = 256;
+
+// Device error word.  The first kernel that meets a bad input records its
+// status; later ones keep the first record.
+struct ErrorWord {
+  int32_t status;
+  int32_t kernel;
+  int64_t detail;
+};
+
+enum KernelId : int32_t {
+  kKernIndexScore = 1,
+  kKernTopk = 2,
+  kKernGather = 3,
+  kKernAttn = 4,
+  kKernSlotFill = 5,
+  kKernSlotSet = 6,
+};
+
+// One decode unit (request slot, layer) of a call.
+struct UnitDesc {
+  int32_t req;                // request slot index
+  int32_t layer;              // QSA layer
+  int64_t n;                  // cached tokens of the request
+  const uint8_t* host_rows;   // device-usable address of host row 0 of this
+                              // (request, layer), or nullptr
+};
+
+// Everything a kernel needs to find a unit's data.  Passed by value.
+struct BatchDesc {
+  int32_t n_units;
+  int32_t n_layers;           // layers per request in the cache layout
+  int64_t ctx_cap;            // ctx_capacity of the cache layout
+  int64_t pool_rows;
+  const uint8_t* index_keys;  // [req][layer][ctx_cap][64]
+  const uint16_t* index_scales;
+  int32_t* slot_table;        // [req][layer][ctx_cap]
+  uint8_t* pool;              // [pool_rows][2048]
+  ErrorWord* err;
+  float* partials;            // [req][layer][splits_max][kPartFloats]
+  int32_t splits_max;
+  int32_t pad0;
+  UnitDesc u[kMaxUnits];
+
+  __host__ __device__ int64_t unit_row(int u_) const {
+    return ((int64_t)u[u_].req * n_layers + u[u_].layer) * ctx_cap;
+  }
+};
+
+__device__ __forceinline__ void report_error(ErrorWord* e, int32_t status, int32_t kernel,
+                                             int64_t detail) {
+  if (atomicCAS(&e->status, 0, status) == 0) {
+    e->kernel = kernel;
+    e->detail = detail;
+  }
+}
+
+// Source address of the 2048-byte row of logical token t of unit u, read
+// through the slot table: pool row when the slot is >= 0, else the host
+// history.  Returns nullptr (and records the error) for an invalid slot.
+__device__ __forceinline__ const uint8_t* row_source(const BatchDesc& b, int u, int64_t t,
+                                                     int32_t kernel) {
+  const int32_t slot = b.slot_table[b.unit_row(u) + t];
+  if (slot >= 0 && (int64_t)slot < b.pool_rows) return b.pool + (int64_t)slot * kRowBytes;
+  if (slot == -1 && b.u[u].host_rows != nullptr) return b.u[u].host_rows + t * kRowBytes;
+  report_error(b.err, QSA_ERR_BAD_SLOT, kernel, ((int64_t)u << 40) | (t & 0xFFFFFFFFFFll));
+  return nullptr;
+}
+
+// ------------------------------------------------------------ launchers
+// Each returns the launch status (cudaGetLastError right after the launch).
+
+cudaError_t launch_index_score(const BatchDesc& b, const float* q_idx, const float* w,
+                               float* blk_scores, int64_t blk_stride, cudaStream_t s);
+
+cudaError_t launch_select_topk(const BatchDesc& b, const float* blk_scores, int64_t blk_stride,
+                               int32_t k_max, int32_t* sel_blocks, int32_t* n_sel,
+                               cudaStream_t s);
+
+cudaError_t launch_gather_rows(const BatchDesc& b, const int32_t* sel_blocks,
+                               const int32_t* n_sel, int32_t budget_tokens, uint8_t* rows_out,
+                               int32_t* n_rows, cudaStream_t s);
+
+cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int32_t* sel_blocks,
+                               const int32_t* n_sel, int32_t budget_tokens,
+                               const uint8_t* gathered, float softmax_scale, float* out,
+                               float* lse, cudaStream_t s);
+
+// Slot-table maintenance.
+cudaError_t launch_slot_fill(int32_t* rows, int32_t n_layers, int64_t ctx_cap, int64_t ctx_len,
+                             int32_t placement, int64_t row_base, int32_t layer_rows,
+                             cudaStream_t s);
+
+cudaError_t launch_slot_set(int32_t* row, int64_t ctx_len, int64_t pool_rows,
+                            const int64_t* tokens, const int32_t* slots, int32_t n,
+                            ErrorWord* err, cudaStream_t s);
+
+}  // namespace qsa

@@ -1,0 +1,271 @@
+// Step 4 of the QSA decode step: GQA decode attention over the selected
+// rows only ("Оффлоадинг KV-кэша Qwen3.8-Flash-Next в RAM через vLLM без
+// потери скорости декодирования", section "Механизм гибридного разреженного
+// оффлоадинга": attention reads only the <= indexer_budget selected rows).
+//
+// Split-K flash-decode: CTA (unit, split) takes 8 selected C4 blocks (32
+// tokens, 64 KiB of K/V), reads their rows through the slot table (pool rows
+// from HBM, cold rows zero-copy from mapped pinned host memory) or from a
+// dense gathered buffer, and writes a partial (m, l, acc) in base-2 logits
+// to the workspace.  A second kernel merges the partials of each (unit,
+// head) with the log-sum-exp rule and writes out and lse.
+//
+// Per CTA (256 threads, 64 KiB dynamic shared memory):
+//   load   : every thread issues 16 independent 16-byte loads, then stores
+//            them to shared memory (all loads in flight before any store);
+//   logits : warp w serves KV head w/2 and 16 tokens; lane l holds dims
+//            4l..4l+3 of the 4 query heads of that KV head, and the four
+//            partial dots are reduced across the warp with a transposing
+//            butterfly (6 shuffles for 4 values);
+//   softmax: warp w owns query heads 2w, 2w+1, lane = token;
+//   P.V    : thread t serves KV head t/64 and dims 2(t%64), 2(t%64)+1 of its
+//            4 query heads.
+// The products are plain FMAs: 4 query heads per KV head make this a
+// 4-row contraction, not a tensor-core shape.
+#include <cuda_bf16.h>
+
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSplitTokens = kAttnTokensPerSplit;  // 32
+constexpr int kChunksPerRow = kRowBytes / 16;      // 128
+constexpr int kSmemBytes = kSplitTokens * kRowBytes;  // 64 KiB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct AttnParams {
+  BatchDesc b;
+  const uint16_t* q;        // [units][16][128] bf16 bits
+  const int32_t* sel;       // [units][k_max]
+  const int32_t* n_sel;
+  int32_t k_max;
+  int32_t budget_tokens;
+  const uint8_t* gathered;  // [units][budget_tokens][2048] or nullptr
+  float scale_log2;         // softmax_scale * log2(e)
+  float* out;               // [units][16][128]
+  float* lse;               // [units][16] or nullptr
+};
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint8_t* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+__device__ __forceinline__ float* partial_ptr(const BatchDesc& b, int u, int split) {
+  const int64_t rl = (int64_t)b.u[u].req * b.n_layers + b.u[u].layer;
+  return b.partials + (rl * b.splits_max + split) * kPartFloats;
+}
+
+__global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p) {
+  extern __shared__ __align__(16) uint8_t rows[];  // [32][2048]
+  __shared__ const uint8_t* src[kSplitTokens];
+  __shared__ float logit[kQHeads][kSplitTokens];
+  __shared__ float m_s[kQHeads], l_s[kQHeads];
+
+  const int u = blockIdx.y;
+  const int split = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n = p.b.u[u].n;
+  const int nsel = p.n_sel[u];
+  if (nsel < 0 || nsel > p.k_max) {
+    if (tid == 0 && split == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
+    return;
+  }
+  const int j0 = split * kAttnBlocksPerSplit;
+  if (j0 >= nsel) return;  // the merge reads only the splits that hold tokens
+
+  // ---- resolve the 32 row sources
+  if (tid < kSplitTokens) {
+    const int j = j0 + tid / 4;
+    const uint8_t* ptr = nullptr;
+    if (j < nsel) {
+      const int64_t b = p.sel[(int64_t)u * p.k_max + j];
+      const int64_t t = 4 * b + (tid & 3);
+      if (b < 0 || 4 * b >= n) {
+        if ((tid & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
+      } else if (t < n) {
+        ptr = p.gathered ? p.gathered + ((int64_t)u * p.budget_tokens + 4 * j + (tid & 3)) * kRowBytes
+                         : row_source(p.b, u, t, kKernAttn);
+      }
+    }
+    src[tid] = ptr;
+  }
+  __syncthreads();
+
+  // ---- rows -> shared memory (16 loads in flight per thread)
+  {
+    constexpr int kPer = kSplitTokens * kChunksPerRow / kThreads;  // 16
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = k * kThreads + tid;
+      const uint8_t* s = src[idx / kChunksPerRow];
+      v[k] = s ? ld_nc_v4(s + (idx % kChunksPerRow) * 16) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      *reinterpret_cast<uint4*>(rows + (k * kThreads + tid) * 16) = v[k];
+  }
+  __syncthreads();
+
+  // ---- logits (base 2): warp -> (KV head g, 16 tokens), lane -> 4 dims
+  {
+    const int g = warp >> 1;
+    const int tok0 = (warp & 1) * 16;
+    float qr[kGroup][4];
+    const uint16_t* qu = p.q + (int64_t)u * kQHeads * kHeadDim;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      const uint2 w2 = *reinterpret_cast<const uint2*>(qu + (g * kGroup + j) * kHeadDim + 4 * lane);
+      qr[j][0] = bf16_lo(w2.x) * p.scale_log2;
+      qr[j][1] = bf16_hi(w2.x) * p.scale_log2;
+      qr[j][2] = bf16_lo(w2.y) * p.scale_log2;
+      qr[j][3] = bf16_hi(w2.y) * p.scale_log2;
+    }
+    const int hsel = (lane >> 3) & 3;  // head this lane ends up holding
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int tok = tok0 + i;
+      const uint2 kk = *reinterpret_cast<const uint2*>(rows + tok * kRowBytes + g * kHeadDim * 2 + lane * 8);
+      const float k0 = bf16_lo(kk.x), k1 = bf16_hi(kk.x), k2 = bf16_lo(kk.y), k3 = bf16_hi(kk.y);
+      float d[kGroup];
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j)
+        d[j] = fmaf(qr[j][3], k3, fmaf(qr[j][2], k2, fmaf(qr[j][1], k1, qr[j][0] * k0)));
+      // transposing butterfly: after it, lane l holds the full dot of head (l>>3)&3
+      const bool up16 = lane & 16;
+      const float a0 = up16 ? d[0] : d[2], a1 = up16 ? d[1] : d[3];
+      const float r0 = __shfl_xor_sync(0xFFFFFFFFu, a0, 16);
+      const float r1 = __shfl_xor_sync(0xFFFFFFFFu, a1, 16);
+      const float v0 = (up16 ? d[2] : d[0]) + r0;
+      const float v1 = (up16 ? d[3] : d[1]) + r1;
+      const bool up8 = lane & 8;
+      const float a = up8 ? v0 : v1;
+      float v = (up8 ? v1 : v0) + __shfl_xor_sync(0xFFFFFFFFu, a, 8);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+      if ((lane & 7) == 0) logit[g * kGroup + hsel][tok] = src[tok] ? v : -INFINITY;
+    }
+  }
+  __syncthreads();
+
+  // ---- softmax within the split: warp -> heads 2w, 2w+1, lane -> token
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = 2 * warp + hh;
+    const float x = logit[h][lane];
+    float m = x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float pr = (x == -INFINITY) ? 0.f : exp2f(x - m);
+    float l = pr;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+    logit[h][lane] = pr;
+    if (lane == 0) { m_s[h] = m; l_s[h] = l; }
+  }
+  __syncthreads();
+
+  // ---- P.V: thread -> KV head g, dims d0, d0+1 of its 4 query heads
+  float* part = partial_ptr(p.b, u, split);
+  {
+    const int g = tid >> 6;
+    const int d0 = 2 * (tid & 63);
+    float acc[kGroup][2];
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) acc[j][0] = acc[j][1] = 0.f;
+#pragma unroll 8
+    for (int tok = 0; tok < kSplitTokens; ++tok) {
+      const uint32_t vv = *reinterpret_cast<const uint32_t*>(
+          rows + tok * kRowBytes + kKvHeads * kHeadDim * 2 + g * kHeadDim * 2 + d0 * 2);
+      const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) {
+        const float pr = logit[g * kGroup + j][tok];
+        acc[j][0] = fmaf(pr, v0, acc[j][0]);
+        acc[j][1] = fmaf(pr, v1, acc[j][1]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j)
+      *reinterpret_cast<float2*>(part + 2 * kQHeads + (g * kGroup + j) * kHeadDim + d0) =
+          make_float2(acc[j][0], acc[j][1]);
+  }
+  if (tid < kQHeads) {
+    part[tid] = m_s[tid];
+    part[kQHeads + tid] = l_s[tid];
+  }
+}
+
+// Merge: CTA (head, unit), thread = output dim.
+__global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const AttnParams p) {
+  const int h = blockIdx.x, u = blockIdx.y, d = threadIdx.x;
+  const int nsel = p.n_sel[u];
+  float* o = p.out + ((int64_t)u * kQHeads + h) * kHeadDim;
+  if (nsel <= 0 || nsel > p.k_max) {
+    o[d] = 0.f;
+    if (p.lse && d == 0) p.lse[(int64_t)u * kQHeads + h] = -INFINITY;
+    return;
+  }
+  const int splits = (nsel + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, partial_ptr(p.b, u, s)[h]);
+  float L = 0.f, acc = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < splits; ++s) {
+      const float* part = partial_ptr(p.b, u, s);
+      const float ms = part[h];
+      if (ms == -INFINITY) continue;
+      const float wgt = exp2f(ms - M);
+      L = fmaf(wgt, part[kQHeads + h], L);
+      acc = fmaf(wgt, part[2 * kQHeads + h * kHeadDim + d], acc);
+    }
+  }
+  o[d] = L > 0.f ? acc / L : 0.f;
+  if (p.lse && d == 0)
+    p.lse[(int64_t)u * kQHeads + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int32_t* sel_blocks,
+                               const int32_t* n_sel, int32_t budget_tokens,
+                               const uint8_t* gathered, float softmax_scale, float* out,
+                               float* lse, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  AttnParams p;
+  p.b = b;
+  p.q = q;
+  p.sel = sel_blocks;
+  p.n_sel = n_sel;
+  p.k_max = budget_tokens / 4;
+  p.budget_tokens = budget_tokens;
+  p.gathered = gathered;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.out = out;
+  p.lse = lse;
+  const int splits = (p.k_max + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit;
+  attn_split_kernel<<<dim3(splits, b.n_units), kThreads, kSmemBytes, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_merge_kernel<<<dim3(kQHeads, b.n_units), kHeadDim, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

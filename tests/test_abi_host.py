@@ -1,0 +1,200 @@
+"""CPU tests of the C-ABI library: it loads, exports every entry point that
+include/qsa.h declares, and its host-side cache manager (leases, generation
+tags, pool row ranges, request recycling) behaves as the pages describe
+("双卡RTX4090跑通Qwen3-Next：8并发满血长上下文实测", section
+"显存账本：热缓存卸载省下约84%": finished or cancelled requests give back KV
+capacity and cache slots, which return to their initial values).
+
+These tests use host-only caches (no device storage), so no GPU is needed.
+"""
+import ctypes as C
+import glob
+import os
+import random
+import re
+
+import pytest
+
+import sparse_attention_decode_qsa_gb300 as Q
+from sparse_attention_decode_qsa_gb300 import _native as N
+from sparse_attention_decode_qsa_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(qsa_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    L = N.lib()
+    declared = _declared_symbols()
+    assert len(declared) >= 17
+    for name in sorted(declared):
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+        assert name in N.SIGNATURES, f"{name} has no Python binding"
+    assert L.qsa_abi_version() == 1
+
+
+def _host_cache(**kw):
+    args = dict(n_layers=12, max_requests=4, ctx_capacity=262144, hbm_pool_rows=200000,
+                budget_tokens=2048, ring_tokens=4096, staging_rows=2048, device=None)
+    args.update(kw)
+    return Q.Cache(**args)
+
+
+def test_workspace_bytes_and_bad_configs():
+    L = N.lib()
+    cfg = N.CacheConfig(n_layers=12, max_requests=8, ctx_capacity=262144, budget_tokens=2048,
+                        ring_tokens=4096, staging_rows=2048, hbm_pool_rows=1 << 20)
+    # error word + 8 req x 12 layers x 64 splits x 2080 floats
+    assert L.qsa_workspace_bytes(C.byref(cfg)) == 256 + 8 * 12 * 64 * 2080 * 4
+    for field, bad in [("budget_tokens", 6), ("budget_tokens", 0), ("budget_tokens", 16384),
+                       ("n_layers", 0), ("ring_tokens", 0), ("ctx_capacity", 0)]:
+        c2 = N.CacheConfig.from_buffer_copy(cfg)
+        setattr(c2, field, bad)
+        assert L.qsa_workspace_bytes(C.byref(c2)) == -1
+        h = C.c_void_p()
+        assert L.qsa_cache_create(C.byref(c2), C.byref(h)) == N.ERR_INVALID_ARG
+    # partial device storage is rejected
+    c3 = N.CacheConfig.from_buffer_copy(cfg)
+    c3.hbm_pool = 4096
+    h = C.c_void_p()
+    assert L.qsa_cache_create(C.byref(c3), C.byref(h)) == N.ERR_INVALID_ARG
+    assert b"completely" in L.qsa_last_error_string()
+    # staging larger than the pool
+    c4 = N.CacheConfig.from_buffer_copy(cfg)
+    c4.hbm_pool_rows = 100
+    assert L.qsa_cache_create(C.byref(c4), C.byref(h)) == N.ERR_CAPACITY
+
+
+def test_lease_lifecycle_and_generations():
+    c = _host_cache()
+    s0 = c.stats()
+    assert s0["free_request_slots"] == 4 and s0["active_requests"] == 0
+    assert s0["staging_rows_total"] == 12 * 2048
+    assert s0["free_hbm_rows"] == 200000 - 12 * 2048
+    h = c.request_begin(262144, Q.KV_HOST_RING, host_rows=1 << 20)
+    assert (h.index, h.generation) == (0, 1)
+    info = c.request_info(h)
+    assert info.layer_rows == 4096 and info.hbm_row_base == 12 * 2048
+    s1 = c.stats()
+    assert s1["hbm_kv_bytes_in_use"] == 12 * 4096 * 2048
+    c.request_end(h)
+    assert c.stats() == s0
+    # stale: ended handle, double end, forged generation, index out of range
+    for bad in [h, Q.Handle(0, 7), Q.Handle(99, 1)]:
+        with pytest.raises(Q.QsaError) as e:
+            c.request_end(bad)
+        assert e.value.status == Q.ERR_STALE_HANDLE
+        with pytest.raises(Q.QsaError) as e:
+            c.request_info(bad)
+        assert e.value.status == Q.ERR_STALE_HANDLE
+    h2 = c.request_begin(1000, Q.KV_HBM)
+    assert (h2.index, h2.generation) == (0, 2)      # same slot, new generation
+    with pytest.raises(Q.QsaError) as e:
+        c.request_info(h)                           # old generation of the same slot
+    assert e.value.status == Q.ERR_STALE_HANDLE
+    c.request_end(h2)
+    assert c.stats() == s0
+
+
+def test_admission_errors_leave_state_unchanged():
+    c = _host_cache(max_requests=2, hbm_pool_rows=12 * 2048 + 12 * 4096 + 10)
+    s0 = c.stats()
+    cases = [
+        (dict(ctx_len=0), Q.ERR_INVALID_ARG),
+        (dict(ctx_len=262145), Q.ERR_CAPACITY),
+        (dict(ctx_len=100, placement=7), Q.ERR_INVALID_ARG),
+        (dict(ctx_len=100, placement=Q.KV_HOST_RING), Q.ERR_INVALID_ARG),     # no host rows
+        (dict(ctx_len=100, placement=Q.KV_HBM, host_rows=4096), Q.ERR_INVALID_ARG),
+        (dict(ctx_len=100, placement=Q.KV_HOST_RING, host_rows=4097), Q.ERR_INVALID_ARG),  # unaligned
+        (dict(ctx_len=5000, placement=Q.KV_HBM), Q.ERR_CAPACITY),             # 60000 rows > pool
+    ]
+    for kw, status in cases:
+        with pytest.raises(Q.QsaError) as e:
+            c.request_begin(**kw)
+        assert e.value.status == status, kw
+        assert c.stats() == s0
+    a = c.request_begin(8, Q.KV_HBM)
+    b = c.request_begin(8, Q.KV_HBM)
+    with pytest.raises(Q.QsaError) as e:
+        c.request_begin(8, Q.KV_HBM)
+    assert e.value.status == Q.ERR_OUT_OF_SLOTS
+    c.request_end(a)
+    c.request_end(b)
+    assert c.stats() == s0
+
+
+def test_compute_calls_need_device_storage():
+    c = _host_cache()
+    h = c.request_begin(100, Q.KV_HBM)
+    L = N.lib()
+    b = N.Batch(1, 0, 1, 0, C.pointer(N.Handle(h.index, h.generation)))
+    st = L.qsa_index_score(c.h, C.byref(b), 16, 16, 16, 100, None)
+    assert st == Q.ERR_NO_DEVICE
+    st = L.qsa_sparse_decode_attn(c.h, C.byref(b), 16, 16, 16, 2048, None, 0.1, 16, None, None)
+    assert st == Q.ERR_NO_DEVICE
+    with pytest.raises(Q.QsaError) as e:
+        c.slot_table_ptr(h, 0)
+    assert e.value.status == Q.ERR_NO_DEVICE
+
+
+def test_free_list_coalesces_after_fragmentation():
+    rows = 12 * 2048 + 12 * 10000
+    c = _host_cache(max_requests=8, hbm_pool_rows=rows)
+    s0 = c.stats()
+    hs = [c.request_begin(1000, Q.KV_HBM) for _ in range(8)]
+    for i in (1, 3, 5):
+        c.request_end(hs[i])
+    s = c.stats()
+    assert s["free_ranges"] == 4        # three holes + the tail
+    for i in (0, 2, 4, 6, 7):
+        c.request_end(hs[i])
+    s = c.stats()
+    assert s == s0 and s["free_ranges"] == 1 and s["largest_free_rows"] == 12 * 10000
+
+
+def test_ragged_batch_recycling_returns_capacity():
+    """64 requests with contexts log-uniform in [4096, 262144] (multiples of
+    4): HBM-resident under 32K tokens, host history + 4096-token tail ring
+    above.  Finish 16 random requests, reissue 16 new ones under new
+    generations, then end everything: every counter returns to its initial
+    value, and stale handles of finished requests are rejected."""
+    ctxs = synth.log_uniform_contexts(64, 4096, 262144, seed=44)
+    rows_needed = sum(12 * (n if n < 32768 else 4096) for n in ctxs)
+    c = _host_cache(max_requests=64, hbm_pool_rows=12 * 2048 + rows_needed + 12 * 32768 * 16)
+    s0 = c.stats()
+    live = {}
+    for n in ctxs:
+        if n < 32768:
+            h = c.request_begin(n, Q.KV_HBM)
+        else:
+            h = c.request_begin(n, Q.KV_HOST_RING, host_rows=1 << 30)
+        live[h.index] = (h, n)
+    assert c.stats()["free_request_slots"] == 0
+    rng = random.Random(7)
+    finished = rng.sample(sorted(live), 16)
+    old = [live.pop(i)[0] for i in finished]
+    for h in old:
+        c.request_end(h)
+    new_ctx = synth.log_uniform_contexts(16, 4096, 262144, seed=45)
+    for n in new_ctx:
+        h = c.request_begin(n, Q.KV_HBM if n < 32768 else Q.KV_HOST_RING,
+                            host_rows=None if n < 32768 else 1 << 30)
+        assert h.generation == 2
+        live[h.index] = (h, n)
+    for h in old:
+        with pytest.raises(Q.QsaError) as e:
+            c.request_end(h)
+        assert e.value.status == Q.ERR_STALE_HANDLE
+    leased = sum(12 * (n if n < 32768 else 4096) for _, n in live.values())
+    assert c.stats()["hbm_kv_bytes_in_use"] == leased * 2048
+    for h, _ in list(live.values()):
+        c.request_end(h)
+    assert c.stats() == s0
