@@ -1,0 +1,364 @@
+"""Benchmark of the QSA decode step on one GB300.
+
+Workload (default): 8 requests x 12 QSA layers x 262144 cached tokens; full
+KV history in pinned host memory with a 4096-token HBM tail ring per request
+and layer; half of the selected blocks in the ring.  One step = one decode
+step of every request through all 12 layers, layer after layer (as a model
+would run them): per layer one index-score + C4-max launch, one top-k launch
+and one attention launch (split-K + merge) over the 8 requests.
+
+Metric: QSA layer-steps per second (96 per step).  Printed as one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload.  Under torchrun (N > 1) every rank runs its own
+replica on its own GPU (no collective on the data path); the time is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "QSA decode layer-steps/sec at 256K ctx; achieved HBM & PCIe GB/s vs peak"
+WORKLOAD = "c256k_x8"
+N_LAYERS, N_REQ, CTX, BUDGET, RING = 12, 8, 262144, 2048, 4096
+ROW = 2048
+IDX_BYTES = 66
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def config_block():
+    return {"workload": WORKLOAD, "requests": N_REQ, "qsa_layers": N_LAYERS, "ctx_tokens": CTX,
+            "indexer_budget": BUDGET, "ring_tokens": RING, "kv_placement": "pinned host + HBM tail ring",
+            "layer_order": "sequential", "l2": "inputs larger than L2 (1.66 GB index keys per step)"}
+
+
+class Clocks:
+    """Sample SM clocks and throttle reasons with nvidia-smi during a region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.summary = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if not self.proc:
+            return
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if sm:
+            self.summary = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def host_link_peak(dev):
+    """Best pinned host->device copy rate (GB/s) over a 1 GiB buffer."""
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(5):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        d.copy_(h, non_blocking=True)
+        e.record()
+        e.synchronize()
+        best = max(best, n / (s.elapsed_time(e) * 1e-3) / 1e9)
+    del h, d
+    return best
+
+
+def run_ours(args, rank, world):
+    from sparse_attention_decode_qsa_gb300 import workloads
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    hbm_peak, peak_kind = peaks()
+    wl = workloads.c256k_x8(device=dev)
+    stream = torch.cuda.current_stream(dev)
+    R, L = wl.n_req, wl.n_layers
+    units = R * L
+
+    # per-launch events for the kernel breakdown (recorded on the launching stream)
+    kinds = ["index_score", "select_topk", "sparse_attn"]
+
+    def step(ev=None):
+        c, hs = wl.cache, wl.handles
+        for l in range(L):
+            sl = slice(l * R, (l + 1) * R)
+            if ev is not None:
+                ev[0][l].record(stream)
+            c.index_score(hs, l, 1, wl.q_idx[sl], wl.w[sl], wl.blk[sl], stream)
+            if ev is not None:
+                ev[1][l].record(stream)
+            c.select_c4_topk(hs, l, 1, wl.blk[sl], BUDGET, wl.sel[sl], wl.nsel[sl], stream)
+            if ev is not None:
+                ev[2][l].record(stream)
+            c.sparse_decode_attn(hs, l, 1, wl.q[sl], wl.sel[sl], wl.nsel[sl], BUDGET, None,
+                                 wl.softmax_scale, wl.out[sl], wl.lse[sl], stream)
+            if ev is not None:
+                ev[3][l].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, det = wl.cache.poll_error()
+    if st != 0:
+        raise RuntimeError(f"device error word {st} ({det}) after warm-up")
+
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(4)]
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with Clocks(dev.index) as clk:
+        t0.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1)
+    per_kind = {k: 0.0 for k in kinds}
+    for k in range(args.steps):
+        for l in range(L):
+            for i, kind in enumerate(kinds):
+                per_kind[kind] += evs[k][i][l].elapsed_time(evs[k][i + 1][l])
+    launches = {k: args.steps * L for k in kinds}
+
+    # ---- end to end: per-step queries from pinned host, outputs back to pinned host
+    hq_idx = wl.q_idx.cpu().pin_memory()
+    hw = wl.w.cpu().pin_memory()
+    hq = wl.q.cpu().pin_memory()
+    hout = torch.empty_like(wl.out, device="cpu").pin_memory()
+    hlse = torch.empty_like(wl.lse, device="cpu").pin_memory()
+    h2d = hq_idx.numel() * 4 + hw.numel() * 4 + hq.numel() * 2
+    d2h = hout.numel() * 4 + hlse.numel() * 4
+
+    def e2e_step():
+        wl.q_idx.copy_(hq_idx, non_blocking=True)
+        wl.w.copy_(hw, non_blocking=True)
+        wl.q.copy_(hq, non_blocking=True)
+        step()
+        hout.copy_(wl.out, non_blocking=True)
+        hlse.copy_(wl.lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1)
+    st, det = wl.cache.poll_error()
+    if st != 0:
+        raise RuntimeError(f"device error word {st} ({det}) after timing")
+
+    link_peak = host_link_peak(dev)
+    wl.close()
+
+    # max over ranks
+    ms_max, ms_e2e_max = ms, ms_e2e
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max, ms_e2e_max = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    step_s = ms_max / 1e3 / args.steps
+    value = units * world / step_s
+    # algorithmic bytes per unit
+    idx_b = IDX_BYTES * CTX
+    rows_b = BUDGET * ROW
+    hot_b = rows_b // 2
+    hbm_step = units * (idx_b + hot_b)
+    host_step = units * (rows_b - hot_b)
+    avg = {k: per_kind[k] / launches[k] for k in kinds}          # ms per launch (8 units)
+    k1_bytes = R * idx_b
+    attn_hbm, attn_host = R * hot_b, R * (rows_b - hot_b)
+    dominant = max(kinds, key=lambda k: per_kind[k])
+    k1_gbs = k1_bytes / (avg["index_score"] * 1e-3) / 1e9
+    attn_link_gbs = attn_host / (avg["sparse_attn"] * 1e-3) / 1e9
+    roofs = {
+        "index_score": {"bound": "hbm", "achieved": round(k1_gbs, 1), "peak": hbm_peak,
+                        "unit": "GB/s", "frac": round(k1_gbs / hbm_peak, 4), "traffic": None,
+                        "bytes_per_launch": k1_bytes, "avg_launch_us": round(avg["index_score"] * 1e3, 2)},
+        "sparse_attn": {"bound": "host_link", "achieved": round(attn_link_gbs, 1),
+                        "peak": round(link_peak, 1), "unit": "GB/s",
+                        "frac": round(attn_link_gbs / link_peak, 4), "traffic": None,
+                        "bytes_per_launch": attn_hbm + attn_host,
+                        "host_bytes_per_launch": attn_host,
+                        "avg_launch_us": round(avg["sparse_attn"] * 1e3, 2)},
+        "select_topk": {"avg_launch_us": round(avg["select_topk"] * 1e3, 2)},
+    }
+    dom = dict(roofs[dominant])
+    dom["kernel"] = dominant
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "layer-steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/bf16->f32",
+        "data": "synthetic (seeded; no public dataset)", "config": config_block(),
+        "impl": "ours",
+        "hbm_gbs": round(hbm_step / step_s / 1e9, 1), "hbm_peak_gbs": hbm_peak,
+        "hbm_frac": round(hbm_step / step_s / 1e9 / hbm_peak, 4), "peak_kind": peak_kind,
+        "host_link_gbs": round(host_step / step_s / 1e9, 1),
+        "host_link_peak_gbs": round(link_peak, 1),
+        "host_link_frac": round(host_step / step_s / 1e9 / link_peak, 4),
+        "roofline": dom, "kernels": roofs,
+        "gpu_launches": args.steps * L * 4,
+        "clocks": clk.summary,
+        "e2e": {"value": round(units * world / (ms_e2e_max / 1e3 / args.steps), 1),
+                "unit": "layer-steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+    }
+    line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return line
+
+
+def _oracle_sample(seconds, budget_units=None):
+    """Time the fp64 oracle on decode units of the benchmark's workload,
+    drawn on the CPU with the same recipe (one unit = one request at one
+    layer: 262144 tokens; host rows drawn only for the tokens it selects)."""
+    from oracle import qsa_oracle as O
+    from sparse_attention_decode_qsa_gb300 import synth
+
+    n = CTX
+    done, t_total = 0, 0.0
+    while (done == 0 or t_total < seconds) and (budget_units is None or done < budget_units):
+        seed = synth.mix_seed(1234, done)
+        planted = synth.planted_hot_cold(n // 4, 512, RING // 4, synth.mix_seed(seed, 9))
+        u = synth.unit_inputs(n, seed, planted, device="cpu")
+        codes = u.codes.numpy()
+        scales = u.scales.view(torch.int16).numpy().view(np.uint16)
+        qb = u.q.view(torch.int16).numpy().view(np.uint16)
+        slot = O.ring_slot_row(n, 0, 0, RING)
+        rows = synth.kv_rows(BUDGET, synth.mix_seed(seed, 4)).numpy()
+
+        class Rows:   # rows of the selected tokens only (the rest are never read)
+            def __init__(self):
+                self.m = {}
+
+            def __getitem__(self, t):
+                return self.m.setdefault(int(t), rows[len(self.m) % BUDGET])
+
+        host, pool = Rows(), Rows()
+        t = time.perf_counter()
+        O.layer_step(codes, scales, u.q_idx.numpy(), u.w.numpy(), qb, slot, pool, host, BUDGET,
+                     1 / math.sqrt(128))
+        t_total += time.perf_counter() - t
+        done += 1
+    return done, t_total
+
+
+def cpu_baseline(seconds=15.0):
+    done, t = _oracle_sample(seconds)
+    return {"value": round(done / t, 3), "unit": "layer-steps/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{done} decode units (1 request x 1 layer, 262144 tokens each) of the "
+                      f"{WORKLOAD} recipe, fp64 numpy oracle, {t:.1f} s of CPU work"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    per_step = []
+    for _ in range(args.warmup):
+        _oracle_sample(0.0, budget_units=1)
+    total_units, total_t = 0, 0.0
+    for _ in range(args.steps):
+        d, t = _oracle_sample(0.0, budget_units=1)
+        total_units += d
+        total_t += t
+        per_step.append(t)
+    value = total_units / total_t
+    sample = (f"{args.steps} timed steps of 1 decode unit each (1 request x 1 layer, "
+              f"262144 tokens) of the {WORKLOAD} recipe; fp64 numpy oracle")
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": "layer-steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_t / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; no public dataset)", "config": config_block(),
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": "layer-steps/s",
+                         "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "layer-steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("gloo")
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -98,7 +98,9 @@ typedef enum qsa_kv_placement {
   QSA_KV_HBM = 0,
   /* Full history in pinned host memory; the newest ring_tokens rows of each
    * layer also in an HBM tail ring (token t in ring row t mod ring_tokens). */
-  QSA_KV_HOST_RING = 1
+  QSA_KV_HOST_RING = 1,
+  /* Full history in pinned host memory only; no HBM rows are leased. */
+  QSA_KV_HOST = 2
 } qsa_kv_placement;
 
 typedef struct qsa_cache_config {
@@ -130,9 +132,9 @@ typedef struct qsa_request_desc {
   int64_t ctx_len;         /* cached tokens, 1 <= ctx_len <= ctx_capacity */
   int32_t placement;       /* qsa_kv_placement */
   int32_t reserved0;
-  /* QSA_KV_HOST_RING: pinned host memory [n_layers][ctx_len][2048] holding
-   * the full history (host address; the library maps it for the device).
-   * QSA_KV_HBM: NULL. */
+  /* QSA_KV_HOST_RING, QSA_KV_HOST: pinned host memory [n_layers][ctx_len][2048]
+   * holding the full history (host address; the library maps it for the
+   * device).  QSA_KV_HBM: NULL. */
   const void* host_rows;
 } qsa_request_desc;
 
@@ -189,11 +191,13 @@ qsa_status_t qsa_cache_destroy(qsa_cache* cache);
 /* ------------------------------------------- leases, slots, bookkeeping */
 
 /* Lease a request slot and an HBM region (ctx_len rows per layer for
- * QSA_KV_HBM, ring_tokens rows per layer for QSA_KV_HOST_RING), bump the
+ * QSA_KV_HBM, ring_tokens rows per layer for QSA_KV_HOST_RING, none for
+ * QSA_KV_HOST), bump the
  * slot's generation, and enqueue on `stream` the fill of the request's
  * slot-table rows: resident token t of layer l -> region row l*layer_rows + t;
  * offloaded token t -> ring row l*ring_tokens + t mod ring_tokens when t is
- * among the newest ring_tokens tokens, else -1 (cold, read from host_rows).
+ * among the newest ring_tokens tokens, else -1 (cold, read from host_rows);
+ * every token of a QSA_KV_HOST request -> -1.
  * [RTX4090 port, memory-ledger section: leases, generation tags, tail ring,
  * logical addresses separate from physical slots.]
  * Errors: INVALID_ARG, CAPACITY (ctx_len > ctx_capacity or no pool range),

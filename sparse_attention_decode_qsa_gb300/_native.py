@@ -29,6 +29,7 @@ OK, ERR_INVALID_ARG, ERR_CUDA, ERR_STALE_HANDLE, ERR_OUT_OF_SLOTS, ERR_CAPACITY,
 
 KV_HBM = 0
 KV_HOST_RING = 1
+KV_HOST = 2
 
 
 class CacheConfig(C.Structure):

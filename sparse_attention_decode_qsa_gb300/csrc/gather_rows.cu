@@ -104,6 +104,8 @@ __global__ void slot_fill_kernel(int32_t* rows, int32_t n_layers, int64_t ctx_ca
     int64_t slot;
     if (placement == QSA_KV_HBM) {
       slot = row_base + l * layer_rows + t;
+    } else if (placement == QSA_KV_HOST) {
+      slot = -1;
     } else {
       slot = (t >= ctx_len - layer_rows) ? row_base + l * layer_rows + (t % layer_rows) : -1;
     }

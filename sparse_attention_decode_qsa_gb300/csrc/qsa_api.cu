@@ -243,10 +243,11 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
   if (desc->ctx_len > c->cfg.ctx_capacity)
     return fail(QSA_ERR_CAPACITY, "ctx_len %lld exceeds capacity %lld", (long long)desc->ctx_len,
                 (long long)c->cfg.ctx_capacity);
-  if (desc->placement != QSA_KV_HBM && desc->placement != QSA_KV_HOST_RING)
+  if (desc->placement != QSA_KV_HBM && desc->placement != QSA_KV_HOST_RING &&
+      desc->placement != QSA_KV_HOST)
     return fail(QSA_ERR_INVALID_ARG, "unknown placement %d", desc->placement);
-  if (desc->placement == QSA_KV_HOST_RING && !desc->host_rows)
-    return fail(QSA_ERR_INVALID_ARG, "host-ring placement needs host_rows");
+  if (desc->placement != QSA_KV_HBM && !desc->host_rows)
+    return fail(QSA_ERR_INVALID_ARG, "host placements need host_rows");
   if (desc->placement == QSA_KV_HBM && desc->host_rows)
     return fail(QSA_ERR_INVALID_ARG, "HBM placement takes no host_rows");
 
@@ -255,11 +256,13 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
     if (!c->leases[i].active) { slot = (int)i; break; }
   if (slot < 0) return fail(QSA_ERR_OUT_OF_SLOTS, "all %d request slots are leased", c->cfg.max_requests);
 
-  const int32_t layer_rows = desc->placement == QSA_KV_HBM ? (int32_t)desc->ctx_len : c->cfg.ring_tokens;
+  const int32_t layer_rows = desc->placement == QSA_KV_HBM        ? (int32_t)desc->ctx_len
+                             : desc->placement == QSA_KV_HOST_RING ? c->cfg.ring_tokens
+                                                                   : 0;
   const int64_t rows = (int64_t)layer_rows * c->cfg.n_layers;
 
   const uint8_t* host_dev = nullptr;
-  if (desc->placement == QSA_KV_HOST_RING) {
+  if (desc->placement != QSA_KV_HBM) {
     if (c->has_device) {
       void* dptr = nullptr;
       cudaError_t e = cudaHostGetDevicePointer(&dptr, const_cast<void*>(desc->host_rows), 0);
@@ -277,7 +280,7 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
   }
 
   int64_t base = 0;
-  if (!c->alloc_rows(rows, &base))
+  if (rows > 0 && !c->alloc_rows(rows, &base))
     return fail(QSA_ERR_CAPACITY, "no free pool range of %lld rows", (long long)rows);
 
   if (c->has_device) {

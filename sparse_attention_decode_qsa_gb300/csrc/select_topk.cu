@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const TopkParams 
     const uint32_t eq_excl = warp_eq[warp] + __popc(be & lt_mask);
     const uint32_t remaining = krem > eq_base ? krem - eq_base : 0u;
     const bool take = gt || (eq && eq_excl < remaining);
-    if (take) sel[out_base + gt_excl + min(eq_excl, remaining)] = (int32_t)i;
+    const uint32_t pos = out_base + gt_excl + min(eq_excl, remaining);
+    if (take && pos < (uint32_t)K) sel[pos] = (int32_t)i;
     const uint32_t tot_gt = s_tot_gt, tot_eq = s_tot_eq;
     out_base += tot_gt + min(tot_eq, remaining);
     eq_base += tot_eq;

@@ -1,0 +1,219 @@
+"""Synthetic decode-step workloads on one GPU: a Cache filled with seeded
+inputs (index keys, KV rows in HBM and/or pinned host memory, queries), plus
+the per-unit output buffers of one decode step.
+
+Recipes (per-layer shapes and distributions as in synth.py):
+  tiny      1 layer, 1 request, 8192 tokens, KV in HBM, 512 planted blocks.
+  c128k     12 layers, 1 request, 131072 tokens, KV in HBM.
+  c256k_x8  12 layers, 8 requests x 262144 tokens; full history in pinned host
+            memory plus a 4096-token HBM tail ring per request and layer;
+            shared staging 2048 x 12 rows; half of the planted blocks inside
+            the tail ring (HBM), half in the cold history (host).
+  c1m_x4    12 layers, 4 requests x 1048576 tokens; KV only in pinned host
+            memory; planted blocks: sinks 0..3 plus a recency-Zipf(1.1) /
+            uniform mixture.
+  ragged    64 requests, contexts log-uniform in [4096, 262144] (multiples of
+            4); KV in HBM under 32768 tokens, host + tail ring above.
+Everything is drawn from seeds; nothing here computes the method.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+from . import _native as N
+from . import synth
+from .api import Cache
+
+
+def register_pinned(t: torch.Tensor):
+    """Page-lock an existing CPU tensor in place (exact size, mapped for the GPU)."""
+    err = torch.cuda.cudart().cudaHostRegister(t.data_ptr(), t.numel() * t.element_size(), 3)
+    if int(err) != 0:
+        raise RuntimeError(f"cudaHostRegister failed: {err}")
+    return t
+
+
+def unregister_pinned(t: torch.Tensor):
+    torch.cuda.cudart().cudaHostUnregister(t.data_ptr())
+
+
+@dataclass
+class Workload:
+    cache: Cache
+    handles: list
+    n_layers: int
+    ctxs: list
+    placements: list
+    host: list               # per request: uint8 [L][n][2048] registered pinned, or None
+    q_idx: torch.Tensor      # fp32 [L*R][8][64], unit u = l*R + r
+    w: torch.Tensor          # fp32 [L*R][8]
+    q: torch.Tensor          # bf16 [L*R][16][128]
+    planted: list            # [L][R] int64 block ids
+    budget: int
+    blk: torch.Tensor = None
+    sel: torch.Tensor = None
+    nsel: torch.Tensor = None
+    out: torch.Tensor = None
+    lse: torch.Tensor = None
+    softmax_scale: float = 1.0 / math.sqrt(128)
+    seeds: dict = field(default_factory=dict)
+    planting: object = None
+
+    @property
+    def n_req(self):
+        return len(self.handles)
+
+    def unit(self, l, r):
+        return l * self.n_req + r
+
+    def layer_slice(self, t: torch.Tensor, l: int):
+        return t[l * self.n_req:(l + 1) * self.n_req]
+
+    def reissue(self, r: int, n: int, placement: int, seed: int):
+        """Finish request r and admit a new request (new lease, new
+        generation) in its place, with freshly drawn inputs."""
+        self.cache.request_end(self.handles[r])
+        old = self.host[r]
+        if old is not None and (placement == N.KV_HBM or old.shape[1] != n):
+            unregister_pinned(old)
+            old = None
+        if placement != N.KV_HBM and old is None:
+            old = register_pinned(torch.empty(self.n_layers, n, N.ROW_BYTES, dtype=torch.uint8))
+        self.host[r] = old
+        self.ctxs[r], self.placements[r] = n, placement
+        self.handles[r] = self.cache.request_begin(n, placement, host_rows=old)
+        _fill_request(self, r, seed, self.planting)
+        return self.handles[r]
+
+    def close(self):
+        for h in self.host:
+            if h is not None:
+                unregister_pinned(h)
+        self.host = []
+        self.cache.close()
+
+    # ------------------------------------------------------- one step
+    def step_layer(self, l: int, stream=None, gathered=None):
+        """Index score, top-k and attention for every request at layer l."""
+        c, hs, R = self.cache, self.handles, self.n_req
+        sl = slice(l * R, (l + 1) * R)
+        c.index_score(hs, l, 1, self.q_idx[sl], self.w[sl], self.blk[sl], stream)
+        c.select_c4_topk(hs, l, 1, self.blk[sl], self.budget, self.sel[sl], self.nsel[sl], stream)
+        c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
+                             gathered, self.softmax_scale, self.out[sl], self.lse[sl], stream)
+
+    def step(self, stream=None):
+        for l in range(self.n_layers):
+            self.step_layer(l, stream)
+
+
+def _fill_request(wl: "Workload", r: int, seed: int, planting):
+    """Draw and place every layer's inputs of request r (current lease)."""
+    cache, h, n, p = wl.cache, wl.handles[r], wl.ctxs[r], wl.placements[r]
+    dev = cache.pool.device
+    ring = cache.ring_tokens
+    info = cache.request_info(h)
+    for l in range(wl.n_layers):
+        s = synth.mix_seed(seed, r, l)
+        blocks = planting(l, r, n)
+        wl.planted[l][r] = torch.as_tensor(blocks, dtype=torch.int64)
+        codes, scales = synth.index_keys(n, synth.mix_seed(s, 1), device=dev)
+        synth.plant(scales, blocks, n)
+        cache.index_keys[h.index, l, :n] = codes
+        cache.index_scales[h.index, l, :n] = scales
+        qi, wi = synth.index_query(synth.mix_seed(s, 2), device=dev)
+        u = wl.unit(l, r)
+        wl.q_idx[u], wl.w[u] = qi, wi
+        wl.q[u] = synth.attn_query(synth.mix_seed(s, 3), device=dev)
+        rows = synth.kv_rows(n, synth.mix_seed(s, 4), device=dev)
+        if p == N.KV_HBM:
+            b0 = info.hbm_row_base + l * n
+            cache.pool[b0:b0 + n] = rows
+        else:
+            wl.host[r][l].copy_(rows)
+            if p == N.KV_HOST_RING:
+                t = torch.arange(max(0, n - ring), n, device=dev)
+                cache.pool[info.hbm_row_base + l * ring + (t % ring)] = rows[t]
+        del rows
+    torch.cuda.synchronize(dev)
+
+
+def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: int = 4096,
+          staging_rows: int = 2048, seed: int = 0, device="cuda", extra_requests: int = 0,
+          spare_rows: int = 0) -> Workload:
+    """planting(l, r, n) -> block ids to plant for unit (l, r)."""
+    dev = torch.device(device)
+    R = len(ctxs)
+    rows_needed = 0
+    for n, p in zip(ctxs, placements):
+        rows_needed += n_layers * (n if p == N.KV_HBM else ring if p == N.KV_HOST_RING else 0)
+    pool_rows = n_layers * staging_rows + rows_needed + spare_rows
+    cache = Cache(n_layers=n_layers, max_requests=R + extra_requests, ctx_capacity=max(ctxs),
+                  hbm_pool_rows=pool_rows, budget_tokens=budget, ring_tokens=ring,
+                  staging_rows=staging_rows, device=dev)
+    handles, host = [], []
+    for r, (n, p) in enumerate(zip(ctxs, placements)):
+        hrows = None
+        if p != N.KV_HBM:
+            hrows = register_pinned(torch.empty(n_layers, n, N.ROW_BYTES, dtype=torch.uint8))
+        host.append(hrows)
+        handles.append(cache.request_begin(n, p, host_rows=hrows))
+    U = n_layers * R
+    wl = Workload(cache, handles, n_layers, list(ctxs), list(placements), host,
+                  torch.empty(U, 8, 64, dtype=torch.float32, device=dev),
+                  torch.empty(U, 8, dtype=torch.float32, device=dev),
+                  torch.empty(U, 16, 128, dtype=torch.bfloat16, device=dev),
+                  [[None] * R for _ in range(n_layers)], budget)
+    wl.planting = planting
+    for r in range(R):
+        _fill_request(wl, r, seed, planting)
+    blk_stride = (max(ctxs) + 3) // 4
+    wl.blk = torch.empty(U, blk_stride, dtype=torch.float32, device=dev)
+    wl.sel = torch.empty(U, budget // 4, dtype=torch.int32, device=dev)
+    wl.nsel = torch.empty(U, dtype=torch.int32, device=dev)
+    wl.out = torch.empty(U, 16, 128, dtype=torch.float32, device=dev)
+    wl.lse = torch.empty(U, 16, dtype=torch.float32, device=dev)
+    wl.seeds = dict(seed=seed)
+    return wl
+
+
+# ------------------------------------------------------------- recipes
+
+def tiny(device="cuda", seed=0):
+    n = 8192
+    return build(1, [n], [N.KV_HBM],
+                 lambda l, r, n: synth.planted_uniform(n // 4, 512, synth.mix_seed(seed, 90, l, r)),
+                 staging_rows=64, seed=seed, device=device)
+
+
+def c128k(device="cuda", seed=1, n_layers=12):
+    n = 131072
+    return build(n_layers, [n], [N.KV_HBM],
+                 lambda l, r, n: synth.planted_uniform(n // 4, 512, synth.mix_seed(seed, 90, l, r)),
+                 staging_rows=64, seed=seed, device=device)
+
+
+def c256k_x8(device="cuda", seed=2, n_layers=12, n_req=8, n=262144):
+    return build(n_layers, [n] * n_req, [N.KV_HOST_RING] * n_req,
+                 lambda l, r, n: synth.planted_hot_cold(n // 4, 512, 4096 // 4,
+                                                        synth.mix_seed(seed, 90, l, r)),
+                 seed=seed, device=device)
+
+
+def c1m_x4(device="cuda", seed=3, n_layers=12, n_req=4, n=1048576):
+    return build(n_layers, [n] * n_req, [N.KV_HOST] * n_req,
+                 lambda l, r, n: synth.planted_zipf_sinks(n // 4, 512, synth.mix_seed(seed, 90, l, r)),
+                 staging_rows=64, seed=seed, device=device)
+
+
+def ragged(device="cuda", seed=4, n_layers=12, n_req=64, lo=4096, hi=262144, extra_requests=16,
+           spare_rows=0):
+    ctxs = synth.log_uniform_contexts(n_req, lo, hi, synth.mix_seed(seed, 80))
+    pl = [N.KV_HBM if n < 32768 else N.KV_HOST_RING for n in ctxs]
+    return build(n_layers, ctxs, pl,
+                 lambda l, r, n: synth.planted_hot_cold(n // 4, min(512, n // 4), 1024,
+                                                        synth.mix_seed(seed, 90, l, r)),
+                 seed=seed, device=device, extra_requests=extra_requests, spare_rows=spare_rows)
