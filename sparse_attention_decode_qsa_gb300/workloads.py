@@ -143,15 +143,16 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
 
 def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: int = 4096,
           staging_rows: int = 2048, seed: int = 0, device="cuda", extra_requests: int = 0,
-          spare_rows: int = 0) -> Workload:
+          spare_rows: int = 0, ctx_capacity: int | None = None) -> Workload:
     """planting(l, r, n) -> block ids to plant for unit (l, r)."""
+    ctx_capacity = ctx_capacity or max(ctxs)
     dev = torch.device(device)
     R = len(ctxs)
     rows_needed = 0
     for n, p in zip(ctxs, placements):
         rows_needed += n_layers * (n if p == N.KV_HBM else ring if p == N.KV_HOST_RING else 0)
     pool_rows = n_layers * staging_rows + rows_needed + spare_rows
-    cache = Cache(n_layers=n_layers, max_requests=R + extra_requests, ctx_capacity=max(ctxs),
+    cache = Cache(n_layers=n_layers, max_requests=R + extra_requests, ctx_capacity=ctx_capacity,
                   hbm_pool_rows=pool_rows, budget_tokens=budget, ring_tokens=ring,
                   staging_rows=staging_rows, device=dev)
     handles, host = [], []
@@ -170,7 +171,7 @@ def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: i
     wl.planting = planting
     for r in range(R):
         _fill_request(wl, r, seed, planting)
-    blk_stride = (max(ctxs) + 3) // 4
+    blk_stride = (ctx_capacity + 3) // 4
     wl.blk = torch.empty(U, blk_stride, dtype=torch.float32, device=dev)
     wl.sel = torch.empty(U, budget // 4, dtype=torch.int32, device=dev)
     wl.nsel = torch.empty(U, dtype=torch.int32, device=dev)
@@ -216,4 +217,5 @@ def ragged(device="cuda", seed=4, n_layers=12, n_req=64, lo=4096, hi=262144, ext
     return build(n_layers, ctxs, pl,
                  lambda l, r, n: synth.planted_hot_cold(n // 4, min(512, n // 4), 1024,
                                                         synth.mix_seed(seed, 90, l, r)),
-                 seed=seed, device=device, extra_requests=extra_requests, spare_rows=spare_rows)
+                 seed=seed, device=device, extra_requests=extra_requests, spare_rows=spare_rows,
+                 ctx_capacity=hi)
