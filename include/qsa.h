@@ -304,6 +304,44 @@ qsa_status_t qsa_sparse_decode_attn(qsa_cache* cache, const qsa_batch* batch,
                                     const void* gathered, float softmax_scale,
                                     float* out, float* lse, void* stream);
 
+/* ------------------------------------------- no-allocation variant */
+
+/* Limits of qsa_sparse_decode_attn_noalloc (its scratch is a fixed 8.5 MB
+ * device array of this library: 16 units x 64 splits of 32 rows). */
+#define QSA_STATIC_MAX_UNITS 16
+#define QSA_STATIC_MAX_ROWS 2048
+
+/* Decode attention over dense gathered rows that needs no device memory from
+ * the caller beyond its inputs and outputs.  The pages have no counterpart
+ * of this entry point; it exists for callers that cannot allocate device
+ * memory where they run attention (a serving engine whose device memory is
+ * carved from a pre-planned arena it may not grow, a plug-in handed only its
+ * input and output buffers, code that must not call cudaMalloc because it
+ * would synchronise the device).  It computes what qsa_sparse_decode_attn
+ * computes when given gathered rows, bit for bit, without a qsa_cache: the
+ * split-K partials live in a static 8.5 MB device array of the library that
+ * every GPU which loads the library holds until the process exits.
+ *  q:      device bf16 bits [n_units][16][128]
+ *  rows:   device [n_units][rows_stride][2048], as written by qsa_gather_rows
+ *          (rows_stride = budget_tokens there); row i of unit u is used when
+ *          i < n_rows[u]
+ *  n_rows: device int32 [n_units], clamped on the device to [0, rows_stride]
+ *  out, lse: as for qsa_sparse_decode_attn (lse may be NULL)
+ * Limits: 1 <= n_units <= QSA_STATIC_MAX_UNITS and 1 <= rows_stride <=
+ * QSA_STATIC_MAX_ROWS; larger calls return QSA_ERR_INVALID_ARG (split the
+ * batch).  No cudaMalloc, cudaFree or allocating library call is made.  The
+ * first call on each device looks up the array's device address with
+ * cudaGetSymbolAddress (with that device current) and sets the kernel's
+ * shared-memory limit; make that first call before any stream capture.
+ * Every call shares the one array and leaves its partials there; nothing in
+ * it needs to start at zero, because each call writes every partial it reads.
+ * Two calls whose work overlaps on the GPU (different streams, or concurrent
+ * host threads) race on the array: serialise them. */
+qsa_status_t qsa_sparse_decode_attn_noalloc(const uint16_t* q, const void* rows,
+                                            const int32_t* n_rows, int32_t n_units,
+                                            int32_t rows_stride, float softmax_scale,
+                                            float* out, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

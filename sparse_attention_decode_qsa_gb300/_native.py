@@ -18,6 +18,8 @@ Q_HEADS = 16
 ROW_BYTES = 2048
 MAX_UNITS = 256
 MAX_BUDGET_TOKENS = 8192
+STATIC_MAX_UNITS = 16
+STATIC_MAX_ROWS = 2048
 
 STATUS = {
     0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_CUDA", 3: "QSA_ERR_STALE_HANDLE",
@@ -102,6 +104,9 @@ SIGNATURES = {
     "qsa_sparse_decode_attn": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p,
                                          C.c_void_p, C.c_int32, C.c_void_p, C.c_float,
                                          C.c_void_p, C.c_void_p, C.c_void_p]),
+    "qsa_sparse_decode_attn_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32,
+                                                 C.c_int32, C.c_float, C.c_void_p, C.c_void_p,
+                                                 C.c_void_p]),
 }
 
 _lib = None

@@ -76,6 +76,11 @@ bool config_sizes_ok(const qsa_cache_config* c) {
 
 }  // namespace
 
+qsa_status_t qsa::set_last_error(qsa_status_t status, const char* message) {
+  g_last_error = message ? message : "";
+  return status;
+}
+
 struct qsa_cache {
   qsa_cache_config cfg;
   bool has_device = false;

@@ -95,6 +95,10 @@ __device__ __forceinline__ const uint8_t* row_source(const BatchDesc& b, int u, 
   return nullptr;
 }
 
+// Record the thread-local message returned by qsa_last_error_string() and
+// pass the status through (defined with the C ABI layer).
+qsa_status_t set_last_error(qsa_status_t status, const char* message);
+
 // ------------------------------------------------------------ launchers
 // Each returns the launch status (cudaGetLastError right after the launch).
 
