@@ -109,6 +109,49 @@ class Workload:
         for l in range(self.n_layers):
             self.step_layer(l, stream)
 
+    def step_group_layer(self, r0: int, r1: int, l: int, stream):
+        """Index score, top-k and attention of requests r0..r1-1 at layer l."""
+        c, R = self.cache, self.n_req
+        hs = self.handles[r0:r1]
+        sl = slice(l * R + r0, l * R + r1)
+        c.index_score(hs, l, 1, self.q_idx[sl], self.w[sl], self.blk[sl], stream)
+        c.select_c4_topk(hs, l, 1, self.blk[sl], self.budget, self.sel[sl], self.nsel[sl], stream)
+        c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
+                             None, self.softmax_scale, self.out[sl], self.lse[sl], stream)
+
+    def step_pipelined(self, streams):
+        """One decode step with the requests split into len(streams) groups
+        (micro-batches), each group on its own stream walking the layers in
+        order.  Groups share no data, so one group's host-link-bound
+        attention overlaps another group's HBM-bound scoring.  Forks from and
+        joins back into the current stream."""
+        main = torch.cuda.current_stream()
+        G = len(streams)
+        bounds = [(g * self.n_req // G, (g + 1) * self.n_req // G) for g in range(G)]
+        for s in streams:
+            s.wait_stream(main)
+        for l in range(self.n_layers):
+            for (r0, r1), s in zip(bounds, streams):
+                if r1 > r0:
+                    self.step_group_layer(r0, r1, l, s)
+        for s in streams:
+            main.wait_stream(s)
+
+    def capture(self, n_groups: int):
+        """Capture step_pipelined into a CUDA graph (after one eager warm-up
+        run, which also sets the kernels' launch attributes)."""
+        streams = [torch.cuda.Stream() for _ in range(n_groups)]
+        self.step_pipelined(streams)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap):
+            self.step_pipelined(streams)
+        torch.cuda.synchronize()
+        self._graph_streams = streams
+        return g
+
 
 def _fill_request(wl: "Workload", r: int, seed: int, planting):
     """Draw and place every layer's inputs of request r (current lease)."""
