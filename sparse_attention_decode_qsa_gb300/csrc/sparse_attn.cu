@@ -3,16 +3,22 @@
 // потери скорости декодирования", section "Механизм гибридного разреженного
 // оффлоадинга": attention reads only the <= indexer_budget selected rows).
 //
-// Split-K flash-decode: CTA (unit, split) takes 8 selected C4 blocks (32
-// tokens, 64 KiB of K/V), reads their rows through the slot table (pool rows
-// from HBM, cold rows zero-copy from mapped pinned host memory) or from a
-// dense gathered buffer, and writes a partial (m, l, acc) in base-2 logits
-// to the workspace.  A second kernel merges the partials of each (unit,
-// head) with the log-sum-exp rule and writes out and lse.
+// Split-K flash-decode.  A work item is (unit, split): 8 selected C4 blocks,
+// i.e. 32 token rows (64 KiB of K/V).  Rows are read through the slot table
+// (pool rows from HBM, cold rows zero-copy from mapped pinned host memory) or
+// from a dense gathered buffer.  Each item yields a partial (m, l, acc) in
+// base-2 logits in the workspace; a second kernel merges the partials of
+// each (unit, head) with the log-sum-exp rule and writes out and lse.
 //
-// Per CTA (256 threads, 64 KiB dynamic shared memory):
-//   load   : every thread issues 16 independent 16-byte loads, then stores
-//            them to shared memory (all loads in flight before any store);
+// The split kernel is persistent: one CTA per SM, each walking items
+// blockIdx.x, blockIdx.x + gridDim.x, ...; kMaxCtasHost CTAs when some row
+// comes from host memory, one per SM otherwise.  Rows of the next
+// item are copied with cp.async into the second of two 64 KiB buffers while
+// the current item is computed, so each CTA keeps 64 KiB in flight.  A few
+// dozen SMs saturate the host link this way, and the other SMs stay free
+// for HBM-bound work of other requests running on other streams.
+//
+// Per item (256 threads):
 //   logits : warp w serves KV head w/2 and 16 tokens; lane l holds dims
 //            4l..4l+3 of the 4 query heads of that KV head, and the four
 //            partial dots are reduced across the warp with a transposing
@@ -30,9 +36,13 @@ namespace qsa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSplitTokens = kAttnTokensPerSplit;  // 32
-constexpr int kChunksPerRow = kRowBytes / 16;      // 128
-constexpr int kSmemBytes = kSplitTokens * kRowBytes;  // 64 KiB
+constexpr int kSplitTokens = kAttnTokensPerSplit;     // 32
+constexpr int kChunksPerRow = kRowBytes / 16;         // 128
+constexpr int kBufBytes = kSplitTokens * kRowBytes;   // 64 KiB
+constexpr int kSmemBytes = 2 * kBufBytes;             // double buffer
+// CTAs of the persistent split kernel when some unit reads host memory: the
+// host link is saturated by this many SMs, and the rest stay free.
+constexpr int kMaxCtasHost = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -43,19 +53,13 @@ struct AttnParams {
   const int32_t* n_sel;
   int32_t k_max;
   int32_t budget_tokens;
+  int32_t splits;           // splits per unit (k_max / 8, rounded up)
+  int32_t n_items;          // units * splits
   const uint8_t* gathered;  // [units][budget_tokens][2048] or nullptr
   float scale_log2;         // softmax_scale * log2(e)
   float* out;               // [units][16][128]
   float* lse;               // [units][16] or nullptr
 };
-
-__device__ __forceinline__ uint4 ld_nc_v4(const uint8_t* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
@@ -65,57 +69,70 @@ __device__ __forceinline__ float* partial_ptr(const BatchDesc& b, int u, int spl
   return b.partials + (rl * b.splits_max + split) * kPartFloats;
 }
 
-__global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p) {
-  extern __shared__ __align__(16) uint8_t rows[];  // [32][2048]
-  __shared__ const uint8_t* src[kSplitTokens];
-  __shared__ float logit[kQHeads][kSplitTokens];
-  __shared__ float m_s[kQHeads], l_s[kQHeads];
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint32_t src_bytes) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-  const int u = blockIdx.y;
-  const int split = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t n = p.b.u[u].n;
+// Number of selected blocks of unit u, or -1 (reported) when out of range.
+__device__ __forceinline__ int unit_nsel(const AttnParams& p, int u, bool report) {
   const int nsel = p.n_sel[u];
   if (nsel < 0 || nsel > p.k_max) {
-    if (tid == 0 && split == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
-    return;
+    if (report) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
+    return -1;
   }
-  const int j0 = split * kAttnBlocksPerSplit;
-  if (j0 >= nsel) return;  // the merge reads only the splits that hold tokens
+  return nsel;
+}
 
-  // ---- resolve the 32 row sources
-  if (tid < kSplitTokens) {
-    const int j = j0 + tid / 4;
-    const uint8_t* ptr = nullptr;
+// Issue the copies of one item's 32 rows into buf; warp w copies rows
+// 4w..4w+3, each lane 4 chunks of each.  valid[t] tells compute which rows
+// exist.  Issues nothing for an item past its unit's selected blocks.
+__device__ __forceinline__ void issue_item(const AttnParams& p, int item, uint8_t* buf,
+                                           uint8_t* valid) {
+  const int u = item / p.splits, split = item % p.splits;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nsel = unit_nsel(p, u, false);
+  const int j0 = split * kAttnBlocksPerSplit;
+  if (nsel < 0 || j0 >= nsel) return;
+  const int64_t n = p.b.u[u].n;
+  // lane l resolves row l of the item (every warp does, so no block barrier)
+  const uint8_t* src = nullptr;
+  {
+    const int j = j0 + lane / 4;
     if (j < nsel) {
       const int64_t b = p.sel[(int64_t)u * p.k_max + j];
-      const int64_t t = 4 * b + (tid & 3);
+      const int64_t t = 4 * b + (lane & 3);
       if (b < 0 || 4 * b >= n) {
-        if ((tid & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
+        if ((lane & 3) == 0 && warp == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
       } else if (t < n) {
-        ptr = p.gathered ? p.gathered + ((int64_t)u * p.budget_tokens + 4 * j + (tid & 3)) * kRowBytes
+        src = p.gathered ? p.gathered + ((int64_t)u * p.budget_tokens + 4 * j + (lane & 3)) * kRowBytes
                          : row_source(p.b, u, t, kKernAttn);
       }
     }
-    src[tid] = ptr;
   }
-  __syncthreads();
-
-  // ---- rows -> shared memory (16 loads in flight per thread)
-  {
-    constexpr int kPer = kSplitTokens * kChunksPerRow / kThreads;  // 16
-    uint4 v[kPer];
+  if (warp == 0) valid[lane] = src != nullptr;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = k * kThreads + tid;
-      const uint8_t* s = src[idx / kChunksPerRow];
-      v[k] = s ? ld_nc_v4(s + (idx % kChunksPerRow) * 16) : make_uint4(0, 0, 0, 0);
+  for (int r = 0; r < 4; ++r) {
+    const int row = 4 * warp + r;
+    const uint8_t* s = reinterpret_cast<const uint8_t*>(
+        __shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(src), row));
+#pragma unroll
+    for (int c = 0; c < kChunksPerRow / 32; ++c) {
+      const int chunk = c * 32 + lane;
+      cp_async16(buf + row * kRowBytes + chunk * 16, s ? s + chunk * 16 : p.b.pool, s ? 16u : 0u);
     }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k)
-      *reinterpret_cast<uint4*>(rows + (k * kThreads + tid) * 16) = v[k];
   }
-  __syncthreads();
+}
+
+__device__ __forceinline__ void compute_item(const AttnParams& p, int item, const uint8_t* rows,
+                                             const uint8_t* valid, float (*logit)[kSplitTokens],
+                                             float* m_s, float* l_s) {
+  const int u = item / p.splits, split = item % p.splits;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // ---- logits (base 2): warp -> (KV head g, 16 tokens), lane -> 4 dims
   {
@@ -154,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-      if ((lane & 7) == 0) logit[g * kGroup + hsel][tok] = src[tok] ? v : -INFINITY;
+      if ((lane & 7) == 0) logit[g * kGroup + hsel][tok] = valid[tok] ? v : -INFINITY;
     }
   }
   __syncthreads();
@@ -207,6 +224,35 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   }
 }
 
+__device__ __forceinline__ bool item_live(const AttnParams& p, int item) {
+  const int u = item / p.splits, split = item % p.splits;
+  const int nsel = unit_nsel(p, u, split == 0 && threadIdx.x == 0);
+  return nsel >= 0 && split * kAttnBlocksPerSplit < nsel;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParams p) {
+  extern __shared__ __align__(16) uint8_t rows[];  // [2][32][2048]
+  __shared__ uint8_t valid[2][kSplitTokens];
+  __shared__ float logit[kQHeads][kSplitTokens];
+  __shared__ float m_s[kQHeads], l_s[kQHeads];
+
+  int buf = 0;
+  int item = blockIdx.x;
+  if (item < p.n_items) issue_item(p, item, rows, valid[0]);
+  cp_async_commit();
+  for (; item < p.n_items; item += gridDim.x) {
+    const int next = item + gridDim.x;
+    if (next < p.n_items) issue_item(p, next, rows + (buf ^ 1) * kBufBytes, valid[buf ^ 1]);
+    cp_async_commit();
+    cp_async_wait_1();  // this item's rows have landed (the next item's may still fly)
+    __syncthreads();
+    if (item_live(p, item)) compute_item(p, item, rows + buf * kBufBytes, valid[buf], logit, m_s, l_s);
+    __syncthreads();    // the buffer is reused by the issue two items ahead
+    buf ^= 1;
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Merge: CTA (head, unit), thread = output dim.
 __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const AttnParams p) {
   const int h = blockIdx.x, u = blockIdx.y, d = threadIdx.x;
@@ -256,12 +302,25 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
   p.n_sel = n_sel;
   p.k_max = budget_tokens / 4;
   p.budget_tokens = budget_tokens;
+  p.splits = (p.k_max + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit;
+  p.n_items = p.splits * b.n_units;
   p.gathered = gathered;
   p.scale_log2 = softmax_scale * kLog2e;
   p.out = out;
   p.lse = lse;
-  const int splits = (p.k_max + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit;
-  attn_split_kernel<<<dim3(splits, b.n_units), kThreads, kSmemBytes, s>>>(p);
+  static int sm_count = 0;
+  if (sm_count == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  bool any_host = false;
+  if (gathered == nullptr)
+    for (int u = 0; u < b.n_units; ++u) any_host |= b.u[u].host_rows != nullptr;
+  const int cap = any_host ? kMaxCtasHost : sm_count;
+  const int ctas = p.n_items < cap ? p.n_items : cap;
+  attn_split_kernel<<<ctas, kThreads, kSmemBytes, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_merge_kernel<<<dim3(kQHeads, b.n_units), kHeadDim, 0, s>>>(p);

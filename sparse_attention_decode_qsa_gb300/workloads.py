@@ -109,38 +109,54 @@ class Workload:
         for l in range(self.n_layers):
             self.step_layer(l, stream)
 
-    def step_group_layer(self, r0: int, r1: int, l: int, stream):
-        """Index score, top-k and attention of requests r0..r1-1 at layer l."""
+    def step_group_layer(self, r0: int, r1: int, l: int, s_score, s_attn=None):
+        """Index score and top-k of requests r0..r1-1 at layer l on s_score,
+        then their attention on s_attn (after the top-k)."""
         c, R = self.cache, self.n_req
         hs = self.handles[r0:r1]
         sl = slice(l * R + r0, l * R + r1)
-        c.index_score(hs, l, 1, self.q_idx[sl], self.w[sl], self.blk[sl], stream)
-        c.select_c4_topk(hs, l, 1, self.blk[sl], self.budget, self.sel[sl], self.nsel[sl], stream)
+        c.index_score(hs, l, 1, self.q_idx[sl], self.w[sl], self.blk[sl], s_score)
+        c.select_c4_topk(hs, l, 1, self.blk[sl], self.budget, self.sel[sl], self.nsel[sl], s_score)
+        if s_attn is not None:
+            s_attn.wait_stream(s_score)
         c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
-                             None, self.softmax_scale, self.out[sl], self.lse[sl], stream)
+                             None, self.softmax_scale, self.out[sl], self.lse[sl],
+                             s_attn if s_attn is not None else s_score)
+        if s_attn is not None:
+            s_score.wait_stream(s_attn)   # the next layer of these requests follows it
 
     def step_pipelined(self, streams):
         """One decode step with the requests split into len(streams) groups
-        (micro-batches), each group on its own stream walking the layers in
-        order.  Groups share no data, so one group's host-link-bound
-        attention overlaps another group's HBM-bound scoring.  Forks from and
-        joins back into the current stream."""
+        (micro-batches).  streams[g] = (score stream, attention stream) of
+        group g; each group walks the layers in order.  Groups share no data,
+        so one group's host-link-bound attention overlaps another group's
+        HBM-bound scoring.  Forks from and joins back into the current stream."""
         main = torch.cuda.current_stream()
         G = len(streams)
         bounds = [(g * self.n_req // G, (g + 1) * self.n_req // G) for g in range(G)]
-        for s in streams:
-            s.wait_stream(main)
+        for ss, sa in streams:
+            ss.wait_stream(main)
         for l in range(self.n_layers):
-            for (r0, r1), s in zip(bounds, streams):
+            for (r0, r1), (ss, sa) in zip(bounds, streams):
                 if r1 > r0:
-                    self.step_group_layer(r0, r1, l, s)
-        for s in streams:
-            main.wait_stream(s)
+                    self.step_group_layer(r0, r1, l, ss, sa)
+        for ss, sa in streams:
+            main.wait_stream(ss)
+
+    def make_streams(self, n_groups: int):
+        """Per group a scoring stream and a higher-priority attention stream,
+        so attention CTAs are dispatched ahead of queued scoring CTAs."""
+        try:
+            _, hi = torch.cuda.Stream.priority_range()
+        except (AttributeError, RuntimeError):
+            hi = -1
+        return [(torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=hi))
+                for _ in range(n_groups)]
 
     def capture(self, n_groups: int):
         """Capture step_pipelined into a CUDA graph (after one eager warm-up
         run, which also sets the kernels' launch attributes)."""
-        streams = [torch.cuda.Stream() for _ in range(n_groups)]
+        streams = self.make_streams(n_groups)
         self.step_pipelined(streams)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
