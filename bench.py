@@ -155,7 +155,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     hbm_peak, peak_kind = peaks()
-    wl = workloads.c256k_x8(device=dev)
+    wl = workloads.c256k_x8(device=dev, n_layers=args.layers, n_req=args.requests)
     stream = torch.cuda.current_stream(dev)
     R, L = wl.n_req, wl.n_layers
     units = R * L
@@ -290,6 +290,7 @@ def run_ours(args, rank, world):
     dom = dict(roofs[dominant])
     dom["kernel"] = dominant
     cfg = config_block()
+    cfg["qsa_layers"], cfg["requests"] = L, R
     cfg["micro_batches"] = args.groups
     cfg["cuda_graph"] = True
     line = {
@@ -395,6 +396,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=N_LAYERS,
+                    help="QSA layers (fewer only for profiling captures)")
+    ap.add_argument("--requests", type=int, default=N_REQ)
     ap.add_argument("--groups", type=int, default=2,
                     help="request micro-batches, each on its own stream")
     args = ap.parse_args()

@@ -318,7 +318,8 @@ qsa_status_t qsa_sparse_decode_attn(qsa_cache* cache, const qsa_batch* batch,
  * carved from a pre-planned arena it may not grow, a plug-in handed only its
  * input and output buffers, code that must not call cudaMalloc because it
  * would synchronise the device).  It computes what qsa_sparse_decode_attn
- * computes when given gathered rows, bit for bit, without a qsa_cache: the
+ * computes when given gathered rows (equal up to rounding: the splits are
+ * merged in another order), without a qsa_cache: the
  * split-K partials live in a static 8.5 MB device array of the library that
  * every GPU which loads the library holds until the process exits.
  *  q:      device bf16 bits [n_units][16][128]

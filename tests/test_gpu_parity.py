@@ -130,7 +130,9 @@ def _host_ring_workload(n_req=2, n_layers=2, n=20000, seed=5):
 def test_host_ring_gather_and_attention_modes():
     """Host history + HBM tail ring: selection and attention match the
     oracle; gathered rows are byte-exact; attention read through the slot
-    table equals attention over the gathered rows bit for bit."""
+    table equals attention over the gathered rows to fp32 rounding (the two
+    modes may spread the splits over a different number of CTAs, which
+    changes only the merge order)."""
     wl = _host_ring_workload()
     try:
         wl.step()
@@ -157,7 +159,8 @@ def test_host_ring_gather_and_attention_modes():
                 assert int(nrows[r]) == m
                 assert np.array_equal(g[r, :m].cpu().numpy(), ref["rows"])
         _clean(wl)
-        assert torch.equal(out_direct, wl.out) and torch.equal(lse_direct, wl.lse)
+        assert torch.allclose(out_direct, wl.out, rtol=1e-5, atol=1e-6)
+        assert torch.allclose(lse_direct, wl.lse, rtol=1e-6, atol=1e-6)
     finally:
         wl.close()
 
@@ -345,7 +348,9 @@ def test_ragged_batch_recycling_on_gpu():
 
 def test_pipelined_graph_step_equals_sequential_step():
     """Request groups on separate streams, captured as a CUDA graph and
-    replayed, give bit-identical outputs to the one-stream layer loop."""
+    replayed, give the same selections as the one-stream layer loop and the
+    same attention to fp32 rounding (smaller calls spread a unit's splits
+    over more CTAs, which changes only the merge order)."""
     wl = _host_ring_workload(n_req=4, n_layers=3, n=20000, seed=12)
     try:
         wl.step()
@@ -360,8 +365,9 @@ def test_pipelined_graph_step_equals_sequential_step():
         g.replay()
         torch.cuda.synchronize()
         _clean(wl)
-        for a, b in zip(ref, (wl.sel, wl.nsel, wl.out, wl.lse)):
-            assert torch.equal(a, b)
+        assert torch.equal(ref[0], wl.sel) and torch.equal(ref[1], wl.nsel)
+        assert torch.allclose(ref[2], wl.out, rtol=1e-5, atol=1e-6)
+        assert torch.allclose(ref[3], wl.lse, rtol=1e-6, atol=1e-6)
         QC.check_unit(wl, 2, 3)
     finally:
         wl.close()
