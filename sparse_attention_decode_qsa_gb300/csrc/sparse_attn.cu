@@ -4,33 +4,34 @@
 // оффлоадинга": attention reads only the <= indexer_budget selected rows).
 //
 // Split-K flash-decode.  A split is 8 selected C4 blocks, i.e. 32 token
-// rows (64 KiB of K/V).  Rows are read through the slot table (pool rows from
-// HBM, cold rows zero-copy from mapped pinned host memory) or from a dense
-// gathered buffer.
+// rows.  Rows are read through the slot table (pool rows from HBM, cold rows
+// zero-copy from mapped pinned host memory) or from a dense gathered buffer.
 //
 // Work layout: `cpu` CTAs per unit; CTA (unit u, slot r) takes the splits
 // r, r + cpu, r + 2*cpu, ... of unit u and visits them alternately from the
 // front and the back of that list.  Selected blocks are in ascending id order,
-// so for a request with an HBM tail ring its early splits are cold (host) and
-// its late splits hot (HBM): the alternation overlaps one split's host
-// transfer with another split's compute.  Rows of the next split are copied
-// with cp.async into the second of two 64 KiB buffers while the current
-// split is computed.  A CTA keeps a running (max, sum, acc) across its splits
-// (online softmax) and writes one partial; a small second kernel merges the
-// cpu partials of each (unit, head) with the log-sum-exp rule.  When some
-// row comes from host memory the grid is capped at kMaxCtasHost CTAs: that
-// many SMs saturate the host link, and the rest stay free for HBM-bound work
-// of other requests on other streams.
+// so for a request with an HBM tail ring the early splits are cold (host) and
+// the late ones hot (HBM): the alternation overlaps host transfers with
+// compute.  When some row comes from host memory the grid is capped at
+// kMaxCtasHost CTAs: that many SMs saturate the host link, and the others
+// stay free for HBM-bound work of other requests on other streams.
 //
-// Per split (256 threads):
-//   logits : warp w serves KV head w/2 and 16 tokens; lane l holds dims
-//            4l..4l+3 of the 4 query heads of that KV head, and the four
-//            partial dots are reduced across the warp with a transposing
-//            butterfly (6 shuffles for 4 values);
-//   softmax: warp w owns query heads 2w, 2w+1, lane = token;
-//   P.V    : thread t serves KV head t/64 and dims 2(t%64), 2(t%64)+1 of its
-//            4 query heads.
-// The products are plain FMAs: 4 query heads per KV head make this a
+// Inside a CTA the 8 warps work independently: warp w serves KV head
+// g = w % 4 (its 4 query heads) for tokens 16*(w/4) .. 16*(w/4)+15 of every
+// split.  A warp copies only its KV head's 512 bytes of each of its 16 rows
+// (K[g] then V[g]) with cp.async into its own double buffer, so no CTA-wide
+// barrier is needed while streaming; it keeps a running online-softmax state
+// (max, sum, acc) for its 4 heads over all its tokens.  At the end the two
+// token halves of each KV head are merged in shared memory and the CTA writes
+// one partial; a small second kernel merges the cpu partials of each
+// (unit, head) with the log-sum-exp rule.
+//
+// Per warp and split: logits with lane l holding dims 4l..4l+3 of the 4 query
+// heads, reduced across the warp with a transposing butterfly (6 shuffles
+// for 4 values); after it the lanes 8j..8j+7 hold head j, lane 8j+k keeping
+// tokens k and k+8.  Softmax statistics are reduced over those 8 lanes; P.V
+// broadcasts each token's 4 probabilities with shuffles and accumulates dims
+// 4l..4l+3.  Plain FMAs throughout: 4 query heads per KV head make this a
 // 4-row contraction, not a tensor-core shape.
 #include <cuda_bf16.h>
 
@@ -40,10 +41,11 @@ namespace qsa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSplitTokens = kAttnTokensPerSplit;     // 32
-constexpr int kChunksPerRow = kRowBytes / 16;         // 128
-constexpr int kBufBytes = kSplitTokens * kRowBytes;   // 64 KiB
-constexpr int kSmemBytes = 2 * kBufBytes;             // double buffer
+constexpr int kWarps = kThreads / 32;
+constexpr int kWarpTokens = 16;                       // tokens per warp and split
+constexpr int kSliceBytes = 2 * kHeadDim * 2;         // K[g] + V[g] of one token: 512
+constexpr int kWarpBufBytes = kWarpTokens * kSliceBytes;  // 8 KiB
+constexpr int kSmemBytes = kWarps * 2 * kWarpBufBytes;    // 128 KiB
 #ifndef QSA_ATTN_HOST_CTAS
 #define QSA_ATTN_HOST_CTAS 64
 #endif
@@ -89,184 +91,187 @@ __device__ __forceinline__ int visit_split(int k, int count, int r, int cpu) {
   return r + idx * cpu;
 }
 
-// Issue the copies of split `split` of unit u into buf; warp w copies rows
-// 4w..4w+3, each lane 4 chunks of each.  valid[t] tells compute which rows
-// exist (written by warp 0).
-__device__ __forceinline__ void issue_split(const AttnParams& p, int u, int split, int nsel,
-                                            uint8_t* buf, uint8_t* valid) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j0 = split * kAttnBlocksPerSplit;
+// Copy this warp's 16 token slices (K[g], V[g]) of `split` into buf.  Lane l
+// resolves token l (l < 16); every lane then copies 16 bytes of each slice.
+// Returns a bitmask of the tokens that exist.
+__device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int split, int nsel,
+                                               int g, int half, uint8_t* buf) {
+  const int lane = threadIdx.x & 31;
   const int64_t n = p.b.u[u].n;
-  // lane l resolves row l of the split (every warp does, so no block barrier)
   const uint8_t* src = nullptr;
-  {
-    const int j = j0 + lane / 4;
+  if (lane < kWarpTokens) {
+    const int tok = half * kWarpTokens + lane;              // token within the split
+    const int j = split * kAttnBlocksPerSplit + tok / 4;    // selected-block index
     if (j < nsel) {
       const int64_t b = p.sel[(int64_t)u * p.k_max + j];
-      const int64_t t = 4 * b + (lane & 3);
+      const int64_t t = 4 * b + (tok & 3);
       if (b < 0 || 4 * b >= n) {
-        if ((lane & 3) == 0 && warp == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
+        if ((tok & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
       } else if (t < n) {
-        src = p.gathered ? p.gathered + ((int64_t)u * p.budget_tokens + 4 * j + (lane & 3)) * kRowBytes
+        src = p.gathered ? p.gathered + ((int64_t)u * p.budget_tokens + 4 * j + (tok & 3)) * kRowBytes
                          : row_source(p.b, u, t, kKernAttn);
       }
     }
   }
-  if (warp == 0) valid[lane] = src != nullptr;
+  const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & 0xFFFFu;
+  // lanes 0..15 copy K[g] (chunks of 16 B), lanes 16..31 copy V[g]
+  const int off = (lane < 16) ? g * kHeadDim * 2 + lane * 16
+                              : kKvHeads * kHeadDim * 2 + g * kHeadDim * 2 + (lane - 16) * 16;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int row = 4 * warp + r;
+  for (int i = 0; i < kWarpTokens; ++i) {
     const uint8_t* s = reinterpret_cast<const uint8_t*>(
-        __shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(src), row));
-#pragma unroll
-    for (int c = 0; c < kChunksPerRow / 32; ++c) {
-      const int chunk = c * 32 + lane;
-      cp_async16(buf + row * kRowBytes + chunk * 16, s ? s + chunk * 16 : p.b.pool, s ? 16u : 0u);
-    }
+        __shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(src), i));
+    cp_async16(buf + i * kSliceBytes + lane * 16, s ? s + off : p.b.pool, s ? 16u : 0u);
   }
+  return valid;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParams p) {
-  extern __shared__ __align__(16) uint8_t rows[];  // [2][32][2048]
-  __shared__ uint8_t valid[2][kSplitTokens];
-  __shared__ float logit[kQHeads][kSplitTokens];
-  __shared__ float m_s[kQHeads], l_s[kQHeads];
+  extern __shared__ __align__(16) uint8_t smem[];  // [warp][2][16][512]
+  __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
+  __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
   const int u = blockIdx.x / p.cpu, r = blockIdx.x % p.cpu;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = warp & 3, half = warp >> 2;
+  uint8_t* wbuf = smem + warp * 2 * kWarpBufBytes;
   int nsel = p.n_sel[u];
   if (nsel < 0 || nsel > p.k_max) {
-    if (r == 0 && tid == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
+    if (r == 0 && threadIdx.x == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
     nsel = 0;
   }
   const int splits = (nsel + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit;
   const int count = r < splits ? (splits - 1 - r) / p.cpu + 1 : 0;
 
-  // query of this unit: warp w (KV head g = w/2) needs dims 4*lane.. of its 4 heads
-  const int g_l = warp >> 1;
+  // query dims 4l..4l+3 of the 4 heads of KV head g, pre-scaled to base 2
   float qr[kGroup][4];
   {
     const uint16_t* qu = p.q + (int64_t)u * kQHeads * kHeadDim;
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
-      const uint2 w2 = *reinterpret_cast<const uint2*>(qu + (g_l * kGroup + j) * kHeadDim + 4 * lane);
+      const uint2 w2 = *reinterpret_cast<const uint2*>(qu + (g * kGroup + j) * kHeadDim + 4 * lane);
       qr[j][0] = bf16_lo(w2.x) * p.scale_log2;
       qr[j][1] = bf16_hi(w2.x) * p.scale_log2;
       qr[j][2] = bf16_lo(w2.y) * p.scale_log2;
       qr[j][3] = bf16_hi(w2.y) * p.scale_log2;
     }
   }
-  // running state of this thread's P.V outputs: KV head g_v, dims d0, d0+1 of 4 heads
-  const int g_v = tid >> 6, d0 = 2 * (tid & 63);
-  float M[kGroup], L[kGroup], acc[kGroup][2];
+  const int hj = (lane >> 3) & 3;      // head whose statistics this lane holds
+  float m_run = -INFINITY, l_run = 0.f;  // statistics of head hj (same in lanes 8hj..8hj+7)
+  float acc[kGroup][4];                // dims 4l..4l+3 of the 4 heads
 #pragma unroll
-  for (int j = 0; j < kGroup; ++j) { M[j] = -INFINITY; L[j] = 0.f; acc[j][0] = acc[j][1] = 0.f; }
+  for (int j = 0; j < kGroup; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
+  uint32_t valid_cur = 0, valid_next = 0;
   int buf = 0;
-  if (count > 0) issue_split(p, u, visit_split(0, count, r, p.cpu), nsel, rows, valid[0]);
+  if (count > 0) valid_next = issue_warp(p, u, visit_split(0, count, r, p.cpu), nsel, g, half, wbuf);
   cp_async_commit();
   for (int k = 0; k < count; ++k) {
+    valid_cur = valid_next;
     if (k + 1 < count)
-      issue_split(p, u, visit_split(k + 1, count, r, p.cpu), nsel, rows + (buf ^ 1) * kBufBytes,
-                  valid[buf ^ 1]);
+      valid_next = issue_warp(p, u, visit_split(k + 1, count, r, p.cpu), nsel, g, half,
+                              wbuf + (buf ^ 1) * kWarpBufBytes);
     cp_async_commit();
-    cp_async_wait_1();  // this split's rows have landed (the next split's may still fly)
-    __syncthreads();
-    const uint8_t* R = rows + buf * kBufBytes;
-    const uint8_t* V = valid[buf];
+    cp_async_wait_1();
+    __syncwarp();
+    const uint8_t* R = wbuf + buf * kWarpBufBytes;
 
-    // ---- logits (base 2): warp -> (KV head g_l, 16 tokens), lane -> 4 dims
-    {
-      const int tok0 = (warp & 1) * 16;
-      const int hsel = (lane >> 3) & 3;  // head this lane ends up holding
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int tok = tok0 + i;
-        const uint2 kk = *reinterpret_cast<const uint2*>(R + tok * kRowBytes + g_l * kHeadDim * 2 + lane * 8);
-        const float k0 = bf16_lo(kk.x), k1 = bf16_hi(kk.x), k2 = bf16_lo(kk.y), k3 = bf16_hi(kk.y);
-        float d[kGroup];
+    // logits: lane 8j+kk ends with tokens kk and kk+8 of head j
+    float x0 = -INFINITY, x1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j)
-          d[j] = fmaf(qr[j][3], k3, fmaf(qr[j][2], k2, fmaf(qr[j][1], k1, qr[j][0] * k0)));
-        // transposing butterfly: after it, lane l holds the full dot of head (l>>3)&3
-        const bool up16 = lane & 16;
-        const float a0 = up16 ? d[0] : d[2], a1 = up16 ? d[1] : d[3];
-        const float r0 = __shfl_xor_sync(0xFFFFFFFFu, a0, 16);
-        const float r1 = __shfl_xor_sync(0xFFFFFFFFu, a1, 16);
-        const float v0 = (up16 ? d[2] : d[0]) + r0;
-        const float v1 = (up16 ? d[3] : d[1]) + r1;
-        const bool up8 = lane & 8;
-        const float a = up8 ? v0 : v1;
-        float v = (up8 ? v1 : v0) + __shfl_xor_sync(0xFFFFFFFFu, a, 8);
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-        v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-        if ((lane & 7) == 0) logit[g_l * kGroup + hsel][tok] = V[tok] ? v : -INFINITY;
+    for (int i = 0; i < kWarpTokens; ++i) {
+      const uint2 kk = *reinterpret_cast<const uint2*>(R + i * kSliceBytes + lane * 8);
+      const float k0 = bf16_lo(kk.x), k1 = bf16_hi(kk.x), k2 = bf16_lo(kk.y), k3 = bf16_hi(kk.y);
+      float d[kGroup];
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j)
+        d[j] = fmaf(qr[j][3], k3, fmaf(qr[j][2], k2, fmaf(qr[j][1], k1, qr[j][0] * k0)));
+      const bool up16 = lane & 16;
+      const float a0 = up16 ? d[0] : d[2], a1 = up16 ? d[1] : d[3];
+      const float r0 = __shfl_xor_sync(0xFFFFFFFFu, a0, 16);
+      const float r1 = __shfl_xor_sync(0xFFFFFFFFu, a1, 16);
+      const float v0 = (up16 ? d[2] : d[0]) + r0;
+      const float v1 = (up16 ? d[3] : d[1]) + r1;
+      const bool up8 = lane & 8;
+      const float a = up8 ? v0 : v1;
+      float v = (up8 ? v1 : v0) + __shfl_xor_sync(0xFFFFFFFFu, a, 8);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+      if ((lane & 7) == (i & 7)) {
+        const float x = ((valid_cur >> i) & 1u) ? v : -INFINITY;
+        if (i < 8) x0 = x; else x1 = x;
       }
     }
-    __syncthreads();
 
-    // ---- softmax within the split: warp -> heads 2w, 2w+1, lane -> token
+    // online softmax of head hj over its 16 tokens of this split
+    float ms = fmaxf(x0, x1);
+    ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 1));
+    ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 2));
+    ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 4));
+    const float m_new = fmaxf(m_run, ms);
+    const float so = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);  // old-state scale
+    const float p0 = (x0 == -INFINITY) ? 0.f : exp2f(x0 - m_new);
+    const float p1 = (x1 == -INFINITY) ? 0.f : exp2f(x1 - m_new);
+    float ps = p0 + p1;
+    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
+    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
+    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 4);
+    l_run = fmaf(l_run, so, ps);
+    m_run = m_new;
+
+    // P.V: rescale, then add this split's tokens
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int h = 2 * warp + hh;
-      const float x = logit[h][lane];
-      float m = x;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      const float pr = (x == -INFINITY) ? 0.f : exp2f(x - m);
-      float l = pr;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-      logit[h][lane] = pr;
-      if (lane == 0) { m_s[h] = m; l_s[h] = l; }
+    for (int j = 0; j < kGroup; ++j) {
+      const float sj = __shfl_sync(0xFFFFFFFFu, so, 8 * j);
+      acc[j][0] *= sj; acc[j][1] *= sj; acc[j][2] *= sj; acc[j][3] *= sj;
     }
-    __syncthreads();
-
-    // ---- P.V and online-softmax update of the running state
-    {
-      float a[kGroup][2];
 #pragma unroll
-      for (int j = 0; j < kGroup; ++j) a[j][0] = a[j][1] = 0.f;
-#pragma unroll 8
-      for (int tok = 0; tok < kSplitTokens; ++tok) {
-        const uint32_t vv = *reinterpret_cast<const uint32_t*>(
-            R + tok * kRowBytes + kKvHeads * kHeadDim * 2 + g_v * kHeadDim * 2 + d0 * 2);
-        const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-          const float pr = logit[g_v * kGroup + j][tok];
-          a[j][0] = fmaf(pr, v0, a[j][0]);
-          a[j][1] = fmaf(pr, v1, a[j][1]);
-        }
-      }
+    for (int i = 0; i < kWarpTokens; ++i) {
+      const uint2 vv = *reinterpret_cast<const uint2*>(R + i * kSliceBytes + kHeadDim * 2 + lane * 8);
+      const float v0 = bf16_lo(vv.x), v1 = bf16_hi(vv.x), v2 = bf16_lo(vv.y), v3 = bf16_hi(vv.y);
+      const float mine = i < 8 ? p0 : p1;
 #pragma unroll
       for (int j = 0; j < kGroup; ++j) {
-        const float ms = m_s[g_v * kGroup + j];
-        if (ms == -INFINITY) continue;                 // no token of this split
-        const float mn = fmaxf(M[j], ms);
-        const float so = exp2f(M[j] - mn), sn = exp2f(ms - mn);
-        L[j] = fmaf(L[j], so, l_s[g_v * kGroup + j] * sn);
-        acc[j][0] = fmaf(acc[j][0], so, a[j][0] * sn);
-        acc[j][1] = fmaf(acc[j][1], so, a[j][1] * sn);
-        M[j] = mn;
+        const float pj = __shfl_sync(0xFFFFFFFFu, mine, 8 * j + (i & 7));
+        acc[j][0] = fmaf(pj, v0, acc[j][0]);
+        acc[j][1] = fmaf(pj, v1, acc[j][1]);
+        acc[j][2] = fmaf(pj, v2, acc[j][2]);
+        acc[j][3] = fmaf(pj, v3, acc[j][3]);
       }
     }
-    __syncthreads();    // logit/m_s/l_s and this buffer are reused
+    __syncwarp();   // this buffer is refilled two splits ahead
     buf ^= 1;
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
 
-  float* part = partial_ptr(p.b, u, r);
+  // merge the two token halves of each KV head, then write the CTA's partial
+  if (half == 1) {
+    if ((lane & 7) == 0) { xm[g][hj] = m_run; xl[g][hj] = l_run; }
 #pragma unroll
-  for (int j = 0; j < kGroup; ++j)
-    *reinterpret_cast<float2*>(part + 2 * kQHeads + (g_v * kGroup + j) * kHeadDim + d0) =
-        make_float2(acc[j][0], acc[j][1]);
-  if ((tid & 63) == 0) {
+    for (int j = 0; j < kGroup; ++j)
+      *reinterpret_cast<float4*>(&xacc[g][j][4 * lane]) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+  }
+  __syncthreads();
+  if (half == 0) {
+    const float mo = xm[g][hj], lo = xl[g][hj];
+    const float mn = fmaxf(m_run, mo);
+    const float sa = (mn == -INFINITY) ? 0.f : exp2f(m_run - mn);
+    const float sb = (mn == -INFINITY) ? 0.f : exp2f(mo - mn);
+    const float L = fmaf(l_run, sa, lo * sb);
+    float* part = partial_ptr(p.b, u, r);
+    if ((lane & 7) == 0) {
+      part[g * kGroup + hj] = mn;
+      part[kQHeads + g * kGroup + hj] = L;
+    }
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
-      part[g_v * kGroup + j] = M[j];
-      part[kQHeads + g_v * kGroup + j] = L[j];
+      const float aj = __shfl_sync(0xFFFFFFFFu, sa, 8 * j);
+      const float bj = __shfl_sync(0xFFFFFFFFu, sb, 8 * j);
+      const float4 o = *reinterpret_cast<const float4*>(&xacc[g][j][4 * lane]);
+      *reinterpret_cast<float4*>(part + 2 * kQHeads + (g * kGroup + j) * kHeadDim + 4 * lane) =
+          make_float4(fmaf(acc[j][0], aj, o.x * bj), fmaf(acc[j][1], aj, o.y * bj),
+                      fmaf(acc[j][2], aj, o.z * bj), fmaf(acc[j][3], aj, o.w * bj));
     }
   }
 }

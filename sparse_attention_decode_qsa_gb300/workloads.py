@@ -109,37 +109,46 @@ class Workload:
         for l in range(self.n_layers):
             self.step_layer(l, stream)
 
-    def step_group_layer(self, r0: int, r1: int, l: int, s_score, s_attn=None):
-        """Index score and top-k of requests r0..r1-1 at layer l on s_score,
-        then their attention on s_attn (after the top-k)."""
+    def score_group_layer(self, r0: int, r1: int, l: int, stream):
+        """Index score and top-k of requests r0..r1-1 at layer l."""
         c, R = self.cache, self.n_req
         hs = self.handles[r0:r1]
         sl = slice(l * R + r0, l * R + r1)
-        c.index_score(hs, l, 1, self.q_idx[sl], self.w[sl], self.blk[sl], s_score)
-        c.select_c4_topk(hs, l, 1, self.blk[sl], self.budget, self.sel[sl], self.nsel[sl], s_score)
-        if s_attn is not None:
-            s_attn.wait_stream(s_score)
-        c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
-                             None, self.softmax_scale, self.out[sl], self.lse[sl],
-                             s_attn if s_attn is not None else s_score)
-        if s_attn is not None:
-            s_score.wait_stream(s_attn)   # the next layer of these requests follows it
+        c.index_score(hs, l, 1, self.q_idx[sl], self.w[sl], self.blk[sl], stream)
+        c.select_c4_topk(hs, l, 1, self.blk[sl], self.budget, self.sel[sl], self.nsel[sl], stream)
 
-    def step_pipelined(self, streams):
+    def attn_group_layer(self, r0: int, r1: int, l: int, stream):
+        """Attention of requests r0..r1-1 at layer l over their selection."""
+        c, R = self.cache, self.n_req
+        hs = self.handles[r0:r1]
+        sl = slice(l * R + r0, l * R + r1)
+        c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
+                             None, self.softmax_scale, self.out[sl], self.lse[sl], stream)
+
+    def step_pipelined(self, streams, stagger: bool = True):
         """One decode step with the requests split into len(streams) groups
-        (micro-batches).  streams[g] = (score stream, attention stream) of
-        group g; each group walks the layers in order.  Groups share no data,
-        so one group's host-link-bound attention overlaps another group's
-        HBM-bound scoring.  Forks from and joins back into the current stream."""
+        (micro-batches); streams[g] = (score stream, attention stream) of
+        group g.  Each group walks the layers in order: scoring, then its
+        attention, then the next layer's scoring.  With stagger, the groups
+        also take turns at scoring (group g+1 scores layer l after group g
+        has), which puts one group's host-link-bound attention beside another
+        group's HBM-bound scoring instead of running all groups in lockstep.
+        Forks from and joins back into the current stream."""
         main = torch.cuda.current_stream()
         G = len(streams)
         bounds = [(g * self.n_req // G, (g + 1) * self.n_req // G) for g in range(G)]
         for ss, sa in streams:
             ss.wait_stream(main)
         for l in range(self.n_layers):
-            for (r0, r1), (ss, sa) in zip(bounds, streams):
-                if r1 > r0:
-                    self.step_group_layer(r0, r1, l, ss, sa)
+            for g, ((r0, r1), (ss, sa)) in enumerate(zip(bounds, streams)):
+                if r1 <= r0:
+                    continue
+                self.score_group_layer(r0, r1, l, ss)
+                if stagger and G > 1:
+                    streams[(g + 1) % G][0].wait_stream(ss)
+                sa.wait_stream(ss)
+                self.attn_group_layer(r0, r1, l, sa)
+                ss.wait_stream(sa)   # the next layer of these requests follows it
         for ss, sa in streams:
             main.wait_stream(ss)
 
