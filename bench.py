@@ -160,43 +160,51 @@ def run_ours(args, rank, world):
     R, L = wl.n_req, wl.n_layers
     units = R * L
     kinds = ["index_score", "select_topk", "sparse_attn"]
-
-    # ---- kernel breakdown: eager layer-sequential steps on one stream, with
-    # CUDA events around every launch (on the launching stream)
-    def step_timed(ev):
-        c, hs = wl.cache, wl.handles
-        for l in range(L):
-            sl = slice(l * R, (l + 1) * R)
-            ev[0][l].record(stream)
-            c.index_score(hs, l, 1, wl.q_idx[sl], wl.w[sl], wl.blk[sl], stream)
-            ev[1][l].record(stream)
-            c.select_c4_topk(hs, l, 1, wl.blk[sl], BUDGET, wl.sel[sl], wl.nsel[sl], stream)
-            ev[2][l].record(stream)
-            c.sparse_decode_attn(hs, l, 1, wl.q[sl], wl.sel[sl], wl.nsel[sl], BUDGET, None,
-                                 wl.softmax_scale, wl.out[sl], wl.lse[sl], stream)
-            ev[3][l].record(stream)
-
+    # ---- kernel breakdown: for each kernel kind, the 12 layers' launches of
+    # one step captured as their own CUDA graph (no host launch gaps), replayed
+    # args.steps times between CUDA events on the launching stream
     for _ in range(args.warmup):
         wl.step(stream)
     torch.cuda.synchronize(dev)
     st, det = wl.cache.poll_error()
     if st != 0:
         raise RuntimeError(f"device error word {st} ({det}) after warm-up")
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(4)]
-           for _ in range(args.steps)]
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for k in range(args.steps):
-        step_timed(evs[k])
-    k1.record(stream)
+    c, hs = wl.cache, wl.handles
+    calls = {
+        "index_score": lambda l, sl, s: c.index_score(hs, l, 1, wl.q_idx[sl], wl.w[sl], wl.blk[sl], s),
+        "select_topk": lambda l, sl, s: c.select_c4_topk(hs, l, 1, wl.blk[sl], BUDGET, wl.sel[sl],
+                                                         wl.nsel[sl], s),
+        "sparse_attn": lambda l, sl, s: c.sparse_decode_attn(hs, l, 1, wl.q[sl], wl.sel[sl], wl.nsel[sl],
+                                                             BUDGET, None, wl.softmax_scale,
+                                                             wl.out[sl], wl.lse[sl], s),
+    }
+    per_kind, launches = {}, {}
+    for kind, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cs):
+            for l in range(L):
+                fn(l, slice(l * R, (l + 1) * R), cs)
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        k1.record(stream)
+        torch.cuda.synchronize(dev)
+        per_kind[kind] = k0.elapsed_time(k1)
+        launches[kind] = args.steps * L
+        del g
+    e0_, e1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0_.record(stream)
+    for _ in range(args.steps):
+        wl.step(stream)
+    e1_.record(stream)
     torch.cuda.synchronize(dev)
-    ms_eager = k0.elapsed_time(k1)
-    per_kind = {k: 0.0 for k in kinds}
-    for k in range(args.steps):
-        for l in range(L):
-            for i, kind in enumerate(kinds):
-                per_kind[kind] += evs[k][i][l].elapsed_time(evs[k][i + 1][l])
-    launches = {k: args.steps * L for k in kinds}
+    ms_eager = e0_.elapsed_time(e1_)
 
     # ---- the measured step: request groups on their own streams, captured
     # once as a CUDA graph and replayed

@@ -10,11 +10,33 @@
 // "双卡RTX4090跑通Qwen3-Next：8并发满血长上下文实测", opening explanation of
 // QSA (C4 blocks of 4 adjacent tokens).
 //
-// Mapping: one thread owns one C4 block (4 tokens, 256 bytes of codes), so
-// every query value read from shared memory feeds four tokens' FMAs.  The
-// query is kept transposed in shared memory ([dim][head]) so one pair of
-// 16-byte loads gives all 8 heads of one dimension.  Tiles of 512 tokens from
-// all units of the call form one flat grid.
+// The scan does 512 multiply-adds per 66 bytes, more than the CUDA cores
+// deliver at HBM speed, and it is a genuine dense contraction
+// (keys[tokens][64] x q^T[64][8 heads]), so it runs on the 5th-generation
+// tensor cores (tcgen05, accumulators in TMEM):
+//
+//  * Tiles of M = 128 tokens.  One thread streams each tile's 8 KiB of codes
+//    into a 4-stage shared-memory ring with TMA bulk copies (cp.async.bulk,
+//    completion counted in bytes on an mbarrier).
+//  * All 128 threads convert the codes exactly to f16 (every e4m3 value is an
+//    f16 value) into the A operand; reads are consecutive 16-byte chunks and
+//    the four K-steps of A sit 4 KiB + 32 B apart, so neither side has bank
+//    conflicts.  The B operand holds the index query split as q = hi + lo
+//    (hi = f16(q), lo = f16(q - hi)), so N = 16 columns: 8 heads x {hi, lo},
+//    which keeps the dot products at fp32 accuracy.
+//  * One thread issues four tcgen05.mma (K = 16 each) per tile into one of two
+//    16-column TMEM accumulators and commits them to an mbarrier; the
+//    epilogue of the previous tile (tcgen05.ld, relu, head weights, scale,
+//    C4 max through shuffles; thread t = token t = TMEM lane t) overlaps them.
+//  * The grid is persistent (three CTAs per SM); CTA c takes a contiguous
+//    range of the flat tile list of all units of the call and rebuilds B
+//    when its range crosses into the next unit.
+//
+// Operand layout: K-major without swizzle, made of core matrices of 8 rows x
+// 16 bytes (8 f16).  Within a K-step of 16, element (row, k) lies at
+// (row/8)*256 + (k/8)*128 + (row%8)*16 + (k%8)*2 bytes: the descriptor's
+// leading byte offset (next core matrix along K) is 128 and its stride byte
+// offset (next 8-row group) is 256.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -30,7 +52,7 @@ constexpr int kTileTokens = kThreads * 4;  // 512
 
 struct IndexScoreParams {
   BatchDesc b;
-  int32_t tile_start[kMaxUnits + 1];  // prefix sums of tiles per unit
+  int32_t tile_start[kMaxUnits + 1];  // prefix sums of tiles (or CTAs) per unit
   const float* q_idx;                 // [units][8][64]
   const float* w;                     // [units][8]
   float* blk;                         // [units][blk_stride]
@@ -133,39 +155,22 @@ __global__ void __launch_bounds__(kThreads) index_score_kernel(const IndexScoreP
 
 #endif  // QSA_INDEX_SCORE_FFMA
 
-// ---------------------------------------------------------------------------
-// Tensor-core version (tcgen05, 5th-generation tensor cores with TMEM
-// accumulators).  The scan does 512 multiply-adds per 66 bytes, more than the
-// CUDA cores deliver at HBM speed, and it is a genuine dense contraction:
-// keys[tokens][64] x q^T[64][8 heads].
-//
-// Per CTA: 8 tiles of M = 128 tokens.  A tile's codes are converted exactly
-// to f16 (every e4m3 value is an f16 value) and stored as the A operand; the
-// B operand holds the index query split as q = hi + lo (both f16, hi = f16(q),
-// lo = f16(q - hi)), so N = 16 columns: 8 heads x {hi, lo}, which keeps the
-// product at fp32 accuracy.  Four tcgen05.mma (K = 16 each) accumulate the
-// fp32 dots of a tile in 16 TMEM columns; two such column blocks alternate
-// between tiles, so the epilogue of tile i-1 (tcgen05.ld, relu, head weights,
-// scale, C4 max through shuffles) runs while the MMAs of tile i execute and
-// the codes of tile i+1 are being loaded.  Thread t owns token t of a tile in
-// every phase: it loads and converts that token's row, and TMEM lane t holds
-// its accumulators.
-//
-// Operand layout: K-major without swizzle, made of core matrices of 8 rows x
-// 16 bytes (8 f16).  Element (row, k) of a K-step of 16 lies at
-// (row/8)*256 + ((k%16)/8)*128 + (row%8)*16 + (k%8)*2 bytes; the descriptor's
-// leading byte offset (next core matrix along K) is 128 and its stride byte
-// offset (next 8-row group) is 256.
 constexpr int kTcThreads = 128;
-constexpr int kTcTile = 128;
-constexpr int kTcTilesPerCta = 8;
-constexpr int kTcCtaTokens = kTcTile * kTcTilesPerCta;  // 1024
-constexpr uint32_t kTmemCols = 32;                     // two 16-column accumulators
-constexpr int kAStageBytes = kTcTile * kIndexDim * 2;  // 16 KiB
-constexpr int kAKStepBytes = kTcTile * 16 * 2;         // 4 KiB
+constexpr int kTcTile = 128;                           // tokens per MMA tile (M)
+constexpr int kStages = 4;                             // TMA ring depth
+constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per tile
+constexpr int kAKStepBytes = kTcTile * 16 * 2;         // 4 KiB: one K-step of A
+constexpr int kAKStride = kAKStepBytes + 32;           // padded: spreads banks
+constexpr int kABufBytes = 4 * kAKStride;
 constexpr int kBBytes = 16 * kIndexDim * 2;            // 2 KiB
 constexpr int kBKStepBytes = 16 * 16 * 2;              // 512 B
-constexpr int kTcSmemBytes = 2 * kAStageBytes + kBBytes + 64;
+constexpr uint32_t kTmemCols = 32;                     // two 16-column accumulators
+constexpr int kCtasPerSm = 3;
+constexpr int kOffRaw = 0;
+constexpr int kOffA = kOffRaw + kStages * kRawBytes;
+constexpr int kOffB = kOffA + 2 * kABufBytes;
+constexpr int kOffBar = kOffB + kBBytes;               // full[kStages], mma[2], tmem slot
+constexpr int kTcSmemBytes = kOffBar + 8 * (kStages + 2) + 16;
 // kind::f16 instruction descriptor: D f32 (bit 4), A = B = f16, both K-major,
 // N/8 at bits 17-22, M/16 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
@@ -175,8 +180,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
   return (uint32_t)__cvta_generic_to_shared(ptr);
 }
 
-__device__ __forceinline__ uint32_t kmajor_off(int row, int k, int kstep_bytes) {
-  return (k >> 4) * kstep_bytes + (row >> 3) * 256 + ((k >> 3) & 1) * 128 + (row & 7) * 16 +
+// Byte offset of element (row, k) of the B operand (16 rows x 64 k).
+__device__ __forceinline__ uint32_t b_off(int row, int k) {
+  return (k >> 4) * kBKStepBytes + (row >> 3) * 256 + ((k >> 3) & 1) * 128 + (row & 7) * 16 +
          (k & 7) * 2;
 }
 
@@ -187,19 +193,44 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46);
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Bounded wait; false (and an error record) if the phase never completes.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, ErrorWord* err,
+                                          int64_t detail) {
+  for (uint32_t polls = 0; !mbar_try_wait(bar, parity);) {
+    if (++polls > kWaitPolls) {
+      report_error(err, QSA_ERR_TIMEOUT, kKernIndexScore, detail);
+      return false;
+    }
+  }
+  return true;
+}
+
+// TMA bulk copy of `bytes` (multiple of 16) from global to shared memory,
+// completing `bytes` transactions on mbarrier `bar`.
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                            uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -218,9 +249,8 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
       : "memory");
 }
 
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
 
@@ -238,38 +268,36 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ uint4 ld_keys(const uint8_t* ptr) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(ptr));
-  return r;
+// Four e4m3 codes (bytes of w, low first) -> two f16x2 words (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair16, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+__device__ __forceinline__ int unit_of_tile(const IndexScoreParams& p, int t) {
+  int lo = 0, hi = p.b.n_units - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
 __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexScoreParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sA = smem;                                         // [2][16 KiB]
-  uint8_t* sB = smem + 2 * kAStageBytes;                      // 2 KiB
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + kBBytes);  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t bar_full = s_base + kOffBar;                 // + 8 * stage
+  const uint32_t bar_mma = s_base + kOffBar + 8 * kStages;    // + 8 * (tile & 1)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (kStages + 2));
 
-  int lo = 0, hi = p.b.n_units - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.tile_start[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
-  }
-  const int u = lo;
-  const int64_t n = p.b.u[u].n;
-  const int64_t t_cta = (int64_t)(blockIdx.x - p.tile_start[u]) * kTcCtaTokens;
-  const int64_t left = n - t_cta;
-  const int n_tiles = (int)((left + kTcTile - 1) / kTcTile < kTcTilesPerCta
-                                ? (left + kTcTile - 1) / kTcTile : kTcTilesPerCta);
+  // this CTA's contiguous range of the flat tile list
+  const int total = p.tile_start[p.b.n_units];
+  const int t0 = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
+  const int t1 = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  const int ntiles = t1 - t0;
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -278,115 +306,138 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(bar_full + 8 * s, 1);
+    mbar_init(bar_mma, 1);
+    mbar_init(bar_mma + 8, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // B operand: rows 0..7 = f16(q_h), rows 8..15 = f16(q_h - f16(q_h))
-  {
-    const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
-    for (int i = tid; i < kIndexHeads * kIndexDim; i += kTcThreads) {
-      const int h = i >> 6, d = i & 63;
-      const float qv = qu[i];
-      const __half qh = __float2half_rn(qv);
-      const __half ql = __float2half_rn(qv - __half2float(qh));
-      *reinterpret_cast<__half*>(sB + kmajor_off(h, d, kBKStepBytes)) = qh;
-      *reinterpret_cast<__half*>(sB + kmajor_off(h + 8, d, kBKStepBytes)) = ql;
-    }
-  }
-  float w[kIndexHeads];
-#pragma unroll
-  for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)u * kIndexHeads + h];
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int64_t row0 = p.b.unit_row(u);
-  const uint8_t* keys = p.b.index_keys + row0 * kIndexDim;
-  const uint16_t* scl = p.b.index_scales + row0;
-  float* out = p.blk + (int64_t)u * p.blk_stride;
-  const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-
-  uint4 raw[4];
-  {
-    const int64_t t = t_cta + tid;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) raw[c] = t < n ? ld_keys(keys + t * kIndexDim + c * 16) : make_uint4(0, 0, 0, 0);
+  // source and byte count of tile t (units are contiguous in the tile list)
+  auto tile_src = [&](int t, uint32_t& bytes) -> const uint8_t* {
+    const int u = unit_of_tile(p, t);
+    const int64_t tok0 = (int64_t)(t - p.tile_start[u]) * kTcTile;
+    const int64_t left = p.b.u[u].n - tok0;
+    bytes = (uint32_t)((left < kTcTile ? left : kTcTile) * kIndexDim);
+    return p.b.index_keys + (p.b.unit_row(u) + tok0) * kIndexDim;
+  };
+  if (tid == 0) {
+    for (int i = 0; i < kStages && i < ntiles; ++i) {
+      uint32_t bytes;
+      const uint8_t* src = tile_src(t0 + i, bytes);
+      tma_load_1d(s_base + kOffRaw + i * kRawBytes, src, bytes, bar_full + 8 * i);
+    }
   }
-  float sc_prev = 0.f;
+
+  // state of the unit being scored, and of the tile whose epilogue is pending
+  int cur_u = -1;
+  float w[kIndexHeads];
+  int64_t n = 0, tok_base = 0;
+  float* out = nullptr;
+  bool pend = false;
+  int pend_i = 0;
+  int64_t pend_tok = 0, pend_n = 0;
+  float pend_sc = 0.f;
+  float* pend_out = nullptr;
+  float pend_w[kIndexHeads];
   bool ok = true;
 
-  // epilogue of tile j: accumulators -> score -> C4 max -> block score
-  auto epilogue = [&](int j, float sc) {
-    const int b = j & 1;
-    uint32_t polls = 0;
-    while (!mbar_try_wait(&bar[b], (uint32_t)(j >> 1) & 1u)) {
-      if (++polls > kWaitPolls) {
-        report_error(p.b.err, QSA_ERR_TIMEOUT, kKernIndexScore, j);
-        ok = false;
-        break;
-      }
-    }
+  auto epilogue = [&]() {
+    const int b = pend_i & 1;
+    ok &= mbar_wait(bar_mma + 8 * b, (uint32_t)(pend_i >> 1) & 1u, p.b.err, pend_i);
     tc_fence_after();
     float v[16];
     tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 16), v);
-    const int64_t tok = t_cta + (int64_t)j * kTcTile + tid;
     float s = -INFINITY;
-    if (tok < n) {
+    if (pend_tok < pend_n) {
       s = 0.f;
 #pragma unroll
-      for (int h = 0; h < kIndexHeads; ++h) s = fmaf(w[h], fmaxf((v[h] + v[h + 8]) * sc, 0.f), s);
+      for (int h = 0; h < kIndexHeads; ++h)
+        s = fmaf(pend_w[h], fmaxf((v[h] + v[h + 8]) * pend_sc, 0.f), s);
     }
     s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
     s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
-    if ((lane & 3) == 0 && tok < n) out[tok >> 2] = s;
+    if ((lane & 3) == 0 && pend_tok < pend_n) pend_out[pend_tok >> 2] = s;
+    pend = false;
   };
 
-  int done = 0;
-  for (int i = 0; i < n_tiles; ++i) {
+  for (int i = 0; i < ntiles; ++i) {
     if (!__syncthreads_and(ok)) break;
-    const int b = i & 1;
-    uint4 cur[4] = {raw[0], raw[1], raw[2], raw[3]};
-    const int64_t tok = t_cta + (int64_t)i * kTcTile + tid;
-    const float sc_cur = tok < n ? __half2float(__ushort_as_half(scl[tok])) : 0.f;
-    if (i + 1 < n_tiles) {
-      const int64_t t = tok + kTcTile;
+    const int t = t0 + i;
+    const int u = unit_of_tile(p, t);
+    if (u != cur_u) {
+      if (pend) epilogue();  // the MMAs still reading B must finish first
+      const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
+      for (int e = tid; e < kIndexHeads * kIndexDim; e += kTcThreads) {
+        const int h = e >> 6, d = e & 63;
+        const float qv = qu[e];
+        const __half qh = __float2half_rn(qv);
+        const __half ql = __float2half_rn(qv - __half2float(qh));
+        *reinterpret_cast<__half*>(smem + kOffB + b_off(h, d)) = qh;
+        *reinterpret_cast<__half*>(smem + kOffB + b_off(h + 8, d)) = ql;
+      }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) raw[c] = t < n ? ld_keys(keys + t * kIndexDim + c * 16) : make_uint4(0, 0, 0, 0);
+      for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)u * kIndexHeads + h];
+      n = p.b.u[u].n;
+      tok_base = -(int64_t)p.tile_start[u] * kTcTile;
+      out = p.blk + (int64_t)u * p.blk_stride;
+      cur_u = u;
     }
-    // convert this thread's token row into A[b]
-    uint8_t* a = sA + b * kAStageBytes + (tid >> 3) * 256 + (tid & 7) * 16;
+    const int64_t tok = tok_base + (int64_t)t * kTcTile + tid;  // this thread's token of tile t
+    const float sc = tok < n ? __half2float(__ushort_as_half(
+                                   p.b.index_scales[p.b.unit_row(u) + tok])) : 0.f;
+
+    // codes of tile t have landed in stage i % kStages
+    const int stage = i % kStages;
+    ok &= mbar_wait(bar_full + 8 * stage, (uint32_t)(i / kStages) & 1u, p.b.err, t);
+    const uint8_t* raw = smem + kOffRaw + stage * kRawBytes;
+    uint8_t* A = smem + kOffA + (i & 1) * kABufBytes;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const uint32_t wd[4] = {cur[c].x, cur[c].y, cur[c].z, cur[c].w};
+      const int lc = c * kTcThreads + tid;        // 16-byte chunk of the tile
+      const int row = lc >> 2, ks = lc & 3;       // token row, K-step
+      const uint4 q = *reinterpret_cast<const uint4*>(raw + lc * 16);
       uint32_t h[8];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        h[2 * m] = e4m3x2_to_f16x2(wd[m] & 0xFFFFu);
-        h[2 * m + 1] = e4m3x2_to_f16x2(wd[m] >> 16);
-      }
-      *reinterpret_cast<uint4*>(a + c * kAKStepBytes) = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(a + c * kAKStepBytes + 128) = make_uint4(h[4], h[5], h[6], h[7]);
+      e4m3x4_to_f16x4(q.x, h[0], h[1]);
+      e4m3x4_to_f16x4(q.y, h[2], h[3]);
+      e4m3x4_to_f16x4(q.z, h[4], h[5]);
+      e4m3x4_to_f16x4(q.w, h[6], h[7]);
+      uint8_t* dst = A + ks * kAKStride + (row >> 3) * 256 + (row & 7) * 16;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(dst + 128) = make_uint4(h[4], h[5], h[6], h[7]);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
-      const uint32_t d = tmem + (uint32_t)(b * 16);
+      if (i + kStages < ntiles) {                 // every thread is done with this stage
+        uint32_t bytes;
+        const uint8_t* src = tile_src(t + kStages, bytes);
+        tma_load_1d(s_base + kOffRaw + stage * kRawBytes, src, bytes, bar_full + 8 * stage);
+      }
+      const uint32_t a0 = s_base + kOffA + (i & 1) * kABufBytes, b0 = s_base + kOffB;
+      const uint32_t d = tmem + (uint32_t)((i & 1) * 16);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        tc_mma_f16(d, smem_desc(a_base + b * kAStageBytes + k * kAKStepBytes, 128, 256),
-                   smem_desc(b_base + k * kBKStepBytes, 128, 256), k > 0 ? 1u : 0u);
-      tc_commit(&bar[b]);
+        tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
+                   smem_desc(b0 + k * kBKStepBytes, 128, 256), k > 0 ? 1u : 0u);
+      tc_commit(bar_mma + 8 * (i & 1));
     }
-    if (i >= 1) epilogue(i - 1, sc_prev);
-    sc_prev = sc_cur;
-    done = i + 1;
+    if (pend) epilogue();
+    pend = true;
+    pend_i = i;
+    pend_tok = tok;
+    pend_n = n;
+    pend_sc = sc;
+    pend_out = out;
+#pragma unroll
+    for (int h = 0; h < kIndexHeads; ++h) pend_w[h] = w[h];
   }
-  if (__syncthreads_and(ok) && done > 0) epilogue(done - 1, sc_prev);
+  if (__syncthreads_and(ok) && pend) epilogue();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -394,32 +445,38 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
 }
+
 }  // namespace
 
 cudaError_t launch_index_score(const BatchDesc& b, const float* q_idx, const float* w,
                                float* blk_scores, int64_t blk_stride, cudaStream_t s) {
-#ifdef QSA_INDEX_SCORE_FFMA
-  const int cta_tokens = kTileTokens;
-#else
-  const int cta_tokens = kTcCtaTokens;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-#endif
   IndexScoreParams p;
   p.b = b;
   p.q_idx = q_idx;
   p.w = w;
   p.blk = blk_scores;
   p.blk_stride = blk_stride;
+#ifdef QSA_INDEX_SCORE_FFMA
+  const int unit_tokens = kTileTokens;
+#else
+  const int unit_tokens = kTcTile;
+  static bool attr_set = false;
+  static int sm_count = 0;
+  if (!attr_set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTcSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+#endif
   int64_t tiles = 0;
   for (int u = 0; u < b.n_units; ++u) {
     p.tile_start[u] = (int32_t)tiles;
-    tiles += (b.u[u].n + cta_tokens - 1) / cta_tokens;
+    tiles += (b.u[u].n + unit_tokens - 1) / unit_tokens;
   }
   p.tile_start[b.n_units] = (int32_t)tiles;
   if (tiles <= 0) return cudaSuccess;
@@ -427,7 +484,9 @@ cudaError_t launch_index_score(const BatchDesc& b, const float* q_idx, const flo
 #ifdef QSA_INDEX_SCORE_FFMA
   index_score_kernel<<<(unsigned)tiles, kThreads, 0, s>>>(p);
 #else
-  index_score_tc_kernel<<<(unsigned)tiles, kTcThreads, kTcSmemBytes, s>>>(p);
+  const int64_t cap = (int64_t)kCtasPerSm * sm_count;
+  const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
+  index_score_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, s>>>(p);
 #endif
   return cudaGetLastError();
 }
