@@ -157,7 +157,13 @@ __global__ void __launch_bounds__(kThreads) index_score_kernel(const IndexScoreP
 
 constexpr int kTcThreads = 128;
 constexpr int kTcTile = 128;                           // tokens per MMA tile (M)
-constexpr int kStages = 4;                             // TMA ring depth
+#ifndef QSA_K1_STAGES
+#define QSA_K1_STAGES 4
+#endif
+#ifndef QSA_K1_CTAS_PER_SM
+#define QSA_K1_CTAS_PER_SM 3
+#endif
+constexpr int kStages = QSA_K1_STAGES;                 // TMA ring depth
 constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per tile
 constexpr int kAKStepBytes = kTcTile * 16 * 2;         // 4 KiB: one K-step of A
 constexpr int kAKStride = kAKStepBytes + 32;           // padded: spreads banks
@@ -165,7 +171,7 @@ constexpr int kABufBytes = 4 * kAKStride;
 constexpr int kBBytes = 16 * kIndexDim * 2;            // 2 KiB
 constexpr int kBKStepBytes = 16 * 16 * 2;              // 512 B
 constexpr uint32_t kTmemCols = 32;                     // two 16-column accumulators
-constexpr int kCtasPerSm = 3;
+constexpr int kCtasPerSm = QSA_K1_CTAS_PER_SM;
 constexpr int kOffRaw = 0;
 constexpr int kOffA = kOffRaw + kStages * kRawBytes;
 constexpr int kOffB = kOffA + 2 * kABufBytes;
@@ -332,6 +338,15 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
     }
   }
 
+  // fp16 scale of this thread's token of tile t (0 past the end of its unit);
+  // loaded a tile ahead so the load latency is never waited for
+  auto load_scale = [&](int t) -> uint16_t {
+    const int uu = unit_of_tile(p, t);
+    const int64_t tk = (int64_t)(t - p.tile_start[uu]) * kTcTile + tid;
+    return tk < p.b.u[uu].n ? p.b.index_scales[p.b.unit_row(uu) + tk] : (uint16_t)0;
+  };
+  uint16_t sc_pref = ntiles > 0 ? load_scale(t0) : (uint16_t)0;
+
   // state of the unit being scored, and of the tile whose epilogue is pending
   int cur_u = -1;
   float w[kIndexHeads];
@@ -387,8 +402,8 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
       cur_u = u;
     }
     const int64_t tok = tok_base + (int64_t)t * kTcTile + tid;  // this thread's token of tile t
-    const float sc = tok < n ? __half2float(__ushort_as_half(
-                                   p.b.index_scales[p.b.unit_row(u) + tok])) : 0.f;
+    const float sc = __half2float(__ushort_as_half(sc_pref));  // loaded one tile ago
+    if (i + 1 < ntiles) sc_pref = load_scale(t + 1);
 
     // codes of tile t have landed in stage i % kStages
     const int stage = i % kStages;
