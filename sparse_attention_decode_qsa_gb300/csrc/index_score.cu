@@ -22,10 +22,11 @@
 //    f16 value) into the A operand; reads are consecutive 16-byte chunks and
 //    the four K-steps of A sit 4 KiB + 32 B apart, so neither side has bank
 //    conflicts.  The B operand holds the index query split as q = hi + lo
-//    (hi = f16(q), lo = f16(q - hi)), so N = 16 columns: 8 heads x {hi, lo},
-//    which keeps the dot products at fp32 accuracy.
-//  * One thread issues four tcgen05.mma (K = 16 each) per tile into one of two
-//    16-column TMEM accumulators and commits them to an mbarrier; the
+//    (hi = f16(q), lo = f16(q - hi)) as two B operands of N = 16 rows (8 heads
+//    and 8 zero rows), which keeps the dot products at fp32 accuracy.
+//  * One thread issues eight tcgen05.mma per tile (K = 16 each; A . q_hi then
+//    A . q_lo accumulated into the same columns) into one of two 16-column
+//    TMEM accumulators and commits them to an mbarrier; the
 //    epilogue of the previous tile (tcgen05.ld, relu, head weights, scale,
 //    C4 max through shuffles; thread t = token t = TMEM lane t) overlaps them.
 //  * The grid is persistent (three CTAs per SM); CTA c takes a contiguous
@@ -168,14 +169,14 @@ constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per til
 constexpr int kAKStepBytes = kTcTile * 16 * 2;         // 4 KiB: one K-step of A
 constexpr int kAKStride = kAKStepBytes + 32;           // padded: spreads banks
 constexpr int kABufBytes = 4 * kAKStride;
-constexpr int kBBytes = 16 * kIndexDim * 2;            // 2 KiB
+constexpr int kBBytes = 16 * kIndexDim * 2;            // 2 KiB per B operand (hi, lo)
 constexpr int kBKStepBytes = 16 * 16 * 2;              // 512 B
 constexpr uint32_t kTmemCols = 32;                     // two 16-column accumulators
 constexpr int kCtasPerSm = QSA_K1_CTAS_PER_SM;
 constexpr int kOffRaw = 0;
 constexpr int kOffA = kOffRaw + kStages * kRawBytes;
 constexpr int kOffB = kOffA + 2 * kABufBytes;
-constexpr int kOffBar = kOffB + kBBytes;               // full[kStages], mma[2], tmem slot
+constexpr int kOffBar = kOffB + 2 * kBBytes;           // full[kStages], mma[2], tmem slot
 constexpr int kTcSmemBytes = kOffBar + 8 * (kStages + 2) + 16;
 // kind::f16 instruction descriptor: D f32 (bit 4), A = B = f16, both K-major,
 // N/8 at bits 17-22, M/16 at bits 24-28.
@@ -260,18 +261,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Four e4m3 codes (bytes of w, low first) -> two f16x2 words (exact).
@@ -323,8 +322,10 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
   const uint32_t tmem = *tmem_slot;
 
   // source and byte count of tile t (units are contiguous in the tile list)
+  int tu = ntiles > 0 ? unit_of_tile(p, t0) : 0;   // unit of the next tile to fetch
   auto tile_src = [&](int t, uint32_t& bytes) -> const uint8_t* {
-    const int u = unit_of_tile(p, t);
+    while (t >= p.tile_start[tu + 1]) ++tu;
+    const int u = tu;
     const int64_t tok0 = (int64_t)(t - p.tile_start[u]) * kTcTile;
     const int64_t left = p.b.u[u].n - tok0;
     bytes = (uint32_t)((left < kTcTile ? left : kTcTile) * kIndexDim);
@@ -340,10 +341,11 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
 
   // fp16 scale of this thread's token of tile t (0 past the end of its unit);
   // loaded a tile ahead so the load latency is never waited for
+  int su = ntiles > 0 ? unit_of_tile(p, t0) : 0;   // unit of the next scale to load
   auto load_scale = [&](int t) -> uint16_t {
-    const int uu = unit_of_tile(p, t);
-    const int64_t tk = (int64_t)(t - p.tile_start[uu]) * kTcTile + tid;
-    return tk < p.b.u[uu].n ? p.b.index_scales[p.b.unit_row(uu) + tk] : (uint16_t)0;
+    while (t >= p.tile_start[su + 1]) ++su;
+    const int64_t tk = (int64_t)(t - p.tile_start[su]) * kTcTile + tid;
+    return tk < p.b.u[su].n ? p.b.index_scales[p.b.unit_row(su) + tk] : (uint16_t)0;
   };
   uint16_t sc_pref = ntiles > 0 ? load_scale(t0) : (uint16_t)0;
 
@@ -364,14 +366,13 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
     const int b = pend_i & 1;
     ok &= mbar_wait(bar_mma + 8 * b, (uint32_t)(pend_i >> 1) & 1u, p.b.err, pend_i);
     tc_fence_after();
-    float v[16];
-    tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 16), v);
+    float v[8];
+    tc_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 16), v);
     float s = -INFINITY;
     if (pend_tok < pend_n) {
       s = 0.f;
 #pragma unroll
-      for (int h = 0; h < kIndexHeads; ++h)
-        s = fmaf(pend_w[h], fmaxf((v[h] + v[h + 8]) * pend_sc, 0.f), s);
+      for (int h = 0; h < kIndexHeads; ++h) s = fmaf(pend_w[h], fmaxf(v[h] * pend_sc, 0.f), s);
     }
     s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
     s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
@@ -379,10 +380,11 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
     pend = false;
   };
 
+  int u = ntiles > 0 ? unit_of_tile(p, t0) : 0;   // units are contiguous in the tile list
   for (int i = 0; i < ntiles; ++i) {
     if (!__syncthreads_and(ok)) break;
     const int t = t0 + i;
-    const int u = unit_of_tile(p, t);
+    while (t >= p.tile_start[u + 1]) ++u;
     if (u != cur_u) {
       if (pend) epilogue();  // the MMAs still reading B must finish first
       const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
@@ -392,7 +394,9 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
         const __half qh = __float2half_rn(qv);
         const __half ql = __float2half_rn(qv - __half2float(qh));
         *reinterpret_cast<__half*>(smem + kOffB + b_off(h, d)) = qh;
-        *reinterpret_cast<__half*>(smem + kOffB + b_off(h + 8, d)) = ql;
+        *reinterpret_cast<__half*>(smem + kOffB + kBBytes + b_off(h, d)) = ql;
+        *reinterpret_cast<__half*>(smem + kOffB + b_off(h + 8, d)) = __ushort_as_half(0);
+        *reinterpret_cast<__half*>(smem + kOffB + kBBytes + b_off(h + 8, d)) = __ushort_as_half(0);
       }
 #pragma unroll
       for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)u * kIndexHeads + h];
@@ -437,9 +441,13 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
       const uint32_t a0 = s_base + kOffA + (i & 1) * kABufBytes, b0 = s_base + kOffB;
       const uint32_t d = tmem + (uint32_t)((i & 1) * 16);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
+      for (int k = 0; k < 4; ++k)   // A . q_hi, then A . q_lo into the same columns
         tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
                    smem_desc(b0 + k * kBKStepBytes, 128, 256), k > 0 ? 1u : 0u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
+                   smem_desc(b0 + kBBytes + k * kBKStepBytes, 128, 256), 1u);
       tc_commit(bar_mma + 8 * (i & 1));
     }
     if (pend) epilogue();
