@@ -156,28 +156,38 @@ __global__ void __launch_bounds__(kThreads) index_score_kernel(const IndexScoreP
 
 #endif  // QSA_INDEX_SCORE_FFMA
 
-constexpr int kTcThreads = 128;
 constexpr int kTcTile = 128;                           // tokens per MMA tile (M)
 #ifndef QSA_K1_STAGES
-#define QSA_K1_STAGES 4
+#define QSA_K1_STAGES 5
 #endif
 #ifndef QSA_K1_CTAS_PER_SM
-#define QSA_K1_CTAS_PER_SM 3
+#define QSA_K1_CTAS_PER_SM 1
 #endif
-constexpr int kStages = QSA_K1_STAGES;                 // TMA ring depth
+// Warp roles of the persistent CTA.
+constexpr int kWarpTma = 0;                            // lane 0 streams codes with TMA
+constexpr int kWarpConv0 = 1;                          // warps 1..4 convert codes to f16
+constexpr int kWarpMma = 5;                            // builds B, lane 0 issues the MMAs
+constexpr int kWarpEpi0 = 6;                           // warps 6..9 read TMEM, score, store
+constexpr int kTcThreads = 10 * 32;
+constexpr int kStages = QSA_K1_STAGES;                 // code ring depth
+constexpr int kABufs = 2;                              // A operand ring
+constexpr int kDBufs = 4;                              // TMEM accumulator ring (16 columns each)
 constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per tile
 constexpr int kAKStepBytes = kTcTile * 16 * 2;         // 4 KiB: one K-step of A
 constexpr int kAKStride = kAKStepBytes + 32;           // padded: spreads banks
 constexpr int kABufBytes = 4 * kAKStride;
 constexpr int kBBytes = 16 * kIndexDim * 2;            // 2 KiB per B operand (hi, lo)
+constexpr int kBSlotBytes = 2 * kBBytes;               // one unit's B: hi then lo
 constexpr int kBKStepBytes = 16 * 16 * 2;              // 512 B
-constexpr uint32_t kTmemCols = 32;                     // two 16-column accumulators
+constexpr uint32_t kTmemCols = 16 * kDBufs;            // 64
 constexpr int kCtasPerSm = QSA_K1_CTAS_PER_SM;
 constexpr int kOffRaw = 0;
 constexpr int kOffA = kOffRaw + kStages * kRawBytes;
-constexpr int kOffB = kOffA + 2 * kABufBytes;
-constexpr int kOffBar = kOffB + 2 * kBBytes;           // full[kStages], mma[2], tmem slot
-constexpr int kTcSmemBytes = kOffBar + 8 * (kStages + 2) + 16;
+constexpr int kOffB = kOffA + kABufs * kABufBytes;
+constexpr int kOffBar = kOffB + 2 * kBSlotBytes;
+// barriers: raw_full[S], raw_empty[S], a_full[2], a_empty[2], d_full[4], d_empty[4]
+constexpr int kNumBars = 2 * kStages + 2 * kABufs + 2 * kDBufs;
+constexpr int kTcSmemBytes = kOffBar + 8 * kNumBars + 16;
 // kind::f16 instruction descriptor: D f32 (bit 4), A = B = f16, both K-major,
 // N/8 at bits 17-22, M/16 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
@@ -202,6 +212,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -290,13 +304,18 @@ __device__ __forceinline__ int unit_of_tile(const IndexScoreParams& p, int t) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexScoreParams p) {
+__global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const IndexScoreParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t s_base = smem_u32(smem);
-  const uint32_t bar_full = s_base + kOffBar;                 // + 8 * stage
-  const uint32_t bar_mma = s_base + kOffBar + 8 * kStages;    // + 8 * (tile & 1)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * (kStages + 2));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bars = sb + kOffBar;
+  auto raw_full = [&](int i) { return bars + 8u * (uint32_t)i; };
+  auto raw_empty = [&](int i) { return bars + 8u * (uint32_t)(kStages + i); };
+  auto a_full = [&](int i) { return bars + 8u * (uint32_t)(2 * kStages + i); };
+  auto a_empty = [&](int i) { return bars + 8u * (uint32_t)(2 * kStages + kABufs + i); };
+  auto d_full = [&](int i) { return bars + 8u * (uint32_t)(2 * kStages + 2 * kABufs + i); };
+  auto d_empty = [&](int i) { return bars + 8u * (uint32_t)(2 * kStages + 2 * kABufs + kDBufs + i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * kNumBars);
 
   // this CTA's contiguous range of the flat tile list
   const int total = p.tile_start[p.b.n_units];
@@ -304,16 +323,16 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
   const int t1 = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
   const int ntiles = t1 - t0;
 
-  if (warp == 0) {
+  if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)), "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(bar_full + 8 * s, 1);
-    mbar_init(bar_mma, 1);
-    mbar_init(bar_mma + 8, 1);
+    for (int i = 0; i < kStages; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), 128); }
+    for (int i = 0; i < kABufs; ++i) { mbar_init(a_full(i), 128); mbar_init(a_empty(i), 1); }
+    for (int i = 0; i < kDBufs; ++i) { mbar_init(d_full(i), 1); mbar_init(d_empty(i), 128); }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -321,150 +340,154 @@ __global__ void __launch_bounds__(kTcThreads) index_score_tc_kernel(const IndexS
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // source and byte count of tile t (units are contiguous in the tile list)
-  int tu = ntiles > 0 ? unit_of_tile(p, t0) : 0;   // unit of the next tile to fetch
-  auto tile_src = [&](int t, uint32_t& bytes) -> const uint8_t* {
-    while (t >= p.tile_start[tu + 1]) ++tu;
-    const int u = tu;
-    const int64_t tok0 = (int64_t)(t - p.tile_start[u]) * kTcTile;
-    const int64_t left = p.b.u[u].n - tok0;
-    bytes = (uint32_t)((left < kTcTile ? left : kTcTile) * kIndexDim);
-    return p.b.index_keys + (p.b.unit_row(u) + tok0) * kIndexDim;
-  };
-  if (tid == 0) {
-    for (int i = 0; i < kStages && i < ntiles; ++i) {
-      uint32_t bytes;
-      const uint8_t* src = tile_src(t0 + i, bytes);
-      tma_load_1d(s_base + kOffRaw + i * kRawBytes, src, bytes, bar_full + 8 * i);
+  if (warp == kWarpTma) {
+    // ---- producer: codes of each tile into the ring
+    if (lane == 0 && ntiles > 0) {
+      int u = unit_of_tile(p, t0);
+      for (int i = 0; i < ntiles; ++i) {
+        const int t = t0 + i, st = i % kStages;
+        if (i >= kStages && !mbar_wait(raw_empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, t))
+          break;
+        while (t >= p.tile_start[u + 1]) ++u;
+        const int64_t tok0 = (int64_t)(t - p.tile_start[u]) * kTcTile;
+        const int64_t left = p.b.u[u].n - tok0;
+        const uint32_t bytes = (uint32_t)((left < kTcTile ? left : kTcTile) * kIndexDim);
+        tma_load_1d(sb + kOffRaw + st * kRawBytes,
+                    p.b.index_keys + (p.b.unit_row(u) + tok0) * kIndexDim, bytes, raw_full(st));
+      }
+    }
+  } else if (warp < kWarpMma) {
+    // ---- converters: e4m3 codes -> f16 A operand (exact)
+    const int c = tid - 32 * kWarpConv0;  // 0..127
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % kStages, ab = i % kABufs;
+      if (!mbar_wait(raw_full(st), (uint32_t)(i / kStages) & 1u, p.b.err, t0 + i)) break;
+      const uint8_t* raw = smem + kOffRaw + st * kRawBytes;
+      uint4 q[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4*>(raw + (k * 128 + c) * 16);
+      mbar_arrive(raw_empty(st));
+      if (i >= kABufs && !mbar_wait(a_empty(ab), (uint32_t)(i / kABufs - 1) & 1u, p.b.err, t0 + i))
+        break;
+      uint8_t* A = smem + kOffA + ab * kABufBytes;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int lc = k * 128 + c;           // 16-byte chunk of the tile
+        const int row = lc >> 2, ks = lc & 3; // token row, K-step
+        uint32_t h[8];
+        e4m3x4_to_f16x4(q[k].x, h[0], h[1]);
+        e4m3x4_to_f16x4(q[k].y, h[2], h[3]);
+        e4m3x4_to_f16x4(q[k].z, h[4], h[5]);
+        e4m3x4_to_f16x4(q[k].w, h[6], h[7]);
+        uint8_t* dst = A + ks * kAKStride + (row >> 3) * 256 + (row & 7) * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + 128) = make_uint4(h[4], h[5], h[6], h[7]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(a_full(ab));
+    }
+  } else if (warp == kWarpMma) {
+    // ---- B operand per unit, and the MMAs
+    int u = ntiles > 0 ? unit_of_tile(p, t0) : 0;
+    int bu = -1, slot = 1;
+    bool ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      const int t = t0 + i;
+      while (t >= p.tile_start[u + 1]) ++u;
+      if (u != bu) {
+        // MMAs still reading the other slot's operand precede tile i
+        if (i >= 1)
+          ok = mbar_wait(d_full((i - 1) % kDBufs), (uint32_t)((i - 1) / kDBufs) & 1u, p.b.err, t);
+        slot ^= 1;
+        uint8_t* B = smem + kOffB + slot * kBSlotBytes;
+        const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
+        for (int e = lane; e < kIndexHeads * kIndexDim; e += 32) {
+          const int h = e >> 6, d = e & 63;
+          const float qv = qu[e];
+          const __half qh = __float2half_rn(qv);
+          const __half ql = __float2half_rn(qv - __half2float(qh));
+          *reinterpret_cast<__half*>(B + b_off(h, d)) = qh;
+          *reinterpret_cast<__half*>(B + kBBytes + b_off(h, d)) = ql;
+          *reinterpret_cast<__half*>(B + b_off(h + 8, d)) = __ushort_as_half(0);
+          *reinterpret_cast<__half*>(B + kBBytes + b_off(h + 8, d)) = __ushort_as_half(0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        bu = u;
+      }
+      if (lane == 0 && ok) {
+        const int ab = i % kABufs, db = i % kDBufs;
+        ok = mbar_wait(a_full(ab), (uint32_t)(i / kABufs) & 1u, p.b.err, t);
+        if (ok && i >= kDBufs)
+          ok = mbar_wait(d_empty(db), (uint32_t)(i / kDBufs - 1) & 1u, p.b.err, t);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t a0 = sb + kOffA + ab * kABufBytes;
+          const uint32_t b0 = sb + kOffB + slot * kBSlotBytes;
+          const uint32_t d = tmem + (uint32_t)(db * 16);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)   // A . q_hi, then A . q_lo into the same columns
+            tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
+                       smem_desc(b0 + k * kBKStepBytes, 128, 256), k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
+                       smem_desc(b0 + kBBytes + k * kBKStepBytes, 128, 256), 1u);
+          tc_commit(a_empty(ab));
+          tc_commit(d_full(db));
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    }
+  } else {
+    // ---- epilogue: TMEM lane quarter = warp % 4, token of the tile = TMEM lane
+    const int qtr = warp & 3;
+    const int e = qtr * 32 + lane;
+    int u = ntiles > 0 ? unit_of_tile(p, t0) : 0, su = u, cu = -1;
+    float w[kIndexHeads];
+    int64_t n = 0;
+    float* out = nullptr;
+    auto load_scale = [&](int t) -> uint16_t {
+      while (t >= p.tile_start[su + 1]) ++su;
+      const int64_t tk = (int64_t)(t - p.tile_start[su]) * kTcTile + e;
+      return tk < p.b.u[su].n ? p.b.index_scales[p.b.unit_row(su) + tk] : (uint16_t)0;
+    };
+    uint16_t sc_pref = ntiles > 0 ? load_scale(t0) : (uint16_t)0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int t = t0 + i, db = i % kDBufs;
+      while (t >= p.tile_start[u + 1]) ++u;
+      if (u != cu) {
+#pragma unroll
+        for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)u * kIndexHeads + h];
+        n = p.b.u[u].n;
+        out = p.blk + (int64_t)u * p.blk_stride;
+        cu = u;
+      }
+      const float sc = __half2float(__ushort_as_half(sc_pref));
+      if (i + 1 < ntiles) sc_pref = load_scale(t + 1);
+      if (!mbar_wait(d_full(db), (uint32_t)(i / kDBufs) & 1u, p.b.err, t)) break;
+      tc_fence_after();
+      float v[8];
+      tc_ld8(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)(db * 16), v);
+      tc_fence_before();
+      mbar_arrive(d_empty(db));
+      const int64_t tok = (int64_t)(t - p.tile_start[u]) * kTcTile + e;
+      float s = -INFINITY;
+      if (tok < n) {
+        s = 0.f;
+#pragma unroll
+        for (int h = 0; h < kIndexHeads; ++h) s = fmaf(w[h], fmaxf(v[h] * sc, 0.f), s);
+      }
+      s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
+      s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
+      if ((lane & 3) == 0 && tok < n) out[tok >> 2] = s;
     }
   }
 
-  // fp16 scale of this thread's token of tile t (0 past the end of its unit);
-  // loaded a tile ahead so the load latency is never waited for
-  int su = ntiles > 0 ? unit_of_tile(p, t0) : 0;   // unit of the next scale to load
-  auto load_scale = [&](int t) -> uint16_t {
-    while (t >= p.tile_start[su + 1]) ++su;
-    const int64_t tk = (int64_t)(t - p.tile_start[su]) * kTcTile + tid;
-    return tk < p.b.u[su].n ? p.b.index_scales[p.b.unit_row(su) + tk] : (uint16_t)0;
-  };
-  uint16_t sc_pref = ntiles > 0 ? load_scale(t0) : (uint16_t)0;
-
-  // state of the unit being scored, and of the tile whose epilogue is pending
-  int cur_u = -1;
-  float w[kIndexHeads];
-  int64_t n = 0, tok_base = 0;
-  float* out = nullptr;
-  bool pend = false;
-  int pend_i = 0;
-  int64_t pend_tok = 0, pend_n = 0;
-  float pend_sc = 0.f;
-  float* pend_out = nullptr;
-  float pend_w[kIndexHeads];
-  bool ok = true;
-
-  auto epilogue = [&]() {
-    const int b = pend_i & 1;
-    ok &= mbar_wait(bar_mma + 8 * b, (uint32_t)(pend_i >> 1) & 1u, p.b.err, pend_i);
-    tc_fence_after();
-    float v[8];
-    tc_ld8(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 16), v);
-    float s = -INFINITY;
-    if (pend_tok < pend_n) {
-      s = 0.f;
-#pragma unroll
-      for (int h = 0; h < kIndexHeads; ++h) s = fmaf(pend_w[h], fmaxf(v[h] * pend_sc, 0.f), s);
-    }
-    s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
-    s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
-    if ((lane & 3) == 0 && pend_tok < pend_n) pend_out[pend_tok >> 2] = s;
-    pend = false;
-  };
-
-  int u = ntiles > 0 ? unit_of_tile(p, t0) : 0;   // units are contiguous in the tile list
-  for (int i = 0; i < ntiles; ++i) {
-    if (!__syncthreads_and(ok)) break;
-    const int t = t0 + i;
-    while (t >= p.tile_start[u + 1]) ++u;
-    if (u != cur_u) {
-      if (pend) epilogue();  // the MMAs still reading B must finish first
-      const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
-      for (int e = tid; e < kIndexHeads * kIndexDim; e += kTcThreads) {
-        const int h = e >> 6, d = e & 63;
-        const float qv = qu[e];
-        const __half qh = __float2half_rn(qv);
-        const __half ql = __float2half_rn(qv - __half2float(qh));
-        *reinterpret_cast<__half*>(smem + kOffB + b_off(h, d)) = qh;
-        *reinterpret_cast<__half*>(smem + kOffB + kBBytes + b_off(h, d)) = ql;
-        *reinterpret_cast<__half*>(smem + kOffB + b_off(h + 8, d)) = __ushort_as_half(0);
-        *reinterpret_cast<__half*>(smem + kOffB + kBBytes + b_off(h + 8, d)) = __ushort_as_half(0);
-      }
-#pragma unroll
-      for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)u * kIndexHeads + h];
-      n = p.b.u[u].n;
-      tok_base = -(int64_t)p.tile_start[u] * kTcTile;
-      out = p.blk + (int64_t)u * p.blk_stride;
-      cur_u = u;
-    }
-    const int64_t tok = tok_base + (int64_t)t * kTcTile + tid;  // this thread's token of tile t
-    const float sc = __half2float(__ushort_as_half(sc_pref));  // loaded one tile ago
-    if (i + 1 < ntiles) sc_pref = load_scale(t + 1);
-
-    // codes of tile t have landed in stage i % kStages
-    const int stage = i % kStages;
-    ok &= mbar_wait(bar_full + 8 * stage, (uint32_t)(i / kStages) & 1u, p.b.err, t);
-    const uint8_t* raw = smem + kOffRaw + stage * kRawBytes;
-    uint8_t* A = smem + kOffA + (i & 1) * kABufBytes;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int lc = c * kTcThreads + tid;        // 16-byte chunk of the tile
-      const int row = lc >> 2, ks = lc & 3;       // token row, K-step
-      const uint4 q = *reinterpret_cast<const uint4*>(raw + lc * 16);
-      uint32_t h[8];
-      e4m3x4_to_f16x4(q.x, h[0], h[1]);
-      e4m3x4_to_f16x4(q.y, h[2], h[3]);
-      e4m3x4_to_f16x4(q.z, h[4], h[5]);
-      e4m3x4_to_f16x4(q.w, h[6], h[7]);
-      uint8_t* dst = A + ks * kAKStride + (row >> 3) * 256 + (row & 7) * 16;
-      *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(dst + 128) = make_uint4(h[4], h[5], h[6], h[7]);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      if (i + kStages < ntiles) {                 // every thread is done with this stage
-        uint32_t bytes;
-        const uint8_t* src = tile_src(t + kStages, bytes);
-        tma_load_1d(s_base + kOffRaw + stage * kRawBytes, src, bytes, bar_full + 8 * stage);
-      }
-      const uint32_t a0 = s_base + kOffA + (i & 1) * kABufBytes, b0 = s_base + kOffB;
-      const uint32_t d = tmem + (uint32_t)((i & 1) * 16);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)   // A . q_hi, then A . q_lo into the same columns
-        tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
-                   smem_desc(b0 + k * kBKStepBytes, 128, 256), k > 0 ? 1u : 0u);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
-                   smem_desc(b0 + kBBytes + k * kBKStepBytes, 128, 256), 1u);
-      tc_commit(bar_mma + 8 * (i & 1));
-    }
-    if (pend) epilogue();
-    pend = true;
-    pend_i = i;
-    pend_tok = tok;
-    pend_n = n;
-    pend_sc = sc;
-    pend_out = out;
-#pragma unroll
-    for (int h = 0; h < kIndexHeads; ++h) pend_w[h] = w[h];
-  }
-  if (__syncthreads_and(ok) && pend) epilogue();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0)
+  if (warp == kWarpMma)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
 }
