@@ -170,7 +170,10 @@ constexpr int kWarpMma = 5;                            // builds B, lane 0 issue
 constexpr int kWarpEpi0 = 6;                           // warps 6..9 read TMEM, score, store
 constexpr int kTcThreads = 10 * 32;
 constexpr int kStages = QSA_K1_STAGES;                 // code ring depth
-constexpr int kABufs = 2;                              // A operand ring
+#ifndef QSA_K1_ABUFS
+#define QSA_K1_ABUFS 2
+#endif
+constexpr int kABufs = QSA_K1_ABUFS;                   // A operand ring
 constexpr int kDBufs = 4;                              // TMEM accumulator ring (16 columns each)
 constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per tile
 constexpr int kAKStepBytes = kTcTile * 16 * 2;         // 4 KiB: one K-step of A
@@ -452,7 +455,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       const int64_t tk = (int64_t)(t - p.tile_start[su]) * kTcTile + e;
       return tk < p.b.u[su].n ? p.b.index_scales[p.b.unit_row(su) + tk] : (uint16_t)0;
     };
-    uint16_t sc_pref = ntiles > 0 ? load_scale(t0) : (uint16_t)0;
+    // scales are fetched three tiles ahead: the epilogue paces the whole
+    // ring, so it must never wait for DRAM
+    uint16_t sc0 = ntiles > 0 ? load_scale(t0) : (uint16_t)0;
+    uint16_t sc1 = ntiles > 1 ? load_scale(t0 + 1) : (uint16_t)0;
+    uint16_t sc2 = ntiles > 2 ? load_scale(t0 + 2) : (uint16_t)0;
     for (int i = 0; i < ntiles; ++i) {
       const int t = t0 + i, db = i % kDBufs;
       while (t >= p.tile_start[u + 1]) ++u;
@@ -463,8 +470,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
         out = p.blk + (int64_t)u * p.blk_stride;
         cu = u;
       }
-      const float sc = __half2float(__ushort_as_half(sc_pref));
-      if (i + 1 < ntiles) sc_pref = load_scale(t + 1);
+      const float sc = __half2float(__ushort_as_half(sc0));
+      sc0 = sc1;
+      sc1 = sc2;
+      if (i + 3 < ntiles) sc2 = load_scale(t + 3);
       if (!mbar_wait(d_full(db), (uint32_t)(i / kDBufs) & 1u, p.b.err, t)) break;
       tc_fence_after();
       float v[8];
