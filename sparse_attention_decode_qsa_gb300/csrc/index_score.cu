@@ -20,8 +20,7 @@
 //    completion counted in bytes on an mbarrier).
 //  * All 128 threads convert the codes exactly to f16 (every e4m3 value is an
 //    f16 value) into the A operand; reads are consecutive 16-byte chunks and
-//    the four K-steps of A sit 4 KiB + 32 B apart, so neither side has bank
-//    conflicts.  The B operand holds the index query split as q = hi + lo
+//    the swizzled layout spreads the stores over all banks.  The B operand holds the index query split as q = hi + lo
 //    (hi = f16(q), lo = f16(q - hi)) as two B operands of N = 16 rows (8 heads
 //    and 8 zero rows), which keeps the dot products at fp32 accuracy.
 //  * One thread issues eight tcgen05.mma per tile (K = 16 each; A . q_hi then
@@ -33,11 +32,11 @@
 //    range of the flat tile list of all units of the call and rebuilds B
 //    when its range crosses into the next unit.
 //
-// Operand layout: K-major without swizzle, made of core matrices of 8 rows x
-// 16 bytes (8 f16).  Within a K-step of 16, element (row, k) lies at
-// (row/8)*256 + (k/8)*128 + (row%8)*16 + (k%8)*2 bytes: the descriptor's
-// leading byte offset (next core matrix along K) is 128 and its stride byte
-// offset (next 8-row group) is 256.
+// Operand layout: K-major with the 128-byte swizzle.  A row (one token of A,
+// one head of B) is 64 f16 = 128 bytes; its 16-byte chunk c is stored at chunk
+// position c ^ (row % 8), so the tensor core reads whole 128-byte lines and
+// the converters' stores hit distinct banks.  The descriptor's stride byte
+// offset is 1024 (8 rows); K-step k starts 32*k bytes into the row.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -176,21 +175,20 @@ constexpr int kStages = QSA_K1_STAGES;                 // code ring depth
 constexpr int kABufs = QSA_K1_ABUFS;                   // A operand ring
 constexpr int kDBufs = 4;                              // TMEM accumulator ring (16 columns each)
 constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per tile
-constexpr int kAKStepBytes = kTcTile * 16 * 2;         // 4 KiB: one K-step of A
-constexpr int kAKStride = kAKStepBytes + 32;           // padded: spreads banks
-constexpr int kABufBytes = 4 * kAKStride;
-constexpr int kBBytes = 16 * kIndexDim * 2;            // 2 KiB per B operand (hi, lo)
+constexpr int kRowBytes128 = kIndexDim * 2;            // one f16 row of A or B: 128 B
+constexpr int kABufBytes = kTcTile * kRowBytes128;     // 16 KiB, 1024-aligned
+constexpr int kBBytes = 16 * kRowBytes128;             // 2 KiB per B operand (hi, lo)
 constexpr int kBSlotBytes = 2 * kBBytes;               // one unit's B: hi then lo
-constexpr int kBKStepBytes = 16 * 16 * 2;              // 512 B
 constexpr uint32_t kTmemCols = 16 * kDBufs;            // 64
 constexpr int kCtasPerSm = QSA_K1_CTAS_PER_SM;
 constexpr int kOffRaw = 0;
-constexpr int kOffA = kOffRaw + kStages * kRawBytes;
+constexpr int kOffA = kOffRaw + kStages * kRawBytes;   // multiple of 1024
 constexpr int kOffB = kOffA + kABufs * kABufBytes;
 constexpr int kOffBar = kOffB + 2 * kBSlotBytes;
 // barriers: raw_full[S], raw_empty[S], a_full[2], a_empty[2], d_full[4], d_empty[4]
 constexpr int kNumBars = 2 * kStages + 2 * kABufs + 2 * kDBufs;
-constexpr int kTcSmemBytes = kOffBar + 8 * kNumBars + 16;
+// + 1 KiB so the operand region can be aligned to 1024 bytes (128-byte swizzle)
+constexpr int kTcSmemBytes = kOffBar + 8 * kNumBars + 16 + 1024;
 // kind::f16 instruction descriptor: D f32 (bit 4), A = B = f16, both K-major,
 // N/8 at bits 17-22, M/16 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
@@ -200,17 +198,20 @@ __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
   return (uint32_t)__cvta_generic_to_shared(ptr);
 }
 
-// Byte offset of element (row, k) of the B operand (16 rows x 64 k).
-__device__ __forceinline__ uint32_t b_off(int row, int k) {
-  return (k >> 4) * kBKStepBytes + (row >> 3) * 256 + ((k >> 3) & 1) * 128 + (row & 7) * 16 +
-         (k & 7) * 2;
+// Byte offset of element (row, k) of a K-major operand with rows of 64 f16
+// (128 bytes) under the 128-byte swizzle: 16-byte chunk c of row r is stored
+// at chunk position c ^ (r % 8).
+__device__ __forceinline__ uint32_t sw128_off(int row, int k) {
+  return row * kRowBytes128 + ((((k >> 3) ^ row) & 7) << 4) + (k & 7) * 2;
 }
 
-// Shared-memory matrix descriptor: start address, leading and stride byte
-// offsets (all >> 4), descriptor version 1 at bit 46, no swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
-         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46);
+// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: start
+// address >> 4, leading byte offset 16 (unused by this layout), stride byte
+// offset 1024 (next group of 8 rows), version 1 at bit 46, layout type 2
+// (SWIZZLE_128B) at bits 61-63.  K-step k of 16 f16 starts 32*k bytes in.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -308,7 +309,9 @@ __device__ __forceinline__ int unit_of_tile(const IndexScoreParams& p, int t) {
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const IndexScoreParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the swizzled operands need 1024-byte alignment
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sb = smem_u32(smem);
   const uint32_t bars = sb + kOffBar;
@@ -375,16 +378,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       uint8_t* A = smem + kOffA + ab * kABufBytes;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int lc = k * 128 + c;           // 16-byte chunk of the tile
-        const int row = lc >> 2, ks = lc & 3; // token row, K-step
+        const int lc = k * 128 + c;           // 16-byte chunk of codes in the tile
+        const int row = lc >> 2, q16 = lc & 3; // token row, which 16 of its 64 codes
         uint32_t h[8];
         e4m3x4_to_f16x4(q[k].x, h[0], h[1]);
         e4m3x4_to_f16x4(q[k].y, h[2], h[3]);
         e4m3x4_to_f16x4(q[k].z, h[4], h[5]);
         e4m3x4_to_f16x4(q[k].w, h[6], h[7]);
-        uint8_t* dst = A + ks * kAKStride + (row >> 3) * 256 + (row & 7) * 16;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(dst + 128) = make_uint4(h[4], h[5], h[6], h[7]);
+        uint8_t* dst = A + row * kRowBytes128;   // f16 chunks 2*q16 and 2*q16+1, swizzled
+        *reinterpret_cast<uint4*>(dst + ((((2 * q16) ^ row) & 7) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + ((((2 * q16 + 1) ^ row) & 7) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(a_full(ab));
@@ -409,10 +412,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
           const float qv = qu[e];
           const __half qh = __float2half_rn(qv);
           const __half ql = __float2half_rn(qv - __half2float(qh));
-          *reinterpret_cast<__half*>(B + b_off(h, d)) = qh;
-          *reinterpret_cast<__half*>(B + kBBytes + b_off(h, d)) = ql;
-          *reinterpret_cast<__half*>(B + b_off(h + 8, d)) = __ushort_as_half(0);
-          *reinterpret_cast<__half*>(B + kBBytes + b_off(h + 8, d)) = __ushort_as_half(0);
+          *reinterpret_cast<__half*>(B + sw128_off(h, d)) = qh;
+          *reinterpret_cast<__half*>(B + kBBytes + sw128_off(h, d)) = ql;
+          *reinterpret_cast<__half*>(B + sw128_off(h + 8, d)) = __ushort_as_half(0);
+          *reinterpret_cast<__half*>(B + kBBytes + sw128_off(h + 8, d)) = __ushort_as_half(0);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -430,12 +433,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
           const uint32_t d = tmem + (uint32_t)(db * 16);
 #pragma unroll
           for (int k = 0; k < 4; ++k)   // A . q_hi, then A . q_lo into the same columns
-            tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
-                       smem_desc(b0 + k * kBKStepBytes, 128, 256), k > 0 ? 1u : 0u);
+            tc_mma_f16(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), k > 0 ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            tc_mma_f16(d, smem_desc(a0 + k * kAKStride, 128, 256),
-                       smem_desc(b0 + kBBytes + k * kBKStepBytes, 128, 256), 1u);
+            tc_mma_f16(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + kBBytes + 32 * k), 1u);
           tc_commit(a_empty(ab));
           tc_commit(d_full(db));
         }
@@ -443,7 +444,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     }
   } else {
-    // ---- epilogue: TMEM lane quarter = warp % 4, token of the tile = TMEM lane
+    // ---- epilogue (warps kWarpEpi0..kWarpEpi0+3): TMEM lane quarter = warp % 4,
+    // token of the tile = TMEM lane
+    static_assert(kWarpEpi0 == kWarpMma + 1 && kTcThreads == 32 * (kWarpEpi0 + 4), "warp roles");
     const int qtr = warp & 3;
     const int e = qtr * 32 + lane;
     int u = ntiles > 0 ? unit_of_tile(p, t0) : 0, su = u, cu = -1;
