@@ -13,24 +13,26 @@
 // The scan does 512 multiply-adds per 66 bytes, more than the CUDA cores
 // deliver at HBM speed, and it is a genuine dense contraction
 // (keys[tokens][64] x q^T[64][8 heads]), so it runs on the 5th-generation
-// tensor cores (tcgen05, accumulators in TMEM):
-//
-//  * Tiles of M = 128 tokens.  One thread streams each tile's 8 KiB of codes
-//    into a 4-stage shared-memory ring with TMA bulk copies (cp.async.bulk,
-//    completion counted in bytes on an mbarrier).
-//  * All 128 threads convert the codes exactly to f16 (every e4m3 value is an
-//    f16 value) into the A operand; reads are consecutive 16-byte chunks and
-//    the swizzled layout spreads the stores over all banks.  The B operand holds the index query split as q = hi + lo
-//    (hi = f16(q), lo = f16(q - hi)) as two B operands of N = 16 rows (8 heads
-//    and 8 zero rows), which keeps the dot products at fp32 accuracy.
-//  * One thread issues eight tcgen05.mma per tile (K = 16 each; A . q_hi then
-//    A . q_lo accumulated into the same columns) into one of two 16-column
-//    TMEM accumulators and commits them to an mbarrier; the
-//    epilogue of the previous tile (tcgen05.ld, relu, head weights, scale,
-//    C4 max through shuffles; thread t = token t = TMEM lane t) overlaps them.
-//  * The grid is persistent (three CTAs per SM); CTA c takes a contiguous
-//    range of the flat tile list of all units of the call and rebuilds B
-//    when its range crosses into the next unit.
+// tensor cores (tcgen05, accumulators in TMEM), in tiles of M = 128 tokens.
+// The grid is persistent (one CTA per SM); CTA c takes a contiguous range of
+// the flat tile list of all units of the call.  Its warps have fixed roles
+// and hand tiles to each other through mbarrier rings, so no role waits for
+// another's latency:
+//  * TMA warp (lane 0): streams each tile's 8 KiB of codes into a ring of
+//    shared-memory stages with bulk copies (cp.async.bulk; completion counted
+//    in bytes on the stage's mbarrier).
+//  * 4 converter warps: turn the codes into the f16 A operand (exact: every
+//    e4m3 value is an f16 value); consecutive 16-byte reads, conflict-free
+//    stores thanks to the swizzle below.
+//  * MMA warp: builds the B operand when the range enters a new unit - the
+//    index query split as q = hi + lo with hi = f16(q), lo = f16(q - hi), rows
+//    0-7 and 8-15 of an N = 16 operand, which keeps the dot products at fp32
+//    accuracy - and its lane 0 issues four tcgen05.mma per tile (K = 16 each)
+//    into one of four 16-column TMEM accumulators, committing to mbarriers
+//    that release the A buffer and publish the accumulator.
+//  * 2 x 4 epilogue warps (alternate tiles): tcgen05.ld of the tile's 16
+//    columns (thread t = token t = TMEM lane t), hi + lo, scale, relu, head
+//    weights, C4 max through shuffles, one fp32 per block to global memory.
 //
 // Operand layout: K-major with the 128-byte swizzle.  A row (one token of A,
 // one head of B) is 64 f16 = 128 bytes; its 16-byte chunk c is stored at chunk
@@ -166,8 +168,9 @@ constexpr int kTcTile = 128;                           // tokens per MMA tile (M
 constexpr int kWarpTma = 0;                            // lane 0 streams codes with TMA
 constexpr int kWarpConv0 = 1;                          // warps 1..4 convert codes to f16
 constexpr int kWarpMma = 5;                            // builds B, lane 0 issues the MMAs
-constexpr int kWarpEpi0 = 6;                           // warps 6..9 read TMEM, score, store
-constexpr int kTcThreads = 10 * 32;
+constexpr int kWarpEpi0 = 6;                           // warps 6.. read TMEM, score, store
+constexpr int kEpiGroups = 2;                          // epilogue groups take alternate tiles
+constexpr int kTcThreads = 32 * (kWarpEpi0 + 4 * kEpiGroups);
 constexpr int kStages = QSA_K1_STAGES;                 // code ring depth
 #ifndef QSA_K1_ABUFS
 #define QSA_K1_ABUFS 2
@@ -177,8 +180,8 @@ constexpr int kDBufs = 4;                              // TMEM accumulator ring 
 constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per tile
 constexpr int kRowBytes128 = kIndexDim * 2;            // one f16 row of A or B: 128 B
 constexpr int kABufBytes = kTcTile * kRowBytes128;     // 16 KiB, 1024-aligned
-constexpr int kBBytes = 16 * kRowBytes128;             // 2 KiB per B operand (hi, lo)
-constexpr int kBSlotBytes = 2 * kBBytes;               // one unit's B: hi then lo
+constexpr int kBBytes = 16 * kRowBytes128;             // 2 KiB: rows 0-7 q_hi, rows 8-15 q_lo
+constexpr int kBSlotBytes = kBBytes;                   // one unit's B
 constexpr uint32_t kTmemCols = 16 * kDBufs;            // 64
 constexpr int kCtasPerSm = QSA_K1_CTAS_PER_SM;
 constexpr int kOffRaw = 0;
@@ -279,16 +282,18 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr)
-               : "memory");
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Four e4m3 codes (bytes of w, low first) -> two f16x2 words (exact).
@@ -413,9 +418,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
           const __half qh = __float2half_rn(qv);
           const __half ql = __float2half_rn(qv - __half2float(qh));
           *reinterpret_cast<__half*>(B + sw128_off(h, d)) = qh;
-          *reinterpret_cast<__half*>(B + kBBytes + sw128_off(h, d)) = ql;
-          *reinterpret_cast<__half*>(B + sw128_off(h + 8, d)) = __ushort_as_half(0);
-          *reinterpret_cast<__half*>(B + kBBytes + sw128_off(h + 8, d)) = __ushort_as_half(0);
+          *reinterpret_cast<__half*>(B + sw128_off(h + 8, d)) = ql;
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -432,11 +435,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
           const uint32_t b0 = sb + kOffB + slot * kBSlotBytes;
           const uint32_t d = tmem + (uint32_t)(db * 16);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)   // A . q_hi, then A . q_lo into the same columns
+          for (int k = 0; k < 4; ++k)   // columns 0-7: A . q_hi, columns 8-15: A . q_lo
             tc_mma_f16(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), k > 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tc_mma_f16(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + kBBytes + 32 * k), 1u);
           tc_commit(a_empty(ab));
           tc_commit(d_full(db));
         }
@@ -444,51 +444,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     }
   } else {
-    // ---- epilogue (warps kWarpEpi0..kWarpEpi0+3): TMEM lane quarter = warp % 4,
-    // token of the tile = TMEM lane
-    static_assert(kWarpEpi0 == kWarpMma + 1 && kTcThreads == 32 * (kWarpEpi0 + 4), "warp roles");
+    // ---- epilogue: kEpiGroups groups of 4 warps; group g scores tiles
+    // i = g, g + kEpiGroups, ...  TMEM lane quarter = warp % 4, and the token
+    // of the tile = TMEM lane.  Unit state is cached and refreshed only when a
+    // tile crosses into the next unit.
+    static_assert(kWarpEpi0 == kWarpMma + 1, "warp roles");
+    const int grp = (warp - kWarpEpi0) >> 2;
     const int qtr = warp & 3;
     const int e = qtr * 32 + lane;
-    int u = ntiles > 0 ? unit_of_tile(p, t0) : 0, su = u, cu = -1;
-    float w[kIndexHeads];
+    int te = -1, ts = 0;               // tile range [ts, te) of the cached unit
     int64_t n = 0;
     float* out = nullptr;
-    auto load_scale = [&](int t) -> uint16_t {
-      while (t >= p.tile_start[su + 1]) ++su;
-      const int64_t tk = (int64_t)(t - p.tile_start[su]) * kTcTile + e;
-      return tk < p.b.u[su].n ? p.b.index_scales[p.b.unit_row(su) + tk] : (uint16_t)0;
+    float w[kIndexHeads];
+    int ste = -1, sts = 0;             // same for the scale cursor
+    int64_t sn = 0;
+    const uint16_t* sp = nullptr;
+    auto scale_of = [&](int t) -> uint16_t {
+      if (t >= ste) {
+        const int su = unit_of_tile(p, t);
+        sts = p.tile_start[su];
+        ste = p.tile_start[su + 1];
+        sn = p.b.u[su].n;
+        sp = p.b.index_scales + p.b.unit_row(su);
+      }
+      const int64_t tk = (int64_t)(t - sts) * kTcTile + e;
+      return tk < sn ? sp[tk] : (uint16_t)0;
     };
-    // scales are fetched three tiles ahead: the epilogue paces the whole
-    // ring, so it must never wait for DRAM
-    uint16_t sc0 = ntiles > 0 ? load_scale(t0) : (uint16_t)0;
-    uint16_t sc1 = ntiles > 1 ? load_scale(t0 + 1) : (uint16_t)0;
-    uint16_t sc2 = ntiles > 2 ? load_scale(t0 + 2) : (uint16_t)0;
-    for (int i = 0; i < ntiles; ++i) {
+    constexpr int G = kEpiGroups;
+    uint16_t scA = grp < ntiles ? scale_of(t0 + grp) : (uint16_t)0;
+    uint16_t scB = grp + G < ntiles ? scale_of(t0 + grp + G) : (uint16_t)0;
+    for (int i = grp; i < ntiles; i += G) {
       const int t = t0 + i, db = i % kDBufs;
-      while (t >= p.tile_start[u + 1]) ++u;
-      if (u != cu) {
-#pragma unroll
-        for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)u * kIndexHeads + h];
+      if (t >= te) {
+        const int u = unit_of_tile(p, t);
+        ts = p.tile_start[u];
+        te = p.tile_start[u + 1];
         n = p.b.u[u].n;
         out = p.blk + (int64_t)u * p.blk_stride;
-        cu = u;
+#pragma unroll
+        for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)u * kIndexHeads + h];
       }
-      const float sc = __half2float(__ushort_as_half(sc0));
-      sc0 = sc1;
-      sc1 = sc2;
-      if (i + 3 < ntiles) sc2 = load_scale(t + 3);
+      const float sc = __half2float(__ushort_as_half(scA));
+      scA = scB;
+      if (i + 2 * G < ntiles) scB = scale_of(t + 2 * G);
       if (!mbar_wait(d_full(db), (uint32_t)(i / kDBufs) & 1u, p.b.err, t)) break;
       tc_fence_after();
-      float v[8];
-      tc_ld8(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)(db * 16), v);
+      float v[16];
+      tc_ld16(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)(db * 16), v);
       tc_fence_before();
       mbar_arrive(d_empty(db));
-      const int64_t tok = (int64_t)(t - p.tile_start[u]) * kTcTile + e;
+      const int64_t tok = (int64_t)(t - ts) * kTcTile + e;
       float s = -INFINITY;
       if (tok < n) {
         s = 0.f;
 #pragma unroll
-        for (int h = 0; h < kIndexHeads; ++h) s = fmaf(w[h], fmaxf(v[h] * sc, 0.f), s);
+        for (int h = 0; h < kIndexHeads; ++h) s = fmaf(w[h], fmaxf((v[h] + v[h + 8]) * sc, 0.f), s);
       }
       s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
       s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
