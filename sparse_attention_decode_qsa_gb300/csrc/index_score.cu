@@ -14,7 +14,7 @@
 // deliver at HBM speed, and it is a genuine dense contraction
 // (keys[tokens][64] x q^T[64][8 heads]), so it runs on the 5th-generation
 // tensor cores (tcgen05, accumulators in TMEM), in tiles of M = 128 tokens.
-// The grid is persistent (one CTA per SM); CTA c takes a contiguous range of
+// The grid is persistent (two CTAs per SM); CTA c takes a contiguous range of
 // the flat tile list of all units of the call.  Its warps have fixed roles
 // and hand tiles to each other through mbarrier rings, so no role waits for
 // another's latency:
@@ -162,7 +162,7 @@ constexpr int kTcTile = 128;                           // tokens per MMA tile (M
 #define QSA_K1_STAGES 5
 #endif
 #ifndef QSA_K1_CTAS_PER_SM
-#define QSA_K1_CTAS_PER_SM 1
+#define QSA_K1_CTAS_PER_SM 2
 #endif
 // Warp roles of the persistent CTA.
 constexpr int kWarpTma = 0;                            // lane 0 streams codes with TMA
@@ -354,17 +354,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
   if (warp == kWarpTma) {
     // ---- producer: codes of each tile into the ring
     if (lane == 0 && ntiles > 0) {
-      int u = unit_of_tile(p, t0);
+      int ts = 0, te = -1;
+      int64_t n = 0;
+      const uint8_t* keys = nullptr;
       for (int i = 0; i < ntiles; ++i) {
         const int t = t0 + i, st = i % kStages;
         if (i >= kStages && !mbar_wait(raw_empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, t))
           break;
-        while (t >= p.tile_start[u + 1]) ++u;
-        const int64_t tok0 = (int64_t)(t - p.tile_start[u]) * kTcTile;
-        const int64_t left = p.b.u[u].n - tok0;
+        if (t >= te) {
+          const int u = unit_of_tile(p, t);
+          ts = p.tile_start[u];
+          te = p.tile_start[u + 1];
+          n = p.b.u[u].n;
+          keys = p.b.index_keys + p.b.unit_row(u) * kIndexDim;
+        }
+        const int64_t tok0 = (int64_t)(t - ts) * kTcTile;
+        const int64_t left = n - tok0;
         const uint32_t bytes = (uint32_t)((left < kTcTile ? left : kTcTile) * kIndexDim);
-        tma_load_1d(sb + kOffRaw + st * kRawBytes,
-                    p.b.index_keys + (p.b.unit_row(u) + tok0) * kIndexDim, bytes, raw_full(st));
+        tma_load_1d(sb + kOffRaw + st * kRawBytes, keys + tok0 * kIndexDim, bytes, raw_full(st));
       }
     }
   } else if (warp < kWarpMma) {
@@ -398,17 +405,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       mbar_arrive(a_full(ab));
     }
   } else if (warp == kWarpMma) {
-    // ---- B operand per unit, and the MMAs
+    // ---- B operand per unit (whole warp, only when the range enters a new
+    // unit), and the MMAs (lane 0 alone, no per-tile warp traffic)
     int u = ntiles > 0 ? unit_of_tile(p, t0) : 0;
+    int te = p.tile_start[u + 1];
     int bu = -1, slot = 1;
     bool ok = true;
-    for (int i = 0; i < ntiles && ok; ++i) {
+    for (int i = 0; i < ntiles; ++i) {
       const int t = t0 + i;
-      while (t >= p.tile_start[u + 1]) ++u;
+      if (t >= te) {
+        u = unit_of_tile(p, t);
+        te = p.tile_start[u + 1];
+      }
       if (u != bu) {
+        __syncwarp();
         // MMAs still reading the other slot's operand precede tile i
         if (i >= 1)
-          ok = mbar_wait(d_full((i - 1) % kDBufs), (uint32_t)((i - 1) / kDBufs) & 1u, p.b.err, t);
+          ok = ok && mbar_wait(d_full((i - 1) % kDBufs), (uint32_t)((i - 1) / kDBufs) & 1u, p.b.err, t);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
         slot ^= 1;
         uint8_t* B = smem + kOffB + slot * kBSlotBytes;
         const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
@@ -441,8 +455,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
           tc_commit(d_full(db));
         }
       }
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     }
+    __syncwarp();
   } else {
     // ---- epilogue: kEpiGroups groups of 4 warps; group g scores tiles
     // i = g, g + kEpiGroups, ...  TMEM lane quarter = warp % 4, and the token
