@@ -3,7 +3,7 @@
 // потери скорости декодирования", section "Механизм гибридного разреженного
 // оффлоадинга": attention reads only the <= indexer_budget selected rows).
 //
-// Split-K flash-decode.  A split is 8 selected C4 blocks, i.e. 32 token
+// Split-K flash-decode.  A split is 4 selected C4 blocks, i.e. 16 token
 // rows.  Rows are read through the slot table (pool rows from HBM, cold rows
 // zero-copy from mapped pinned host memory) or from a dense gathered buffer.
 //
@@ -17,9 +17,10 @@
 // stay free for HBM-bound work of other requests on other streams.
 //
 // Inside a CTA the 8 warps work independently: warp w serves KV head
-// g = w % 4 (its 4 query heads) for tokens 16*(w/4) .. 16*(w/4)+15 of every
-// split.  A warp copies only its KV head's 512 bytes of each of its 16 rows
-// (K[g] then V[g]) with cp.async into its own double buffer, so no CTA-wide
+// g = w % 4 (its 4 query heads) for tokens 8*(w/4) .. 8*(w/4)+7 of every
+// split.  A warp copies only its KV head's 512 bytes of each of its 8 rows
+// (K[g] then V[g]) with cp.async into its own double buffer (64 KiB per CTA,
+// small enough to share an SM with the index-score CTAs), so no CTA-wide
 // barrier is needed while streaming; it keeps a running online-softmax state
 // (max, sum, acc) for its 4 heads over all its tokens.  At the end the two
 // token halves of each KV head are merged in shared memory and the CTA writes
@@ -29,7 +30,7 @@
 // Per warp and split: logits with lane l holding dims 4l..4l+3 of the 4 query
 // heads, reduced across the warp with a transposing butterfly (6 shuffles
 // for 4 values); after it the lanes 8j..8j+7 hold head j, lane 8j+k keeping
-// tokens k and k+8.  Softmax statistics are reduced over those 8 lanes; P.V
+// token k.  Softmax statistics are reduced over those 8 lanes; P.V
 // broadcasts each token's 4 probabilities with shuffles and accumulates dims
 // 4l..4l+3.  Plain FMAs throughout: 4 query heads per KV head make this a
 // 4-row contraction, not a tensor-core shape.
@@ -42,10 +43,11 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kWarpTokens = 16;                       // tokens per warp and split
+constexpr int kBlocksPerSplit = 4;                    // selected C4 blocks per split
+constexpr int kWarpTokens = 8;                        // tokens per warp and split
 constexpr int kSliceBytes = 2 * kHeadDim * 2;         // K[g] + V[g] of one token: 512
-constexpr int kWarpBufBytes = kWarpTokens * kSliceBytes;  // 8 KiB
-constexpr int kSmemBytes = kWarps * 2 * kWarpBufBytes;    // 128 KiB
+constexpr int kWarpBufBytes = kWarpTokens * kSliceBytes;  // 4 KiB
+constexpr int kSmemBytes = kWarps * 2 * kWarpBufBytes;    // 64 KiB: fits beside other CTAs
 #ifndef QSA_ATTN_HOST_CTAS
 #define QSA_ATTN_HOST_CTAS 64
 #endif
@@ -91,8 +93,8 @@ __device__ __forceinline__ int visit_split(int k, int count, int r, int cpu) {
   return r + idx * cpu;
 }
 
-// Copy this warp's 16 token slices (K[g], V[g]) of `split` into buf.  Lane l
-// resolves token l (l < 16); every lane then copies 16 bytes of each slice.
+// Copy this warp's 8 token slices (K[g], V[g]) of `split` into buf.  Lane l
+// resolves token l (l < 8); every lane then copies 16 bytes of each slice.
 // Returns a bitmask of the tokens that exist.
 __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int split, int nsel,
                                                int g, int half, uint8_t* buf) {
@@ -101,7 +103,7 @@ __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int s
   const uint8_t* src = nullptr;
   if (lane < kWarpTokens) {
     const int tok = half * kWarpTokens + lane;              // token within the split
-    const int j = split * kAttnBlocksPerSplit + tok / 4;    // selected-block index
+    const int j = split * kBlocksPerSplit + tok / 4;        // selected-block index
     if (j < nsel) {
       const int64_t b = p.sel[(int64_t)u * p.k_max + j];
       const int64_t t = 4 * b + (tok & 3);
@@ -113,7 +115,7 @@ __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int s
       }
     }
   }
-  const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & 0xFFFFu;
+  const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & ((1u << kWarpTokens) - 1u);
   // lanes 0..15 copy K[g] (chunks of 16 B), lanes 16..31 copy V[g]
   const int off = (lane < 16) ? g * kHeadDim * 2 + lane * 16
                               : kKvHeads * kHeadDim * 2 + g * kHeadDim * 2 + (lane - 16) * 16;
@@ -127,7 +129,7 @@ __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int s
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];  // [warp][2][16][512]
+  extern __shared__ __align__(16) uint8_t smem[];  // [warp][2][8][512]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParam
     if (r == 0 && threadIdx.x == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
     nsel = 0;
   }
-  const int splits = (nsel + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit;
+  const int splits = (nsel + kBlocksPerSplit - 1) / kBlocksPerSplit;
   const int count = r < splits ? (splits - 1 - r) / p.cpu + 1 : 0;
 
   // query dims 4l..4l+3 of the 4 heads of KV head g, pre-scaled to base 2
@@ -176,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParam
     __syncwarp();
     const uint8_t* R = wbuf + buf * kWarpBufBytes;
 
-    // logits: lane 8j+kk ends with tokens kk and kk+8 of head j
-    float x0 = -INFINITY, x1 = -INFINITY;
+    // logits: lane 8j+kk ends with token kk of head j
+    float x0 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kWarpTokens; ++i) {
       const uint2 kk = *reinterpret_cast<const uint2*>(R + i * kSliceBytes + lane * 8);
@@ -198,22 +200,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParam
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-      if ((lane & 7) == (i & 7)) {
-        const float x = ((valid_cur >> i) & 1u) ? v : -INFINITY;
-        if (i < 8) x0 = x; else x1 = x;
-      }
+      if ((lane & 7) == i) x0 = ((valid_cur >> i) & 1u) ? v : -INFINITY;
     }
 
-    // online softmax of head hj over its 16 tokens of this split
-    float ms = fmaxf(x0, x1);
+    // online softmax of head hj over its 8 tokens of this split
+    float ms = x0;
     ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 1));
     ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 2));
     ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 4));
     const float m_new = fmaxf(m_run, ms);
     const float so = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);  // old-state scale
     const float p0 = (x0 == -INFINITY) ? 0.f : exp2f(x0 - m_new);
-    const float p1 = (x1 == -INFINITY) ? 0.f : exp2f(x1 - m_new);
-    float ps = p0 + p1;
+    float ps = p0;
     ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
     ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
     ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 4);
@@ -230,10 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParam
     for (int i = 0; i < kWarpTokens; ++i) {
       const uint2 vv = *reinterpret_cast<const uint2*>(R + i * kSliceBytes + kHeadDim * 2 + lane * 8);
       const float v0 = bf16_lo(vv.x), v1 = bf16_hi(vv.x), v2 = bf16_lo(vv.y), v3 = bf16_hi(vv.y);
-      const float mine = i < 8 ? p0 : p1;
 #pragma unroll
       for (int j = 0; j < kGroup; ++j) {
-        const float pj = __shfl_sync(0xFFFFFFFFu, mine, 8 * j + (i & 7));
+        const float pj = __shfl_sync(0xFFFFFFFFu, p0, 8 * j + i);
         acc[j][0] = fmaf(pj, v0, acc[j][0]);
         acc[j][1] = fmaf(pj, v1, acc[j][1]);
         acc[j][2] = fmaf(pj, v2, acc[j][2]);
@@ -330,11 +327,12 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
   bool any_host = false;
   if (gathered == nullptr)
     for (int u = 0; u < b.n_units; ++u) any_host |= b.u[u].host_rows != nullptr;
-  const int splits = (p.k_max + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit;
+  const int splits = (p.k_max + kBlocksPerSplit - 1) / kBlocksPerSplit;
   const int cap = any_host ? kMaxCtasHost : sm_count;
   int cpu = cap / b.n_units;
   if (cpu < 1) cpu = 1;
   if (cpu > splits) cpu = splits;
+  if (cpu > b.splits_max) cpu = b.splits_max;   // partial slots in the workspace
   p.cpu = cpu;
   attn_split_kernel<<<b.n_units * cpu, kThreads, kSmemBytes, s>>>(p);
   cudaError_t e = cudaGetLastError();
