@@ -176,8 +176,9 @@ typedef struct qsa_cache qsa_cache;
 int32_t qsa_abi_version(void);
 const char* qsa_last_error_string(void);
 
-/* Bytes of device workspace a cache with this config needs (error word plus
- * split-K partials of every request x layer).  Returns -1 on a bad config. */
+/* Bytes of device workspace a cache with this config needs (error word,
+ * split-K partials of every request x layer, and two int32 work counters per
+ * request x layer for qsa_index_score).  Returns -1 on a bad config. */
 int64_t qsa_workspace_bytes(const qsa_cache_config* config);
 
 /* Create a cache.  Checks the config; with device storage, also zeroes the
@@ -253,7 +254,11 @@ qsa_status_t qsa_poll_error(qsa_cache* cache, void* stream, int32_t* dev_status,
  * opening explanation: C4 blocks of 4 adjacent tokens.]
  * q_idx: device fp32 [units][8][64]; w: device fp32 [units][8];
  * blk_scores: device fp32 [units][blk_stride], blk_stride >= ceil(ctx/4) of
- * every unit.  Errors: INVALID_ARG, STALE_HANDLE, NO_DEVICE, CUDA. */
+ * every unit.  The CTAs take 128-token tiles from a work counter in the
+ * workspace that belongs to the batch's first unit (its request and layer)
+ * and reset it when the last CTA ends: two calls that overlap on the GPU and
+ * share their first unit race.
+ * Errors: INVALID_ARG, STALE_HANDLE, NO_DEVICE, CUDA. */
 qsa_status_t qsa_index_score(qsa_cache* cache, const qsa_batch* batch,
                              const float* q_idx, const float* w,
                              float* blk_scores, int64_t blk_stride, void* stream);

@@ -140,6 +140,14 @@ cudaError_t launch_gather_rows(const BatchDesc& b, const int32_t* sel_blocks,
   p.budget_tokens = budget_tokens;
   p.out = rows_out;
   p.n_rows = n_rows;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        gather_rows_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+        cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   dim3 grid((p.k_max + kGatherBlocks - 1) / kGatherBlocks, b.n_units);
   gather_rows_kernel<<<grid, kGatherThreads, 0, s>>>(p);
   return cudaGetLastError();

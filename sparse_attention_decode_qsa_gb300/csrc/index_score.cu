@@ -14,17 +14,22 @@
 // deliver at HBM speed, and it is a genuine dense contraction
 // (keys[tokens][64] x q^T[64][8 heads]), so it runs on the 5th-generation
 // tensor cores (tcgen05, accumulators in TMEM), in tiles of M = 128 tokens.
-// The grid is persistent (two CTAs per SM); CTA c takes a contiguous range of
-// the flat tile list of all units of the call.  Its warps have fixed roles
-// and hand tiles to each other through mbarrier rings, so no role waits for
-// another's latency:
-//  * TMA warp (lane 0): streams each tile's 8 KiB of codes into a ring of
-//    shared-memory stages with bulk copies (cp.async.bulk; completion counted
-//    in bytes on the stage's mbarrier).
+// The grid is persistent (up to two CTAs per SM) and the work is handed out
+// dynamically: CTAs take chunks of the flat tile list of all units of the
+// call from an atomic counter, large chunks first and single tiles at the
+// end.  A CTA that starts late (its SM busy with another kernel, e.g. the
+// attention of other requests on another stream) then simply takes less work
+// instead of holding up the whole call with a fixed share.  The last CTA to
+// finish re-arms the counter.  Its warps have fixed roles and hand tiles to
+// each other through mbarrier rings, so no role waits for another's latency:
+//  * TMA warp (lane 0): takes the chunks, streams each tile's 8 KiB of codes
+//    into a ring of shared-memory stages with bulk copies (cp.async.bulk;
+//    completion counted in bytes on the stage's mbarrier) and publishes the
+//    tile's id in a ring read by the MMA warp and the epilogue.
 //  * 4 converter warps: turn the codes into the f16 A operand (exact: every
 //    e4m3 value is an f16 value); consecutive 16-byte reads, conflict-free
 //    stores thanks to the swizzle below.
-//  * MMA warp: builds the B operand when the range enters a new unit - the
+//  * MMA warp: builds the B operand when the stream enters a new unit - the
 //    index query split as q = hi + lo with hi = f16(q), lo = f16(q - hi), rows
 //    0-7 and 8-15 of an N = 16 operand, which keeps the dot products at fp32
 //    accuracy - and its lane 0 issues four tcgen05.mma per tile (K = 16 each)
@@ -159,10 +164,15 @@ __global__ void __launch_bounds__(kThreads) index_score_kernel(const IndexScoreP
 
 constexpr int kTcTile = 128;                           // tokens per MMA tile (M)
 #ifndef QSA_K1_STAGES
-#define QSA_K1_STAGES 5
+#define QSA_K1_STAGES 4
 #endif
 #ifndef QSA_K1_CTAS_PER_SM
 #define QSA_K1_CTAS_PER_SM 2
+#endif
+// Register budget per thread: two CTAs at 48 (43 K registers) leave room on
+// the SM for one attention CTA.
+#ifndef QSA_K1_MAXREG
+#define QSA_K1_MAXREG 48
 #endif
 // Warp roles of the persistent CTA.
 constexpr int kWarpTma = 0;                            // lane 0 streams codes with TMA
@@ -177,6 +187,8 @@ constexpr int kStages = QSA_K1_STAGES;                 // code ring depth
 #endif
 constexpr int kABufs = QSA_K1_ABUFS;                   // A operand ring
 constexpr int kDBufs = 4;                              // TMEM accumulator ring (16 columns each)
+constexpr int kIdRing = 16;                            // tile-id ring (producer -> epilogue)
+constexpr int kIdReaders = 4;                          // the owning group's 4 warps
 constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per tile
 constexpr int kRowBytes128 = kIndexDim * 2;            // one f16 row of A or B: 128 B
 constexpr int kABufBytes = kTcTile * kRowBytes128;     // 16 KiB, 1024-aligned
@@ -188,14 +200,31 @@ constexpr int kOffRaw = 0;
 constexpr int kOffA = kOffRaw + kStages * kRawBytes;   // multiple of 1024
 constexpr int kOffB = kOffA + kABufs * kABufBytes;
 constexpr int kOffBar = kOffB + 2 * kBSlotBytes;
-// barriers: raw_full[S], raw_empty[S], a_full[2], a_empty[2], d_full[4], d_empty[4]
-constexpr int kNumBars = 2 * kStages + 2 * kABufs + 2 * kDBufs;
+// barriers: raw_full[S], raw_empty[S], a_full[A], a_empty[A], d_full[D],
+// d_empty[D], id_full[R], id_empty[R], b_full[2], b_empty[2]
+constexpr int kNumBars = 2 * kStages + 2 * kABufs + 2 * kDBufs + 2 * kIdRing + 4;
+constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+constexpr int kOffStageMeta = kOffTmemSlot + 16;       // int32 [kStages]: run of each stage
+constexpr int kOffAMeta = kOffStageMeta + 4 * kStages; // int32 [kABufs]: run of each A buffer
+constexpr int kOffIdRing = kOffAMeta + 4 * kABufs;     // int32 [kIdRing]
 // + 1 KiB so the operand region can be aligned to 1024 bytes (128-byte swizzle)
-constexpr int kTcSmemBytes = kOffBar + 8 * kNumBars + 16 + 1024;
+constexpr int kTcSmemBytes = kOffIdRing + 4 * kIdRing + 1024;
 // kind::f16 instruction descriptor: D f32 (bit 4), A = B = f16, both K-major,
 // N/8 at bits 17-22, M/16 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kWaitPolls = 1u << 20;              // bounded mbarrier waits
+// Guided chunks: a grab takes 1/kChunkDiv of the unit's remaining tiles per
+// CTA sharing it, at most kChunkMax.
+#ifndef QSA_K1_CHUNK_DIV
+#define QSA_K1_CHUNK_DIV 4
+#endif
+#ifndef QSA_K1_CHUNK_MAX
+#define QSA_K1_CHUNK_MAX 16
+#endif
+constexpr int kChunkDiv = QSA_K1_CHUNK_DIV;
+constexpr int kChunkMax = QSA_K1_CHUNK_MAX;
+constexpr int kEndOfWork = -1;                         // tile id that ends a role's loop
+constexpr int kWaitFailed = -2;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
   return (uint32_t)__cvta_generic_to_shared(ptr);
@@ -313,26 +342,55 @@ __device__ __forceinline__ int unit_of_tile(const IndexScoreParams& p, int t) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const IndexScoreParams p) {
+// Work counter of unit u for the current call (the workspace keeps two
+// int32 per request x layer; the first counts the unit's tiles handed out).
+__device__ __forceinline__ int32_t* unit_counter(const BatchDesc& b, int u) {
+  return b.tickets + 2 * ((int64_t)b.u[u].req * b.n_layers + b.u[u].layer);
+}
+
+__device__ __forceinline__ int ld_relaxed_gpu(const int32_t* ptr) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// Tile range [ts, te) of the unit that holds tile t, cached between calls.
+struct UnitCursor {
+  int u = -1, ts = 0, te = 0;
+  __device__ __forceinline__ bool move_to(const IndexScoreParams& p, int t) {
+    if (t >= ts && t < te) return false;
+    u = unit_of_tile(p, t);
+    ts = p.tile_start[u];
+    te = p.tile_start[u + 1];
+    return true;
+  }
+};
+
+__global__ void __maxnreg__(QSA_K1_MAXREG)
+index_score_tc_kernel(const IndexScoreParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the swizzled operands need 1024-byte alignment
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sb = smem_u32(smem);
   const uint32_t bars = sb + kOffBar;
+  constexpr int kBarA = 2 * kStages, kBarD = kBarA + 2 * kABufs, kBarId = kBarD + 2 * kDBufs;
+  constexpr int kBarB = kBarId + 2 * kIdRing;
   auto raw_full = [&](int i) { return bars + 8u * (uint32_t)i; };
   auto raw_empty = [&](int i) { return bars + 8u * (uint32_t)(kStages + i); };
-  auto a_full = [&](int i) { return bars + 8u * (uint32_t)(2 * kStages + i); };
-  auto a_empty = [&](int i) { return bars + 8u * (uint32_t)(2 * kStages + kABufs + i); };
-  auto d_full = [&](int i) { return bars + 8u * (uint32_t)(2 * kStages + 2 * kABufs + i); };
-  auto d_empty = [&](int i) { return bars + 8u * (uint32_t)(2 * kStages + 2 * kABufs + kDBufs + i); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * kNumBars);
-
-  // this CTA's contiguous range of the flat tile list
+  auto a_full = [&](int i) { return bars + 8u * (uint32_t)(kBarA + i); };
+  auto a_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarA + kABufs + i); };
+  auto d_full = [&](int i) { return bars + 8u * (uint32_t)(kBarD + i); };
+  auto d_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarD + kDBufs + i); };
+  auto id_full = [&](int i) { return bars + 8u * (uint32_t)(kBarId + i); };
+  auto id_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarId + kIdRing + i); };
+  auto b_full = [&](int i) { return bars + 8u * (uint32_t)(kBarB + i); };
+  auto b_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarB + 2 + i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+  volatile int32_t* stage_meta = reinterpret_cast<volatile int32_t*>(smem + kOffStageMeta);
+  volatile int32_t* a_meta = reinterpret_cast<volatile int32_t*>(smem + kOffAMeta);
+  volatile int32_t* id_ring = reinterpret_cast<volatile int32_t*>(smem + kOffIdRing);
   const int total = p.tile_start[p.b.n_units];
-  const int t0 = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
-  const int t1 = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
-  const int ntiles = t1 - t0;
 
   if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -344,6 +402,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
     for (int i = 0; i < kStages; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), 128); }
     for (int i = 0; i < kABufs; ++i) { mbar_init(a_full(i), 128); mbar_init(a_empty(i), 1); }
     for (int i = 0; i < kDBufs; ++i) { mbar_init(d_full(i), 1); mbar_init(d_empty(i), 128); }
+    for (int i = 0; i < kIdRing; ++i) { mbar_init(id_full(i), 1); mbar_init(id_empty(i), kIdReaders); }
+    for (int i = 0; i < 2; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -352,41 +412,166 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kWarpTma) {
-    // ---- producer: codes of each tile into the ring
-    if (lane == 0 && ntiles > 0) {
-      int ts = 0, te = -1;
-      int64_t n = 0;
-      const uint8_t* keys = nullptr;
-      for (int i = 0; i < ntiles; ++i) {
-        const int t = t0 + i, st = i % kStages;
-        if (i >= kStages && !mbar_wait(raw_empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, t))
-          break;
-        if (t >= te) {
-          const int u = unit_of_tile(p, t);
-          ts = p.tile_start[u];
-          te = p.tile_start[u + 1];
+    // ---- producer (whole warp; lane 0 does the atomics, waits and copies).
+    // Work comes in chunks of one unit's tiles from that unit's counter; a
+    // CTA starts on its home unit (CTAs spread over the units in proportion
+    // to their tiles) and stays on a unit until it runs dry, then moves to
+    // the unit with the most tiles left.  Chunks shrink as a unit's work runs
+    // out, and the next chunk is taken one chunk early.  Consecutive tiles of
+    // one unit form a run; for each run the warp writes the unit's B operand
+    // into one of two slots.  Each tile's codes go into the ring (with the
+    // run number for the converters and the MMA lane) and its flat id into
+    // the id ring (for the epilogue).  After the last tile the producer marks
+    // the end: one stage for the converters (which pass it on to the MMA
+    // lane) and kEpiGroups id slots for the epilogue groups (each group reads
+    // ahead to its next own tile).
+    const int grid = (int)gridDim.x, n_units = p.b.n_units;
+    auto tiles_of = [&](int uu) { return p.tile_start[uu + 1] - p.tile_start[uu]; };
+    auto chunk = [&](int uu, int seen) {
+      const int64_t share = (int64_t)grid * tiles_of(uu) / total;
+      const int c = (int)((tiles_of(uu) - seen) / (kChunkDiv * (share < 1 ? 1 : share)));
+      return c < 1 ? 1 : (c > kChunkMax ? kChunkMax : c);
+    };
+    int u = unit_of_tile(p, (int)((int64_t)blockIdx.x * total / grid));
+    int t = 0, t_end = 0;            // current chunk: local tiles [t, t_end) of unit u
+    int pref = 0, pref_sz = 0;       // next chunk of unit u (value valid in lane 0)
+    bool have_pref = false, first = true, done = false, ok = true;
+    int run = -1, run_u = -1;        // current run and its unit
+    int64_t n = 0;
+    const uint8_t* keys = nullptr;
+    int i = 0;
+    for (;; ++i) {
+      while (t >= t_end) {
+        if (have_pref) {
+          have_pref = false;
+          const int s0 = __shfl_sync(0xFFFFFFFFu, pref, 0);
+          if (s0 < tiles_of(u)) {
+            t = s0;
+            t_end = s0 + pref_sz < tiles_of(u) ? s0 + pref_sz : tiles_of(u);
+          }
+        } else {
+          int uu = u, rem = tiles_of(u);
+          if (!first) {
+            // the unit with the most tiles left (lowest index on ties)
+            uu = -1;
+            rem = 0;
+            for (int v = lane; v < n_units; v += 32) {
+              const int r = tiles_of(v) - ld_relaxed_gpu(unit_counter(p.b, v));
+              if (r > rem) { rem = r; uu = v; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const int r2 = __shfl_xor_sync(0xFFFFFFFFu, rem, o);
+              const int u2 = __shfl_xor_sync(0xFFFFFFFFu, uu, o);
+              if (r2 > rem || (r2 == rem && (unsigned)u2 < (unsigned)uu)) { rem = r2; uu = u2; }
+            }
+            if (uu < 0) { done = true; break; }
+          }
+          first = false;
+          const int sz = chunk(uu, tiles_of(uu) - rem);
+          int s0 = 0;
+          if (lane == 0) s0 = atomicAdd(unit_counter(p.b, uu), sz);
+          s0 = __shfl_sync(0xFFFFFFFFu, s0, 0);
+          if (s0 >= tiles_of(uu)) continue;   // ran dry meanwhile: look again
+          u = uu;
+          t = s0;
+          t_end = s0 + sz < tiles_of(u) ? s0 + sz : tiles_of(u);
+        }
+        if (t < t_end && t_end < tiles_of(u)) {   // take the next chunk early
+          pref_sz = chunk(u, t_end);
+          if (lane == 0) pref = atomicAdd(unit_counter(p.b, u), pref_sz);
+          have_pref = true;
+        }
+      }
+      if (done) break;
+      if (u != run_u) {
+        // new run: B operand of unit u into slot run & 1, once the MMAs of
+        // run - 2 (the slot's last user) have completed
+        ++run;
+        run_u = u;
+        const int slot = run & 1;
+        if (run >= 2) {
+          if (lane == 0)
+            ok = mbar_wait(b_empty(slot), (uint32_t)((run >> 1) - 1) & 1u, p.b.err, run);
+          if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) break;
+        }
+        uint8_t* B = smem + kOffB + slot * kBSlotBytes;
+        const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
+        constexpr int kPerLane = kIndexHeads * kIndexDim / 32;
+        float qv[kPerLane];            // all loads in flight before the first store
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) qv[k] = qu[lane + 32 * k];
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+          const int e = lane + 32 * k, h = e >> 6, d = e & 63;
+          const __half qh = __float2half_rn(qv[k]);
+          const __half ql = __float2half_rn(qv[k] - __half2float(qh));
+          *reinterpret_cast<__half*>(B + sw128_off(h, d)) = qh;
+          *reinterpret_cast<__half*>(B + sw128_off(h + 8, d)) = ql;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(b_full(slot));
           n = p.b.u[u].n;
           keys = p.b.index_keys + p.b.unit_row(u) * kIndexDim;
         }
-        const int64_t tok0 = (int64_t)(t - ts) * kTcTile;
-        const int64_t left = n - tok0;
-        const uint32_t bytes = (uint32_t)((left < kTcTile ? left : kTcTile) * kIndexDim);
-        tma_load_1d(sb + kOffRaw + st * kRawBytes, keys + tok0 * kIndexDim, bytes, raw_full(st));
+      }
+      const int tg = p.tile_start[u] + t;      // flat tile id
+      if (lane == 0) {
+        const int st = i % kStages, rs = i % kIdRing;
+        if (i >= kStages) ok = mbar_wait(raw_empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, tg);
+        if (ok && i >= kIdRing)
+          ok = mbar_wait(id_empty(rs), (uint32_t)(i / kIdRing - 1) & 1u, p.b.err, tg);
+        if (ok) {
+          id_ring[rs] = tg;
+          mbar_arrive(id_full(rs));
+          stage_meta[st] = run;
+          const int64_t tok0 = (int64_t)t * kTcTile;
+          const int64_t left = n - tok0;
+          const uint32_t bytes = (uint32_t)((left < kTcTile ? left : kTcTile) * kIndexDim);
+          tma_load_1d(sb + kOffRaw + st * kRawBytes, keys + tok0 * kIndexDim, bytes, raw_full(st));
+        }
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) break;
+      ++t;
+    }
+    if (ok && lane == 0) {
+      const int st = i % kStages;
+      if (i < kStages || mbar_wait(raw_empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, -1)) {
+        stage_meta[st] = kEndOfWork;
+        mbar_arrive(raw_full(st));
+      }
+      for (int j = i; j < i + kEpiGroups; ++j) {
+        const int rs = j % kIdRing;
+        if (j >= kIdRing && !mbar_wait(id_empty(rs), (uint32_t)(j / kIdRing - 1) & 1u, p.b.err, -1))
+          break;
+        id_ring[rs] = kEndOfWork;
+        mbar_arrive(id_full(rs));
       }
     }
   } else if (warp < kWarpMma) {
-    // ---- converters: e4m3 codes -> f16 A operand (exact)
+    // ---- converters: e4m3 codes -> f16 A operand (exact); the stage's run
+    // number travels on with the A buffer
     const int c = tid - 32 * kWarpConv0;  // 0..127
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = 0;; ++i) {
       const int st = i % kStages, ab = i % kABufs;
-      if (!mbar_wait(raw_full(st), (uint32_t)(i / kStages) & 1u, p.b.err, t0 + i)) break;
-      const uint8_t* raw = smem + kOffRaw + st * kRawBytes;
+      if (!mbar_wait(raw_full(st), (uint32_t)(i / kStages) & 1u, p.b.err, i)) break;
+      const int run = stage_meta[st];
       uint4 q[4];
+      if (run >= 0) {
+        const uint8_t* raw = smem + kOffRaw + st * kRawBytes;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4*>(raw + (k * 128 + c) * 16);
-      mbar_arrive(raw_empty(st));
-      if (i >= kABufs && !mbar_wait(a_empty(ab), (uint32_t)(i / kABufs - 1) & 1u, p.b.err, t0 + i))
+        for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4*>(raw + (k * 128 + c) * 16);
+        mbar_arrive(raw_empty(st));
+      }
+      if (i >= kABufs && !mbar_wait(a_empty(ab), (uint32_t)(i / kABufs - 1) & 1u, p.b.err, i))
         break;
+      if (c == 0) a_meta[ab] = run;
+      if (run < 0) {                  // end of the stream: hand it to the MMA lane
+        mbar_arrive(a_full(ab));
+        break;
+      }
       uint8_t* A = smem + kOffA + ab * kABufBytes;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -405,109 +590,91 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       mbar_arrive(a_full(ab));
     }
   } else if (warp == kWarpMma) {
-    // ---- B operand per unit (whole warp, only when the range enters a new
-    // unit), and the MMAs (lane 0 alone, no per-tile warp traffic)
-    int u = ntiles > 0 ? unit_of_tile(p, t0) : 0;
-    int te = p.tile_start[u + 1];
-    int bu = -1, slot = 1;
-    bool ok = true;
-    for (int i = 0; i < ntiles; ++i) {
-      const int t = t0 + i;
-      if (t >= te) {
-        u = unit_of_tile(p, t);
-        te = p.tile_start[u + 1];
-      }
-      if (u != bu) {
-        __syncwarp();
-        // MMAs still reading the other slot's operand precede tile i
-        if (i >= 1)
-          ok = ok && mbar_wait(d_full((i - 1) % kDBufs), (uint32_t)((i - 1) / kDBufs) & 1u, p.b.err, t);
-        if (!__all_sync(0xFFFFFFFFu, ok)) break;
-        slot ^= 1;
-        uint8_t* B = smem + kOffB + slot * kBSlotBytes;
-        const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
-        for (int e = lane; e < kIndexHeads * kIndexDim; e += 32) {
-          const int h = e >> 6, d = e & 63;
-          const float qv = qu[e];
-          const __half qh = __float2half_rn(qv);
-          const __half ql = __float2half_rn(qv - __half2float(qh));
-          *reinterpret_cast<__half*>(B + sw128_off(h, d)) = qh;
-          *reinterpret_cast<__half*>(B + sw128_off(h + 8, d)) = ql;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        bu = u;
-      }
-      if (lane == 0 && ok) {
+    // ---- MMA issue, lane 0 alone: per tile four tcgen05.mma (K = 16 each)
+    // into a 16-column accumulator; at a new run it releases the previous
+    // run's B slot (commit: arrives once those MMAs are done) and waits for
+    // the new slot to be written.
+    if (lane == 0) {
+      int cur_run = -1;
+      for (int i = 0;; ++i) {
         const int ab = i % kABufs, db = i % kDBufs;
-        ok = mbar_wait(a_full(ab), (uint32_t)(i / kABufs) & 1u, p.b.err, t);
-        if (ok && i >= kDBufs)
-          ok = mbar_wait(d_empty(db), (uint32_t)(i / kDBufs - 1) & 1u, p.b.err, t);
-        if (ok) {
-          tc_fence_after();
-          const uint32_t a0 = sb + kOffA + ab * kABufBytes;
-          const uint32_t b0 = sb + kOffB + slot * kBSlotBytes;
-          const uint32_t d = tmem + (uint32_t)(db * 16);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)   // columns 0-7: A . q_hi, columns 8-15: A . q_lo
-            tc_mma_f16(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), k > 0 ? 1u : 0u);
-          tc_commit(a_empty(ab));
-          tc_commit(d_full(db));
+        if (!mbar_wait(a_full(ab), (uint32_t)(i / kABufs) & 1u, p.b.err, i)) break;
+        const int run = a_meta[ab];
+        if (run < 0) break;
+        if (run != cur_run) {
+          if (cur_run >= 0) tc_commit(b_empty(cur_run & 1));
+          cur_run = run;
+          if (!mbar_wait(b_full(run & 1), (uint32_t)(run >> 1) & 1u, p.b.err, run)) break;
         }
+        if (i >= kDBufs && !mbar_wait(d_empty(db), (uint32_t)(i / kDBufs - 1) & 1u, p.b.err, i)) break;
+        tc_fence_after();
+        const uint32_t a0 = sb + kOffA + ab * kABufBytes;
+        const uint32_t b0 = sb + kOffB + (run & 1) * kBSlotBytes;
+        const uint32_t d = tmem + (uint32_t)(db * 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)   // columns 0-7: A . q_hi, columns 8-15: A . q_lo
+          tc_mma_f16(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), k > 0 ? 1u : 0u);
+        tc_commit(a_empty(ab));
+        tc_commit(d_full(db));
       }
     }
     __syncwarp();
   } else {
-    // ---- epilogue: kEpiGroups groups of 4 warps; group g scores tiles
-    // i = g, g + kEpiGroups, ...  TMEM lane quarter = warp % 4, and the token
-    // of the tile = TMEM lane.  Unit state is cached and refreshed only when a
-    // tile crosses into the next unit.
+    // ---- epilogue: kEpiGroups groups of 4 warps; group g scores the tiles
+    // at stream positions g, g + kEpiGroups, ...  TMEM lane quarter =
+    // warp % 4, and the token of the tile = TMEM lane.  Each warp reads the
+    // tile ids two own tiles ahead and fetches those tiles' scales early.
     static_assert(kWarpEpi0 == kWarpMma + 1, "warp roles");
+    constexpr int G = kEpiGroups;
     const int grp = (warp - kWarpEpi0) >> 2;
     const int qtr = warp & 3;
     const int e = qtr * 32 + lane;
-    int te = -1, ts = 0;               // tile range [ts, te) of the cached unit
-    int64_t n = 0;
-    float* out = nullptr;
-    float w[kIndexHeads];
-    int ste = -1, sts = 0;             // same for the scale cursor
+    auto peek = [&](int pos) -> int {
+      const int rs = pos % kIdRing;
+      int t = kWaitFailed;
+      if (lane == 0) {
+        if (mbar_wait(id_full(rs), (uint32_t)(pos / kIdRing) & 1u, p.b.err, pos)) t = id_ring[rs];
+        if (t >= 0) mbar_arrive(id_empty(rs));
+      }
+      return __shfl_sync(0xFFFFFFFFu, t, 0);
+    };
+    UnitCursor sc_cur;                 // unit of the scale cursor
     int64_t sn = 0;
     const uint16_t* sp = nullptr;
     auto scale_of = [&](int t) -> uint16_t {
-      if (t >= ste) {
-        const int su = unit_of_tile(p, t);
-        sts = p.tile_start[su];
-        ste = p.tile_start[su + 1];
-        sn = p.b.u[su].n;
-        sp = p.b.index_scales + p.b.unit_row(su);
+      if (t < 0) return (uint16_t)0;
+      if (sc_cur.move_to(p, t)) {
+        sn = p.b.u[sc_cur.u].n;
+        sp = p.b.index_scales + p.b.unit_row(sc_cur.u);
       }
-      const int64_t tk = (int64_t)(t - sts) * kTcTile + e;
+      const int64_t tk = (int64_t)(t - sc_cur.ts) * kTcTile + e;
       return tk < sn ? sp[tk] : (uint16_t)0;
     };
-    constexpr int G = kEpiGroups;
-    uint16_t scA = grp < ntiles ? scale_of(t0 + grp) : (uint16_t)0;
-    uint16_t scB = grp + G < ntiles ? scale_of(t0 + grp + G) : (uint16_t)0;
-    for (int i = grp; i < ntiles; i += G) {
-      const int t = t0 + i, db = i % kDBufs;
-      if (t >= te) {
-        const int u = unit_of_tile(p, t);
-        ts = p.tile_start[u];
-        te = p.tile_start[u + 1];
-        n = p.b.u[u].n;
-        out = p.blk + (int64_t)u * p.blk_stride;
+    UnitCursor cur;
+    int64_t n = 0;
+    float* out = nullptr;
+    float w[kIndexHeads];
+    int idA = peek(grp);
+    int idB = idA >= 0 ? peek(grp + G) : kEndOfWork;
+    uint16_t scA = scale_of(idA), scB = scale_of(idB);
+    for (int i = grp; idA >= 0; i += G) {
+      const int t = idA, db = i % kDBufs;
+      const int idC = idB >= 0 ? peek(i + 2 * G) : kEndOfWork;
+      const uint16_t scC = scale_of(idC);
+      if (cur.move_to(p, t)) {
+        n = p.b.u[cur.u].n;
+        out = p.blk + (int64_t)cur.u * p.blk_stride;
 #pragma unroll
-        for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)u * kIndexHeads + h];
+        for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)cur.u * kIndexHeads + h];
       }
       const float sc = __half2float(__ushort_as_half(scA));
-      scA = scB;
-      if (i + 2 * G < ntiles) scB = scale_of(t + 2 * G);
       if (!mbar_wait(d_full(db), (uint32_t)(i / kDBufs) & 1u, p.b.err, t)) break;
       tc_fence_after();
       float v[16];
       tc_ld16(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)(db * 16), v);
       tc_fence_before();
       mbar_arrive(d_empty(db));
-      const int64_t tok = (int64_t)(t - ts) * kTcTile + e;
+      const int64_t tok = (int64_t)(t - cur.ts) * kTcTile + e;
       float s = -INFINITY;
       if (tok < n) {
         s = 0.f;
@@ -517,6 +684,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
       s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
       if ((lane & 3) == 0 && tok < n) out[tok >> 2] = s;
+      idA = idB; idB = idC;
+      scA = scB; scB = scC;
     }
   }
 
@@ -526,6 +695,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
   if (warp == kWarpMma)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
+  // the last CTA to finish re-arms the work counters for the next call
+  if (tid == 0) {
+    int32_t* finished = unit_counter(p.b, 0) + 1;
+    __threadfence();
+    if (atomicAdd(finished, 1) == (int)gridDim.x - 1) {
+      __threadfence();
+      for (int uu = 0; uu < p.b.n_units; ++uu) *reinterpret_cast<volatile int32_t*>(unit_counter(p.b, uu)) = 0;
+      *reinterpret_cast<volatile int32_t*>(finished) = 0;
+    }
+  }
 }
 
 }  // namespace
@@ -549,8 +728,7 @@ cudaError_t launch_index_score(const BatchDesc& b, const float* q_idx, const flo
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kTcSmemBytes);
+      e = prefer_max_shared(index_score_tc_kernel, kTcSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

@@ -10,7 +10,8 @@
 //
 // Host state: one lease per request slot and a first-fit free list of HBM
 // pool row ranges.  Device state (all caller-allocated): the pool, the index
-// keys, the slot table and the workspace (error word + split-K partials).
+// keys, the slot table and the workspace (error word, split-K partials, and
+// the index-score work counters of every request x layer).
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -93,6 +94,10 @@ struct qsa_cache {
   float* partials() const {
     return reinterpret_cast<float*>(static_cast<uint8_t*>(cfg.workspace) + kErrBytes);
   }
+  int32_t* tickets() const {
+    return reinterpret_cast<int32_t*>(partials() + (int64_t)cfg.max_requests * cfg.n_layers *
+                                                       splits_max * kPartFloats);
+  }
 
   bool alloc_rows(int64_t n, int64_t* base) {
     for (auto it = free_rows.begin(); it != free_rows.end(); ++it) {
@@ -156,6 +161,7 @@ struct qsa_cache {
     d->pool = static_cast<uint8_t*>(cfg.hbm_pool);
     d->err = err();
     d->partials = partials();
+    d->tickets = tickets();
     d->splits_max = (int32_t)splits_max;
     d->pad0 = 0;
     for (int i = 0; i < b->n_req; ++i) {
@@ -186,8 +192,9 @@ const char* qsa_last_error_string(void) { return g_last_error.c_str(); }
 
 int64_t qsa_workspace_bytes(const qsa_cache_config* c) {
   if (!config_sizes_ok(c)) return -1;
-  return kErrBytes + (int64_t)c->max_requests * c->n_layers * splits_max_of(*c) * kPartFloats *
-                         (int64_t)sizeof(float);
+  const int64_t units = (int64_t)c->max_requests * c->n_layers;
+  return kErrBytes + units * splits_max_of(*c) * kPartFloats * (int64_t)sizeof(float) +
+         units * 2 * (int64_t)sizeof(int32_t);
 }
 
 qsa_status_t qsa_cache_create(const qsa_cache_config* c, qsa_cache** out) {

@@ -66,6 +66,7 @@ struct BatchDesc {
   uint8_t* pool;              // [pool_rows][2048]
   ErrorWord* err;
   float* partials;            // [req][layer][splits_max][kPartFloats]
+  int32_t* tickets;           // [req][layer][2]: work counter, finished CTAs
   int32_t splits_max;
   int32_t pad0;
   UnitDesc u[kMaxUnits];
@@ -98,6 +99,22 @@ __device__ __forceinline__ const uint8_t* row_source(const BatchDesc& b, int u, 
 // Record the thread-local message returned by qsa_last_error_string() and
 // pass the status through (defined with the C ABI layer).
 qsa_status_t set_last_error(qsa_status_t status, const char* message);
+
+// Kernels of different calls share SMs (index score of some requests beside
+// the attention of others on another stream).  An SM's split between L1 and
+// shared memory is fixed while CTAs are resident on it, so every big kernel
+// of the library asks for the largest shared-memory carveout: then a CTA
+// never waits for an SM to drain just because another kernel chose a
+// smaller split.
+template <class Kernel>
+cudaError_t prefer_max_shared(Kernel kernel, int dynamic_smem_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       dynamic_smem_bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
+}
 
 // ------------------------------------------------------------ launchers
 // Each returns the launch status (cudaGetLastError right after the launch).

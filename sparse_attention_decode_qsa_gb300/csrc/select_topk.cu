@@ -371,8 +371,7 @@ cudaError_t launch_select_topk(const BatchDesc& b, const float* blk_scores, int6
   }
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(select_topk_cluster_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kClusterSmem);
+    cudaError_t e = prefer_max_shared(select_topk_cluster_kernel, kClusterSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

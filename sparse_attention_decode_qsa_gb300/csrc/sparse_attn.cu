@@ -52,6 +52,11 @@ constexpr int kSmemBytes = kWarps * 2 * kWarpBufBytes;    // 64 KiB: fits beside
 #define QSA_ATTN_HOST_CTAS 64
 #endif
 constexpr int kMaxCtasHost = QSA_ATTN_HOST_CTAS;
+// Register budget per thread: at 80 one CTA (20 K registers) fits on an SM
+// beside two index-score CTAs.
+#ifndef QSA_ATTN_MAXREG
+#define QSA_ATTN_MAXREG 80
+#endif
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -128,7 +133,7 @@ __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int s
   return valid;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(const AttnParams p) {
+__global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams p) {
   extern __shared__ __align__(16) uint8_t smem[];  // [warp][2][8][512]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
@@ -308,8 +313,10 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
+      e = prefer_max_shared(attn_split_kernel, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

@@ -53,7 +53,7 @@ def test_workspace_bytes_and_bad_configs():
     cfg = N.CacheConfig(n_layers=12, max_requests=8, ctx_capacity=262144, budget_tokens=2048,
                         ring_tokens=4096, staging_rows=2048, hbm_pool_rows=1 << 20)
     # error word + 8 req x 12 layers x 64 splits x 2080 floats
-    assert L.qsa_workspace_bytes(C.byref(cfg)) == 256 + 8 * 12 * 64 * 2080 * 4
+    assert L.qsa_workspace_bytes(C.byref(cfg)) == 256 + 8 * 12 * 64 * 2080 * 4 + 8 * 12 * 8
     for field, bad in [("budget_tokens", 6), ("budget_tokens", 0), ("budget_tokens", 16384),
                        ("n_layers", 0), ("ring_tokens", 0), ("ctx_capacity", 0)]:
         c2 = N.CacheConfig.from_buffer_copy(cfg)

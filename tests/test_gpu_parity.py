@@ -371,3 +371,47 @@ def test_pipelined_graph_step_equals_sequential_step():
         QC.check_unit(wl, 2, 3)
     finally:
         wl.close()
+
+
+def test_index_score_work_counter_rearms_and_is_per_first_unit():
+    """The index-score CTAs take tiles from a work counter that the call's
+    last CTA re-arms.  Back-to-back calls, calls on two streams at once
+    (different first units) and one call over several layers must all give
+    the block scores of a single call, bit for bit (each score is computed
+    by exactly one thread, whatever the schedule)."""
+    ctxs = [70000, 9000, 130001, 4096]
+    wl = workloads.build(
+        3, ctxs, [Q.KV_HBM] * 4,
+        lambda l, r, n: synth.planted_uniform(n // 4, 512, synth.mix_seed(31, 90, l, r)),
+        staging_rows=64, seed=31)
+    try:
+        c, hs, R = wl.cache, wl.handles, wl.n_req
+        wl.blk.fill_(7.0)       # entries past a unit's last block stay untouched
+        c.index_score(hs, 0, 3, wl.q_idx, wl.w, wl.blk)
+        torch.cuda.synchronize()
+        ref = wl.blk.clone()
+        for _ in range(4):
+            wl.blk.fill_(7.0)
+            c.index_score(hs, 0, 3, wl.q_idx, wl.w, wl.blk)
+            torch.cuda.synchronize()
+            assert torch.equal(ref, wl.blk)
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        for l in range(3):
+            sl = slice(l * R, (l + 1) * R)
+            wl.blk[sl].fill_(7.0)
+            s1.wait_stream(torch.cuda.current_stream())
+            s2.wait_stream(torch.cuda.current_stream())
+            for _ in range(3):
+                wl.score_group_layer(0, 2, l, s1)
+                wl.score_group_layer(2, 4, l, s2)
+            torch.cuda.synchronize()
+            assert torch.equal(ref[sl], wl.blk[sl])
+        for l in range(3):
+            wl.attn_group_layer(0, R, l, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        _clean(wl)
+        for l in range(3):
+            QC.check_unit(wl, l, 2)
+            QC.check_unit(wl, l, 3)
+    finally:
+        wl.close()
