@@ -13,37 +13,40 @@
 // The scan does 512 multiply-adds per 66 bytes, more than the CUDA cores
 // deliver at HBM speed, and it is a genuine dense contraction
 // (keys[tokens][64] x q^T[64][8 heads]), so it runs on the 5th-generation
-// tensor cores (tcgen05, accumulators in TMEM), in tiles of M = 128 tokens.
-// The grid is persistent (up to two CTAs per SM) and the work is handed out
-// dynamically: CTAs take chunks of the flat tile list of all units of the
-// call from an atomic counter, large chunks first and single tiles at the
-// end.  A CTA that starts late (its SM busy with another kernel, e.g. the
-// attention of other requests on another stream) then simply takes less work
-// instead of holding up the whole call with a fixed share.  The last CTA to
-// finish re-arms the counter.  Its warps have fixed roles and hand tiles to
-// each other through mbarrier rings, so no role waits for another's latency:
-//  * TMA warp (lane 0): takes the chunks, streams each tile's 8 KiB of codes
-//    into a ring of shared-memory stages with bulk copies (cp.async.bulk;
-//    completion counted in bytes on the stage's mbarrier) and publishes the
-//    tile's id in a ring read by the MMA warp and the epilogue.
-//  * 4 converter warps: turn the codes into the f16 A operand (exact: every
-//    e4m3 value is an f16 value); consecutive 16-byte reads, conflict-free
-//    stores thanks to the swizzle below.
-//  * MMA warp: builds the B operand when the stream enters a new unit - the
-//    index query split as q = hi + lo with hi = f16(q), lo = f16(q - hi), rows
-//    0-7 and 8-15 of an N = 16 operand, which keeps the dot products at fp32
-//    accuracy - and its lane 0 issues four tcgen05.mma per tile (K = 16 each)
-//    into one of four 16-column TMEM accumulators, committing to mbarriers
-//    that release the A buffer and publish the accumulator.
-//  * 2 x 4 epilogue warps (alternate tiles): tcgen05.ld of the tile's 16
-//    columns (thread t = token t = TMEM lane t), hi + lo, scale, relu, head
-//    weights, C4 max through shuffles, one fp32 per block to global memory.
+// tensor cores (tcgen05, kind::f8f6f4): per tile of M = 128 tokens,
+// D[128][48] = A . B^T with
+//  * A = the tile's e4m3 codes exactly as TMA lands them: 128 rows of 64
+//    bytes under the 64-byte swizzle, which is the tensor core's K-major
+//    SWIZZLE_64B layout, so the codes are never touched by a thread;
+//  * B = the index query as e4m3 "pieces": q * 2^s = sum_p piece_p * 16^-p
+//    (p = 0..4; each piece the round-to-nearest e4m3 of the remaining
+//    residual times 16), one B row per (piece, head).  Five pieces carry
+//    20 bits of every query element, so sum_p 16^-p * D[:, 8p + h] / 2^s
+//    equals the fp32 dot product to about 2^-20 relative.  Every product of
+//    two e4m3 values is exact, and the tensor core accumulates in fp32.
+// Per tile that is two MMAs (K = 32 each); a tensor core spends ~160 cycles
+// on an MMA of this size whatever its N, so the instruction count per token
+// is what bounds the kernel, and fp8 operands halve it against f16 ones.
 //
-// Operand layout: K-major with the 128-byte swizzle.  A row (one token of A,
-// one head of B) is 64 f16 = 128 bytes; its 16-byte chunk c is stored at chunk
-// position c ^ (row % 8), so the tensor core reads whole 128-byte lines and
-// the converters' stores hit distinct banks.  The descriptor's stride byte
-// offset is 1024 (8 rows); K-step k starts 32*k bytes into the row.
+// The grid is persistent (two CTAs per SM).  Work is handed out in chunks of
+// kChunk consecutive tiles of the call's flat tile list from a counter in the
+// workspace, so a CTA that starts late (its SM busy with another kernel, e.g.
+// the attention of other requests on another stream) takes less work instead
+// of holding up the call; the last CTA to finish re-arms the counter.  Warp
+// roles, handing tiles over through mbarrier rings (all waits bounded):
+//  * producer warp: takes chunks (lane 0, one chunk ahead), builds a group's
+//    B operand when the group's stream of tiles enters a new unit (a "run";
+//    two B slots per group), issues the TMA loads of each tile (codes, and
+//    the tile's fp16 scales) and publishes the tile's (unit, tile, run)
+//    in the stage's metadata.
+//  * two MMA warps, one per worker group (the first also allocates tensor
+//    memory): lane 0 issues the tile's two tcgen05.mma, A and B from shared
+//    memory, into one of four accumulators, then releases the stage.
+//  * two groups of 4 worker warps, taking alternate tiles: thread = token row
+//    = tensor-memory lane.  Each reads its token's scale, then its row of
+//    the accumulator, and computes relu, head weights, scale and the C4 max
+//    (shuffles); one fp32 per block goes to global memory.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -52,198 +55,98 @@
 namespace qsa {
 namespace {
 
-#ifdef QSA_INDEX_SCORE_FFMA
-constexpr int kThreads = 128;              // one C4 block per thread
-constexpr int kTileTokens = kThreads * 4;  // 512
+constexpr int kTile = 128;                      // tokens per tile (MMA M)
+#ifndef QSA_K1_PIPES
+#define QSA_K1_PIPES 2
 #endif
+constexpr int kPipes = QSA_K1_PIPES;            // independent pipelines per CTA
+#ifndef QSA_K1_STAGES
+#define QSA_K1_STAGES 3
+#endif
+constexpr int kStages = QSA_K1_STAGES;          // code ring depth per pipeline (8 KiB each)
+constexpr int kPieces = 5;                      // e4m3 pieces of the query
+constexpr int kN = 48;                          // B rows: 8 heads x 5 pieces, padded to 16
+constexpr int kDBufs = 2;                       // accumulators per pipeline in tensor memory
+constexpr int kDStride = 64;                    // tensor-memory columns per accumulator
+// Warp roles within a pipeline (6 warps): producer, MMA, 4 workers.
+constexpr int kPipeWarps = 6;
+constexpr int kRoleProd = 0, kRoleMma = 1, kRoleWork0 = 2;
+constexpr int kThreadsTc = 32 * kPipeWarps * kPipes;   // 384
+#ifndef QSA_K1_CTAS_PER_SM
+#define QSA_K1_CTAS_PER_SM 2
+#endif
+constexpr int kCtasPerSm = QSA_K1_CTAS_PER_SM;
+// Register budget per thread: two CTAs of 12 warps at 56 (43008 registers)
+// leave room for one attention CTA (20480) on the SM, and no third CTA of
+// this kernel fits (so two always find their tensor memory free).
+#ifndef QSA_K1_MAXREG
+#define QSA_K1_MAXREG 56
+#endif
+#ifndef QSA_K1_CHUNK
+#define QSA_K1_CHUNK 4
+#endif
+constexpr int kChunk = QSA_K1_CHUNK;            // tiles per grab from a unit's work counter
+constexpr int kRawBytes = kTile * kIndexDim;    // 8 KiB of codes per tile
+constexpr int kBBytes = 1024 * ((kN * kIndexDim + 1023) / 1024);   // 3 KiB of pieces
+constexpr int kBSlots = 2;                      // per pipeline: current and next run
+constexpr uint32_t kPipeCols = kDBufs * kDStride;                  // 128
+constexpr uint32_t kTmemCols = kPipeCols * kPipes;                 // 256
+// Scales of a tile come with its codes: a 1-D TMA box of kScaleBox fp16
+// values starting at the tile's first scale rounded down to a multiple of 8
+// (TMA starts on 16-byte boundaries), so the tile's 128 scales sit at an
+// offset of 0..7 values into the box.
+constexpr int kScaleBox = kTile + 8;            // 136 values = 272 bytes
+constexpr int kScaleSlot = 384;                 // bytes per stage, 128-aligned
+// Shared memory of one pipeline (1024-aligned stages and B slots first).
+constexpr int kOffRaw = 0;
+constexpr int kOffB = kOffRaw + kStages * kRawBytes;
+constexpr int kOffScale = kOffB + kBSlots * kBBytes;
+constexpr int kOffBar = kOffScale + kStages * kScaleSlot;
+// barriers: full[S], empty[S], d_full[D], d_empty[D], b_full[B], b_empty[B], mma_done
+constexpr int kNumBars = 2 * kStages + 2 * kDBufs + 2 * kBSlots + 1;
+constexpr int kOffStageMeta = (kOffBar + 8 * kNumBars + 15) / 16 * 16;   // int4 [kStages]
+constexpr int kPipeBytes = (kOffStageMeta + 16 * kStages + 1023) / 1024 * 1024;
+constexpr int kOffTmemSlot = kPipes * kPipeBytes;
+// + 1 KiB so the pipelines can be aligned to 1024 bytes
+constexpr int kSmemBytes = kOffTmemSlot + 16 + 1024;
+static_assert(kRawBytes % 1024 == 0 && kOffB % 1024 == 0 && kBBytes % 1024 == 0 &&
+                  kPipeBytes % 1024 == 0, "swizzled operands need 1024-byte alignment");
+static_assert(kOffScale % 128 == 0 && kScaleSlot % 128 == 0 && kScaleBox * 2 <= kScaleSlot &&
+                  (kScaleBox * 2) % 16 == 0, "scale boxes: 16-byte multiples in 128-byte slots");
+static_assert(kOffBar % 8 == 0 && kOffStageMeta % 16 == 0,
+              "mbarriers need 8-byte, int4 metadata 16-byte alignment");
+static_assert(kPieces * kIndexHeads <= kN && kN % 16 == 0 && kN <= kDStride, "B rows");
+static_assert(kPipeWarps - kRoleWork0 == 4, "four worker warps cover the four lane quarters");
+// kind::f8f6f4 instruction descriptor: D f32 (bit 4), A = B = e4m3 (type 0 at
+// bits 7-9 and 10-12), both K-major, N/8 at bits 17-22, M/16 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kWaitPolls = 1u << 20;       // bounded mbarrier waits
+constexpr int kEndOfWork = -1;
+constexpr int kRunBits = 20;                    // stage meta .z = run | (s + 1024) << 20
 
 struct IndexScoreParams {
+  CUtensorMap keys_map;               // uint8 [rows][64], box 64 x 128, 64-byte swizzle
+  CUtensorMap scales_map;             // fp16 [rows], box kScaleBox
   BatchDesc b;
-  int32_t tile_start[kMaxUnits + 1];  // prefix sums of tiles (or CTAs) per unit
+  int32_t tile_start[kMaxUnits + 1];  // prefix sums of tiles per unit
   const float* q_idx;                 // [units][8][64]
   const float* w;                     // [units][8]
   float* blk;                         // [units][blk_stride]
   int64_t blk_stride;
 };
 
-#ifdef QSA_INDEX_SCORE_FFMA
-// CUDA-core version (fp32 FMAs), kept for A/B comparison builds.
-__device__ __forceinline__ uint4 ldg_stream(const uint8_t* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-// Two e4m3 codes (low byte first) to two floats, via the hardware
-// e4m3x2 -> f16x2 conversion (exact: every e4m3 value is an f16 value).
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t pair16) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair16, __NV_E4M3);
-  return __half22float2(*reinterpret_cast<__half2*>(&h));
-}
-
-__global__ void __launch_bounds__(kThreads) index_score_kernel(const IndexScoreParams p) {
-  __shared__ __align__(16) float qs[kIndexDim][kIndexHeads];
-  __shared__ float ws[kIndexHeads];
-
-  const int tile = blockIdx.x;
-  int lo = 0, hi = p.b.n_units - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
-  }
-  const int u = lo;
-
-  const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
-  for (int i = threadIdx.x; i < kIndexHeads * kIndexDim; i += kThreads)
-    qs[i % kIndexDim][i / kIndexDim] = qu[i];
-  if (threadIdx.x < kIndexHeads) ws[threadIdx.x] = p.w[(int64_t)u * kIndexHeads + threadIdx.x];
-  __syncthreads();
-
-  const int64_t n = p.b.u[u].n;
-  const int64_t blk = (int64_t)(tile - p.tile_start[u]) * kThreads + threadIdx.x;
-  const int64_t t0 = blk * 4;
-  if (t0 >= n) return;
-  const int nt = (n - t0) < 4 ? (int)(n - t0) : 4;
-  const int64_t row = p.b.unit_row(u) + t0;
-  const uint8_t* kp = p.b.index_keys + row * kIndexDim;
-  const uint16_t* sp = p.b.index_scales + row;
-
-  float acc[4][kIndexHeads];
-#pragma unroll
-  for (int t = 0; t < 4; ++t)
-#pragma unroll
-    for (int h = 0; h < kIndexHeads; ++h) acc[t][h] = 0.f;
-
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {  // 16-dim chunks of the 64 dims
-    uint4 kv[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      kv[t] = (t < nt) ? ldg_stream(kp + t * kIndexDim + c * 16) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {  // dim pairs within the chunk
-      const int d = c * 16 + 2 * j;
-      const float4 qa0 = *reinterpret_cast<const float4*>(&qs[d][0]);
-      const float4 qa1 = *reinterpret_cast<const float4*>(&qs[d][4]);
-      const float4 qb0 = *reinterpret_cast<const float4*>(&qs[d + 1][0]);
-      const float4 qb1 = *reinterpret_cast<const float4*>(&qs[d + 1][4]);
-      const float qa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
-      const float qb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint32_t word = (j >> 1) == 0 ? kv[t].x : (j >> 1) == 1 ? kv[t].y
-                            : (j >> 1) == 2 ? kv[t].z : kv[t].w;
-        const float2 kf = e4m3x2_to_float2((j & 1) ? (word >> 16) : (word & 0xFFFFu));
-#pragma unroll
-        for (int h = 0; h < kIndexHeads; ++h) {
-          acc[t][h] = fmaf(kf.x, qa[h], acc[t][h]);
-          acc[t][h] = fmaf(kf.y, qb[h], acc[t][h]);
-        }
-      }
-    }
-  }
-
-  float best = -INFINITY;
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    if (t < nt) {
-      const float sc = __half2float(__ushort_as_half(sp[t]));
-      float s = 0.f;
-#pragma unroll
-      for (int h = 0; h < kIndexHeads; ++h) s = fmaf(ws[h], fmaxf(acc[t][h] * sc, 0.f), s);
-      best = fmaxf(best, s);
-    }
-  }
-  p.blk[(int64_t)u * p.blk_stride + blk] = best;
-}
-
-
-#endif  // QSA_INDEX_SCORE_FFMA
-
-constexpr int kTcTile = 128;                           // tokens per MMA tile (M)
-#ifndef QSA_K1_STAGES
-#define QSA_K1_STAGES 4
-#endif
-#ifndef QSA_K1_CTAS_PER_SM
-#define QSA_K1_CTAS_PER_SM 2
-#endif
-// Register budget per thread: two CTAs at 48 (43 K registers) leave room on
-// the SM for one attention CTA.
-#ifndef QSA_K1_MAXREG
-#define QSA_K1_MAXREG 48
-#endif
-// Warp roles of the persistent CTA.
-constexpr int kWarpTma = 0;                            // lane 0 streams codes with TMA
-constexpr int kWarpConv0 = 1;                          // warps 1..4 convert codes to f16
-constexpr int kWarpMma = 5;                            // builds B, lane 0 issues the MMAs
-constexpr int kWarpEpi0 = 6;                           // warps 6.. read TMEM, score, store
-constexpr int kEpiGroups = 2;                          // epilogue groups take alternate tiles
-constexpr int kTcThreads = 32 * (kWarpEpi0 + 4 * kEpiGroups);
-constexpr int kStages = QSA_K1_STAGES;                 // code ring depth
-#ifndef QSA_K1_ABUFS
-#define QSA_K1_ABUFS 2
-#endif
-constexpr int kABufs = QSA_K1_ABUFS;                   // A operand ring
-constexpr int kDBufs = 4;                              // TMEM accumulator ring (16 columns each)
-constexpr int kIdRing = 16;                            // tile-id ring (producer -> epilogue)
-constexpr int kIdReaders = 4;                          // the owning group's 4 warps
-constexpr int kRawBytes = kTcTile * kIndexDim;         // 8 KiB of codes per tile
-constexpr int kRowBytes128 = kIndexDim * 2;            // one f16 row of A or B: 128 B
-constexpr int kABufBytes = kTcTile * kRowBytes128;     // 16 KiB, 1024-aligned
-constexpr int kBBytes = 16 * kRowBytes128;             // 2 KiB: rows 0-7 q_hi, rows 8-15 q_lo
-constexpr int kBSlotBytes = kBBytes;                   // one unit's B
-constexpr uint32_t kTmemCols = 16 * kDBufs;            // 64
-constexpr int kCtasPerSm = QSA_K1_CTAS_PER_SM;
-constexpr int kOffRaw = 0;
-constexpr int kOffA = kOffRaw + kStages * kRawBytes;   // multiple of 1024
-constexpr int kOffB = kOffA + kABufs * kABufBytes;
-constexpr int kOffBar = kOffB + 2 * kBSlotBytes;
-// barriers: raw_full[S], raw_empty[S], a_full[A], a_empty[A], d_full[D],
-// d_empty[D], id_full[R], id_empty[R], b_full[2], b_empty[2]
-constexpr int kNumBars = 2 * kStages + 2 * kABufs + 2 * kDBufs + 2 * kIdRing + 4;
-constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
-constexpr int kOffStageMeta = kOffTmemSlot + 16;       // int32 [kStages]: run of each stage
-constexpr int kOffAMeta = kOffStageMeta + 4 * kStages; // int32 [kABufs]: run of each A buffer
-constexpr int kOffIdRing = kOffAMeta + 4 * kABufs;     // int32 [kIdRing]
-// + 1 KiB so the operand region can be aligned to 1024 bytes (128-byte swizzle)
-constexpr int kTcSmemBytes = kOffIdRing + 4 * kIdRing + 1024;
-// kind::f16 instruction descriptor: D f32 (bit 4), A = B = f16, both K-major,
-// N/8 at bits 17-22, M/16 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
-constexpr uint32_t kWaitPolls = 1u << 20;              // bounded mbarrier waits
-// Guided chunks: a grab takes 1/kChunkDiv of the unit's remaining tiles per
-// CTA sharing it, at most kChunkMax.
-#ifndef QSA_K1_CHUNK_DIV
-#define QSA_K1_CHUNK_DIV 4
-#endif
-#ifndef QSA_K1_CHUNK_MAX
-#define QSA_K1_CHUNK_MAX 16
-#endif
-constexpr int kChunkDiv = QSA_K1_CHUNK_DIV;
-constexpr int kChunkMax = QSA_K1_CHUNK_MAX;
-constexpr int kEndOfWork = -1;                         // tile id that ends a role's loop
-constexpr int kWaitFailed = -2;
-
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
   return (uint32_t)__cvta_generic_to_shared(ptr);
 }
 
-// Byte offset of element (row, k) of a K-major operand with rows of 64 f16
-// (128 bytes) under the 128-byte swizzle: 16-byte chunk c of row r is stored
-// at chunk position c ^ (r % 8).
-__device__ __forceinline__ uint32_t sw128_off(int row, int k) {
-  return row * kRowBytes128 + ((((k >> 3) ^ row) & 7) << 4) + (k & 7) * 2;
-}
-
-// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: start
+// Shared-memory matrix descriptor, K-major with the 64-byte swizzle (rows of
+// 64 bytes, 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)): start
 // address >> 4, leading byte offset 16 (unused by this layout), stride byte
-// offset 1024 (next group of 8 rows), version 1 at bit 46, layout type 2
-// (SWIZZLE_128B) at bits 61-63.  K-step k of 16 f16 starts 32*k bytes in.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         (1ull << 46) | (2ull << 61);
+// offset 512 (next group of 8 rows), version 1 at bit 46, layout type 4
+// (SWIZZLE_64B) at bits 61-63.  K-step k of 32 e4m3 starts 32*k bytes in.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(512 >> 4) << 32) |
+         (1ull << 46) | (4ull << 61);
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -277,16 +180,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, ErrorWo
   return true;
 }
 
-// TMA bulk copy of `bytes` (multiple of 16) from global to shared memory,
-// completing `bytes` transactions on mbarrier `bar`.
-__device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes,
-                                            uint32_t bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+// TMA loads of one tile, both completing on mbarrier bar: rows [y, y + 128)
+// of the key tensor (all 64 bytes of each) into dst with the 64-byte
+// swizzle, and scales [x, x + kScaleBox) into sdst.  Elements past the end of
+// a tensor read as 0.
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap* keys, int32_t y,
+                                              uint32_t sdst, const CUtensorMap* scales, int32_t x,
+                                              uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"((uint32_t)(kRawBytes + 2 * kScaleBox))
                : "memory");
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2}], [%3];" ::"r"(sdst),
+      "l"(reinterpret_cast<uint64_t>(scales)), "r"(x), "r"(bar)
+      : "memory");
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(keys)), "r"(0), "r"(y), "r"(bar)
       : "memory");
 }
 
@@ -297,12 +209,13 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                           uint32_t accumulate) {
+// D (tensor memory) [+]= A (shared) . B (shared)^T, e4m3 x e4m3 -> f32
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %4, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(accumulate), "r"(kIdesc)
       : "memory");
 }
 
@@ -311,8 +224,10 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// This thread's tensor-memory lane, 16 / 8 consecutive 32-bit columns.  The
+// registers are valid only after tc_wait_ld(); tc_reg_fence() after the wait
+// keeps the compiler from reading them earlier.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
@@ -320,17 +235,28 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void tc_reg_fence(uint32_t (&r)[N]) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-// Four e4m3 codes (bytes of w, low first) -> two f16x2 words (exact).
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
-      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
+// e4m3 code (round to nearest even, saturating at +-448) of x, and its value.
+__device__ __forceinline__ uint8_t to_e4m3(float x) {
+  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+  return __half2float(__half(h));
 }
 
 __device__ __forceinline__ int unit_of_tile(const IndexScoreParams& p, int t) {
@@ -342,8 +268,9 @@ __device__ __forceinline__ int unit_of_tile(const IndexScoreParams& p, int t) {
   return lo;
 }
 
-// Work counter of unit u for the current call (the workspace keeps two
-// int32 per request x layer; the first counts the unit's tiles handed out).
+// Work counters: the workspace keeps two int32 per request x layer.  The
+// first of unit u counts the unit's tiles handed out; the second of the
+// call's first unit counts the CTAs that have finished.
 __device__ __forceinline__ int32_t* unit_counter(const BatchDesc& b, int u) {
   return b.tickets + 2 * ((int64_t)b.u[u].req * b.n_layers + b.u[u].layer);
 }
@@ -354,253 +281,207 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int32_t* ptr) {
   return v;
 }
 
-// Tile range [ts, te) of the unit that holds tile t, cached between calls.
-struct UnitCursor {
-  int u = -1, ts = 0, te = 0;
-  __device__ __forceinline__ bool move_to(const IndexScoreParams& p, int t) {
-    if (t >= ts && t < te) return false;
-    u = unit_of_tile(p, t);
-    ts = p.tile_start[u];
-    te = p.tile_start[u + 1];
-    return true;
+// Write unit u's query pieces into the B slot at B (whole warp) and return the
+// exponent s of the common scale 2^s (so that max |q| * 2^s is in [128, 256)).
+__device__ __forceinline__ int build_pieces(const IndexScoreParams& p, int u, uint8_t* B, int lane) {
+  const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
+  constexpr int kPerLane = kIndexHeads * kIndexDim / 32;   // 16
+  float qv[kPerLane];
+  float m = 0.f;
+#pragma unroll
+  for (int k = 0; k < kPerLane; ++k) {
+    qv[k] = qu[lane + 32 * k];
+    m = fmaxf(m, fabsf(qv[k]));
   }
-};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  int e = 0;
+  if (m > 0.f) frexpf(m, &e);                // m = f * 2^e, f in [0.5, 1)
+  int s = m > 0.f ? 8 - e : 0;
+  s = s < -126 ? -126 : (s > 126 ? 126 : s);   // 2^s a normal fp32
+  const float two_s = __int_as_float((127 + s) << 23);
+  // zero the padding rows kPieces*8 .. kN-1 (whole 16-byte chunks)
+  for (int c = lane; c < (kN - kPieces * kIndexHeads) * kIndexDim / 16; c += 32)
+    *reinterpret_cast<uint4*>(B + kPieces * kIndexHeads * kIndexDim + 16 * c) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int k = 0; k < kPerLane; ++k) {
+    const int el = lane + 32 * k, h = el >> 6, d = el & 63;
+    float r = qv[k] * two_s;                 // exact
+#pragma unroll
+    for (int pc = 0; pc < kPieces; ++pc) {
+      const uint8_t c = to_e4m3(r);
+      r = (r - e4m3_value(c)) * 16.f;        // exact residual, scaled up for the next piece
+      const int row = pc * kIndexHeads + h;
+      // 64-byte swizzle: chunk (d >> 4) of row `row` at chunk (d >> 4) ^ ((row >> 1) & 3)
+      B[row * kIndexDim + ((((d >> 4) ^ (row >> 1)) & 3) << 4) + (d & 15)] = c;
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  return s;
+}
 
 __global__ void __maxnreg__(QSA_K1_MAXREG)
-index_score_tc_kernel(const IndexScoreParams p) {
+index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  // the swizzled operands need 1024-byte alignment
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  // the swizzled stages and B slots need 1024-byte alignment
+  uint8_t* smem0 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pl = warp / kPipeWarps, role = warp % kPipeWarps;
+  uint8_t* smem = smem0 + pl * kPipeBytes;          // this warp's pipeline
   const uint32_t sb = smem_u32(smem);
   const uint32_t bars = sb + kOffBar;
-  constexpr int kBarA = 2 * kStages, kBarD = kBarA + 2 * kABufs, kBarId = kBarD + 2 * kDBufs;
-  constexpr int kBarB = kBarId + 2 * kIdRing;
-  auto raw_full = [&](int i) { return bars + 8u * (uint32_t)i; };
-  auto raw_empty = [&](int i) { return bars + 8u * (uint32_t)(kStages + i); };
-  auto a_full = [&](int i) { return bars + 8u * (uint32_t)(kBarA + i); };
-  auto a_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarA + kABufs + i); };
+  constexpr int kBarD = 2 * kStages, kBarB = kBarD + 2 * kDBufs, kBarDone = kBarB + 2 * kBSlots;
+  auto full = [&](int i) { return bars + 8u * (uint32_t)i; };
+  auto empty = [&](int i) { return bars + 8u * (uint32_t)(kStages + i); };
   auto d_full = [&](int i) { return bars + 8u * (uint32_t)(kBarD + i); };
   auto d_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarD + kDBufs + i); };
-  auto id_full = [&](int i) { return bars + 8u * (uint32_t)(kBarId + i); };
-  auto id_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarId + kIdRing + i); };
   auto b_full = [&](int i) { return bars + 8u * (uint32_t)(kBarB + i); };
-  auto b_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarB + 2 + i); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
-  volatile int32_t* stage_meta = reinterpret_cast<volatile int32_t*>(smem + kOffStageMeta);
-  volatile int32_t* a_meta = reinterpret_cast<volatile int32_t*>(smem + kOffAMeta);
-  volatile int32_t* id_ring = reinterpret_cast<volatile int32_t*>(smem + kOffIdRing);
+  auto b_empty = [&](int i) { return bars + 8u * (uint32_t)(kBarB + kBSlots + i); };
+  const uint32_t mma_done = bars + 8u * (uint32_t)kBarDone;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem0 + kOffTmemSlot);
+  int4* stage_meta = reinterpret_cast<int4*>(smem + kOffStageMeta);  // ordered by the mbarrier asm
   const int total = p.tile_start[p.b.n_units];
 
-  if (warp == kWarpMma) {
+  if (warp == kRoleMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)), "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), 128); }
-    for (int i = 0; i < kABufs; ++i) { mbar_init(a_full(i), 128); mbar_init(a_empty(i), 1); }
+  if (role == kRoleProd && lane == 0) {
+    // a stage is free again once its MMAs have read the codes (one commit)
+    // and the 128 workers have read the metadata and scales
+    for (int i = 0; i < kStages; ++i) { mbar_init(full(i), 1); mbar_init(empty(i), 129); }
     for (int i = 0; i < kDBufs; ++i) { mbar_init(d_full(i), 1); mbar_init(d_empty(i), 128); }
-    for (int i = 0; i < kIdRing; ++i) { mbar_init(id_full(i), 1); mbar_init(id_empty(i), kIdReaders); }
-    for (int i = 0; i < 2; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
+    for (int i = 0; i < kBSlots; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
+    mbar_init(mma_done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.keys_map)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.scales_map)) : "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = *tmem_slot + (uint32_t)pl * kPipeCols;   // this pipeline's columns
 
-  if (warp == kWarpTma) {
+  if (role == kRoleProd) {
     // ---- producer (whole warp; lane 0 does the atomics, waits and copies).
-    // Work comes in chunks of one unit's tiles from that unit's counter; a
-    // CTA starts on its home unit (CTAs spread over the units in proportion
-    // to their tiles) and stays on a unit until it runs dry, then moves to
-    // the unit with the most tiles left.  Chunks shrink as a unit's work runs
-    // out, and the next chunk is taken one chunk early.  Consecutive tiles of
-    // one unit form a run; for each run the warp writes the unit's B operand
-    // into one of two slots.  Each tile's codes go into the ring (with the
-    // run number for the converters and the MMA lane) and its flat id into
-    // the id ring (for the epilogue).  After the last tile the producer marks
-    // the end: one stage for the converters (which pass it on to the MMA
-    // lane) and kEpiGroups id slots for the epilogue groups (each group reads
-    // ahead to its next own tile).
-    const int grid = (int)gridDim.x, n_units = p.b.n_units;
-    auto tiles_of = [&](int uu) { return p.tile_start[uu + 1] - p.tile_start[uu]; };
-    auto chunk = [&](int uu, int seen) {
-      const int64_t share = (int64_t)grid * tiles_of(uu) / total;
-      const int c = (int)((tiles_of(uu) - seen) / (kChunkDiv * (share < 1 ? 1 : share)));
-      return c < 1 ? 1 : (c > kChunkMax ? kChunkMax : c);
-    };
-    int u = unit_of_tile(p, (int)((int64_t)blockIdx.x * total / grid));
-    int t = 0, t_end = 0;            // current chunk: local tiles [t, t_end) of unit u
-    int pref = 0, pref_sz = 0;       // next chunk of unit u (value valid in lane 0)
-    bool have_pref = false, first = true, done = false, ok = true;
-    int run = -1, run_u = -1;        // current run and its unit
-    int64_t n = 0;
-    const uint8_t* keys = nullptr;
-    int i = 0;
-    for (;; ++i) {
-      while (t >= t_end) {
-        if (have_pref) {
-          have_pref = false;
-          const int s0 = __shfl_sync(0xFFFFFFFFu, pref, 0);
-          if (s0 < tiles_of(u)) {
-            t = s0;
-            t_end = s0 + pref_sz < tiles_of(u) ? s0 + pref_sz : tiles_of(u);
-          }
-        } else {
-          int uu = u, rem = tiles_of(u);
-          if (!first) {
-            // the unit with the most tiles left (lowest index on ties)
-            uu = -1;
-            rem = 0;
-            for (int v = lane; v < n_units; v += 32) {
-              const int r = tiles_of(v) - ld_relaxed_gpu(unit_counter(p.b, v));
-              if (r > rem) { rem = r; uu = v; }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              const int r2 = __shfl_xor_sync(0xFFFFFFFFu, rem, o);
-              const int u2 = __shfl_xor_sync(0xFFFFFFFFu, uu, o);
-              if (r2 > rem || (r2 == rem && (unsigned)u2 < (unsigned)uu)) { rem = r2; uu = u2; }
-            }
-            if (uu < 0) { done = true; break; }
-          }
-          first = false;
-          const int sz = chunk(uu, tiles_of(uu) - rem);
-          int s0 = 0;
-          if (lane == 0) s0 = atomicAdd(unit_counter(p.b, uu), sz);
-          s0 = __shfl_sync(0xFFFFFFFFu, s0, 0);
-          if (s0 >= tiles_of(uu)) continue;   // ran dry meanwhile: look again
-          u = uu;
-          t = s0;
-          t_end = s0 + sz < tiles_of(u) ? s0 + sz : tiles_of(u);
+    // Stream position i holds the i-th tile this pipeline takes; after the
+    // last one the producer marks the end in the next position.
+    // Work: chunks of kChunk tiles of one unit from that unit's counter.  A
+    // pipeline starts on its home unit (pipelines spread over the units in
+    // proportion to their tiles) and stays on a unit until it runs dry, then
+    // moves to the unit with the most tiles left; so it switches units (and
+    // builds query pieces) rarely.  The next chunk is taken one chunk early.
+    const int n_units = p.b.n_units;
+    const int n_pipes = (int)gridDim.x * kPipes, me = (int)blockIdx.x * kPipes + pl;
+    auto tiles_of = [&](int v) { return p.tile_start[v + 1] - p.tile_start[v]; };
+    int cu = unit_of_tile(p, (int)((int64_t)me * total / n_pipes));
+    int c0 = 0, c1 = 0;               // current chunk: local tiles [c0, c1) of unit cu
+    int pre = 0;                      // next chunk of unit cu (lane 0), valid when have_pre
+    bool have_pre = false, first = true;
+    int i = 0, run = -1, run_u = -1, s_run = 0;
+    int64_t row0 = p.b.unit_row(cu);
+    bool ok = true;
+    for (;;) {
+      // ---- next chunk
+      bool done = false;
+      for (;;) {
+        if (have_pre) {
+          have_pre = false;
+          const int t = __shfl_sync(0xFFFFFFFFu, pre, 0);
+          if (t < tiles_of(cu)) { c0 = t; break; }
         }
-        if (t < t_end && t_end < tiles_of(u)) {   // take the next chunk early
-          pref_sz = chunk(u, t_end);
-          if (lane == 0) pref = atomicAdd(unit_counter(p.b, u), pref_sz);
-          have_pref = true;
+        int uu = cu;
+        if (!first) {
+          // the unit with the most tiles left (lowest index on ties)
+          int rem = 0;
+          uu = -1;
+          for (int v = lane; v < n_units; v += 32) {
+            const int rv = tiles_of(v) - ld_relaxed_gpu(unit_counter(p.b, v));
+            if (rv > rem) { rem = rv; uu = v; }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const int r2 = __shfl_xor_sync(0xFFFFFFFFu, rem, o);
+            const int u2 = __shfl_xor_sync(0xFFFFFFFFu, uu, o);
+            if (r2 > rem || (r2 == rem && (unsigned)u2 < (unsigned)uu)) { rem = r2; uu = u2; }
+          }
+          if (uu < 0) { done = true; break; }
+        }
+        first = false;
+        int t = 0;
+        if (lane == 0) t = atomicAdd(unit_counter(p.b, uu), kChunk);
+        t = __shfl_sync(0xFFFFFFFFu, t, 0);
+        if (t < tiles_of(uu)) {
+          if (uu != cu) { cu = uu; row0 = p.b.unit_row(cu); }
+          c0 = t;
+          break;
         }
       }
       if (done) break;
-      if (u != run_u) {
-        // new run: B operand of unit u into slot run & 1, once the MMAs of
+      c1 = c0 + kChunk < tiles_of(cu) ? c0 + kChunk : tiles_of(cu);
+      if (c1 < tiles_of(cu)) {          // take the next chunk of this unit early
+        if (lane == 0) pre = atomicAdd(unit_counter(p.b, cu), kChunk);
+        have_pre = true;
+      }
+      if (cu != run_u) {
+        // new run: pieces of unit cu into slot run & 1, once the MMAs of
         // run - 2 (the slot's last user) have completed
         ++run;
-        run_u = u;
         const int slot = run & 1;
         if (run >= 2) {
-          if (lane == 0)
-            ok = mbar_wait(b_empty(slot), (uint32_t)((run >> 1) - 1) & 1u, p.b.err, run);
-          if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) break;
+          if (lane == 0) ok = mbar_wait(b_empty(slot), (uint32_t)((run >> 1) - 1) & 1u, p.b.err, run);
+          ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
+          if (!ok) break;
         }
-        uint8_t* B = smem + kOffB + slot * kBSlotBytes;
-        const float* qu = p.q_idx + (int64_t)u * kIndexHeads * kIndexDim;
-        constexpr int kPerLane = kIndexHeads * kIndexDim / 32;
-        float qv[kPerLane];            // all loads in flight before the first store
-#pragma unroll
-        for (int k = 0; k < kPerLane; ++k) qv[k] = qu[lane + 32 * k];
-#pragma unroll
-        for (int k = 0; k < kPerLane; ++k) {
-          const int e = lane + 32 * k, h = e >> 6, d = e & 63;
-          const __half qh = __float2half_rn(qv[k]);
-          const __half ql = __float2half_rn(qv[k] - __half2float(qh));
-          *reinterpret_cast<__half*>(B + sw128_off(h, d)) = qh;
-          *reinterpret_cast<__half*>(B + sw128_off(h + 8, d)) = ql;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(b_full(slot));
-          n = p.b.u[u].n;
-          keys = p.b.index_keys + p.b.unit_row(u) * kIndexDim;
-        }
+        s_run = build_pieces(p, cu, smem + kOffB + slot * kBBytes, lane);
+        run_u = cu;
+        if (lane == 0) mbar_arrive(b_full(slot));
       }
-      const int tg = p.tile_start[u] + t;      // flat tile id
       if (lane == 0) {
-        const int st = i % kStages, rs = i % kIdRing;
-        if (i >= kStages) ok = mbar_wait(raw_empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, tg);
-        if (ok && i >= kIdRing)
-          ok = mbar_wait(id_empty(rs), (uint32_t)(i / kIdRing - 1) & 1u, p.b.err, tg);
-        if (ok) {
-          id_ring[rs] = tg;
-          mbar_arrive(id_full(rs));
-          stage_meta[st] = run;
-          const int64_t tok0 = (int64_t)t * kTcTile;
-          const int64_t left = n - tok0;
-          const uint32_t bytes = (uint32_t)((left < kTcTile ? left : kTcTile) * kIndexDim);
-          tma_load_1d(sb + kOffRaw + st * kRawBytes, keys + tok0 * kIndexDim, bytes, raw_full(st));
+        for (int t = c0; t < c1; ++t, ++i) {
+          const int st = i % kStages;
+          if (i >= kStages && !(ok = mbar_wait(empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, t)))
+            break;
+          const int64_t row = row0 + (int64_t)t * kTile;   // first row of the tile
+          const int64_t x0 = row & ~7ll;
+          stage_meta[st] = make_int4(cu, t, run | ((s_run + 1024) << kRunBits), (int)(row - x0));
+          tma_load_tile(sb + kOffRaw + st * kRawBytes, &p.keys_map, (int32_t)row,
+                        sb + kOffScale + st * kScaleSlot, &p.scales_map, (int32_t)x0, full(st));
         }
       }
-      if (!__shfl_sync(0xFFFFFFFFu, (int)ok, 0)) break;
-      ++t;
+      ok = __shfl_sync(0xFFFFFFFFu, (int)ok, 0) != 0;
+      i = __shfl_sync(0xFFFFFFFFu, i, 0);
+      if (!ok) break;
     }
-    if (ok && lane == 0) {
+    if (lane == 0) {
+      // no copy of this pipeline may still be landing when the CTA exits:
+      // wait for the last load of every stage (on the normal path the
+      // consumers do too)
+      for (int j = (i > kStages ? i - kStages : 0); j < i && ok; ++j)
+        ok = mbar_wait(full(j % kStages), (uint32_t)(j / kStages) & 1u, p.b.err, -1);
+      // end marker (the MMA lane and the workers read it)
       const int st = i % kStages;
-      if (i < kStages || mbar_wait(raw_empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, -1)) {
-        stage_meta[st] = kEndOfWork;
-        mbar_arrive(raw_full(st));
-      }
-      for (int j = i; j < i + kEpiGroups; ++j) {
-        const int rs = j % kIdRing;
-        if (j >= kIdRing && !mbar_wait(id_empty(rs), (uint32_t)(j / kIdRing - 1) & 1u, p.b.err, -1))
-          break;
-        id_ring[rs] = kEndOfWork;
-        mbar_arrive(id_full(rs));
+      if (ok && (i < kStages || mbar_wait(empty(st), (uint32_t)(i / kStages - 1) & 1u, p.b.err, -1))) {
+        stage_meta[st] = make_int4(kEndOfWork, 0, 0, 0);
+        mbar_arrive(full(st));
       }
     }
-  } else if (warp < kWarpMma) {
-    // ---- converters: e4m3 codes -> f16 A operand (exact); the stage's run
-    // number travels on with the A buffer
-    const int c = tid - 32 * kWarpConv0;  // 0..127
-    for (int i = 0;; ++i) {
-      const int st = i % kStages, ab = i % kABufs;
-      if (!mbar_wait(raw_full(st), (uint32_t)(i / kStages) & 1u, p.b.err, i)) break;
-      const int run = stage_meta[st];
-      uint4 q[4];
-      if (run >= 0) {
-        const uint8_t* raw = smem + kOffRaw + st * kRawBytes;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4*>(raw + (k * 128 + c) * 16);
-        mbar_arrive(raw_empty(st));
-      }
-      if (i >= kABufs && !mbar_wait(a_empty(ab), (uint32_t)(i / kABufs - 1) & 1u, p.b.err, i))
-        break;
-      if (c == 0) a_meta[ab] = run;
-      if (run < 0) {                  // end of the stream: hand it to the MMA lane
-        mbar_arrive(a_full(ab));
-        break;
-      }
-      uint8_t* A = smem + kOffA + ab * kABufBytes;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int lc = k * 128 + c;           // 16-byte chunk of codes in the tile
-        const int row = lc >> 2, q16 = lc & 3; // token row, which 16 of its 64 codes
-        uint32_t h[8];
-        e4m3x4_to_f16x4(q[k].x, h[0], h[1]);
-        e4m3x4_to_f16x4(q[k].y, h[2], h[3]);
-        e4m3x4_to_f16x4(q[k].z, h[4], h[5]);
-        e4m3x4_to_f16x4(q[k].w, h[6], h[7]);
-        uint8_t* dst = A + row * kRowBytes128;   // f16 chunks 2*q16 and 2*q16+1, swizzled
-        *reinterpret_cast<uint4*>(dst + ((((2 * q16) ^ row) & 7) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(dst + ((((2 * q16 + 1) ^ row) & 7) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(a_full(ab));
-    }
-  } else if (warp == kWarpMma) {
-    // ---- MMA issue, lane 0 alone: per tile four tcgen05.mma (K = 16 each)
-    // into a 16-column accumulator; at a new run it releases the previous
-    // run's B slot (commit: arrives once those MMAs are done) and waits for
-    // the new slot to be written.
+  } else if (role == kRoleMma) {
+    // ---- MMA issue, lane 0 alone: per tile two tcgen05.mma (K = 32 each)
+    // into one accumulator, then commits that free the stage and publish the
+    // accumulator.  At a new run the lane releases the previous run's B slot
+    // (commit: arrives once those MMAs are done) and waits for the new slot.
     if (lane == 0) {
       int cur_run = -1;
       for (int i = 0;; ++i) {
-        const int ab = i % kABufs, db = i % kDBufs;
-        if (!mbar_wait(a_full(ab), (uint32_t)(i / kABufs) & 1u, p.b.err, i)) break;
-        const int run = a_meta[ab];
-        if (run < 0) break;
+        const int st = i % kStages, db = i % kDBufs;
+        if (!mbar_wait(full(st), (uint32_t)(i / kStages) & 1u, p.b.err, i)) break;
+        const int4 m = stage_meta[st];
+        if (m.x < 0) break;
+        const int run = m.z & ((1 << kRunBits) - 1);
         if (run != cur_run) {
           if (cur_run >= 0) tc_commit(b_empty(cur_run & 1));
           cur_run = run;
@@ -608,92 +489,88 @@ index_score_tc_kernel(const IndexScoreParams p) {
         }
         if (i >= kDBufs && !mbar_wait(d_empty(db), (uint32_t)(i / kDBufs - 1) & 1u, p.b.err, i)) break;
         tc_fence_after();
-        const uint32_t a0 = sb + kOffA + ab * kABufBytes;
-        const uint32_t b0 = sb + kOffB + (run & 1) * kBSlotBytes;
-        const uint32_t d = tmem + (uint32_t)(db * 16);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)   // columns 0-7: A . q_hi, columns 8-15: A . q_lo
-          tc_mma_f16(d, smem_desc_sw128(a0 + 32 * k), smem_desc_sw128(b0 + 32 * k), k > 0 ? 1u : 0u);
-        tc_commit(a_empty(ab));
+        const uint32_t a0 = sb + kOffRaw + st * kRawBytes;
+        const uint32_t b0 = sb + kOffB + (run & 1) * kBBytes;
+        const uint32_t d = tmem + (uint32_t)(db * kDStride);
+        tc_mma_f8(d, smem_desc_sw64(a0), smem_desc_sw64(b0), 0u);
+        tc_mma_f8(d, smem_desc_sw64(a0 + 32), smem_desc_sw64(b0 + 32), 1u);
+        tc_commit(empty(st));
         tc_commit(d_full(db));
       }
+      // every MMA issued above has completed once this arrives
+      tc_commit(mma_done);
+      mbar_wait(mma_done, 0, p.b.err, -1);
     }
     __syncwarp();
   } else {
-    // ---- epilogue: kEpiGroups groups of 4 warps; group g scores the tiles
-    // at stream positions g, g + kEpiGroups, ...  TMEM lane quarter =
-    // warp % 4, and the token of the tile = TMEM lane.  Each warp reads the
-    // tile ids two own tiles ahead and fetches those tiles' scales early.
-    static_assert(kWarpEpi0 == kWarpMma + 1, "warp roles");
-    constexpr int G = kEpiGroups;
-    const int grp = (warp - kWarpEpi0) >> 2;
+    // ---- workers: thread = token row r of the tile = tensor-memory lane r
+    // (lane quarter warp % 4).
     const int qtr = warp & 3;
-    const int e = qtr * 32 + lane;
-    auto peek = [&](int pos) -> int {
-      const int rs = pos % kIdRing;
-      int t = kWaitFailed;
-      if (lane == 0) {
-        if (mbar_wait(id_full(rs), (uint32_t)(pos / kIdRing) & 1u, p.b.err, pos)) t = id_ring[rs];
-        if (t >= 0) mbar_arrive(id_empty(rs));
-      }
-      return __shfl_sync(0xFFFFFFFFu, t, 0);
-    };
-    UnitCursor sc_cur;                 // unit of the scale cursor
-    int64_t sn = 0;
-    const uint16_t* sp = nullptr;
-    auto scale_of = [&](int t) -> uint16_t {
-      if (t < 0) return (uint16_t)0;
-      if (sc_cur.move_to(p, t)) {
-        sn = p.b.u[sc_cur.u].n;
-        sp = p.b.index_scales + p.b.unit_row(sc_cur.u);
-      }
-      const int64_t tk = (int64_t)(t - sc_cur.ts) * kTcTile + e;
-      return tk < sn ? sp[tk] : (uint16_t)0;
-    };
-    UnitCursor cur;
-    int64_t n = 0;
+    const int r = qtr * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(qtr * 32) << 16);
+    int eu = -1;                       // unit of the scoring cursor
+    int64_t en = 0;
     float* out = nullptr;
-    float w[kIndexHeads];
-    int idA = peek(grp);
-    int idB = idA >= 0 ? peek(grp + G) : kEndOfWork;
-    uint16_t scA = scale_of(idA), scB = scale_of(idB);
-    for (int i = grp; idA >= 0; i += G) {
-      const int t = idA, db = i % kDBufs;
-      const int idC = idB >= 0 ? peek(i + 2 * G) : kEndOfWork;
-      const uint16_t scC = scale_of(idC);
-      if (cur.move_to(p, t)) {
-        n = p.b.u[cur.u].n;
-        out = p.blk + (int64_t)cur.u * p.blk_stride;
-#pragma unroll
-        for (int h = 0; h < kIndexHeads; ++h) w[h] = p.w[(int64_t)cur.u * kIndexHeads + h];
+    for (int i = 0;; ++i) {
+      const int st = i % kStages, db = i % kDBufs;
+      if (!mbar_wait(full(st), (uint32_t)(i / kStages) & 1u, p.b.err, i)) break;
+      const int4 m = stage_meta[st];
+      if (m.x < 0) break;
+      const float sc_raw = __half2float(__ushort_as_half(
+          *reinterpret_cast<const uint16_t*>(smem + kOffScale + st * kScaleSlot + 2 * (m.w + r))));
+      mbar_arrive(empty(st));
+      // undo the pieces' common scale 2^s together with the token's scale
+      const float sc = ldexpf(sc_raw, -((m.z >> kRunBits) - 1024));
+      if (m.x != eu) {
+        eu = m.x;
+        en = p.b.u[eu].n;
+        out = p.blk + (int64_t)eu * p.blk_stride;
       }
-      const float sc = __half2float(__ushort_as_half(scA));
-      if (!mbar_wait(d_full(db), (uint32_t)(i / kDBufs) & 1u, p.b.err, t)) break;
+      const float* wu = p.w + (int64_t)eu * kIndexHeads;
+      if (!mbar_wait(d_full(db), (uint32_t)(i / kDBufs) & 1u, p.b.err, i)) break;
       tc_fence_after();
-      float v[16];
-      tc_ld16(tmem + ((uint32_t)(qtr * 32) << 16) + (uint32_t)(db * 16), v);
+      // columns 8p + h: piece p of head h; y_h = sum_p 16^-p * D[8p + h] (Horner)
+      const uint32_t dcol = lane_base + (uint32_t)(db * kDStride);
+      float y[kIndexHeads];
+      {
+        uint32_t v4[8], v23[16], v01[16];
+        tc_ld8(dcol + 32, v4);
+        tc_ld16(dcol + 16, v23);
+        tc_ld16(dcol, v01);
+        tc_wait_ld();
+        tc_reg_fence(v4);
+        tc_reg_fence(v23);
+        tc_reg_fence(v01);
+        auto f = [](uint32_t x) { return __uint_as_float(x); };
+#pragma unroll
+        for (int h = 0; h < kIndexHeads; ++h) {
+          float a = fmaf(f(v4[h]), 0.0625f, f(v23[8 + h]));
+          a = fmaf(a, 0.0625f, f(v23[h]));
+          a = fmaf(a, 0.0625f, f(v01[8 + h]));
+          y[h] = fmaf(a, 0.0625f, f(v01[h]));
+        }
+      }
       tc_fence_before();
       mbar_arrive(d_empty(db));
-      const int64_t tok = (int64_t)(t - cur.ts) * kTcTile + e;
+      const int64_t tok = (int64_t)m.y * kTile + r;
       float s = -INFINITY;
-      if (tok < n) {
+      if (tok < en) {
         s = 0.f;
 #pragma unroll
-        for (int h = 0; h < kIndexHeads; ++h) s = fmaf(w[h], fmaxf((v[h] + v[h + 8]) * sc, 0.f), s);
+        for (int h = 0; h < kIndexHeads; ++h) s = fmaf(__ldg(wu + h), fmaxf(y[h] * sc, 0.f), s);
       }
       s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
       s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));
-      if ((lane & 3) == 0 && tok < n) out[tok >> 2] = s;
-      idA = idB; idB = idC;
-      scA = scB; scB = scC;
+      if ((lane & 3) == 0 && tok < en) out[tok >> 2] = s;
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kWarpMma)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+  if (warp == kRoleMma)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot),
+                 "r"(kTmemCols)
                  : "memory");
   // the last CTA to finish re-arms the work counters for the next call
   if (tid == 0) {
@@ -701,7 +578,8 @@ index_score_tc_kernel(const IndexScoreParams p) {
     __threadfence();
     if (atomicAdd(finished, 1) == (int)gridDim.x - 1) {
       __threadfence();
-      for (int uu = 0; uu < p.b.n_units; ++uu) *reinterpret_cast<volatile int32_t*>(unit_counter(p.b, uu)) = 0;
+      for (int uu = 0; uu < p.b.n_units; ++uu)
+        *reinterpret_cast<volatile int32_t*>(unit_counter(p.b, uu)) = 0;
       *reinterpret_cast<volatile int32_t*>(finished) = 0;
     }
   }
@@ -709,45 +587,73 @@ index_score_tc_kernel(const IndexScoreParams p) {
 
 }  // namespace
 
-cudaError_t launch_index_score(const BatchDesc& b, const float* q_idx, const float* w,
+cudaError_t make_index_maps(CUtensorMap* keys_map, const void* keys, CUtensorMap* scales_map,
+                            const void* scales, int64_t rows) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+  static Encode encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<Encode>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)kIndexDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kIndexDim};
+  const cuuint32_t box[2] = {(cuuint32_t)kIndexDim, (cuuint32_t)kTile};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = encode(keys_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(keys), dims,
+                      strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const cuuint64_t sdims[1] = {(cuuint64_t)rows};
+  const cuuint32_t sbox[1] = {(cuuint32_t)kScaleBox};
+  r = encode(scales_map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, const_cast<void*>(scales), sdims,
+             strides /* unused at rank 1 */, sbox, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_index_score(const BatchDesc& b, const CUtensorMap* keys_map,
+                               const CUtensorMap* scales_map, const float* q_idx, const float* w,
                                float* blk_scores, int64_t blk_stride, cudaStream_t s) {
-  IndexScoreParams p;
-  p.b = b;
-  p.q_idx = q_idx;
-  p.w = w;
-  p.blk = blk_scores;
-  p.blk_stride = blk_stride;
-#ifdef QSA_INDEX_SCORE_FFMA
-  const int unit_tokens = kTileTokens;
-#else
-  const int unit_tokens = kTcTile;
   static bool attr_set = false;
   static int sm_count = 0;
   if (!attr_set) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = prefer_max_shared(index_score_tc_kernel, kTcSmemBytes);
+    if (e == cudaSuccess) e = prefer_max_shared(index_score_tc_kernel, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-#endif
+  IndexScoreParams p;
+  p.keys_map = *keys_map;
+  p.scales_map = *scales_map;
+  p.b = b;
+  p.q_idx = q_idx;
+  p.w = w;
+  p.blk = blk_scores;
+  p.blk_stride = blk_stride;
   int64_t tiles = 0;
   for (int u = 0; u < b.n_units; ++u) {
     p.tile_start[u] = (int32_t)tiles;
-    tiles += (b.u[u].n + unit_tokens - 1) / unit_tokens;
+    tiles += (b.u[u].n + kTile - 1) / kTile;
   }
   p.tile_start[b.n_units] = (int32_t)tiles;
   if (tiles <= 0) return cudaSuccess;
-  if (tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-#ifdef QSA_INDEX_SCORE_FFMA
-  index_score_kernel<<<(unsigned)tiles, kThreads, 0, s>>>(p);
-#else
+  if (tiles > (1ll << 30)) return cudaErrorInvalidValue;
   const int64_t cap = (int64_t)kCtasPerSm * sm_count;
-  const unsigned grid = (unsigned)(tiles < cap ? tiles : cap);
-  index_score_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, s>>>(p);
-#endif
+  const int64_t chunks = (tiles + kChunk - 1) / kChunk;
+  const unsigned grid = (unsigned)(chunks < cap ? chunks : cap);
+  index_score_tc_kernel<<<grid, kThreadsTc, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -83,6 +83,8 @@ qsa_status_t qsa::set_last_error(qsa_status_t status, const char* message) {
 }
 
 struct qsa_cache {
+  CUtensorMap keys_map;       // TMA views of the index keys and scales (64-byte aligned)
+  CUtensorMap scales_map;
   qsa_cache_config cfg;
   bool has_device = false;
   int64_t staging_total = 0;
@@ -229,7 +231,19 @@ qsa_status_t qsa_cache_create(const qsa_cache_config* c, qsa_cache** out) {
   if (c->hbm_pool_rows > staging) cache->free_rows[staging] = c->hbm_pool_rows - staging;
 
   if (all) {
-    cudaError_t e = cudaMemset(c->workspace, 0, (size_t)c->workspace_bytes);
+    const int64_t key_rows = (int64_t)c->max_requests * c->n_layers * c->ctx_capacity;
+    if (key_rows >= (1ll << 31)) {
+      delete cache;
+      return fail(QSA_ERR_INVALID_ARG, "%lld index-key rows exceed the 2^31 rows a TMA view addresses",
+                  (long long)key_rows);
+    }
+    cudaError_t e = make_index_maps(&cache->keys_map, c->index_keys, &cache->scales_map,
+                                    c->index_scales, key_rows);
+    if (e != cudaSuccess) {
+      delete cache;
+      return cuda_fail(e, "encoding the index-key tensor maps");
+    }
+    e = cudaMemset(c->workspace, 0, (size_t)c->workspace_bytes);
     if (e == cudaSuccess)
       e = cudaMemset(c->slot_table, 0xFF,
                      (size_t)c->max_requests * c->n_layers * c->ctx_capacity * sizeof(int32_t));
@@ -419,7 +433,7 @@ qsa_status_t qsa_index_score(qsa_cache* c, const qsa_batch* batch, const float* 
     if (blk_stride < (d.u[u].n + 3) / 4)
       return fail(QSA_ERR_INVALID_ARG, "blk_stride %lld < %lld blocks of unit %d",
                   (long long)blk_stride, (long long)((d.u[u].n + 3) / 4), u);
-  cudaError_t e = launch_index_score(d, q_idx, w, blk_scores, blk_stride,
+  cudaError_t e = launch_index_score(d, &c->keys_map, &c->scales_map, q_idx, w, blk_scores, blk_stride,
                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "index-score launch");
   return ok();

@@ -2,6 +2,7 @@
 // QSA decode-step library.  Not part of the public interface (include/qsa.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -119,8 +120,17 @@ cudaError_t prefer_max_shared(Kernel kernel, int dynamic_smem_bytes) {
 // ------------------------------------------------------------ launchers
 // Each returns the launch status (cudaGetLastError right after the launch).
 
-cudaError_t launch_index_score(const BatchDesc& b, const float* q_idx, const float* w,
+// keys_map, scales_map: TMA tensor maps of the index keys (uint8 [rows][64])
+// and scales (fp16 [rows]), rows = max_requests * n_layers * ctx_capacity
+// (made by make_index_maps).
+cudaError_t launch_index_score(const BatchDesc& b, const CUtensorMap* keys_map,
+                               const CUtensorMap* scales_map, const float* q_idx, const float* w,
                                float* blk_scores, int64_t blk_stride, cudaStream_t s);
+
+// Encode the tensor maps of the index keys at `keys` and the scales at
+// `scales`, `rows` rows each.
+cudaError_t make_index_maps(CUtensorMap* keys_map, const void* keys, CUtensorMap* scales_map,
+                            const void* scales, int64_t rows);
 
 cudaError_t launch_select_topk(const BatchDesc& b, const float* blk_scores, int64_t blk_stride,
                                int32_t k_max, int32_t* sel_blocks, int32_t* n_sel,
