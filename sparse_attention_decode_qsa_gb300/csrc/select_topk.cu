@@ -10,9 +10,10 @@
 // find the key T of the K-th best block and how many blocks equal to T must
 // be kept; then one stable compaction in id order keeps every block above T
 // and the first (lowest-id) blocks equal to T.  The compaction order gives the
-// ascending-id output directly, and the tie rule falls out of it.  One CTA of
-// 1024 threads per unit; the block scores were just written by the indexer
-// and are read from L2.
+// ascending-id output directly, and the tie rule falls out of it.  Units of
+// up to 1M tokens use a cluster of 8 CTAs (below); longer ones one CTA of
+// 1024 threads.  The block scores were just written by the indexer and are
+// read from L2.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -137,24 +138,36 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const TopkParams 
 
 
 // ---------------------------------------------------------------------------
-// Cluster version: a cluster of kClusterCtas CTAs per unit.  CTA r keeps the
-// keys of its slice [r*S, (r+1)*S) of the unit's blocks in shared memory, so
-// the three radix passes (11, 11 and 10 bits) read no global memory.  Each
-// pass builds a local histogram, then every CTA sums all CTAs' histograms
-// through distributed shared memory and finds the threshold digit itself
-// (all CTAs reach the same answer).  The compaction exchanges per-CTA counts
-// of blocks above and equal to the threshold the same way, so every CTA
-// writes its selected ids at their global ascending-id positions.
+// Cluster version: a cluster of kClusterCtas CTAs of 512 threads per unit.
+// CTA r keeps the keys of its slice [r*S, (r+1)*S) of the unit's blocks in
+// shared memory.  The first digit (the top 11 bits of the key) is found from
+// a histogram that every CTA sums over all CTAs through distributed shared
+// memory (warp-aggregated atomics: block scores crowd into a few exponent
+// bins).  If the boundary bin holds at most kCandMax keys - the usual case -
+// the CTAs send those keys to CTA 0, which finishes the radix select alone
+// and publishes the threshold key T and the number of T-ties to keep; else
+// two more cluster-wide passes (11 and 10 bits) do it.  The compaction
+// exchanges per-CTA counts of blocks above and equal to T, so every CTA
+// writes its selected ids at their global ascending-id positions.  A CTA
+// takes half an SM's registers, so it can share an SM with other kernels.
 constexpr int kClusterCtas = 8;
+constexpr int kCThreads = 512;
+constexpr int kCWarps = kCThreads / 32;
 constexpr int kMaxSlice = 32768;  // keys per CTA: 8 x 32768 blocks = 1M tokens
 constexpr int kBins = 2048;
-constexpr int kClusterSmem = kMaxSlice * 4;
+constexpr int kCandMax = 2048;    // boundary-bin keys finished by CTA 0
+constexpr int kSubHists = 4;      // first-digit histogram copies (warps w % 4), less contention
+static_assert(kCandMax * 8 <= kSubHists * kBins * 4, "candidates reuse the sub-histograms");
 
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -172,16 +185,77 @@ __device__ __forceinline__ uint32_t ld_dsmem(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_dsmem(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
-__global__ void __launch_bounds__(kThreads, 1) select_topk_cluster_kernel(const TopkParams p) {
-  extern __shared__ __align__(16) uint32_t keys[];  // [kMaxSlice]
+// Digit of the krem-th largest key from a histogram of nbins bins (counted
+// from the top): *digit, and *krem_out = its rank within that bin.  Called by
+// the whole CTA; the results are valid after the closing __syncthreads().
+__device__ __forceinline__ void find_digit(const uint32_t* h, uint32_t nbins, uint32_t krem,
+                                           uint32_t* warp_sum, uint32_t* digit,
+                                           uint32_t* krem_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (int)nbins / kCWarps;  // bins per warp, from the top: 128 or 64
+  {
+    uint32_t sum = 0;
+    for (int j = lane; j < per; j += 32) sum += h[nbins - 1 - (warp * per + j)];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane == 0) warp_sum[warp] = sum;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t ws = lane < kCWarps ? warp_sum[lane] : 0u;
+    uint32_t incl = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - ws;
+    const bool mine = lane < kCWarps && excl < krem && krem <= incl;
+    const uint32_t owners = __ballot_sync(0xFFFFFFFFu, mine);
+    const uint32_t owner = owners ? (uint32_t)(__ffs(owners) - 1) : 0u;  // always one by construction
+    uint32_t cum = __shfl_sync(0xFFFFFFFFu, excl, owner);
+    for (int j0 = 0; j0 < per; j0 += 32) {
+      const uint32_t c = h[nbins - 1 - (owner * per + j0 + lane)];
+      uint32_t ic = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+        if (lane >= o) ic += v;
+      }
+      const uint32_t ex = cum + ic - c;
+      const uint32_t hb = __ballot_sync(0xFFFFFFFFu, ex < krem && krem <= cum + ic);
+      if (hb) {
+        const int hl = __ffs(hb) - 1;
+        if (lane == hl) {
+          *digit = nbins - 1 - (owner * per + j0 + hl);
+          *krem_out = krem - ex;
+        }
+        break;
+      }
+      cum += __shfl_sync(0xFFFFFFFFu, ic, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// 40 registers x 512 threads: a CTA fits on an SM beside two index-score CTAs.
+__global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, int slice_cap) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  uint32_t* keys = dyn;                                   // [slice_cap]
+  uint32_t* sub = dyn + slice_cap;                        // [kSubHists][kBins], first digit
+  // later, in CTA 0, the same space holds the boundary-bin candidates
+  uint32_t* cand_key = sub;                               // [kCandMax]: low 21 bits
+  uint32_t* cand_id = sub + kCandMax;                     // [kCandMax]: block ids
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t tot[kBins];
-  __shared__ uint32_t warp_sum[kWarps];
-  __shared__ uint32_t s_digit, s_krem;
+  __shared__ uint32_t warp_sum[kCWarps];
+  __shared__ uint32_t s_digit, s_krem, s_T, s_base, s_pos;
   __shared__ uint32_t s_cnt[2];
-  __shared__ uint32_t warp_gt[kWarps], warp_eq[kWarps];
-  __shared__ uint32_t s_tot_gt, s_tot_eq;
+  __shared__ uint32_t warp_gt[kCWarps], warp_eq[kCWarps];
 
   const uint32_t rank = cluster_rank();
   const int u = blockIdx.x / kClusterCtas;
@@ -197,155 +271,185 @@ __global__ void __launch_bounds__(kThreads, 1) select_topk_cluster_kernel(const 
   if (rank == 0 && tid == 0) p.n_sel[u] = K;
 
   if (K == nb) {  // dense path: every block, in order
-    for (int i = tid; i < cnt; i += kThreads) sel[lo + i] = (int32_t)(lo + i);
+    for (int i = tid; i < cnt; i += kCThreads) sel[lo + i] = (int32_t)(lo + i);
     return;       // uniform across the cluster: no DSMEM access follows
   }
 
-  for (int i = tid; i < cnt; i += kThreads) keys[i] = order_key(s[lo + i]);
+  for (int i = tid; i < kSubHists * kBins; i += kCThreads) sub[i] = 0;
+  __syncthreads();
 
-  uint32_t prefix = 0, mask = 0, krem = (uint32_t)K;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);  // digits of 11, 11, 10 bits
-    const uint32_t nbins = pass == 2 ? 1024u : 2048u;
-    if (pass > 0) cluster_wait();            // every CTA finished reading my hist
-    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < cnt; i += kThreads) {
-      const uint32_t k = keys[i];
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
+  // ---- first digit: bits 31..21, counted into kSubHists copies while the
+  // keys are loaded, then folded into hist
+  {
+    uint32_t* h = sub + (warp % kSubHists) * kBins;
+    for (int i = tid; i < cnt; i += kCThreads) {
+      const uint32_t k = order_key(s[lo + i]);
+      keys[i] = k;
+      atomicAdd(&h[k >> 21], 1u);
     }
-    __syncthreads();
-    cluster_arrive();
-    cluster_wait();                           // all histograms complete
-    for (int b = tid; b < (int)nbins; b += kThreads) {
+  }
+  __syncthreads();
+  for (int b = tid; b < kBins; b += kCThreads) {
+    uint32_t t = 0;
+#pragma unroll
+    for (int c = 0; c < kSubHists; ++c) t += sub[c * kBins + b];
+    hist[b] = t;
+  }
+  __syncthreads();
+  cluster_sync();                              // all histograms complete
+  {
+    constexpr int kPer = kBins / kCThreads;    // 4 bins per thread, all loads in flight at once
+    uint32_t v[kPer][kClusterCtas];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+#pragma unroll
+      for (int c = 0; c < kClusterCtas; ++c) v[j][c] = ld_dsmem(dsmem_addr(&hist[tid + j * kCThreads], c));
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
       uint32_t t = 0;
 #pragma unroll
-      for (int c = 0; c < kClusterCtas; ++c) t += ld_dsmem(dsmem_addr(&hist[b], c));
-      tot[b] = t;
+      for (int c = 0; c < kClusterCtas; ++c) t += v[j][c];
+      tot[tid + j * kCThreads] = t;
     }
-    cluster_arrive();                         // done reading the others' hist
-    __syncthreads();
-    // threshold digit: scan bins from the top; warp w owns nbins/32 bins
-    const int per = (int)nbins / kWarps;      // 64 or 32
-    {
-      uint32_t sum = 0;
-      for (int j = lane; j < per; j += 32) sum += tot[nbins - 1 - (warp * per + j)];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-      if (lane == 0) warp_sum[warp] = sum;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t ws = warp_sum[lane];
-      uint32_t incl = ws;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const uint32_t excl = incl - ws;
-      const bool mine = excl < krem && krem <= incl;
-      const uint32_t owners = __ballot_sync(0xFFFFFFFFu, mine);
-      const uint32_t owner = owners ? (uint32_t)(__ffs(owners) - 1) : 0u;  // always one by construction
-      const uint32_t base = __shfl_sync(0xFFFFFFFFu, excl, owner);
-      // owner warp range, bins from the top: index j -> bin nbins-1-(owner*per+j)
-      uint32_t cum = base;
-      for (int j0 = 0; j0 < per; j0 += 32) {
-        const uint32_t c = tot[nbins - 1 - (owner * per + j0 + lane)];
-        uint32_t ic = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, ic, o);
-          if (lane >= o) ic += v;
-        }
-        const uint32_t ex = cum + ic - c;
-        const bool hit = ex < krem && krem <= cum + ic;
-        const uint32_t hb = __ballot_sync(0xFFFFFFFFu, hit);
-        if (hb) {
-          const int hl = __ffs(hb) - 1;
-          if (lane == hl) {
-            s_digit = nbins - 1 - (owner * per + j0 + hl);
-            s_krem = krem - ex;
-          }
-          break;
-        }
-        cum += __shfl_sync(0xFFFFFFFFu, ic, 31);
-      }
-    }
-    __syncthreads();
-    prefix |= s_digit << shift;
-    mask |= (nbins - 1) << shift;
-    krem = s_krem;
   }
-  const uint32_t T = prefix;
-
-  // ---- per-CTA counts above / equal to T, exchanged through DSMEM
-  {
-    uint32_t g = 0, e = 0;
-    for (int i = tid; i < cnt; i += kThreads) {
-      g += keys[i] > T;
-      e += keys[i] == T;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
-      e += __shfl_xor_sync(0xFFFFFFFFu, e, o);
-    }
-    if (lane == 0) { warp_gt[warp] = g; warp_eq[warp] = e; }
-    cluster_wait();                           // pass-2 readers of hist are done (s_cnt is separate)
-    __syncthreads();
+  __syncthreads();
+  find_digit(tot, kBins, (uint32_t)K, warp_sum, &s_digit, &s_krem);
+  const uint32_t d1 = s_digit;
+  uint32_t krem = s_krem;
+  uint32_t T;
+  if (tot[d1] <= (uint32_t)kCandMax) {
+    // ---- fast path: the boundary bin's keys go to CTA 0, which finishes
+    // the select on the low 21 bits (11 + 10) alone.  No CTA changes its
+    // histogram before the next cluster barrier, so the offsets read here
+    // (earlier CTAs' counts of bin d1) are stable.
     if (tid == 0) {
-      uint32_t tg = 0, te = 0;
-      for (int w = 0; w < kWarps; ++w) { tg += warp_gt[w]; te += warp_eq[w]; }
-      s_cnt[0] = tg;
-      s_cnt[1] = te;
+      uint32_t base = 0;
+      for (uint32_t c = 0; c < rank; ++c) base += ld_dsmem(dsmem_addr(&hist[d1], c));
+      s_base = base;
+      s_pos = 0;
     }
     __syncthreads();
+    for (int i = tid; i < cnt; i += kCThreads) {
+      const uint32_t k = keys[i];
+      if ((k >> 21) == d1) {
+        const uint32_t pos = s_base + atomicAdd(&s_pos, 1u);
+        st_dsmem(dsmem_addr(&cand_key[pos], 0), k & 0x1FFFFFu);
+        st_dsmem(dsmem_addr(&cand_id[pos], 0), (uint32_t)(lo + i));
+      }
+    }
+    cluster_sync();                            // candidates complete in CTA 0
+    if (rank == 0) {
+      const uint32_t ncand = tot[d1];
+      uint32_t prefix = 0, mask = 0;
+      for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const uint32_t nbins = pass == 0 ? 2048u : 1024u;
+        for (int i = tid; i < (int)nbins; i += kCThreads) hist[i] = 0;
+        __syncthreads();
+        for (int j = tid; j < (int)ncand; j += kCThreads) {
+          const uint32_t k = cand_key[j];
+          if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
+        }
+        __syncthreads();
+        find_digit(hist, nbins, krem, warp_sum, &s_digit, &s_krem);
+        prefix |= s_digit << shift;
+        mask |= (nbins - 1) << shift;
+        krem = s_krem;
+        __syncthreads();
+      }
+      if (tid == 0) s_T = (d1 << 21) | prefix;   // s_krem already holds the ties to keep
+    }
+    cluster_sync();                            // CTA 0 published T and the ties
+    T = ld_dsmem(dsmem_addr(&s_T, 0));
+    krem = ld_dsmem(dsmem_addr(&s_krem, 0));
+  } else {
+    // ---- general path: two more cluster-wide passes over every key
+    uint32_t prefix = d1 << 21, mask = 0x7FFu << 21;
+    for (int pass = 1; pass < 3; ++pass) {
+      const int shift = pass == 1 ? 10 : 0;
+      const uint32_t nbins = pass == 1 ? 2048u : 1024u;
+      cluster_sync();                          // every CTA finished reading my hist
+      for (int i = tid; i < kBins; i += kCThreads) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < cnt; i += kCThreads) {
+        const uint32_t k = keys[i];
+        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
+      }
+      __syncthreads();
+      cluster_sync();                          // all histograms complete
+      for (int b = tid; b < (int)nbins; b += kCThreads) {
+        uint32_t t = 0;
+#pragma unroll
+        for (int c = 0; c < kClusterCtas; ++c) t += ld_dsmem(dsmem_addr(&hist[b], c));
+        tot[b] = t;
+      }
+      __syncthreads();
+      find_digit(tot, nbins, krem, warp_sum, &s_digit, &s_krem);
+      prefix |= s_digit << shift;
+      mask |= (nbins - 1) << shift;
+      krem = s_krem;
+    }
+    T = prefix;
   }
-  cluster_arrive();
-  cluster_wait();
+
+  // ---- thread tid owns the contiguous keys [tid*per, tid*per + per) of the
+  // slice: it counts those above / equal to T, a block scan gives its
+  // offsets within the CTA, the CTAs exchange their totals through DSMEM,
+  // and the thread writes its selected ids (few) in id order.
+  const int per = (cnt + kCThreads - 1) / kCThreads;       // <= kPerThread
+  const int k0 = tid * per, k1 = k0 + per < cnt ? k0 + per : cnt;
+  uint32_t g = 0, e = 0;
+  for (int i = k0; i < k1; ++i) {
+    g += keys[i] > T;
+    e += keys[i] == T;
+  }
+  uint32_t ig = g, ie = e;                                 // inclusive scans within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, ig, o);
+    const uint32_t ve = __shfl_up_sync(0xFFFFFFFFu, ie, o);
+    if (lane >= o) { ig += vg; ie += ve; }
+  }
+  if (lane == 31) { warp_gt[warp] = ig; warp_eq[warp] = ie; }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t wg = lane < kCWarps ? warp_gt[lane] : 0u, we = lane < kCWarps ? warp_eq[lane] : 0u;
+    uint32_t sg = wg, se = we;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, sg, o);
+      const uint32_t ve = __shfl_up_sync(0xFFFFFFFFu, se, o);
+      if (lane >= o) { sg += vg; se += ve; }
+    }
+    if (lane < kCWarps) { warp_gt[lane] = sg - wg; warp_eq[lane] = se - we; }
+    if (lane == 31) { s_cnt[0] = sg; s_cnt[1] = se; }
+  }
+  __syncthreads();
+  cluster_sync();                                          // every CTA's totals are published
   uint32_t base_gt = 0, base_eq = 0;
   for (uint32_t c = 0; c < rank; ++c) {
     base_gt += ld_dsmem(dsmem_addr(&s_cnt[0], c));
     base_eq += ld_dsmem(dsmem_addr(&s_cnt[1], c));
   }
-
-  // ---- stable compaction of this slice in id order
-  uint32_t out_base = base_gt, eq_base = base_eq;  // counts before this chunk, globally
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < cnt; c0 += kThreads) {
-    const int i = c0 + tid;
-    const uint32_t k = i < cnt ? keys[i] : 0u;
-    const bool gt = i < cnt && k > T;
-    const bool eq = i < cnt && k == T;
-    const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), be = __ballot_sync(0xFFFFFFFFu, eq);
-    if (lane == 0) { warp_gt[warp] = __popc(bg); warp_eq[warp] = __popc(be); }
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t g = warp_gt[lane], e = warp_eq[lane];
-      uint32_t ig = g, ie = e;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, ig, o);
-        const uint32_t ve = __shfl_up_sync(0xFFFFFFFFu, ie, o);
-        if (lane >= o) { ig += vg; ie += ve; }
+  uint32_t gt_before = base_gt + warp_gt[warp] + ig - g;   // greater keys before mine, globally
+  uint32_t eq_before = base_eq + warp_eq[warp] + ie - e;   // T-equal keys before mine, globally
+  if (g + e > 0) {
+    for (int i = k0; i < k1; ++i) {
+      const uint32_t k = keys[i];
+      if (k > T) {
+        const uint32_t pos = gt_before + min(eq_before, krem);
+        if (pos < (uint32_t)K) sel[pos] = (int32_t)(lo + i);
+        ++gt_before;
+      } else if (k == T) {
+        if (eq_before < krem) {
+          const uint32_t pos = gt_before + eq_before;
+          if (pos < (uint32_t)K) sel[pos] = (int32_t)(lo + i);
+        }
+        ++eq_before;
       }
-      warp_gt[lane] = ig - g;
-      warp_eq[lane] = ie - e;
-      if (lane == 31) { s_tot_gt = ig; s_tot_eq = ie; }
     }
-    __syncthreads();
-    const uint32_t gt_before = out_base + warp_gt[warp] + __popc(bg & lt_mask);
-    const uint32_t eq_before = eq_base + warp_eq[warp] + __popc(be & lt_mask);
-    const bool take = gt || (eq && eq_before < krem);
-    const uint32_t pos = gt_before + min(eq_before, krem);
-    if (take && pos < (uint32_t)K) sel[pos] = (int32_t)(lo + i);
-    out_base += s_tot_gt;
-    eq_base += s_tot_eq;
-    __syncthreads();
   }
-  cluster_arrive();                            // keep s_cnt alive until every CTA read it
-  cluster_wait();
+  cluster_sync();                              // keep s_cnt and s_T alive until every CTA read them
 }
 
 }  // namespace
@@ -369,16 +473,19 @@ cudaError_t launch_select_topk(const BatchDesc& b, const float* blk_scores, int6
     select_topk_kernel<<<b.n_units, kThreads, 0, s>>>(p);
     return cudaGetLastError();
   }
+  constexpr int kMaxDynSmem = kMaxSlice * 4 + kSubHists * kBins * 4;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = prefer_max_shared(select_topk_cluster_kernel, kClusterSmem);
+    cudaError_t e = prefer_max_shared(select_topk_cluster_kernel, kMaxDynSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  // keys per CTA of the largest unit, rounded up to 16-byte multiples
+  const int slice_cap = (int)(((nb_max + kClusterCtas - 1) / kClusterCtas + 3) / 4 * 4);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(b.n_units * kClusterCtas);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kClusterSmem;
+  cfg.blockDim = dim3(kCThreads);
+  cfg.dynamicSmemBytes = (size_t)slice_cap * 4 + kSubHists * kBins * 4;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -387,7 +494,7 @@ cudaError_t launch_select_topk(const BatchDesc& b, const float* blk_scores, int6
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, select_topk_cluster_kernel, p);
+  return cudaLaunchKernelEx(&cfg, select_topk_cluster_kernel, p, slice_cap);
 }
 
 }  // namespace qsa

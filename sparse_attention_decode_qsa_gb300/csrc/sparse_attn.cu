@@ -49,7 +49,7 @@ constexpr int kSliceBytes = 2 * kHeadDim * 2;         // K[g] + V[g] of one toke
 constexpr int kWarpBufBytes = kWarpTokens * kSliceBytes;  // 4 KiB
 constexpr int kSmemBytes = kWarps * 2 * kWarpBufBytes;    // 64 KiB: fits beside other CTAs
 #ifndef QSA_ATTN_HOST_CTAS
-#define QSA_ATTN_HOST_CTAS 64
+#define QSA_ATTN_HOST_CTAS 32
 #endif
 constexpr int kMaxCtasHost = QSA_ATTN_HOST_CTAS;
 // Register budget per thread: at 80 one CTA (20 K registers) fits on an SM
