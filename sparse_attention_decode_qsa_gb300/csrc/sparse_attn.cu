@@ -25,7 +25,9 @@
 // (max, sum, acc) for its 4 heads over all its tokens.  At the end the two
 // token halves of each KV head are merged in shared memory and the CTA writes
 // one partial; a small second kernel merges the cpu partials of each
-// (unit, head) with the log-sum-exp rule.
+// (unit, head) with the log-sum-exp rule.  (Merging in the split kernel's
+// last CTA per unit was measured: the extra epilogue code halved the
+// streaming loop's host-read rate, even on launches that did not run it.)
 //
 // Per warp and split: logits with lane l holding dims 4l..4l+3 of the 4 query
 // heads, reduced across the warp with a transposing butterfly (6 shuffles
@@ -47,7 +49,11 @@ constexpr int kBlocksPerSplit = 4;                    // selected C4 blocks per 
 constexpr int kWarpTokens = 8;                        // tokens per warp and split
 constexpr int kSliceBytes = 2 * kHeadDim * 2;         // K[g] + V[g] of one token: 512
 constexpr int kWarpBufBytes = kWarpTokens * kSliceBytes;  // 4 KiB
-constexpr int kSmemBytes = kWarps * 2 * kWarpBufBytes;    // 64 KiB: fits beside other CTAs
+#ifndef QSA_ATTN_STAGES
+#define QSA_ATTN_STAGES 2
+#endif
+constexpr int kAStages = QSA_ATTN_STAGES;                 // splits in flight per warp
+constexpr int kSmemBytes = kWarps * kAStages * kWarpBufBytes;  // 64 KiB at 2 stages
 #ifndef QSA_ATTN_HOST_CTAS
 #define QSA_ATTN_HOST_CTAS 32
 #endif
@@ -89,7 +95,8 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint32_
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // The k-th split this CTA visits (0 <= k < count): alternately from the front
 // and the back of its list r, r + cpu, ...
@@ -134,14 +141,15 @@ __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int s
 }
 
 __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];  // [warp][2][8][512]
+  extern __shared__ __align__(16) uint8_t smem[];  // [warp][stage][8][512]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
+  __shared__ uint32_t vmask[kWarps][kAStages];     // tokens present in each stage
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
   const int u = blockIdx.x / p.cpu, r = blockIdx.x % p.cpu;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = warp & 3, half = warp >> 2;
-  uint8_t* wbuf = smem + warp * 2 * kWarpBufBytes;
+  uint8_t* wbuf = smem + warp * kAStages * kWarpBufBytes;
   int nsel = p.n_sel[u];
   if (nsel < 0 || nsel > p.k_max) {
     if (r == 0 && threadIdx.x == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
@@ -169,19 +177,28 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
 #pragma unroll
   for (int j = 0; j < kGroup; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  uint32_t valid_cur = 0, valid_next = 0;
-  int buf = 0;
-  if (count > 0) valid_next = issue_warp(p, u, visit_split(0, count, r, p.cpu), nsel, g, half, wbuf);
-  cp_async_commit();
-  for (int k = 0; k < count; ++k) {
-    valid_cur = valid_next;
-    if (k + 1 < count)
-      valid_next = issue_warp(p, u, visit_split(k + 1, count, r, p.cpu), nsel, g, half,
-                              wbuf + (buf ^ 1) * kWarpBufBytes);
+  // splits k + 1 .. k + kAStages - 1 are in flight while split k is computed
+#pragma unroll
+  for (int k = 0; k < kAStages - 1; ++k) {
+    if (k < count) {
+      const uint32_t v = issue_warp(p, u, visit_split(k, count, r, p.cpu), nsel, g, half,
+                                    wbuf + k * kWarpBufBytes);
+      if (lane == 0) vmask[warp][k] = v;
+    }
     cp_async_commit();
-    cp_async_wait_1();
+  }
+  for (int k = 0; k < count; ++k) {
+    const int kn = k + kAStages - 1;
+    if (kn < count) {   // its buffer was last read in iteration k - 1
+      const uint32_t v = issue_warp(p, u, visit_split(kn, count, r, p.cpu), nsel, g, half,
+                                    wbuf + (kn % kAStages) * kWarpBufBytes);
+      if (lane == 0) vmask[warp][kn % kAStages] = v;
+    }
+    cp_async_commit();
+    cp_async_wait<kAStages - 1>();
     __syncwarp();
-    const uint8_t* R = wbuf + buf * kWarpBufBytes;
+    const uint32_t valid_cur = vmask[warp][k % kAStages];
+    const uint8_t* R = wbuf + (k % kAStages) * kWarpBufBytes;
 
     // logits: lane 8j+kk ends with token kk of head j
     float x0 = -INFINITY;
@@ -242,8 +259,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
         acc[j][3] = fmaf(pj, v3, acc[j][3]);
       }
     }
-    __syncwarp();   // this buffer is refilled two splits ahead
-    buf ^= 1;
+    __syncwarp();   // this buffer is refilled in the next iteration
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
 
