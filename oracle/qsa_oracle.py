@@ -243,3 +243,77 @@ def boundary_gap(blk, budget_tokens: int) -> float:
         return float("inf")
     s = np.sort(blk)[::-1]
     return float(s[k - 1] - s[k])
+
+
+# ------------------------------------------------ 6. producer side: append
+
+# The 127 non-negative finite E4M3 values in code order (codes 0x00..0x7E):
+# the magnitude encoding is monotonic, so code order is value order.
+E4M3_POSITIVE = np.array([e4m3_value(c) for c in range(0x7F)], dtype=np.float64)
+
+
+def encode_e4m3(x) -> np.ndarray:
+    """FP8 E4M3 code of each value (OCP 8-bit floating point specification,
+    E4M3 variant, as e4m3_value above): round to nearest, a value halfway
+    between two neighbours goes to the one with the even code, magnitudes
+    above the largest finite value 448 saturate to 448 (E4M3 has no
+    infinity).  The sign bit follows the sign of the input, so -0.0 and
+    negative values that round to zero give 0x80."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(E4M3_POSITIVE, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = E4M3_POSITIVE[hi] - a
+    d_lo = a - E4M3_POSITIVE[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(pick_lo, lo, hi).astype(np.uint8)
+    return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def quantize_index_key(k) -> tuple[np.ndarray, int]:
+    """Index key of a new token as the producer stores it: 64 FP8-e4m3 codes
+    and one fp16 scale (the 66-byte key of the offload digest, section
+    "Эффективность и память"; split into codes + per-token absmax scale as
+    this library reads it).  The rounding decisions are taken in fp32, the
+    precision the key arrives in:
+      scale = binary16 round-to-nearest-even of (absmax / 448), the division
+              in fp32; a quotient above the largest finite binary16 (65504)
+              saturates to 65504;
+      code_d = encode_e4m3(clamp(k_d / scale, -448, 448)), the division in fp32.
+    A key whose scale is 0 (all zeros, or absmax / 448 below the smallest
+    binary16) keeps scale 0 and 64 zero codes.  Returns (codes uint8 [64],
+    scale bits uint16)."""
+    k = np.asarray(k, dtype=np.float32).reshape(-1)
+    amax = np.float32(np.max(np.abs(k)))
+    q = np.float32(amax / np.float32(448.0))
+    q = np.minimum(q, np.float32(65504.0))
+    s16 = np.float16(q)
+    if s16 == 0:
+        return np.zeros(k.size, dtype=np.uint8), 0
+    x = (k / np.float32(s16)).astype(np.float32)
+    x = np.clip(x, np.float32(-448.0), np.float32(448.0))
+    return encode_e4m3(x), int(np.array(s16).view(np.uint16))
+
+
+def append_slot_writes(t: int, placement: str, base_row: int, layer: int, layer_rows: int,
+                       ring_tokens: int) -> list:
+    """Slot-table writes, as (token, slot) pairs, when token t - the newest
+    one of its request - is stored at one layer.  RTX4090 port page, section
+    "显存账本：热缓存卸载省下约84%" (full history in pinned host memory, a tail
+    ring buffer of the newest tokens in HBM, logical tokens kept apart from
+    physical slots):
+      "hbm":  the token's own row base_row + layer*layer_rows + t;
+      "host": cold (-1), its row lives in the host history only;
+      "ring": ring row base_row + layer*ring_tokens + (t mod ring_tokens),
+              and the token that held that ring row before, t - ring_tokens,
+              becomes cold (its row stays in the host history)."""
+    if placement == "hbm":
+        return [(t, base_row + layer * layer_rows + t)]
+    if placement == "host":
+        return [(t, -1)]
+    if placement == "ring":
+        w = [(t, base_row + layer * ring_tokens + t % ring_tokens)]
+        if t >= ring_tokens:
+            w.append((t - ring_tokens, -1))
+        return w
+    raise ValueError(placement)

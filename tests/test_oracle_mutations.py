@@ -121,7 +121,48 @@ def _bf16_drop_subnormal(bits):
     return np.where(((b >> 7) & 0xFF) == 0, 0.0, v)
 
 
+def _encode_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    pos = O.E4M3_POSITIVE
+    hi = np.clip(np.searchsorted(pos, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    code = np.where(a - pos[lo] < pos[hi] - a, lo, hi).astype(np.uint8)
+    return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def _encode_no_saturation(x):
+    x = np.asarray(x, dtype=np.float64)
+    code = O._orig_encode(x)
+    return np.where(np.abs(x) > 448.0, code | np.uint8(0x7F), code).astype(np.uint8)
+
+
+def _quantize_fp32_scale(k):
+    k = np.asarray(k, dtype=np.float32).reshape(-1)
+    q = np.float32(np.max(np.abs(k)) / np.float32(448.0))
+    if q == 0:
+        return np.zeros(k.size, dtype=np.uint8), 0
+    x = np.clip((k / q).astype(np.float32), -448, 448)
+    return O.encode_e4m3(x), int(np.array(np.float16(q)).view(np.uint16))
+
+
+def _append_no_eviction(t, placement, base_row, layer, layer_rows, ring_tokens):
+    w = O._orig_append(t, placement, base_row, layer, layer_rows, ring_tokens)
+    return w[:1]
+
+
+def _append_hbm_ring_stride(t, placement, base_row, layer, layer_rows, ring_tokens):
+    if placement == "hbm":
+        return [(t, base_row + layer * ring_tokens + t)]
+    return O._orig_append(t, placement, base_row, layer, layer_rows, ring_tokens)
+
+
 MUTATIONS = {
+    "e4m3 encoder ties away from zero": {"encode_e4m3": _encode_ties_away},
+    "e4m3 encoder without saturation": {"encode_e4m3": _encode_no_saturation},
+    "key scale not rounded to fp16": {"quantize_index_key": _quantize_fp32_scale},
+    "ring append without eviction": {"append_slot_writes": _append_no_eviction},
+    "resident append with the ring stride": {"append_slot_writes": _append_hbm_ring_stride},
     "e4m3 bias 8": {"E4M3_TABLE": _table(bias=8)},
     "e4m3 no subnormals": {"E4M3_TABLE": _table(subnormals=False)},
     "fp16 wrong bias": {"decode_fp16": _fp16_bias16},
@@ -155,6 +196,8 @@ def test_pins_catch_mutation(name, monkeypatch):
     monkeypatch.setattr(O, "_orig_attn", O.decode_attention, raising=False)
     monkeypatch.setattr(O, "_orig_fp16", O.decode_fp16, raising=False)
     monkeypatch.setattr(O, "_orig_bf16", O.decode_bf16, raising=False)
+    monkeypatch.setattr(O, "_orig_encode", O.encode_e4m3, raising=False)
+    monkeypatch.setattr(O, "_orig_append", O.append_slot_writes, raising=False)
     for attr, val in MUTATIONS[name].items():
         monkeypatch.setattr(O, attr, val)
     caught = 0

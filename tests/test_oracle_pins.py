@@ -331,3 +331,86 @@ def test_page_byte_accounting():
     assert len(toks) == g["indexer_budget_tokens"]["value"]
     assert len(toks) * O.ROW_BYTES * g["qsa_layers"]["value"] == g["bytes_moved_per_decode_step"]["value"]
     assert 4 * len(O.select_blocks(blk, 2048)) == 2048 and g["c4_block_tokens"]["value"] == 4
+
+
+# ---------------------------------------------------- producer side: append
+
+def test_encode_e4m3_round_trips_every_finite_code():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = O.decode_e4m3(codes)
+    vals = np.where(codes == 0x80, -0.0, vals)          # the decoder returns -0.0 as 0.0 * -1
+    assert np.array_equal(O.encode_e4m3(vals), codes)
+
+
+def test_encode_e4m3_nearest_ties_to_even_and_saturation():
+    pos = O.E4M3_POSITIVE
+    mid = (pos[:-1] + pos[1:]) / 2
+    lo_codes = np.arange(0x7E, dtype=np.uint8)
+    even = np.where(lo_codes % 2 == 0, lo_codes, lo_codes + 1).astype(np.uint8)
+    assert np.array_equal(O.encode_e4m3(mid), even)
+    assert np.array_equal(O.encode_e4m3(-mid), even | 0x80)
+    step = (pos[1:] - pos[:-1]) * 1e-3
+    assert np.array_equal(O.encode_e4m3(mid - step), lo_codes)
+    assert np.array_equal(O.encode_e4m3(mid + step), lo_codes + 1)
+    assert list(O.encode_e4m3([448.0, 449.0, 464.0, 1e30, -500.0])) == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+
+
+def test_encode_e4m3_matches_torch_on_in_range_values():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.standard_normal(20000),
+                        rng.standard_normal(2000) * 1e-3, (O.E4M3_POSITIVE[:-1] + O.E4M3_POSITIVE[1:]) / 2])
+    x = x.astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.encode_e4m3(x), ref)
+
+
+def test_quantize_index_key_hand_worked():
+    cases = _load("quantize_hand.json")["cases"]
+    for c in cases:
+        k = np.zeros(64, dtype=np.float32)
+        for d, v in c["nonzero"]:
+            k[d] = v
+        codes, sbits = O.quantize_index_key(k)
+        want = np.zeros(64, dtype=np.uint8)
+        for d, code in c["codes"]:
+            want[d] = int(code, 16)
+        assert sbits == int(c["scale_bits"], 16), c["why"]
+        assert np.array_equal(codes, want), c["why"]
+
+
+def test_quantize_index_key_matches_the_input_generator():
+    """The generator's torch rounding (fp16 scale, float8_e4m3fn codes) and
+    the oracle's own encoders agree on random keys of every magnitude."""
+    rng = np.random.default_rng(9)
+    keys = rng.standard_normal((300, 64)).astype(np.float32)
+    keys *= np.exp2(rng.integers(-20, 20, size=(300, 1))).astype(np.float32)
+    keys[0] = 0.0
+    kt = torch.from_numpy(keys)
+    sc = (kt.abs().amax(dim=1) / 448.0).to(torch.float16)
+    x = (kt / torch.where(sc.float() > 0, sc.float(), torch.ones(300))[:, None]).clamp(-448, 448)
+    x = torch.where((sc.float() > 0)[:, None], x, torch.zeros_like(x))
+    ref_codes = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref_bits = sc.view(torch.int16).numpy().view(np.uint16)
+    for i in range(300):
+        codes, sbits = O.quantize_index_key(keys[i])
+        assert sbits == int(ref_bits[i])
+        assert np.array_equal(codes, ref_codes[i]), i
+
+
+def test_append_slot_writes_reproduce_the_ring_and_resident_layouts():
+    ring, base = 16, 100
+    for layer in (0, 2):
+        row = list(O.ring_slot_row(5, layer, base, ring)) + [-1] * 60
+        for t in range(5, 60):
+            for tok, s in O.append_slot_writes(t, "ring", base, layer, 0, ring):
+                row[tok] = s
+        assert np.array_equal(np.array(row[:60]), O.ring_slot_row(60, layer, base, ring))
+    cap = 80
+    row = [-1] * cap
+    for t in range(cap):
+        for tok, s in O.append_slot_writes(t, "hbm", base, 3, cap, ring):
+            row[tok] = s
+    assert row == [base + 3 * cap + t for t in range(cap)]
+    assert O.append_slot_writes(7, "host", base, 1, 0, ring) == [(7, -1)]
+    # hand-worked: ring of 4 at base 10, layer 1; token 9 takes ring row 10+4+1 and evicts token 5
+    assert O.append_slot_writes(9, "ring", 10, 1, 0, 4) == [(9, 15), (5, -1)]
