@@ -13,6 +13,9 @@
  *                           read through the slot table (HBM rows from the
  *                           pool, cold rows straight from pinned host memory)
  *                           or from the dense buffer of step 3.
+ * Producer side: qsa_request_advance reserves the position of a new token and
+ * qsa_append_token stores its quantised index key and KV row (per layer,
+ * before that layer's step 1).
  * Request leases with generation tags return a finished request's rows and
  * slot-table region to the cache.
  *
@@ -65,7 +68,7 @@
 extern "C" {
 #endif
 
-#define QSA_ABI_VERSION 1
+#define QSA_ABI_VERSION 2
 
 #define QSA_INDEX_HEADS 8
 #define QSA_INDEX_DIM 64
@@ -131,10 +134,16 @@ typedef struct qsa_handle {
 typedef struct qsa_request_desc {
   int64_t ctx_len;         /* cached tokens, 1 <= ctx_len <= ctx_capacity */
   int32_t placement;       /* qsa_kv_placement */
-  int32_t reserved0;
-  /* QSA_KV_HOST_RING, QSA_KV_HOST: pinned host memory [n_layers][ctx_len][2048]
+  /* Largest context the request may grow to with qsa_request_advance
+   * (ctx_len <= max_ctx <= ctx_capacity); 0 means ctx_len (no growth).  It
+   * sets the request's row stride M = max(ctx_len, max_ctx): a QSA_KV_HBM
+   * request leases n_layers * M pool rows, and a host history is laid out
+   * [n_layers][M][2048]. */
+  int32_t max_ctx;
+  /* QSA_KV_HOST_RING, QSA_KV_HOST: pinned host memory [n_layers][M][2048]
    * holding the full history (host address; the library maps it for the
-   * device).  QSA_KV_HBM: NULL. */
+   * device, and qsa_append_token writes the rows of new tokens into it).
+   * QSA_KV_HBM: NULL. */
   const void* host_rows;
 } qsa_request_desc;
 
@@ -145,6 +154,7 @@ typedef struct qsa_request_info {
   int64_t hbm_row_base;    /* first pool row of the region; layer l starts at
                               hbm_row_base + l * layer_rows */
   const void* host_rows;   /* device-usable address of the host history, or NULL */
+  int64_t max_ctx;         /* the request's row stride M (see qsa_request_desc) */
 } qsa_request_info;
 
 typedef struct qsa_stats {
@@ -191,9 +201,9 @@ qsa_status_t qsa_cache_destroy(qsa_cache* cache);
 
 /* ------------------------------------------- leases, slots, bookkeeping */
 
-/* Lease a request slot and an HBM region (ctx_len rows per layer for
- * QSA_KV_HBM, ring_tokens rows per layer for QSA_KV_HOST_RING, none for
- * QSA_KV_HOST), bump the
+/* Lease a request slot and an HBM region (M = max(ctx_len, max_ctx) rows
+ * per layer for QSA_KV_HBM, ring_tokens rows per layer for
+ * QSA_KV_HOST_RING, none for QSA_KV_HOST), bump the
  * slot's generation, and enqueue on `stream` the fill of the request's
  * slot-table rows: resident token t of layer l -> region row l*layer_rows + t;
  * offloaded token t -> ring row l*ring_tokens + t mod ring_tokens when t is
@@ -201,7 +211,7 @@ qsa_status_t qsa_cache_destroy(qsa_cache* cache);
  * every token of a QSA_KV_HOST request -> -1.
  * [RTX4090 port, memory-ledger section: leases, generation tags, tail ring,
  * logical addresses separate from physical slots.]
- * Errors: INVALID_ARG, CAPACITY (ctx_len > ctx_capacity or no pool range),
+ * Errors: INVALID_ARG, CAPACITY (ctx_len or max_ctx > ctx_capacity, or no pool range),
  * OUT_OF_SLOTS, CUDA.  On error nothing is leased. */
 qsa_status_t qsa_request_begin(qsa_cache* cache, const qsa_request_desc* desc,
                                void* stream, qsa_handle* out);
@@ -241,6 +251,44 @@ qsa_status_t qsa_staging_ptr(qsa_cache* cache, int32_t layer, void** out);
  * *dev_status receives a qsa_status_t recorded by a kernel (QSA_OK if none)
  * and *detail the offending value. */
 qsa_status_t qsa_poll_error(qsa_cache* cache, void* stream, int32_t* dev_status, int64_t* detail);
+
+/* ---------------------------------------------------- producer side */
+
+/* Reserve the positions of n_new new tokens of a request: they are
+ * ctx_len .. ctx_len + n_new - 1, and ctx_len grows by n_new.  Host
+ * bookkeeping only (no device work).  In a decode step call it once, before
+ * the step; then store the new token at every layer with qsa_append_token
+ * before that layer's qsa_index_score, since until then the new position's
+ * key, row and slot are unset.  QSA_ERR_CAPACITY beyond the request's
+ * max_ctx, QSA_ERR_INVALID_ARG for n_new < 1, QSA_ERR_STALE_HANDLE for a
+ * stale handle; nothing changes on error. */
+qsa_status_t qsa_request_advance(qsa_cache* cache, qsa_handle request, int32_t n_new);
+
+/* Store the newest token (position t = ctx_len - 1) of every unit u of the
+ * batch (request r, layer l), as the producer side of the decode step
+ * ("Оффлоадинг KV-кэша Qwen3.8-Flash-Next в RAM через vLLM без потери
+ * скорости декодирования", section "Эффективность и память": 66-byte index
+ * key and 2048-byte row per token and layer; "双卡RTX4090跑通Qwen3-Next：
+ * 8并发满血长上下文实测", section "显存账本：热缓存卸载省下约84%": full history
+ * in pinned host memory, newest tokens in the HBM tail ring, logical tokens
+ * kept apart from physical slots).
+ *   k_new   device fp32 [units][64]: the token's index key.  Stored as
+ *           scale = binary16 round-to-nearest-even of (absmax / 448), the
+ *           division in fp32, saturating at 65504; codes = E4M3
+ *           round-to-nearest-even of clamp(k / scale, -448, 448), the
+ *           division in fp32; a zero scale stores 64 zero codes.
+ *   kv_new  device [units][2048]: the token's KV row (K[4][128] then
+ *           V[4][128], bf16), copied unchanged.
+ * Where the row goes, by placement, and the slot-table writes:
+ *   QSA_KV_HBM        pool row hbm_row_base + l*M + t; slot[t] = that row.
+ *   QSA_KV_HOST       host history row (l, t); slot[t] = -1.
+ *   QSA_KV_HOST_RING  host history row (l, t) and ring row
+ *                     hbm_row_base + l*ring_tokens + t mod ring_tokens;
+ *                     slot[t] = that ring row, and the token that held it,
+ *                     t - ring_tokens (if >= 0), becomes cold: slot = -1.
+ * Both buffers 16-byte aligned.  Every unit needs ctx_len >= 1. */
+qsa_status_t qsa_append_token(qsa_cache* cache, const qsa_batch* batch, const float* k_new,
+                              const void* kv_new, void* stream);
 
 /* ------------------------------------------------------------ hot path */
 

@@ -167,10 +167,14 @@ def ring_slot_row(ctx_len: int, layer: int, base_row: int, ring_tokens: int) -> 
     return np.where(hot, slots, -1).astype(np.int32)
 
 
-def resident_slot_row(ctx_len: int, layer: int, base_row: int) -> np.ndarray:
+def resident_slot_row(ctx_len: int, layer: int, base_row: int,
+                      layer_rows: int | None = None) -> np.ndarray:
     """Slot-table row of one layer of a fully HBM-resident request: token t
-    of layer l sits in row base_row + l * ctx_len + t."""
-    return (base_row + layer * ctx_len + np.arange(ctx_len, dtype=np.int64)).astype(np.int32)
+    of layer l sits in row base_row + l * layer_rows + t, where layer_rows is
+    the region's rows per layer (the request's capacity; ctx_len when it was
+    leased without room to grow)."""
+    stride = ctx_len if layer_rows is None else layer_rows
+    return (base_row + layer * stride + np.arange(ctx_len, dtype=np.int64)).astype(np.int32)
 
 
 def gather_rows(tokens, slot_row, hbm_pool_rows, host_rows) -> np.ndarray:

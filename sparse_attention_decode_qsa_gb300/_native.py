@@ -52,13 +52,13 @@ class Handle(C.Structure):
 
 
 class RequestDesc(C.Structure):
-    _fields_ = [("ctx_len", C.c_int64), ("placement", C.c_int32), ("reserved0", C.c_int32),
+    _fields_ = [("ctx_len", C.c_int64), ("placement", C.c_int32), ("max_ctx", C.c_int32),
                 ("host_rows", C.c_void_p)]
 
 
 class RequestInfo(C.Structure):
     _fields_ = [("ctx_len", C.c_int64), ("placement", C.c_int32), ("layer_rows", C.c_int32),
-                ("hbm_row_base", C.c_int64), ("host_rows", C.c_void_p)]
+                ("hbm_row_base", C.c_int64), ("host_rows", C.c_void_p), ("max_ctx", C.c_int64)]
 
 
 class Stats(C.Structure):
@@ -90,6 +90,8 @@ SIGNATURES = {
     "qsa_request_end": (C.c_int, [C.c_void_p, Handle]),
     "qsa_request_info_get": (C.c_int, [C.c_void_p, Handle, C.POINTER(RequestInfo)]),
     "qsa_cache_stats": (C.c_int, [C.c_void_p, C.POINTER(Stats)]),
+    "qsa_request_advance": (C.c_int, [C.c_void_p, Handle, C.c_int32]),
+    "qsa_append_token": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p, C.c_void_p]),
     "qsa_slot_table_ptr": (C.c_int, [C.c_void_p, Handle, C.c_int32, C.POINTER(C.c_void_p)]),
     "qsa_slot_table_set": (C.c_int, [C.c_void_p, Handle, C.c_int32, C.c_void_p, C.c_void_p,
                                      C.c_int32, C.c_void_p]),

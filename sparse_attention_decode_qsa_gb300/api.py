@@ -100,8 +100,11 @@ class Cache:
 
     # ------------------------------------------------------- bookkeeping
     def request_begin(self, ctx_len: int, placement: int = N.KV_HBM, host_rows=None,
-                      stream=None) -> N.Handle:
-        d = N.RequestDesc(ctx_len, placement, 0, None)
+                      stream=None, max_ctx: int = 0) -> N.Handle:
+        """Lease a request of ctx_len tokens that may grow to max_ctx (0: no
+        growth).  host_rows: pinned host history [n_layers][max(ctx_len,
+        max_ctx)][2048] for the host placements."""
+        d = N.RequestDesc(ctx_len, placement, max_ctx, None)
         if host_rows is not None:
             d.host_rows = host_rows.data_ptr() if isinstance(host_rows, torch.Tensor) else int(host_rows)
         out = N.Handle()
@@ -119,6 +122,10 @@ class Cache:
         out = N.RequestInfo()
         check(self.L.qsa_request_info_get(self.h, handle, C.byref(out)), "qsa_request_info_get")
         return out
+
+    def advance(self, handle: N.Handle, n_new: int = 1):
+        """Reserve the positions of n_new new tokens (ctx_len grows by n_new)."""
+        check(self.L.qsa_request_advance(self.h, handle, n_new), "qsa_request_advance")
 
     def stats(self) -> dict:
         out = N.Stats()
@@ -144,6 +151,14 @@ class Cache:
         check(self.L.qsa_poll_error(self.h, _stream(stream), C.byref(st), C.byref(det)),
               "qsa_poll_error")
         return st.value, det.value
+
+    # ------------------------------------------------------ producer side
+    def append_token(self, handles, layer0, n_layers, k_new, kv_new, stream=None):
+        """Store each unit's newest token: k_new fp32 [units][64] index keys,
+        kv_new uint8 [units][2048] KV rows (unit u = i_layer * n_req + i_req)."""
+        b = _batch(handles, layer0, n_layers)
+        check(self.L.qsa_append_token(self.h, C.byref(b), _ptr(k_new), _ptr(kv_new),
+                                      _stream(stream)), "qsa_append_token")
 
     # ---------------------------------------------------------- hot path
     def index_score(self, handles, layer0, n_layers, q_idx, w, blk_scores, stream=None):

@@ -55,6 +55,7 @@ struct Lease {
   uint32_t generation = 0;
   bool active = false;
   int64_t ctx_len = 0;
+  int64_t max_ctx = 0;                 // row stride of the HBM region / host history
   int32_t placement = 0;
   int32_t layer_rows = 0;
   int64_t row_base = 0;
@@ -178,7 +179,7 @@ struct qsa_cache {
         u.req = (int32_t)b->requests[i].index;
         u.layer = b->layer0 + li;
         u.n = l->ctx_len;
-        u.host_rows = l->host_rows ? l->host_rows + (int64_t)u.layer * l->ctx_len * kRowBytes
+        u.host_rows = l->host_rows ? l->host_rows + (int64_t)u.layer * l->max_ctx * kRowBytes
                                    : nullptr;
       }
     }
@@ -269,6 +270,13 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
   if (desc->ctx_len > c->cfg.ctx_capacity)
     return fail(QSA_ERR_CAPACITY, "ctx_len %lld exceeds capacity %lld", (long long)desc->ctx_len,
                 (long long)c->cfg.ctx_capacity);
+  if (desc->max_ctx < 0 || desc->max_ctx > c->cfg.ctx_capacity)
+    return fail(QSA_ERR_CAPACITY, "max_ctx %d outside [0, %lld]", desc->max_ctx,
+                (long long)c->cfg.ctx_capacity);
+  if (desc->max_ctx > 0 && desc->max_ctx < desc->ctx_len)
+    return fail(QSA_ERR_INVALID_ARG, "max_ctx %d < ctx_len %lld", desc->max_ctx,
+                (long long)desc->ctx_len);
+  const int64_t max_ctx = desc->max_ctx > 0 ? desc->max_ctx : desc->ctx_len;
   if (desc->placement != QSA_KV_HBM && desc->placement != QSA_KV_HOST_RING &&
       desc->placement != QSA_KV_HOST)
     return fail(QSA_ERR_INVALID_ARG, "unknown placement %d", desc->placement);
@@ -282,7 +290,7 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
     if (!c->leases[i].active) { slot = (int)i; break; }
   if (slot < 0) return fail(QSA_ERR_OUT_OF_SLOTS, "all %d request slots are leased", c->cfg.max_requests);
 
-  const int32_t layer_rows = desc->placement == QSA_KV_HBM        ? (int32_t)desc->ctx_len
+  const int32_t layer_rows = desc->placement == QSA_KV_HBM        ? (int32_t)max_ctx
                              : desc->placement == QSA_KV_HOST_RING ? c->cfg.ring_tokens
                                                                    : 0;
   const int64_t rows = (int64_t)layer_rows * c->cfg.n_layers;
@@ -324,6 +332,7 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
   l.generation += 1;
   l.active = true;
   l.ctx_len = desc->ctx_len;
+  l.max_ctx = max_ctx;
   l.placement = desc->placement;
   l.layer_rows = layer_rows;
   l.row_base = base;
@@ -342,6 +351,7 @@ qsa_status_t qsa_request_end(qsa_cache* c, qsa_handle h) {
   c->release_rows(l.row_base, l.rows);
   l.active = false;
   l.ctx_len = 0;
+  l.max_ctx = 0;
   l.rows = 0;
   l.host_rows = nullptr;
   return ok();
@@ -356,6 +366,20 @@ qsa_status_t qsa_request_info_get(qsa_cache* c, qsa_handle h, qsa_request_info* 
   out->layer_rows = l->layer_rows;
   out->hbm_row_base = l->row_base;
   out->host_rows = l->host_rows;
+  out->max_ctx = l->max_ctx;
+  return ok();
+}
+
+qsa_status_t qsa_request_advance(qsa_cache* c, qsa_handle h, int32_t n_new) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  const Lease* cl;
+  if (qsa_status_t st = c->check_handle(h, &cl)) return st;
+  if (n_new < 1) return fail(QSA_ERR_INVALID_ARG, "n_new %d < 1", n_new);
+  Lease& l = c->leases[h.index];
+  if (l.ctx_len + n_new > l.max_ctx)
+    return fail(QSA_ERR_CAPACITY, "ctx_len %lld + %d exceeds the request's max_ctx %lld",
+                (long long)l.ctx_len, n_new, (long long)l.max_ctx);
+  l.ctx_len += n_new;
   return ok();
 }
 
@@ -473,6 +497,34 @@ qsa_status_t qsa_gather_rows(qsa_cache* c, const qsa_batch* batch, const int32_t
                                      static_cast<uint8_t*>(rows_out), n_rows,
                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  return ok();
+}
+
+qsa_status_t qsa_append_token(qsa_cache* c, const qsa_batch* batch, const float* k_new,
+                              const void* kv_new, void* stream) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  BatchDesc d;
+  if (qsa_status_t st = c->build_batch(batch, &d)) return st;
+  if (!k_new || !kv_new) return fail(QSA_ERR_INVALID_ARG, "null k_new or kv_new");
+  if (reinterpret_cast<uintptr_t>(k_new) % 16 || reinterpret_cast<uintptr_t>(kv_new) % 16)
+    return fail(QSA_ERR_INVALID_ARG, "k_new and kv_new must be 16-byte aligned");
+  AppendTargets tg;
+  for (int u = 0; u < d.n_units; ++u) {
+    const Lease& l = c->leases[d.u[u].req];
+    const int64_t t = l.ctx_len - 1;
+    const int64_t layer = d.u[u].layer;
+    tg.pool_row[u] = -1;
+    tg.evict[u] = -1;
+    if (l.placement == QSA_KV_HBM) {
+      tg.pool_row[u] = l.row_base + layer * l.layer_rows + t;
+    } else if (l.placement == QSA_KV_HOST_RING) {
+      tg.pool_row[u] = l.row_base + layer * l.layer_rows + t % l.layer_rows;
+      if (t >= l.layer_rows) tg.evict[u] = t - l.layer_rows;
+    }
+  }
+  cudaError_t e = launch_append_token(d, tg, k_new, static_cast<const uint8_t*>(kv_new),
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
   return ok();
 }
 

@@ -44,6 +44,7 @@ enum KernelId : int32_t {
   kKernAttn = 4,
   kKernSlotFill = 5,
   kKernSlotSet = 6,
+  kKernAppend = 7,
 };
 
 // One decode unit (request slot, layer) of a call.
@@ -144,6 +145,18 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
                                const int32_t* n_sel, int32_t budget_tokens,
                                const uint8_t* gathered, float softmax_scale, float* out,
                                float* lse, cudaStream_t s);
+
+// Producer side: where each unit's newest token goes (computed from the
+// leases on the host).  pool_row: the pool row that receives the row and
+// becomes the token's slot (-1: none, the token is cold); evict: a token
+// whose slot becomes -1 (a ring row handed to the new token), or -1.
+struct AppendTargets {
+  int64_t pool_row[kMaxUnits];
+  int64_t evict[kMaxUnits];
+};
+
+cudaError_t launch_append_token(const BatchDesc& b, const AppendTargets& tg, const float* k_new,
+                                const uint8_t* kv_new, cudaStream_t s);
 
 // Slot-table maintenance.
 cudaError_t launch_slot_fill(int32_t* rows, int32_t n_layers, int64_t ctx_cap, int64_t ctx_len,

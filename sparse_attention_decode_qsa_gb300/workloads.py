@@ -184,6 +184,7 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
     dev = cache.pool.device
     ring = cache.ring_tokens
     info = cache.request_info(h)
+    stride = info.max_ctx            # rows per layer of the HBM region / host history
     for l in range(wl.n_layers):
         s = synth.mix_seed(seed, r, l)
         blocks = planting(l, r, n)
@@ -198,10 +199,10 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
         wl.q[u] = synth.attn_query(synth.mix_seed(s, 3), device=dev)
         rows = synth.kv_rows(n, synth.mix_seed(s, 4), device=dev)
         if p == N.KV_HBM:
-            b0 = info.hbm_row_base + l * n
+            b0 = info.hbm_row_base + l * stride
             cache.pool[b0:b0 + n] = rows
         else:
-            wl.host[r][l].copy_(rows)
+            wl.host[r][l, :n].copy_(rows)
             if p == N.KV_HOST_RING:
                 t = torch.arange(max(0, n - ring), n, device=dev)
                 cache.pool[info.hbm_row_base + l * ring + (t % ring)] = rows[t]
@@ -211,14 +212,15 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
 
 def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: int = 4096,
           staging_rows: int = 2048, seed: int = 0, device="cuda", extra_requests: int = 0,
-          spare_rows: int = 0, ctx_capacity: int | None = None) -> Workload:
-    """planting(l, r, n) -> block ids to plant for unit (l, r)."""
-    ctx_capacity = ctx_capacity or max(ctxs)
+          spare_rows: int = 0, ctx_capacity: int | None = None, grow: int = 0) -> Workload:
+    """planting(l, r, n) -> block ids to plant for unit (l, r).  grow: tokens
+    every request may still append (its max_ctx is ctx + grow)."""
+    ctx_capacity = ctx_capacity or (max(ctxs) + grow)
     dev = torch.device(device)
     R = len(ctxs)
     rows_needed = 0
     for n, p in zip(ctxs, placements):
-        rows_needed += n_layers * (n if p == N.KV_HBM else ring if p == N.KV_HOST_RING else 0)
+        rows_needed += n_layers * (n + grow if p == N.KV_HBM else ring if p == N.KV_HOST_RING else 0)
     pool_rows = n_layers * staging_rows + rows_needed + spare_rows
     cache = Cache(n_layers=n_layers, max_requests=R + extra_requests, ctx_capacity=ctx_capacity,
                   hbm_pool_rows=pool_rows, budget_tokens=budget, ring_tokens=ring,
@@ -227,9 +229,9 @@ def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: i
     for r, (n, p) in enumerate(zip(ctxs, placements)):
         hrows = None
         if p != N.KV_HBM:
-            hrows = register_pinned(torch.empty(n_layers, n, N.ROW_BYTES, dtype=torch.uint8))
+            hrows = register_pinned(torch.empty(n_layers, n + grow, N.ROW_BYTES, dtype=torch.uint8))
         host.append(hrows)
-        handles.append(cache.request_begin(n, p, host_rows=hrows))
+        handles.append(cache.request_begin(n, p, host_rows=hrows, max_ctx=n + grow if grow else 0))
     U = n_layers * R
     wl = Workload(cache, handles, n_layers, list(ctxs), list(placements), host,
                   torch.empty(U, 8, 64, dtype=torch.float32, device=dev),

@@ -39,7 +39,7 @@ def oracle_slot_row(wl, l, r):
     n = wl.ctxs[r]
     p = wl.placements[r]
     if p == N.KV_HBM:
-        return O.resident_slot_row(n, l, info.hbm_row_base)
+        return O.resident_slot_row(n, l, info.hbm_row_base, info.layer_rows)
     if p == N.KV_HOST_RING:
         return O.ring_slot_row(n, l, info.hbm_row_base, wl.cache.ring_tokens)
     return np.full(n, -1, dtype=np.int32)
@@ -72,7 +72,7 @@ def oracle_unit(wl, l, r, budget=None):
     toks = O.selected_tokens(sel, n)
     slot = oracle_slot_row(wl, l, r)
     pool = PoolRows(wl.cache.pool, slot[toks])
-    host = wl.host[r][l].numpy() if wl.host[r] is not None else None
+    host = wl.host[r][l, :n].numpy() if wl.host[r] is not None else None
     rows = O.gather_rows(toks, slot, pool, host)
     out, lse = O.decode_attention(x["q"], rows, wl.softmax_scale)
     # tolerance scale per token: sum_h w_h |sc| sum_d |q_hd e4m3(code_d)|

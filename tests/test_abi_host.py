@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol():
     for name in sorted(declared):
         assert hasattr(L, name), f"{name} declared in include/ but not exported"
         assert name in N.SIGNATURES, f"{name} has no Python binding"
-    assert L.qsa_abi_version() == 1
+    assert L.qsa_abi_version() == 2
 
 
 def _host_cache(**kw):
@@ -198,3 +198,43 @@ def test_ragged_batch_recycling_returns_capacity():
     for h, _ in list(live.values()):
         c.request_end(h)
     assert c.stats() == s0
+
+
+def test_request_growth_bookkeeping():
+    """max_ctx sizes a resident request's region; qsa_request_advance grows
+    ctx_len up to it and no further; bad arguments change nothing."""
+    c = _host_cache()
+    try:
+        s0 = c.stats()
+        h = c.request_begin(100, Q.KV_HBM, max_ctx=130)
+        info = c.request_info(h)
+        assert (info.ctx_len, info.max_ctx, info.layer_rows) == (100, 130, 130)
+        assert c.stats()["free_hbm_rows"] == s0["free_hbm_rows"] - c.n_layers * 130
+        c.advance(h, 25)
+        c.advance(h)
+        assert c.request_info(h).ctx_len == 126
+        with pytest.raises(Q.QsaError) as e:
+            c.advance(h, 5)
+        assert e.value.status == Q.ERR_CAPACITY
+        with pytest.raises(Q.QsaError) as e:
+            c.advance(h, 0)
+        assert e.value.status == Q.ERR_INVALID_ARG
+        assert c.request_info(h).ctx_len == 126
+        c.advance(h, 4)
+        assert c.request_info(h).ctx_len == 130
+        h2 = c.request_begin(10, Q.KV_HOST, host_rows=0x1000, max_ctx=20)
+        assert c.request_info(h2).max_ctx == 20 and c.request_info(h2).layer_rows == 0
+        with pytest.raises(Q.QsaError) as e:
+            c.request_begin(10, Q.KV_HBM, max_ctx=5)          # max_ctx below ctx_len
+        assert e.value.status == Q.ERR_INVALID_ARG
+        with pytest.raises(Q.QsaError) as e:
+            c.request_begin(10, Q.KV_HBM, max_ctx=c.ctx_capacity + 1)
+        assert e.value.status == Q.ERR_CAPACITY
+        c.request_end(h)
+        with pytest.raises(Q.QsaError) as e:
+            c.advance(h)
+        assert e.value.status == Q.ERR_STALE_HANDLE
+        c.request_end(h2)
+        assert c.stats() == s0
+    finally:
+        c.close()

@@ -143,7 +143,9 @@ def _quantize_fp32_scale(k):
     if q == 0:
         return np.zeros(k.size, dtype=np.uint8), 0
     x = np.clip((k / q).astype(np.float32), -448, 448)
-    return O.encode_e4m3(x), int(np.array(np.float16(q)).view(np.uint16))
+    with np.errstate(over="ignore"):
+        s16 = np.float16(q)
+    return O.encode_e4m3(x), int(np.array(s16).view(np.uint16))
 
 
 def _append_no_eviction(t, placement, base_row, layer, layer_rows, ring_tokens):
