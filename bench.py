@@ -165,6 +165,24 @@ def zero_copy_peak(dev, n_req=8, n=262144, budget=8192):
             workloads.unregister_pinned(h)
 
 
+def max_over_ranks(times, world):
+    """Each timing's maximum over the ranks (replicas on their own GPUs; the
+    slowest rank sets the job's time).  Host tensors, so it runs on any
+    process group backend."""
+    if world <= 1:
+        return list(times)
+    t = torch.tensor(list(times), dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_rate(units_per_rank, world, step_s):
+    """Layer-steps per second of the whole job: every rank's units of a step
+    over the slowest rank's step time (weak scaling: each rank owns its
+    requests, no data is exchanged)."""
+    return units_per_rank * world / step_s
+
+
 def append_timing(dev, n_req=8, n_layers=12, steps=20):
     """Per-launch time of qsa_append_token for n_req units (one layer), on a
     cache of its own (8 HBM-resident requests of 4096 tokens with room to
@@ -322,17 +340,12 @@ def run_ours(args, rank, world):
     link_zc = zero_copy_peak(dev)
     link_peak = max(link_copy, link_zc)
 
-    # max over ranks
-    ms_max, ms_e2e_max = ms, ms_e2e
-    if world > 1:
-        t = torch.tensor([ms, ms_e2e], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max, ms_e2e_max = float(t[0]), float(t[1])
+    ms_max, ms_e2e_max = max_over_ranks([ms, ms_e2e], world)
     if rank != 0:
         return None
 
     step_s = ms_max / 1e3 / args.steps
-    value = units * world / step_s
+    value = whole_job_rate(units, world, step_s)
     idx_b = IDX_BYTES * CTX          # algorithmic bytes per unit: index keys
     rows_b = BUDGET * ROW            # selected rows per unit
     hot_b = rows_b // 2              # half of them from the HBM tail ring
