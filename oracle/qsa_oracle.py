@@ -45,6 +45,7 @@ HEAD_DIM = 128
 Q_HEADS = 16
 GQA_GROUP = Q_HEADS // KV_HEADS
 ROW_BYTES = 2048
+ROW_BYTES_FP8 = 1040
 
 
 # ------------------------------------------------------------------ formats
@@ -177,11 +178,12 @@ def resident_slot_row(ctx_len: int, layer: int, base_row: int,
     return (base_row + layer * stride + np.arange(ctx_len, dtype=np.int64)).astype(np.int32)
 
 
-def gather_rows(tokens, slot_row, hbm_pool_rows, host_rows) -> np.ndarray:
+def gather_rows(tokens, slot_row, hbm_pool_rows, host_rows, row_bytes: int = ROW_BYTES) -> np.ndarray:
     """Bytes of the rows of the given logical tokens: pool row slot_row[t]
-    when it is >= 0, else host row t (step 4 above).  Returns uint8 [m][2048].
-    hbm_pool_rows / host_rows: anything indexable by row giving 2048 bytes."""
-    out = np.empty((len(tokens), ROW_BYTES), dtype=np.uint8)
+    when it is >= 0, else host row t (step 4 above).  Returns uint8
+    [m][row_bytes].  hbm_pool_rows / host_rows: anything indexable by row
+    giving row_bytes bytes (2048 for bf16 rows, 1040 for FP8 rows)."""
+    out = np.empty((len(tokens), row_bytes), dtype=np.uint8)
     for i, t in enumerate(tokens):
         s = int(slot_row[int(t)])
         out[i] = hbm_pool_rows[s] if s >= 0 else host_rows[int(t)]
@@ -196,10 +198,27 @@ def split_kv(rows_u8) -> tuple[np.ndarray, np.ndarray]:
     return decode_bf16(r[:, 0]), decode_bf16(r[:, 1])          # [m][4][128] each
 
 
-def decode_attention(q_bits, rows_u8, softmax_scale: float):
+def split_kv_fp8(rows_u8) -> tuple[np.ndarray, np.ndarray]:
+    """A 1040-byte FP8 row holds K codes [4][128] E4M3, V codes [4][128]
+    E4M3, then fp16 scales for K heads 0-3 and V heads 0-3; an element's
+    value is its head's scale times e4m3(code).  This is the library's
+    reading of an FP8 KV cache: the RTX 5090 page runs one (FP8 KV), and the
+    RTX4090 port's per-card memory figure fits about 1 KiB per token and
+    layer.  The per-head absmax scale is the same reading as the index
+    key's."""
+    r = np.ascontiguousarray(rows_u8, dtype=np.uint8).reshape(-1, ROW_BYTES_FP8)
+    kc = r[:, :512].reshape(-1, KV_HEADS, HEAD_DIM)
+    vc = r[:, 512:1024].reshape(-1, KV_HEADS, HEAD_DIM)
+    sc = np.ascontiguousarray(r[:, 1024:1040]).view(np.uint16).reshape(-1, 2, KV_HEADS)
+    ks, vs = decode_fp16(sc[:, 0]), decode_fp16(sc[:, 1])      # [m][4]
+    return decode_e4m3(kc) * ks[:, :, None], decode_e4m3(vc) * vs[:, :, None]
+
+
+def decode_attention(q_bits, rows_u8, softmax_scale: float, kv_format: str = "bf16"):
     """GQA decode attention over the gathered rows (step 5 above; sparse
     attention over the selected rows only, offload digest section
-    "Механизм гибридного разреженного оффлоадинга").
+    "Механизм гибридного разреженного оффлоадинга").  kv_format "bf16":
+    2048-byte rows (split_kv); "fp8": 1040-byte rows (split_kv_fp8).
 
     q_bits: uint16 [16][128] bf16 bits.  Returns (out float64 [16][128],
     lse float64 [16]); with no rows, out = 0 and lse = -inf.
@@ -209,7 +228,7 @@ def decode_attention(q_bits, rows_u8, softmax_scale: float):
     lse = np.full(Q_HEADS, -np.inf)
     if len(rows_u8) == 0:
         return out, lse
-    K, V = split_kv(rows_u8)
+    K, V = split_kv(rows_u8) if kv_format == "bf16" else split_kv_fp8(rows_u8)
     for h in range(Q_HEADS):
         g = h // GQA_GROUP
         logits = softmax_scale * (K[:, g, :] @ q[h])               # [m]
@@ -274,6 +293,12 @@ def encode_e4m3(x) -> np.ndarray:
     return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
 
 
+def quantize_vector(x) -> tuple[np.ndarray, int]:
+    """Codes and scale bits of one vector under the producer's rule (see
+    quantize_index_key); shared by index keys and FP8 KV rows."""
+    return quantize_index_key(x)
+
+
 def quantize_index_key(k) -> tuple[np.ndarray, int]:
     """Index key of a new token as the producer stores it: 64 FP8-e4m3 codes
     and one fp16 scale (the 66-byte key of the offload digest, section
@@ -321,3 +346,23 @@ def append_slot_writes(t: int, placement: str, base_row: int, layer: int, layer_
             w.append((t - ring_tokens, -1))
         return w
     raise ValueError(placement)
+
+
+def quantize_kv_row_fp8(row_u8) -> np.ndarray:
+    """FP8 row (1040 bytes, layout of split_kv_fp8) of a bf16 KV row (2048
+    bytes, layout of split_kv): each of the 8 vectors K[h], V[h] (128 values,
+    exact in fp32) is quantised under the index key's rule - fp16 scale =
+    round-to-nearest-even of absmax/448 in fp32, E4M3 codes of clamp(x/scale,
+    +-448) - and stored as codes K[4][128], V[4][128], scales K[4], V[4]."""
+    bits = np.ascontiguousarray(row_u8, dtype=np.uint8).view(np.uint16).reshape(2, KV_HEADS, HEAD_DIM)
+    vals = decode_bf16(bits).astype(np.float32)
+    out = np.zeros(ROW_BYTES_FP8, dtype=np.uint8)
+    scales = np.zeros(2 * KV_HEADS, dtype=np.uint16)
+    for kv in range(2):
+        for h in range(KV_HEADS):
+            codes, sbits = quantize_vector(vals[kv, h])
+            off = kv * 512 + h * HEAD_DIM
+            out[off:off + HEAD_DIM] = codes
+            scales[kv * KV_HEADS + h] = sbits
+    out[1024:1040] = scales.view(np.uint8)
+    return out

@@ -159,7 +159,23 @@ def _append_hbm_ring_stride(t, placement, base_row, layer, layer_rows, ring_toke
     return O._orig_append(t, placement, base_row, layer, layer_rows, ring_tokens)
 
 
+def _fp8_kv_swapped(rows_u8):
+    K, V = O._orig_split_fp8(rows_u8)
+    return V, K
+
+
+def _fp8_one_scale(rows_u8):
+    r = np.ascontiguousarray(rows_u8, dtype=np.uint8).reshape(-1, O.ROW_BYTES_FP8)
+    kc = r[:, :512].reshape(-1, 4, 128)
+    vc = r[:, 512:1024].reshape(-1, 4, 128)
+    sc = np.ascontiguousarray(r[:, 1024:1040]).view(np.uint16).reshape(-1, 2, 4)
+    ks = O.decode_fp16(sc[:, 0])
+    return O.decode_e4m3(kc) * ks[:, :, None], O.decode_e4m3(vc) * ks[:, :, None]
+
+
 MUTATIONS = {
+    "fp8 row with K and V swapped": {"split_kv_fp8": _fp8_kv_swapped},
+    "fp8 row with the K scales on V": {"split_kv_fp8": _fp8_one_scale},
     "e4m3 encoder ties away from zero": {"encode_e4m3": _encode_ties_away},
     "e4m3 encoder without saturation": {"encode_e4m3": _encode_no_saturation},
     "key scale not rounded to fp16": {"quantize_index_key": _quantize_fp32_scale},
@@ -200,6 +216,7 @@ def test_pins_catch_mutation(name, monkeypatch):
     monkeypatch.setattr(O, "_orig_bf16", O.decode_bf16, raising=False)
     monkeypatch.setattr(O, "_orig_encode", O.encode_e4m3, raising=False)
     monkeypatch.setattr(O, "_orig_append", O.append_slot_writes, raising=False)
+    monkeypatch.setattr(O, "_orig_split_fp8", O.split_kv_fp8, raising=False)
     for attr, val in MUTATIONS[name].items():
         monkeypatch.setattr(O, attr, val)
     caught = 0

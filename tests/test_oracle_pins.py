@@ -414,3 +414,84 @@ def test_append_slot_writes_reproduce_the_ring_and_resident_layouts():
     assert O.append_slot_writes(7, "host", base, 1, 0, ring) == [(7, -1)]
     # hand-worked: ring of 4 at base 10, layer 1; token 9 takes ring row 10+4+1 and evicts token 5
     assert O.append_slot_writes(9, "ring", 10, 1, 0, 4) == [(9, 15), (5, -1)]
+
+
+# ------------------------------------------------------------- FP8 KV rows
+
+def _bf16_bits(vals):
+    return torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_fp8_row_decode_hand_worked():
+    """Layout: K codes [4][128] at 0, V codes [4][128] at 512, fp16 scales
+    K[0..3] at 1024, V[0..3] at 1032."""
+    row = np.zeros(1040, dtype=np.uint8)
+    sc = np.zeros(8, dtype=np.uint16)
+    row[0 * 128 + 0] = 0x38            # K head 0 dim 0: 1.0 ...
+    sc[0] = 0x3C00                     # ... times scale 1.0 = 1.0
+    row[2 * 128 + 5] = 0x7E            # K head 2 dim 5: 448 ...
+    sc[2] = 0x2000                     # ... times 2^-7 = 3.5
+    row[512 + 1 * 128 + 127] = 0xB8    # V head 1 dim 127: -1.0 ...
+    sc[4 + 1] = 0x4000                 # ... times 2.0 = -2.0
+    row[512 + 3 * 128 + 64] = 0x01     # V head 3 dim 64: 2^-9 ...
+    sc[4 + 3] = 0x7BFF                 # ... times 65504 = 127.9375
+    row[1024:1040] = sc.view(np.uint8)
+    K, V = O.split_kv_fp8(row[None])
+    assert K.shape == (1, 4, 128) and V.shape == (1, 4, 128)
+    want_k = np.zeros((4, 128)); want_k[0, 0] = 1.0; want_k[2, 5] = 3.5
+    want_v = np.zeros((4, 128)); want_v[1, 127] = -2.0; want_v[3, 64] = 127.9375
+    assert np.array_equal(K[0], want_k) and np.array_equal(V[0], want_v)
+
+
+def test_fp8_row_quantize_hand_worked():
+    k = np.zeros((4, 128), dtype=np.float32)
+    v = np.zeros((4, 128), dtype=np.float32)
+    k[1, 0], k[1, 1], k[1, 2] = 448.0, 1.0625, -1.1875     # scale 1.0: 0x7E, tie -> 0x38, tie -> 0xBA
+    v[3, 0], v[3, 1] = -3.5, 1.75                         # scale 2^-7: -448 -> 0xFE, 224 -> 0x76
+    row = np.concatenate([_bf16_bits(k.reshape(-1)), _bf16_bits(v.reshape(-1))]).view(np.uint8)
+    f = O.quantize_kv_row_fp8(row)
+    codes, scales = f[:1024], f[1024:].view(np.uint16)
+    assert list(scales) == [0, 0x3C00, 0, 0, 0, 0, 0, 0x2000]
+    assert list(codes[128:131]) == [0x7E, 0x38, 0xBA]
+    assert list(codes[512 + 384:512 + 386]) == [0xFE, 0x76]
+    assert np.count_nonzero(codes) == 5
+
+
+def test_fp8_row_quantize_matches_torch_rounding_and_bound():
+    rng = np.random.default_rng(11)
+    for _ in range(40):
+        x = torch.from_numpy(rng.standard_normal(1024).astype(np.float32) *
+                             np.float32(2.0 ** rng.integers(-12, 12)))
+        bf = x.to(torch.bfloat16)
+        row = bf.view(torch.int16).numpy().view(np.uint8)
+        f = O.quantize_kv_row_fp8(row)
+        v = bf.float().view(8, 128)
+        sc = (v.abs().amax(dim=1) / 448.0).to(torch.float16)
+        q = (v / torch.where(sc.float() > 0, sc.float(), torch.ones(8))[:, None]).clamp(-448, 448)
+        ref_codes = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy().reshape(-1)
+        assert np.array_equal(f[:1024], ref_codes)
+        assert np.array_equal(f[1024:].view(np.uint16), sc.view(torch.int16).numpy().view(np.uint16))
+        K, V = O.split_kv(row[None])
+        Kq, Vq = O.split_kv_fp8(f[None])
+        vals = np.concatenate([K, V], axis=1)[0]
+        deq = np.concatenate([Kq, Vq], axis=1)[0]
+        scale = O.decode_fp16(f[1024:].view(np.uint16))[:, None]
+        # E4M3 round-to-nearest: half a step of 2^-3 relative, or of 2^-9 * scale below 2^-6
+        assert np.all(np.abs(deq - vals) <= np.maximum(np.abs(vals) * 2.0 ** -4, scale * 2.0 ** -10) + 1e-30)
+
+
+def test_fp8_attention_matches_torch_sdpa_on_dequantised_rows():
+    rng = np.random.default_rng(12)
+    m = 37
+    rows = np.stack([O.quantize_kv_row_fp8(
+        torch.from_numpy(rng.standard_normal(1024).astype(np.float32)).to(torch.bfloat16)
+        .view(torch.int16).numpy().view(np.uint8)) for _ in range(m)])
+    qb = torch.randn(16, 128).to(torch.bfloat16)
+    out, lse = O.decode_attention(qb.view(torch.int16).numpy().view(np.uint16), rows, 0.1, "fp8")
+    K, V = O.split_kv_fp8(rows)
+    kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(4, dim=0)      # [16][m][128]
+    vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(4, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(qb.double()[:, None, :], kt, vt, scale=0.1)
+    assert np.abs(out - ref[:, 0].numpy()).max() < 1e-12
+    logits = 0.1 * torch.einsum("hd,hmd->hm", qb.double(), kt)
+    assert np.abs(lse - torch.logsumexp(logits, dim=1).numpy()).max() < 1e-12
