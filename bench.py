@@ -228,6 +228,42 @@ def append_timing(dev, n_req=8, n_layers=12, steps=20):
         c.close()
 
 
+def fp8_attention_timing(dev, steps=20):
+    """The attention of the benchmark's shape over FP8 rows (QSA_KV_FP8, 1040
+    bytes a row): 8 requests x 262144 tokens at one layer, host history +
+    4096-token tail ring, half of the selected rows cold.  Returns the
+    average launch time (us) of 12 launches captured as a CUDA graph."""
+    import sparse_attention_decode_qsa_gb300 as Q
+    from sparse_attention_decode_qsa_gb300 import workloads
+    wl = workloads.c256k_x8(device=dev, n_layers=1, kv_format=Q.KV_FP8)
+    try:
+        cur = torch.cuda.current_stream(dev)
+        wl.step(cur)
+        torch.cuda.synchronize(dev)
+        c, hs = wl.cache, wl.handles
+        s = torch.cuda.Stream()
+        s.wait_stream(cur)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(N_LAYERS):
+                c.sparse_decode_attn(hs, 0, 1, wl.q, wl.sel, wl.nsel, BUDGET, None, wl.softmax_scale,
+                                     wl.out, wl.lse, s)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for _ in range(steps):
+            g.replay()
+        e1.record(cur)
+        torch.cuda.synchronize(dev)
+        st, det = c.poll_error()
+        if st != 0:
+            raise RuntimeError(f"device error word {st} ({det}) in the FP8 attention timing")
+        return e0.elapsed_time(e1) * 1e3 / (steps * N_LAYERS)
+    finally:
+        wl.close()
+
+
 def run_ours(args, rank, world):
     from sparse_attention_decode_qsa_gb300 import workloads
 
@@ -336,6 +372,7 @@ def run_ours(args, rank, world):
     del graph
     wl.close()
     append_us = append_timing(dev)
+    fp8_attn_us = fp8_attention_timing(dev)
     link_copy = host_link_peak(dev)
     link_zc = zero_copy_peak(dev)
     link_peak = max(link_copy, link_zc)
@@ -376,6 +413,14 @@ def run_ours(args, rank, world):
         # row store and slot update; not part of the timed decode step
         "append_token": {"bound": "latency", "avg_launch_us": round(append_us, 2),
                          "units_per_launch": 8},
+        # FP8 KV variant (1040-byte rows) of the same attention launch; not
+        # part of the timed decode step, whose rows are BF16
+        "sparse_attn_fp8": {"bound": "host_link",
+                            "achieved": round(R * (BUDGET // 2) * 1040 / (fp8_attn_us * 1e-6) / 1e9, 1),
+                            "peak": round(link_peak, 1), "unit": "GB/s",
+                            "frac": round(R * (BUDGET // 2) * 1040 / (fp8_attn_us * 1e-6) / 1e9 / link_peak, 4),
+                            "host_bytes_per_launch": R * (BUDGET // 2) * 1040,
+                            "avg_launch_us": round(fp8_attn_us, 2)},
     }
     dom = dict(roofs[dominant])
     dom["kernel"] = dominant

@@ -76,6 +76,9 @@ extern "C" {
 #define QSA_HEAD_DIM 128
 #define QSA_Q_HEADS 16
 #define QSA_ROW_BYTES 2048
+/* Row of an FP8 KV cache: K codes [4][128] E4M3, V codes [4][128] E4M3, then
+ * fp16 scales K[0..3], V[0..3] (value = scale of its head * e4m3(code)). */
+#define QSA_ROW_BYTES_FP8 1040
 #define QSA_C4 4
 /* Largest number of decode units (request x layer pairs) in one call. */
 #define QSA_MAX_UNITS 256
@@ -106,6 +109,18 @@ typedef enum qsa_kv_placement {
   QSA_KV_HOST = 2
 } qsa_kv_placement;
 
+/* Format of the KV rows of a cache (pool, staging, host histories, gathered
+ * rows).  BF16: QSA_ROW_BYTES-byte rows, K[4][128] then V[4][128] bf16.
+ * FP8: QSA_ROW_BYTES_FP8-byte rows (layout above), each of the 8 head
+ * vectors quantised like an index key: fp16 scale = round-to-nearest-even
+ * of absmax/448, codes = E4M3 of clamp(x/scale, +-448) (this library's
+ * reading of the FP8 KV cache the RTX 5090 page runs; the RTX4090 port's
+ * per-card memory figure fits about 1 KiB per token and layer). */
+typedef enum qsa_kv_format {
+  QSA_KV_BF16 = 0,
+  QSA_KV_FP8 = 1
+} qsa_kv_format;
+
 typedef struct qsa_cache_config {
   int32_t n_layers;        /* QSA layers managed per request (e.g. 12) */
   int32_t max_requests;    /* request slots */
@@ -113,12 +128,12 @@ typedef struct qsa_cache_config {
   int32_t budget_tokens;   /* largest indexer budget; multiple of 4, <= QSA_MAX_BUDGET_TOKENS */
   int32_t ring_tokens;     /* tail ring length per offloaded request and layer (> 0) */
   int32_t staging_rows;    /* shared staging rows per layer, carved from the pool front */
-  int32_t reserved0;
-  int64_t hbm_pool_rows;   /* rows of 2048 B in hbm_pool */
+  int32_t kv_format;       /* qsa_kv_format; row bytes R = QSA_ROW_BYTES or QSA_ROW_BYTES_FP8 */
+  int64_t hbm_pool_rows;   /* rows of R bytes in hbm_pool */
   /* Device storage (all caller-allocated, 16-byte aligned).  Leave every one
    * NULL for a host-only cache: the bookkeeping entry points then work
    * without a GPU and the compute entry points return QSA_ERR_NO_DEVICE. */
-  void* hbm_pool;          /* device [hbm_pool_rows][2048]: staging, rings, resident rows */
+  void* hbm_pool;          /* device [hbm_pool_rows][R]: staging, rings, resident rows */
   uint8_t* index_keys;     /* device [max_requests][n_layers][ctx_capacity][64] e4m3 codes */
   uint16_t* index_scales;  /* device [max_requests][n_layers][ctx_capacity] fp16 bits */
   int32_t* slot_table;     /* device [max_requests][n_layers][ctx_capacity] int32 */
@@ -138,9 +153,9 @@ typedef struct qsa_request_desc {
    * (ctx_len <= max_ctx <= ctx_capacity); 0 means ctx_len (no growth).  It
    * sets the request's row stride M = max(ctx_len, max_ctx): a QSA_KV_HBM
    * request leases n_layers * M pool rows, and a host history is laid out
-   * [n_layers][M][2048]. */
+   * [n_layers][M][R]. */
   int32_t max_ctx;
-  /* QSA_KV_HOST_RING, QSA_KV_HOST: pinned host memory [n_layers][M][2048]
+  /* QSA_KV_HOST_RING, QSA_KV_HOST: pinned host memory [n_layers][M][R]
    * holding the full history (host address; the library maps it for the
    * device, and qsa_append_token writes the rows of new tokens into it).
    * QSA_KV_HBM: NULL. */
@@ -244,7 +259,7 @@ qsa_status_t qsa_slot_table_set(qsa_cache* cache, qsa_handle handle, int32_t lay
                                 void* stream);
 
 /* Device pointer to the staging rows of a layer inside the pool
- * ([staging_rows][2048]); a landing zone for qsa_gather_rows. */
+ * ([staging_rows][R]); a landing zone for qsa_gather_rows. */
 qsa_status_t qsa_staging_ptr(qsa_cache* cache, int32_t layer, void** out);
 
 /* Read and clear the device error word (synchronises `stream`).
@@ -278,7 +293,9 @@ qsa_status_t qsa_request_advance(qsa_cache* cache, qsa_handle request, int32_t n
  *           round-to-nearest-even of clamp(k / scale, -448, 448), the
  *           division in fp32; a zero scale stores 64 zero codes.
  *   kv_new  device [units][2048]: the token's KV row (K[4][128] then
- *           V[4][128], bf16), copied unchanged.
+ *           V[4][128], bf16); stored unchanged in a BF16 cache, quantised
+ *           to an FP8 row (QSA_ROW_BYTES_FP8, rule of qsa_kv_format) in an
+ *           FP8 cache.
  * Where the row goes, by placement, and the slot-table writes:
  *   QSA_KV_HBM        pool row hbm_row_base + l*M + t; slot[t] = that row.
  *   QSA_KV_HOST       host history row (l, t); slot[t] = -1.
@@ -332,7 +349,8 @@ qsa_status_t qsa_select_c4_topk(qsa_cache* cache, const qsa_batch* batch,
  * host history for layer l.  n_rows[u] (device, may be NULL) receives the
  * row count.  [RTX4090 port, memory-ledger section: missing blocks are moved
  * back from pinned host memory on demand; offload digest: only the selected
- * rows cross the bus.]  rows_out: device [units][budget_tokens][2048]. */
+ * rows cross the bus.]  rows_out: device [units][budget_tokens][R] (R: the
+ * cache's row bytes). */
 qsa_status_t qsa_gather_rows(qsa_cache* cache, const qsa_batch* batch,
                              const int32_t* sel_blocks, const int32_t* n_sel,
                              int32_t budget_tokens, void* rows_out, int32_t* n_rows,
@@ -342,7 +360,7 @@ qsa_status_t qsa_gather_rows(qsa_cache* cache, const qsa_batch* batch,
  * for query head h (KV head g = h/4), logits_i = softmax_scale * q[u][h] .
  * K_i[g], out[u][h] = sum_i softmax(logits)_i V_i[g], lse[u][h] =
  * log sum_i exp(logits_i) (natural log; -inf and out = 0 with no tokens).
- * Rows come from `gathered` ([units][budget_tokens][2048], as written by
+ * Rows come from `gathered` ([units][budget_tokens][R], as written by
  * qsa_gather_rows) when it is not NULL, else through the slot table exactly
  * as qsa_gather_rows reads them (pool rows from HBM, cold rows zero-copy
  * from pinned host memory).  Split-K over the tokens with a log-sum-exp merge;
@@ -376,7 +394,7 @@ qsa_status_t qsa_sparse_decode_attn(qsa_cache* cache, const qsa_batch* batch,
  * split-K partials live in a static 8.5 MB device array of the library that
  * every GPU which loads the library holds until the process exits.
  *  q:      device bf16 bits [n_units][16][128]
- *  rows:   device [n_units][rows_stride][2048], as written by qsa_gather_rows
+ *  rows:   device [n_units][rows_stride][2048] BF16 rows, as written by qsa_gather_rows
  *          (rows_stride = budget_tokens there); row i of unit u is used when
  *          i < n_rows[u]
  *  n_rows: device int32 [n_units], clamped on the device to [0, rows_stride]

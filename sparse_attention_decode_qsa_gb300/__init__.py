@@ -7,5 +7,5 @@ the library has not been built.
 """
 from ._native import (ERR_BAD_BLOCK, ERR_BAD_SLOT, ERR_CAPACITY, ERR_CUDA, ERR_INVALID_ARG,  # noqa: F401
                       ERR_NO_DEVICE, ERR_OUT_OF_SLOTS, ERR_STALE_HANDLE, ERR_TIMEOUT, KV_HBM,
-                      KV_HOST, KV_HOST_RING, OK, Handle, QsaError, lib)
+                      KV_BF16, KV_FP8, KV_HOST, KV_HOST_RING, OK, Handle, QsaError, lib)
 from .api import Cache  # noqa: F401

@@ -16,6 +16,9 @@ KV_HEADS = 4
 HEAD_DIM = 128
 Q_HEADS = 16
 ROW_BYTES = 2048
+ROW_BYTES_FP8 = 1040
+KV_BF16 = 0
+KV_FP8 = 1
 MAX_UNITS = 256
 MAX_BUDGET_TOKENS = 8192
 STATIC_MAX_UNITS = 16
@@ -38,7 +41,7 @@ class CacheConfig(C.Structure):
     _fields_ = [
         ("n_layers", C.c_int32), ("max_requests", C.c_int32), ("ctx_capacity", C.c_int64),
         ("budget_tokens", C.c_int32), ("ring_tokens", C.c_int32), ("staging_rows", C.c_int32),
-        ("reserved0", C.c_int32), ("hbm_pool_rows", C.c_int64),
+        ("kv_format", C.c_int32), ("hbm_pool_rows", C.c_int64),
         ("hbm_pool", C.c_void_p), ("index_keys", C.c_void_p), ("index_scales", C.c_void_p),
         ("slot_table", C.c_void_p), ("workspace", C.c_void_p), ("workspace_bytes", C.c_int64),
     ]

@@ -41,7 +41,7 @@ class Cache:
 
     With device=None the cache is host-only (bookkeeping without a GPU).
     Storage layout (all owned here, passed to the library as raw pointers):
-      pool         uint8 [hbm_pool_rows][2048]
+      pool         uint8 [hbm_pool_rows][row_bytes] (2048 BF16 rows, 1040 FP8 rows)
       index_keys   uint8 [max_requests][n_layers][ctx_capacity][64]
       index_scales fp16  [max_requests][n_layers][ctx_capacity]
       slot_table   int32 [max_requests][n_layers][ctx_capacity]
@@ -50,7 +50,7 @@ class Cache:
 
     def __init__(self, n_layers: int, max_requests: int, ctx_capacity: int,
                  hbm_pool_rows: int, budget_tokens: int = 2048, ring_tokens: int = 4096,
-                 staging_rows: int = 2048, device="cuda"):
+                 staging_rows: int = 2048, device="cuda", kv_format: int = N.KV_BF16):
         self.L = N.lib()
         cfg = N.CacheConfig()
         cfg.n_layers = n_layers
@@ -60,6 +60,9 @@ class Cache:
         cfg.ring_tokens = ring_tokens
         cfg.staging_rows = staging_rows
         cfg.hbm_pool_rows = hbm_pool_rows
+        cfg.kv_format = kv_format
+        self.kv_format = kv_format
+        self.row_bytes = N.ROW_BYTES_FP8 if kv_format == N.KV_FP8 else N.ROW_BYTES
         self.n_layers, self.max_requests, self.ctx_capacity = n_layers, max_requests, ctx_capacity
         self.budget_tokens, self.ring_tokens, self.staging_rows = budget_tokens, ring_tokens, staging_rows
         self.device = device
@@ -67,7 +70,7 @@ class Cache:
             ws = self.L.qsa_workspace_bytes(C.byref(cfg))
             if ws < 0:
                 raise QsaError(N.ERR_INVALID_ARG, "qsa_workspace_bytes", "bad config")
-            self.pool = torch.empty(hbm_pool_rows, N.ROW_BYTES, dtype=torch.uint8, device=device)
+            self.pool = torch.empty(hbm_pool_rows, self.row_bytes, dtype=torch.uint8, device=device)
             self.index_keys = torch.zeros(max_requests, n_layers, ctx_capacity, N.INDEX_DIM,
                                           dtype=torch.uint8, device=device)
             self.index_scales = torch.zeros(max_requests, n_layers, ctx_capacity,

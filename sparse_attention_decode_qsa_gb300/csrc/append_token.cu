@@ -11,11 +11,13 @@
 // One CTA of 128 threads per unit.  Threads 0-63 hold the 64 key elements:
 // absmax by warp shuffles, scale = fp16 round-to-nearest-even of absmax/448
 // (fp32 division, saturating at 65504), codes = E4M3 round-to-nearest-even
-// (saturating) of clamp(k/scale, +-448) (fp32 division).  All 128 threads
-// copy the row, 16 bytes each, to the pool row and/or the host history row
-// (a store through the mapped pointer crosses the host link).  Thread 0
-// writes the token's slot and, when a ring row is handed over, marks the
-// token that held it cold.
+// (saturating) of clamp(k/scale, +-448) (fp32 division).  The row goes to
+// the pool row and/or the host history row (a store through the mapped
+// pointer crosses the host link): a BF16 row unchanged, 16 bytes per thread;
+// for an FP8 cache each thread quantises 8 of the row's 1024 values under
+// the same rule, one scale per 128-value head vector (16 threads each).
+// Thread 0 writes the token's slot and, when a ring row is handed over,
+// marks the token that held it cold.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -71,20 +73,58 @@ __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendPara
   // ---- KV row
   const uint4 v = reinterpret_cast<const uint4*>(p.kv_new + (int64_t)u * kRowBytes)[tid];
   const int64_t pool_row = p.tg.pool_row[u];
-  if (pool_row >= 0) {
-    if (pool_row < p.b.pool_rows) {
-      reinterpret_cast<uint4*>(p.b.pool + pool_row * kRowBytes)[tid] = v;
-    } else if (tid == 0) {
-      report_error(p.b.err, QSA_ERR_BAD_SLOT, kKernAppend, pool_row);
+  const bool to_pool = pool_row >= 0 && pool_row < p.b.pool_rows;
+  if (pool_row >= p.b.pool_rows && tid == 0) report_error(p.b.err, QSA_ERR_BAD_SLOT, kKernAppend, pool_row);
+  uint8_t* dst_pool = to_pool ? p.b.pool + pool_row * p.b.row_bytes : nullptr;
+  uint8_t* dst_host = p.b.u[u].host_rows ? const_cast<uint8_t*>(p.b.u[u].host_rows) + t * p.b.row_bytes
+                                         : nullptr;
+  if (p.b.row_bytes == kRowBytes) {
+    if (dst_pool) reinterpret_cast<uint4*>(dst_pool)[tid] = v;
+    if (dst_host) reinterpret_cast<uint4*>(dst_host)[tid] = v;
+  } else {
+    // head vector hv = tid / 16 (K heads 0-3, then V heads 0-3), values
+    // 8 (tid % 16) .. +7 of it; the BF16 row holds them in this order
+    float x[8];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float va = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) va = fmaxf(va, fabsf(x[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) va = fmaxf(va, __shfl_xor_sync(0xFFFFFFFFu, va, o));
+    const __half vs16 = __float2half_rn(fminf(va / 448.0f, 65504.0f));
+    const float vsf = __half2float(vs16);
+    uint32_t packed[2] = {0u, 0u};
+    if (vsf > 0.f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float y = fminf(fmaxf(x[i] / vsf, -448.0f), 448.0f);
+        packed[i >> 2] |= (uint32_t)(uint8_t)__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3)
+                          << (8 * (i & 3));
+      }
+    }
+    const uint2 codes = make_uint2(packed[0], packed[1]);
+    const int hv = tid >> 4;
+    const int off = hv * kHeadDim + (tid & 15) * 8;          // K codes, then V codes
+    const uint16_t sbits = vsf > 0.f ? __half_as_ushort(vs16) : (uint16_t)0;
+    if (dst_pool) {
+      *reinterpret_cast<uint2*>(dst_pool + off) = codes;
+      if ((tid & 15) == 0) reinterpret_cast<uint16_t*>(dst_pool + 2 * kKvHeads * kHeadDim)[hv] = sbits;
+    }
+    if (dst_host) {
+      *reinterpret_cast<uint2*>(dst_host + off) = codes;
+      if ((tid & 15) == 0) reinterpret_cast<uint16_t*>(dst_host + 2 * kKvHeads * kHeadDim)[hv] = sbits;
     }
   }
-  if (p.b.u[u].host_rows)
-    reinterpret_cast<uint4*>(const_cast<uint8_t*>(p.b.u[u].host_rows) + t * kRowBytes)[tid] = v;
 
   // ---- slot table
   if (tid == 0) {
     int32_t* slots = p.b.slot_table + p.b.unit_row(u);
-    slots[t] = pool_row >= 0 && pool_row < p.b.pool_rows ? (int32_t)pool_row : -1;
+    slots[t] = to_pool ? (int32_t)pool_row : -1;
     const int64_t ev = p.tg.evict[u];
     if (ev >= 0 && ev < t) slots[ev] = -1;
   }

@@ -8,10 +8,11 @@
 // Qwen3.8-Flash-Next в RAM через vLLM без потери скорости декодирования",
 // section "Механизм гибридного разреженного оффлоадинга").
 //
-// Gather mapping: a CTA owns 8 selected blocks (32 token rows, 64 KiB).  Its
-// first warp resolves the 32 row sources into shared memory; then all 256
-// threads copy 16-byte chunks, 16 per thread, all loads issued before the
-// stores so that many requests are in flight on the host link.
+// Gather mapping: a CTA owns 8 selected blocks (32 token rows: 64 KiB of BF16
+// rows, 32.5 KiB of FP8 rows).  Its first warp resolves the 32 row sources
+// into shared memory; then all 256 threads copy 16-byte chunks (16 each for
+// BF16 rows, 9 for FP8 rows), all loads issued before the stores so that
+// many requests are in flight on the host link.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -20,7 +21,6 @@ namespace {
 constexpr int kGatherThreads = 256;
 constexpr int kGatherBlocks = 8;
 constexpr int kGatherRows = kGatherBlocks * 4;
-constexpr int kChunksPerRow = kRowBytes / 16;  // 128
 
 struct GatherParams {
   BatchDesc b;
@@ -28,7 +28,7 @@ struct GatherParams {
   const int32_t* n_sel;
   int32_t k_max;
   int32_t budget_tokens;
-  uint8_t* out;      // [units][budget_tokens][2048]
+  uint8_t* out;      // [units][budget_tokens][row bytes]
   int32_t* n_rows;   // [units] or nullptr
 };
 
@@ -40,6 +40,8 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint8_t* p) {
   return r;
 }
 
+// kChunksPerRow: 16-byte chunks of a row (128 for BF16 rows, 65 for FP8 rows)
+template <int kChunksPerRow>
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const GatherParams p) {
   __shared__ const uint8_t* src[kGatherRows];
   const int u = blockIdx.y;
@@ -77,19 +79,20 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
   }
   __syncthreads();
 
-  uint8_t* dst = p.out + ((int64_t)u * p.budget_tokens + 4 * (int64_t)j0) * kRowBytes;
-  constexpr int kPer = kGatherRows * kChunksPerRow / kGatherThreads;  // 16
+  uint8_t* dst = p.out + ((int64_t)u * p.budget_tokens + 4 * (int64_t)j0) * (kChunksPerRow * 16);
+  constexpr int kTotal = kGatherRows * kChunksPerRow;
+  constexpr int kPer = (kTotal + kGatherThreads - 1) / kGatherThreads;  // 16 or 9
   uint4 v[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int idx = k * kGatherThreads + threadIdx.x;
-    const uint8_t* s = src[idx / kChunksPerRow];
+    const uint8_t* s = idx < kTotal ? src[idx / kChunksPerRow] : nullptr;
     v[k] = s ? ld_nc_v4(s + (idx % kChunksPerRow) * 16) : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int idx = k * kGatherThreads + threadIdx.x;
-    if (src[idx / kChunksPerRow])
+    if (idx < kTotal && src[idx / kChunksPerRow])
       *reinterpret_cast<uint4*>(dst + (int64_t)idx * 16) = v[k];
   }
 }
@@ -142,14 +145,21 @@ cudaError_t launch_gather_rows(const BatchDesc& b, const int32_t* sel_blocks,
   p.n_rows = n_rows;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        gather_rows_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-        cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = cudaFuncSetAttribute(gather_rows_kernel<kRowBytes / 16>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gather_rows_kernel<kRowBytesFp8 / 16>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid((p.k_max + kGatherBlocks - 1) / kGatherBlocks, b.n_units);
-  gather_rows_kernel<<<grid, kGatherThreads, 0, s>>>(p);
+  if (b.row_bytes == kRowBytesFp8)
+    gather_rows_kernel<kRowBytesFp8 / 16><<<grid, kGatherThreads, 0, s>>>(p);
+  else
+    gather_rows_kernel<kRowBytes / 16><<<grid, kGatherThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -73,7 +73,7 @@ bool config_sizes_ok(const qsa_cache_config* c) {
          c->ctx_capacity <= 0x7FFFFFFFll && c->budget_tokens >= 4 &&
          c->budget_tokens % 4 == 0 && c->budget_tokens <= QSA_MAX_BUDGET_TOKENS &&
          c->ring_tokens > 0 && c->staging_rows >= 0 && c->hbm_pool_rows >= 0 &&
-         c->hbm_pool_rows <= 0x7FFFFFFFll;
+         c->hbm_pool_rows <= 0x7FFFFFFFll && (c->kv_format == QSA_KV_BF16 || c->kv_format == QSA_KV_FP8);
 }
 
 }  // namespace
@@ -94,6 +94,7 @@ struct qsa_cache {
   std::map<int64_t, int64_t> free_rows;  // start -> length
 
   ErrorWord* err() const { return reinterpret_cast<ErrorWord*>(cfg.workspace); }
+  int64_t row_bytes() const { return cfg.kv_format == QSA_KV_FP8 ? kRowBytesFp8 : kRowBytes; }
   float* partials() const {
     return reinterpret_cast<float*>(static_cast<uint8_t*>(cfg.workspace) + kErrBytes);
   }
@@ -166,7 +167,7 @@ struct qsa_cache {
     d->partials = partials();
     d->tickets = tickets();
     d->splits_max = (int32_t)splits_max;
-    d->pad0 = 0;
+    d->row_bytes = (int32_t)row_bytes();
     for (int i = 0; i < b->n_req; ++i) {
       const Lease* l;
       if (qsa_status_t st = check_handle(b->requests[i], &l)) return st;
@@ -179,7 +180,7 @@ struct qsa_cache {
         u.req = (int32_t)b->requests[i].index;
         u.layer = b->layer0 + li;
         u.n = l->ctx_len;
-        u.host_rows = l->host_rows ? l->host_rows + (int64_t)u.layer * l->max_ctx * kRowBytes
+        u.host_rows = l->host_rows ? l->host_rows + (int64_t)u.layer * l->max_ctx * row_bytes()
                                    : nullptr;
       }
     }
@@ -399,7 +400,7 @@ qsa_status_t qsa_cache_stats(const qsa_cache* c, qsa_stats* out) {
     if (kv.second > out->largest_free_rows) out->largest_free_rows = kv.second;
   }
   out->staging_rows_total = c->staging_total;
-  out->hbm_kv_bytes_in_use = leased * kRowBytes;
+  out->hbm_kv_bytes_in_use = leased * c->row_bytes();
   return ok();
 }
 
@@ -429,7 +430,7 @@ qsa_status_t qsa_staging_ptr(qsa_cache* c, int32_t layer, void** out) {
   if (!c || !out) return fail(QSA_ERR_INVALID_ARG, "null argument");
   if (!c->has_device) return fail(QSA_ERR_NO_DEVICE, "cache has no device storage");
   if (layer < 0 || layer >= c->cfg.n_layers) return fail(QSA_ERR_INVALID_ARG, "bad layer %d", layer);
-  *out = static_cast<uint8_t*>(c->cfg.hbm_pool) + (int64_t)layer * c->cfg.staging_rows * kRowBytes;
+  *out = static_cast<uint8_t*>(c->cfg.hbm_pool) + (int64_t)layer * c->cfg.staging_rows * c->row_bytes();
   return ok();
 }
 

@@ -16,7 +16,8 @@ constexpr int kKvHeads = QSA_KV_HEADS;        // 4
 constexpr int kHeadDim = QSA_HEAD_DIM;        // 128
 constexpr int kQHeads = QSA_Q_HEADS;          // 16
 constexpr int kGroup = kQHeads / kKvHeads;    // 4 query heads per KV head
-constexpr int kRowBytes = QSA_ROW_BYTES;      // 2048
+constexpr int kRowBytes = QSA_ROW_BYTES;      // 2048: BF16 row
+constexpr int kRowBytesFp8 = QSA_ROW_BYTES_FP8;  // 1040: FP8 row
 constexpr int kMaxUnits = QSA_MAX_UNITS;
 
 // Split-K granularity of the attention: one CTA covers this many selected
@@ -70,7 +71,7 @@ struct BatchDesc {
   float* partials;            // [req][layer][splits_max][kPartFloats]
   int32_t* tickets;           // [req][layer][2]: work counter, finished CTAs
   int32_t splits_max;
-  int32_t pad0;
+  int32_t row_bytes;          // kRowBytes (BF16 rows) or kRowBytesFp8 (FP8 rows)
   UnitDesc u[kMaxUnits];
 
   __host__ __device__ int64_t unit_row(int u_) const {
@@ -92,8 +93,8 @@ __device__ __forceinline__ void report_error(ErrorWord* e, int32_t status, int32
 __device__ __forceinline__ const uint8_t* row_source(const BatchDesc& b, int u, int64_t t,
                                                      int32_t kernel) {
   const int32_t slot = b.slot_table[b.unit_row(u) + t];
-  if (slot >= 0 && (int64_t)slot < b.pool_rows) return b.pool + (int64_t)slot * kRowBytes;
-  if (slot == -1 && b.u[u].host_rows != nullptr) return b.u[u].host_rows + t * kRowBytes;
+  if (slot >= 0 && (int64_t)slot < b.pool_rows) return b.pool + (int64_t)slot * b.row_bytes;
+  if (slot == -1 && b.u[u].host_rows != nullptr) return b.u[u].host_rows + t * b.row_bytes;
   report_error(b.err, QSA_ERR_BAD_SLOT, kernel, ((int64_t)u << 40) | (t & 0xFFFFFFFFFFll));
   return nullptr;
 }

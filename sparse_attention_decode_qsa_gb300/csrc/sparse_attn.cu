@@ -37,6 +37,7 @@
 // 4l..4l+3.  Plain FMAs throughout: 4 query heads per KV head make this a
 // 4-row contraction, not a tensor-core shape.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "qsa_internal.cuh"
 
@@ -138,6 +139,43 @@ __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int s
     cp_async16(buf + i * kSliceBytes + lane * 16, s ? s + off : p.b.pool, s ? 16u : 0u);
   }
   return valid;
+}
+
+// End of a split CTA: merge the two token halves of each KV head through
+// shared memory, then write the CTA's partial (m, l, acc) for the merge.
+__device__ __forceinline__ void finish_split(const AttnParams& p, int u, int r, int g, int half,
+                                             int lane, int hj, float m_run, float l_run,
+                                             float (&acc)[kGroup][4], float (&xm)[kKvHeads][kGroup],
+                                             float (&xl)[kKvHeads][kGroup],
+                                             float (&xacc)[kKvHeads][kGroup][kHeadDim]) {
+  if (half == 1) {
+    if ((lane & 7) == 0) { xm[g][hj] = m_run; xl[g][hj] = l_run; }
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j)
+      *reinterpret_cast<float4*>(&xacc[g][j][4 * lane]) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+  }
+  __syncthreads();
+  if (half == 0) {
+    const float mo = xm[g][hj], lo = xl[g][hj];
+    const float mn = fmaxf(m_run, mo);
+    const float sa = (mn == -INFINITY) ? 0.f : exp2f(m_run - mn);
+    const float sb = (mn == -INFINITY) ? 0.f : exp2f(mo - mn);
+    const float L = fmaf(l_run, sa, lo * sb);
+    float* part = partial_ptr(p.b, u, r);
+    if ((lane & 7) == 0) {
+      part[g * kGroup + hj] = mn;
+      part[kQHeads + g * kGroup + hj] = L;
+    }
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      const float aj = __shfl_sync(0xFFFFFFFFu, sa, 8 * j);
+      const float bj = __shfl_sync(0xFFFFFFFFu, sb, 8 * j);
+      const float4 o = *reinterpret_cast<const float4*>(&xacc[g][j][4 * lane]);
+      *reinterpret_cast<float4*>(part + 2 * kQHeads + (g * kGroup + j) * kHeadDim + 4 * lane) =
+          make_float4(fmaf(acc[j][0], aj, o.x * bj), fmaf(acc[j][1], aj, o.y * bj),
+                      fmaf(acc[j][2], aj, o.z * bj), fmaf(acc[j][3], aj, o.w * bj));
+    }
+  }
 }
 
 __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams p) {
@@ -263,35 +301,200 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
 
-  // merge the two token halves of each KV head, then write the CTA's partial
-  if (half == 1) {
-    if ((lane & 7) == 0) { xm[g][hj] = m_run; xl[g][hj] = l_run; }
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j)
-      *reinterpret_cast<float4*>(&xacc[g][j][4 * lane]) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
-  }
-  __syncthreads();
-  if (half == 0) {
-    const float mo = xm[g][hj], lo = xl[g][hj];
-    const float mn = fmaxf(m_run, mo);
-    const float sa = (mn == -INFINITY) ? 0.f : exp2f(m_run - mn);
-    const float sb = (mn == -INFINITY) ? 0.f : exp2f(mo - mn);
-    const float L = fmaf(l_run, sa, lo * sb);
-    float* part = partial_ptr(p.b, u, r);
-    if ((lane & 7) == 0) {
-      part[g * kGroup + hj] = mn;
-      part[kQHeads + g * kGroup + hj] = L;
+  finish_split(p, u, r, g, half, lane, hj, m_run, l_run, acc, xm, xl, xacc);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 rows (QSA_ROW_BYTES_FP8: E4M3 codes of K and V, then fp16 scales per
+// KV head).  Same work layout as the BF16 kernel; per token and KV head a
+// warp copies 272 bytes - the 128 K codes and 128 V codes of head g and the
+// row's 16 bytes of scales - half the host-link bytes of a BF16 row.  A
+// token's K scale multiplies its logit after the dot product, its V scale
+// its probability in P.V.
+constexpr int kSliceFp8 = 272;                        // K[g] codes | V[g] codes | scales
+constexpr int kChunksFp8 = kSliceFp8 / 16;            // 17
+constexpr int kWarpBufFp8 = kWarpTokens * kSliceFp8;  // 2176 B
+#ifndef QSA_ATTN_STAGES_FP8
+#define QSA_ATTN_STAGES_FP8 2
+#endif
+#ifndef QSA_ATTN_HOST_CTAS_FP8
+#define QSA_ATTN_HOST_CTAS_FP8 64
+#endif
+constexpr int kAStagesFp8 = QSA_ATTN_STAGES_FP8;      // splits in flight per warp
+constexpr int kMaxCtasHostFp8 = QSA_ATTN_HOST_CTAS_FP8;
+constexpr int kSmemFp8 = kWarps * kAStagesFp8 * kWarpBufFp8;
+
+// Four E4M3 codes (bytes of w, low first) -> four floats (exact).
+__device__ __forceinline__ void e4m3x4_to_float4(uint32_t w, float& a, float& b, float& c, float& d) {
+  uint32_t lo, hi;
+  asm("{\n .reg .b16 x, y;\n mov.b32 {x, y}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, x;\n cvt.rn.f16x2.e4m3x2 %1, y;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+  const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  a = f0.x; b = f0.y; c = f1.x; d = f1.y;
+}
+
+__device__ __forceinline__ uint32_t issue_warp_fp8(const AttnParams& p, int u, int split, int nsel,
+                                                   int g, int half, uint8_t* buf) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = p.b.u[u].n;
+  const uint8_t* src = nullptr;
+  if (lane < kWarpTokens) {
+    const int tok = half * kWarpTokens + lane;              // token within the split
+    const int j = split * kBlocksPerSplit + tok / 4;        // selected-block index
+    if (j < nsel) {
+      const int64_t b = p.sel[(int64_t)u * p.k_max + j];
+      const int64_t t = 4 * b + (tok & 3);
+      if (b < 0 || 4 * b >= n) {
+        if ((tok & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
+      } else if (t < n) {
+        src = p.gathered ? p.gathered + ((int64_t)u * p.budget_tokens + 4 * j + (tok & 3)) * kRowBytesFp8
+                         : row_source(p.b, u, t, kKernAttn);
+      }
     }
+  }
+  const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & ((1u << kWarpTokens) - 1u);
+  // 8 tokens x 17 chunks: chunk c < 8 of K[g], 8..15 of V[g], 16 = scales
+#pragma unroll
+  for (int it = 0; it < (kWarpTokens * kChunksFp8 + 31) / 32; ++it) {
+    const int idx = it * 32 + lane;
+    const int tok = idx < kWarpTokens * kChunksFp8 ? idx / kChunksFp8 : 0;
+    const uint8_t* s = reinterpret_cast<const uint8_t*>(
+        __shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(src), tok));
+    if (idx < kWarpTokens * kChunksFp8) {
+      const int c = idx - tok * kChunksFp8;
+      const int off = c < 8 ? g * kHeadDim + c * 16
+                            : (c < 16 ? kKvHeads * kHeadDim + g * kHeadDim + (c - 8) * 16
+                                      : 2 * kKvHeads * kHeadDim);
+      cp_async16(buf + tok * kSliceFp8 + c * 16, s ? s + off : p.b.pool, s ? 16u : 0u);
+    }
+  }
+  return valid;
+}
+
+__global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];  // [warp][stage][8][272]
+  __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
+  __shared__ uint32_t vmask[kWarps][kAStagesFp8];
+  __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
+
+  const int u = blockIdx.x / p.cpu, r = blockIdx.x % p.cpu;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = warp & 3, half = warp >> 2;
+  uint8_t* wbuf = smem + warp * kAStagesFp8 * kWarpBufFp8;
+  int nsel = p.n_sel[u];
+  if (nsel < 0 || nsel > p.k_max) {
+    if (r == 0 && threadIdx.x == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
+    nsel = 0;
+  }
+  const int splits = (nsel + kBlocksPerSplit - 1) / kBlocksPerSplit;
+  const int count = r < splits ? (splits - 1 - r) / p.cpu + 1 : 0;
+
+  float qr[kGroup][4];
+  {
+    const uint16_t* qu = p.q + (int64_t)u * kQHeads * kHeadDim;
 #pragma unroll
     for (int j = 0; j < kGroup; ++j) {
-      const float aj = __shfl_sync(0xFFFFFFFFu, sa, 8 * j);
-      const float bj = __shfl_sync(0xFFFFFFFFu, sb, 8 * j);
-      const float4 o = *reinterpret_cast<const float4*>(&xacc[g][j][4 * lane]);
-      *reinterpret_cast<float4*>(part + 2 * kQHeads + (g * kGroup + j) * kHeadDim + 4 * lane) =
-          make_float4(fmaf(acc[j][0], aj, o.x * bj), fmaf(acc[j][1], aj, o.y * bj),
-                      fmaf(acc[j][2], aj, o.z * bj), fmaf(acc[j][3], aj, o.w * bj));
+      const uint2 w2 = *reinterpret_cast<const uint2*>(qu + (g * kGroup + j) * kHeadDim + 4 * lane);
+      qr[j][0] = bf16_lo(w2.x) * p.scale_log2;
+      qr[j][1] = bf16_hi(w2.x) * p.scale_log2;
+      qr[j][2] = bf16_lo(w2.y) * p.scale_log2;
+      qr[j][3] = bf16_hi(w2.y) * p.scale_log2;
     }
   }
+  const int hj = (lane >> 3) & 3;
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[kGroup][4];
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+#pragma unroll
+  for (int k = 0; k < kAStagesFp8 - 1; ++k) {
+    if (k < count) {
+      const uint32_t v = issue_warp_fp8(p, u, visit_split(k, count, r, p.cpu), nsel, g, half,
+                                        wbuf + k * kWarpBufFp8);
+      if (lane == 0) vmask[warp][k] = v;
+    }
+    cp_async_commit();
+  }
+  for (int k = 0; k < count; ++k) {
+    const int kn = k + kAStagesFp8 - 1;
+    if (kn < count) {
+      const uint32_t v = issue_warp_fp8(p, u, visit_split(kn, count, r, p.cpu), nsel, g, half,
+                                        wbuf + (kn % kAStagesFp8) * kWarpBufFp8);
+      if (lane == 0) vmask[warp][kn % kAStagesFp8] = v;
+    }
+    cp_async_commit();
+    cp_async_wait<kAStagesFp8 - 1>();
+    __syncwarp();
+    const uint32_t valid_cur = vmask[warp][k % kAStagesFp8];
+    const uint8_t* R = wbuf + (k % kAStagesFp8) * kWarpBufFp8;
+
+    float x0 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kWarpTokens; ++i) {
+      float k0, k1, k2, k3;
+      e4m3x4_to_float4(*reinterpret_cast<const uint32_t*>(R + i * kSliceFp8 + 4 * lane), k0, k1, k2, k3);
+      float d[kGroup];
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j)
+        d[j] = fmaf(qr[j][3], k3, fmaf(qr[j][2], k2, fmaf(qr[j][1], k1, qr[j][0] * k0)));
+      const bool up16 = lane & 16;
+      const float a0 = up16 ? d[0] : d[2], a1 = up16 ? d[1] : d[3];
+      const float r0 = __shfl_xor_sync(0xFFFFFFFFu, a0, 16);
+      const float r1 = __shfl_xor_sync(0xFFFFFFFFu, a1, 16);
+      const float v0 = (up16 ? d[2] : d[0]) + r0;
+      const float v1 = (up16 ? d[3] : d[1]) + r1;
+      const bool up8 = lane & 8;
+      const float a = up8 ? v0 : v1;
+      float v = (up8 ? v1 : v0) + __shfl_xor_sync(0xFFFFFFFFu, a, 8);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+      const float ks = __half2float(*reinterpret_cast<const __half*>(R + i * kSliceFp8 + 256 + 2 * g));
+      if ((lane & 7) == i) x0 = ((valid_cur >> i) & 1u) ? v * ks : -INFINITY;
+    }
+
+    float ms = x0;
+    ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 1));
+    ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 2));
+    ms = fmaxf(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, 4));
+    const float m_new = fmaxf(m_run, ms);
+    const float so = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+    const float p0 = (x0 == -INFINITY) ? 0.f : exp2f(x0 - m_new);
+    float ps = p0;
+    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
+    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
+    ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 4);
+    l_run = fmaf(l_run, so, ps);
+    m_run = m_new;
+
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      const float sj = __shfl_sync(0xFFFFFFFFu, so, 8 * j);
+      acc[j][0] *= sj; acc[j][1] *= sj; acc[j][2] *= sj; acc[j][3] *= sj;
+    }
+#pragma unroll
+    for (int i = 0; i < kWarpTokens; ++i) {
+      float v0, v1, v2, v3;
+      e4m3x4_to_float4(*reinterpret_cast<const uint32_t*>(R + i * kSliceFp8 + kHeadDim + 4 * lane),
+                       v0, v1, v2, v3);
+      const float vs = __half2float(*reinterpret_cast<const __half*>(R + i * kSliceFp8 + 256 + 8 + 2 * g));
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) {
+        const float pj = __shfl_sync(0xFFFFFFFFu, p0, 8 * j + i) * vs;
+        acc[j][0] = fmaf(pj, v0, acc[j][0]);
+        acc[j][1] = fmaf(pj, v1, acc[j][1]);
+        acc[j][2] = fmaf(pj, v2, acc[j][2]);
+        acc[j][3] = fmaf(pj, v3, acc[j][3]);
+      }
+    }
+    __syncwarp();
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  finish_split(p, u, r, g, half, lane, hj, m_run, l_run, acc, xm, xl, xacc);
 }
 
 // Merge: CTA (head, unit), thread = output dim; reads the cpu partials.
@@ -331,6 +534,8 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
     if (e == cudaSuccess)
       e = prefer_max_shared(attn_split_kernel, kSmemBytes);
     if (e == cudaSuccess)
+      e = prefer_max_shared(attn_split_fp8_kernel, kSmemFp8);
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
@@ -351,13 +556,17 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
   if (gathered == nullptr)
     for (int u = 0; u < b.n_units; ++u) any_host |= b.u[u].host_rows != nullptr;
   const int splits = (p.k_max + kBlocksPerSplit - 1) / kBlocksPerSplit;
-  const int cap = any_host ? kMaxCtasHost : sm_count;
+  const bool fp8 = b.row_bytes == kRowBytesFp8;
+  const int cap = any_host ? (fp8 ? kMaxCtasHostFp8 : kMaxCtasHost) : sm_count;
   int cpu = cap / b.n_units;
   if (cpu < 1) cpu = 1;
   if (cpu > splits) cpu = splits;
   if (cpu > b.splits_max) cpu = b.splits_max;   // partial slots in the workspace
   p.cpu = cpu;
-  attn_split_kernel<<<b.n_units * cpu, kThreads, kSmemBytes, s>>>(p);
+  if (fp8)
+    attn_split_fp8_kernel<<<b.n_units * cpu, kThreads, kSmemFp8, s>>>(p);
+  else
+    attn_split_kernel<<<b.n_units * cpu, kThreads, kSmemBytes, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_merge_kernel<<<dim3(kQHeads, b.n_units), kHeadDim, 0, s>>>(p);

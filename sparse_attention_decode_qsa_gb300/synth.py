@@ -87,6 +87,25 @@ def index_keys(n: int, seed: int, device="cpu", chunk: int = 1 << 20):
     return codes, scales
 
 
+def fp8_kv_rows(rows: torch.Tensor) -> torch.Tensor:
+    """FP8 rows (uint8 [m][1040]) of BF16 KV rows (uint8 [m][2048]): each of
+    the 8 head vectors (K heads 0-3, V heads 0-3, 128 values) gets the index
+    keys' recipe - scale = fp16(absmax/448), codes = E4M3 of clamp(x/scale,
+    +-448), zero codes for a zero scale - stored as codes K[4][128],
+    V[4][128], then the 8 fp16 scales."""
+    m = rows.shape[0]
+    x = rows.contiguous().view(torch.bfloat16).float().view(m, 8, 128)
+    sc = (x.abs().amax(dim=2) / E4M3_MAX).to(torch.float16)
+    scf = sc.float()
+    safe = torch.where(scf > 0, scf, torch.ones_like(scf))
+    q = (x / safe[:, :, None]).clamp(-E4M3_MAX, E4M3_MAX)
+    q = torch.where((scf > 0)[:, :, None], q, torch.zeros_like(q))
+    out = torch.empty(m, 1040, dtype=torch.uint8, device=rows.device)
+    out[:, :1024] = q.to(torch.float8_e4m3fn).view(torch.uint8).view(m, 1024)
+    out[:, 1024:] = sc.contiguous().view(torch.uint8).view(m, 16)
+    return out
+
+
 def plant(scales: torch.Tensor, blocks, n: int, factor: float = PLANT_FACTOR):
     """Multiply the fp16 scale of every token of the given C4 blocks by factor."""
     blocks = torch.as_tensor(blocks, dtype=torch.int64, device=scales.device)

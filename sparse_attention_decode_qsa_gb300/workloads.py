@@ -81,7 +81,7 @@ class Workload:
             unregister_pinned(old)
             old = None
         if placement != N.KV_HBM and old is None:
-            old = register_pinned(torch.empty(self.n_layers, n, N.ROW_BYTES, dtype=torch.uint8))
+            old = register_pinned(torch.empty(self.n_layers, n, self.cache.row_bytes, dtype=torch.uint8))
         self.host[r] = old
         self.ctxs[r], self.placements[r] = n, placement
         self.handles[r] = self.cache.request_begin(n, placement, host_rows=old)
@@ -198,6 +198,8 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
         wl.q_idx[u], wl.w[u] = qi, wi
         wl.q[u] = synth.attn_query(synth.mix_seed(s, 3), device=dev)
         rows = synth.kv_rows(n, synth.mix_seed(s, 4), device=dev)
+        if cache.kv_format == N.KV_FP8:
+            rows = synth.fp8_kv_rows(rows)
         if p == N.KV_HBM:
             b0 = info.hbm_row_base + l * stride
             cache.pool[b0:b0 + n] = rows
@@ -212,7 +214,8 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
 
 def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: int = 4096,
           staging_rows: int = 2048, seed: int = 0, device="cuda", extra_requests: int = 0,
-          spare_rows: int = 0, ctx_capacity: int | None = None, grow: int = 0) -> Workload:
+          spare_rows: int = 0, ctx_capacity: int | None = None, grow: int = 0,
+          kv_format: int = N.KV_BF16) -> Workload:
     """planting(l, r, n) -> block ids to plant for unit (l, r).  grow: tokens
     every request may still append (its max_ctx is ctx + grow)."""
     ctx_capacity = ctx_capacity or (max(ctxs) + grow)
@@ -224,12 +227,12 @@ def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: i
     pool_rows = n_layers * staging_rows + rows_needed + spare_rows
     cache = Cache(n_layers=n_layers, max_requests=R + extra_requests, ctx_capacity=ctx_capacity,
                   hbm_pool_rows=pool_rows, budget_tokens=budget, ring_tokens=ring,
-                  staging_rows=staging_rows, device=dev)
+                  staging_rows=staging_rows, device=dev, kv_format=kv_format)
     handles, host = [], []
     for r, (n, p) in enumerate(zip(ctxs, placements)):
         hrows = None
         if p != N.KV_HBM:
-            hrows = register_pinned(torch.empty(n_layers, n + grow, N.ROW_BYTES, dtype=torch.uint8))
+            hrows = register_pinned(torch.empty(n_layers, n + grow, cache.row_bytes, dtype=torch.uint8))
         host.append(hrows)
         handles.append(cache.request_begin(n, p, host_rows=hrows, max_ctx=n + grow if grow else 0))
     U = n_layers * R
@@ -267,11 +270,11 @@ def c128k(device="cuda", seed=1, n_layers=12):
                  staging_rows=64, seed=seed, device=device)
 
 
-def c256k_x8(device="cuda", seed=2, n_layers=12, n_req=8, n=262144):
+def c256k_x8(device="cuda", seed=2, n_layers=12, n_req=8, n=262144, kv_format=N.KV_BF16):
     return build(n_layers, [n] * n_req, [N.KV_HOST_RING] * n_req,
                  lambda l, r, n: synth.planted_hot_cold(n // 4, 512, 4096 // 4,
                                                         synth.mix_seed(seed, 90, l, r)),
-                 seed=seed, device=device)
+                 seed=seed, device=device, kv_format=kv_format)
 
 
 def c1m_x4(device="cuda", seed=3, n_layers=12, n_req=4, n=1048576):

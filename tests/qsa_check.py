@@ -73,8 +73,9 @@ def oracle_unit(wl, l, r, budget=None):
     slot = oracle_slot_row(wl, l, r)
     pool = PoolRows(wl.cache.pool, slot[toks])
     host = wl.host[r][l, :n].numpy() if wl.host[r] is not None else None
-    rows = O.gather_rows(toks, slot, pool, host)
-    out, lse = O.decode_attention(x["q"], rows, wl.softmax_scale)
+    fp8 = wl.cache.kv_format == N.KV_FP8
+    rows = O.gather_rows(toks, slot, pool, host, O.ROW_BYTES_FP8 if fp8 else O.ROW_BYTES)
+    out, lse = O.decode_attention(x["q"], rows, wl.softmax_scale, "fp8" if fp8 else "bf16")
     # tolerance scale per token: sum_h w_h |sc| sum_d |q_hd e4m3(code_d)|
     absk = np.abs(O.decode_e4m3(x["codes"])) * np.abs(O.decode_fp16(x["scales"]))[:, None]
     mag = (absk @ np.abs(x["q_idx"]).T) @ np.abs(x["w"])
