@@ -31,6 +31,11 @@ layer):
    h // 4, logits = scale * q_h . K_i, softmax over the selected tokens,
    output = sum_i p_i V_i, plus lse_h = log sum_i exp(logit_i).
 
+Beside the step: the producer side (quantising and storing a new token's
+index key and KV row, with the slot-table writes), FP8 KV rows, and the
+cross-step hot cache (hot_cache_step: which selected cold tokens are copied
+into a unit's hot HBM rows, and which tokens those rows held go cold).
+
 Every function below names the passage it follows.  Pins that tie this
 oracle to facts outside itself live in tests/test_oracle_pins.py.
 """
@@ -188,6 +193,60 @@ def gather_rows(tokens, slot_row, hbm_pool_rows, host_rows, row_bytes: int = ROW
         s = int(slot_row[int(t)])
         out[i] = hbm_pool_rows[s] if s >= 0 else host_rows[int(t)]
     return out
+
+
+
+def hot_cache_step(tokens, slot_row, owner, cursor: int, hot_base: int):
+    """One decode step of a unit's cross-step hot cache.  RTX4090 port page,
+    section "显存账本：热缓存卸载省下约84%": the full history stays in pinned
+    host memory, missing blocks are moved back to the GPU on demand, and the
+    GPU keeps a hot cache whose rows are found through the slot table.  This
+    library's reading: the unit owns H = len(owner) pool rows hot_base ..
+    hot_base + H - 1; owner[v] is the token row v holds (-1: none) and
+    `cursor` the next row to hand out.  For the selected tokens (ascending):
+      - a token whose slot is one of the unit's hot rows is a hit; its row is
+        in use by this step;
+      - a token whose slot is -1 is a miss; misses take rows in ascending
+        token order;
+      - the rows handed out are the first rows not in use by this step in the
+        circular order cursor, cursor + 1, ... (mod H); when there are fewer
+        such rows than misses, the remaining misses stay cold;
+      - a row's previous owner e becomes cold (slot -1) if its slot still
+        names that row (a slot remapped elsewhere is left alone);
+      - the miss takes the row (owner, slot) and its host row is copied in;
+      - the cursor moves one past the last row handed out.
+    Tokens whose slot is any other pool row (tail ring, staging) are left
+    alone.  Returns (new slot row, new owner, new cursor, fills) with fills
+    the (token, pool row) pairs whose host rows are copied."""
+    slot = np.array(slot_row, dtype=np.int32, copy=True)
+    own = np.array(owner, dtype=np.int32, copy=True)
+    H = len(own)
+    in_use = set()
+    misses = []
+    for t in sorted(int(x) for x in tokens):
+        s_ = int(slot[t])
+        if hot_base <= s_ < hot_base + H:
+            in_use.add(s_ - hot_base)
+        elif s_ == -1:
+            misses.append(t)
+    rows = []
+    k = 0
+    while len(rows) < len(misses) and k < H:
+        v = (cursor + k) % H
+        if v not in in_use:
+            rows.append(v)
+        k += 1
+    fills = []
+    for t, v in zip(misses, rows):
+        e = int(own[v])
+        if e >= 0 and int(slot[e]) == hot_base + v:
+            slot[e] = -1
+        own[v] = t
+        slot[t] = hot_base + v
+        fills.append((t, hot_base + v))
+    if rows:
+        cursor = (rows[-1] + 1) % H
+    return slot, own, int(cursor), fills
 
 
 # ----------------------------------------------------------- 5. attention

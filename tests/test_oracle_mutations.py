@@ -173,7 +173,50 @@ def _fp8_one_scale(rows_u8):
     return O.decode_e4m3(kc) * ks[:, :, None], O.decode_e4m3(vc) * ks[:, :, None]
 
 
+
+def _hot_mutant(kind):
+    """hot_cache_step with one slip (kind)."""
+    def step(tokens, slot_row, owner, cursor, hot_base):
+        slot = np.array(slot_row, dtype=np.int32, copy=True)
+        own = np.array(owner, dtype=np.int32, copy=True)
+        H = len(own)
+        order = sorted(int(x) for x in tokens)
+        if kind == "misses descending":
+            order = order[::-1]
+        in_use, misses = set(), []
+        for t in order:
+            s = int(slot[t])
+            if hot_base <= s < hot_base + H:
+                in_use.add(s - hot_base)
+            elif s == -1:
+                misses.append(t)
+        if kind == "rows in use handed out":
+            in_use = set()
+        rows = [v for v in ((cursor + i) % H for i in range(H)) if v not in in_use][:len(misses)]
+        fills = []
+        for t, v in zip(misses, rows):
+            e = int(own[v])
+            if kind == "stale owner cleared":
+                if e >= 0:
+                    slot[e] = -1
+            elif kind != "evicted token keeps its slot" and e >= 0 and int(slot[e]) == hot_base + v:
+                slot[e] = -1
+            own[v] = t
+            slot[t] = hot_base + v
+            fills.append((t, hot_base + v))
+        if rows and kind != "cursor not advanced":
+            cursor = rows[-1] if kind == "cursor on the last row" else (rows[-1] + 1) % H
+        return slot, own, int(cursor), fills
+    return step
+
+
 MUTATIONS = {
+    "hot cache: misses take rows in descending token order": {"hot_cache_step": _hot_mutant("misses descending")},
+    "hot cache: rows in use by the step handed out": {"hot_cache_step": _hot_mutant("rows in use handed out")},
+    "hot cache: evicted token keeps its slot": {"hot_cache_step": _hot_mutant("evicted token keeps its slot")},
+    "hot cache: stale owner cleared": {"hot_cache_step": _hot_mutant("stale owner cleared")},
+    "hot cache: cursor not advanced": {"hot_cache_step": _hot_mutant("cursor not advanced")},
+    "hot cache: cursor left on the last row": {"hot_cache_step": _hot_mutant("cursor on the last row")},
     "fp8 row with K and V swapped": {"split_kv_fp8": _fp8_kv_swapped},
     "fp8 row with the K scales on V": {"split_kv_fp8": _fp8_one_scale},
     "e4m3 encoder ties away from zero": {"encode_e4m3": _encode_ties_away},

@@ -495,3 +495,74 @@ def test_fp8_attention_matches_torch_sdpa_on_dequantised_rows():
     assert np.abs(out - ref[:, 0].numpy()).max() < 1e-12
     logits = 0.1 * torch.einsum("hd,hmd->hm", qb.double(), kt)
     assert np.abs(lse - torch.logsumexp(logits, dim=1).numpy()).max() < 1e-12
+
+
+# ------------------------------------------------ cross-step hot cache
+
+def test_hot_cache_hand_worked():
+    """Seven steps worked out by hand: cold start, hits and evictions, a
+    returning token, the circular walk skipping a row in use, an all-hit step,
+    a stale owner after a remap, and more misses than free rows."""
+    g = _load("hot_cache_hand.json")
+    slot = np.array(g["initial_slots"], dtype=np.int32)
+    own = np.full(g["hot_rows"], -1, dtype=np.int32)
+    cur = 0
+    for i, st in enumerate(g["steps"]):
+        for t, s in st.get("remap", []):
+            slot[t] = s
+        slot, own, cur, fills = O.hot_cache_step(st["tokens"], slot, own, cur, g["hot_base"])
+        assert slot.tolist() == st["slots"], (i, st["note"])
+        assert own.tolist() == st["owner"], (i, st["note"])
+        assert cur == st["cursor"], (i, st["note"])
+        assert [list(f) for f in fills] == st["fills"], (i, st["note"])
+
+
+def test_hot_cache_invariants_on_drifting_selections():
+    """Random selections that drift step to step (some steps keep everything,
+    some redraw everything), with tail-ring tokens among them: after every
+    step each selected token has a pool slot, hits and ring tokens keep
+    theirs, exactly the selected cold tokens are filled, into distinct hot
+    rows, which are the free rows nearest the cursor in circular order; other
+    tokens only lose hot rows; the owner array and the slot table agree; and
+    a gather through the new slot table returns the host bytes."""
+    rng = np.random.default_rng(11)
+    n, ring, H, base, ring_base, k = 400, 32, 48, 1000, 5000, 40
+    host = rng.integers(0, 256, (n, 16), dtype=np.uint8)
+    slot = np.full(n, -1, dtype=np.int32)
+    pool = {}
+    for t in range(n - ring, n):
+        slot[t] = ring_base + t % ring
+        pool[int(slot[t])] = host[t]
+    own = np.full(H, -1, dtype=np.int32)
+    cur = 0
+    sel = np.sort(rng.choice(n, k, replace=False))
+    for step in range(80):
+        churn = [0.0, 0.1, 0.5, 1.0][step % 4]
+        keep = sel[rng.random(k) >= churn]
+        fresh = rng.permutation(np.setdiff1d(np.arange(n), keep))[:k - len(keep)]
+        sel = np.sort(np.concatenate([keep, fresh]))
+        before = slot.copy()
+        slot, own, new_cur, fills = O.hot_cache_step(sel, slot, own, cur, base)
+        for t, r in fills:
+            pool[r] = host[t]
+        in_sel = set(sel.tolist())
+        assert all(slot[t] >= 0 for t in sel)
+        assert all(slot[t] == before[t] for t in sel if before[t] >= 0)
+        assert [t for t, _ in fills] == [t for t in sel if before[t] == -1]
+        rows = [r - base for _, r in fills]
+        assert all(0 <= v < H for v in rows) and len(set(rows)) == len(rows)
+        in_use = {int(before[t]) - base for t in sel if base <= before[t] < base + H}
+        nearest = sorted((v for v in range(H) if v not in in_use), key=lambda v: (v - cur) % H)
+        assert rows == nearest[:len(rows)]
+        if rows:
+            assert new_cur == (rows[-1] + 1) % H
+        else:
+            assert new_cur == cur
+        for t in range(n):
+            if t not in in_sel and slot[t] != before[t]:
+                assert slot[t] == -1 and base <= before[t] < base + H
+        hot = [t for t in range(n) if base <= slot[t] < base + H]
+        assert len({int(slot[t]) for t in hot}) == len(hot)
+        assert all(own[slot[t] - base] == t for t in hot)
+        assert np.array_equal(O.gather_rows(sel, slot, pool, host, row_bytes=16), host[sel])
+        cur = new_cur
