@@ -264,6 +264,75 @@ def fp8_attention_timing(dev, steps=20):
         wl.close()
 
 
+def _cold_selected_rows(wl):
+    """Selected tokens of the offloaded units that are cold (slot -1) before
+    the next step: the rows that step fetches from host memory.  The
+    selection of a unit is its planted set."""
+    c = wl.cache
+    idx = []
+    for l in range(wl.n_layers):
+        for r, h in enumerate(wl.handles):
+            if wl.placements[r] == 0:
+                continue
+            b = torch.as_tensor(wl.planted[l][r], dtype=torch.int64)
+            t = (b[:, None] * 4 + torch.arange(4)[None, :]).reshape(-1)
+            t = t[t < wl.ctxs[r]]
+            idx.append(((h.index * wl.n_layers + l) * c.ctx_capacity) + t)
+    flat = torch.cat(idx).to(c.slot_table.device)
+    return int((c.slot_table.view(-1)[flat] == -1).sum())
+
+
+def hot_cache_timing(wl, dev, args, churns=(0.0, 0.1, 0.25, 1.0)):
+    """The cross-step hot cache on the benchmark workload: the same requests
+    in a cache with BUDGET hot rows per request and layer, the step (with
+    qsa_hot_cache_fetch before each attention) captured as a CUDA graph, and
+    between steps a fraction `churn` of every unit's cold planted blocks
+    moved elsewhere (the selection drift of consecutive decode steps; 1.0
+    makes every cold block new at every step).  Each step is timed with CUDA
+    events around its replay; the drift runs outside them.  Consumes wl."""
+    from sparse_attention_decode_qsa_gb300 import synth, workloads
+    hw = workloads.with_hot_rows(wl, BUDGET)
+    try:
+        stream = torch.cuda.current_stream(dev)
+        graph = hw.capture(args.groups)
+        units = hw.n_req * hw.n_layers
+        levels = []
+        k = 0
+        for f in churns:
+            for _ in range(args.warmup):
+                k += 1
+                if f:
+                    hw.drift(f, synth.mix_seed(77, k))
+                graph.replay()
+            torch.cuda.synchronize(dev)
+            total_ms, miss = 0.0, 0
+            for _ in range(args.steps):
+                k += 1
+                if f:
+                    hw.drift(f, synth.mix_seed(77, k))
+                miss += _cold_selected_rows(hw)
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                total_ms += e0.elapsed_time(e1)
+            st, det = hw.cache.poll_error()
+            if st != 0:
+                raise RuntimeError(f"device error word {st} ({det}) in the hot-cache timing")
+            step_s = total_ms / 1e3 / args.steps
+            levels.append({"churn": f, "ms_per_step": round(step_s * 1e3, 4),
+                           "layer_steps_per_s": round(units / step_s, 1),
+                           "host_rows_per_step": round(miss / args.steps, 1),
+                           "host_gbs": round(miss / args.steps * ROW / step_s / 1e9, 1)})
+        del graph
+        return {"hot_rows": BUDGET, "selection_drift": "churn = fraction of each unit's cold "
+                "planted blocks moved between steps", "levels": levels}
+    finally:
+        hw.close()
+
+
 def run_ours(args, rank, world):
     from sparse_attention_decode_qsa_gb300 import workloads
 
@@ -370,7 +439,7 @@ def run_ours(args, rank, world):
     if st != 0:
         raise RuntimeError(f"device error word {st} ({det}) after timing")
     del graph
-    wl.close()
+    hot = hot_cache_timing(wl, dev, args)        # closes wl
     append_us = append_timing(dev)
     fp8_attn_us = fp8_attention_timing(dev)
     link_copy = host_link_peak(dev)
@@ -442,7 +511,7 @@ def run_ours(args, rank, world):
                                  "zero_copy_gather_gbs": round(link_zc, 1)},
         "host_link_frac": round(host_step / step_s / 1e9 / link_peak, 4),
         "eager_sequential_ms_per_step": round(ms_eager / args.steps, 4),
-        "roofline": dom, "kernels": roofs,
+        "roofline": dom, "kernels": roofs, "hot_cache": hot,
         "gpu_launches": args.steps * L * args.groups * 4,
         "clocks": clk.summary,
         "e2e": {"value": round(units * world / (ms_e2e_max / 1e3 / args.steps), 1),

@@ -68,7 +68,7 @@
 extern "C" {
 #endif
 
-#define QSA_ABI_VERSION 2
+#define QSA_ABI_VERSION 3
 
 #define QSA_INDEX_HEADS 8
 #define QSA_INDEX_DIM 64
@@ -84,6 +84,8 @@ extern "C" {
 #define QSA_MAX_UNITS 256
 /* Largest indexer budget, in tokens. */
 #define QSA_MAX_BUDGET_TOKENS 8192
+/* Largest hot_rows of a cache (see qsa_cache_config). */
+#define QSA_MAX_HOT_ROWS 65536
 
 typedef enum qsa_status_t {
   QSA_OK = 0,
@@ -139,6 +141,11 @@ typedef struct qsa_cache_config {
   int32_t* slot_table;     /* device [max_requests][n_layers][ctx_capacity] int32 */
   void* workspace;         /* device, qsa_workspace_bytes(config) bytes */
   int64_t workspace_bytes;
+  /* Cross-step hot cache: pool rows per offloaded request and layer that keep
+   * cold rows fetched by qsa_hot_cache_fetch for later steps.  0: no hot
+   * cache; else budget_tokens <= hot_rows <= QSA_MAX_HOT_ROWS. */
+  int32_t hot_rows;
+  int32_t reserved1;       /* must be 0 */
 } qsa_cache_config;
 
 typedef struct qsa_handle {
@@ -170,6 +177,8 @@ typedef struct qsa_request_info {
                               hbm_row_base + l * layer_rows */
   const void* host_rows;   /* device-usable address of the host history, or NULL */
   int64_t max_ctx;         /* the request's row stride M (see qsa_request_desc) */
+  int64_t hot_row_base;    /* first hot row (layer l: hot_row_base + l * hot_rows), or -1
+                              when the request has none */
 } qsa_request_info;
 
 typedef struct qsa_stats {
@@ -202,8 +211,11 @@ int32_t qsa_abi_version(void);
 const char* qsa_last_error_string(void);
 
 /* Bytes of device workspace a cache with this config needs (error word,
- * split-K partials of every request x layer, and two int32 work counters per
- * request x layer for qsa_index_score).  Returns -1 on a bad config. */
+ * split-K partials of every request x layer, two int32 work counters per
+ * request x layer for qsa_index_score, and with hot_rows > 0 the hot-cache
+ * state of every request x layer: a fill list of budget_tokens entries, its
+ * length, the cursor and hot_rows owner entries).  Returns -1 on a bad
+ * config. */
 int64_t qsa_workspace_bytes(const qsa_cache_config* config);
 
 /* Create a cache.  Checks the config; with device storage, also zeroes the
@@ -218,7 +230,9 @@ qsa_status_t qsa_cache_destroy(qsa_cache* cache);
 
 /* Lease a request slot and an HBM region (M = max(ctx_len, max_ctx) rows
  * per layer for QSA_KV_HBM, ring_tokens rows per layer for
- * QSA_KV_HOST_RING, none for QSA_KV_HOST), bump the
+ * QSA_KV_HOST_RING, none for QSA_KV_HOST; with hot_rows > 0 an offloaded
+ * request also gets hot_rows rows per layer after its ring rows, all of
+ * them free, with the hot-cache cursor at row 0), bump the
  * slot's generation, and enqueue on `stream` the fill of the request's
  * slot-table rows: resident token t of layer l -> region row l*layer_rows + t;
  * offloaded token t -> ring row l*ring_tokens + t mod ring_tokens when t is
@@ -356,6 +370,34 @@ qsa_status_t qsa_gather_rows(qsa_cache* cache, const qsa_batch* batch,
                              int32_t budget_tokens, void* rows_out, int32_t* n_rows,
                              void* stream);
 
+/* Step 3a (caches with hot_rows > 0).  Cross-step hot cache: per unit of
+ * an offloaded request, move the rows of the selected tokens that are cold
+ * (slot -1) from pinned host memory into the unit's hot rows and point their
+ * slots there, so that qsa_gather_rows and qsa_sparse_decode_attn read every
+ * selected row from HBM, and rows fetched in one step serve later steps.
+ * [RTX4090 port, memory-ledger section: the full history stays in pinned
+ * host memory and missing blocks are moved back to the GPU on demand, into a
+ * hot cache found through the slot table.]  Replacement (this library's
+ * reading; the page names no rule): for the selected tokens (tokens 4b ..
+ * 4b+3 of each selected block, clipped to ctx_len), a token whose slot is
+ * one of the unit's hot rows is a hit and its row is in use by this step; the
+ * cold ones (misses) take rows in ascending token order; the rows handed out
+ * are the first rows not in use by this step in circular order from the
+ * unit's cursor, which then moves one past the last row handed out; the
+ * token a handed-out row held becomes cold (slot -1) if its slot still names
+ * that row.  Since hot_rows >= budget_tokens, every miss gets a row.
+ * Tokens whose slot is another pool row (tail ring, staging) are untouched.
+ * Units of QSA_KV_HBM requests, and every unit of a cache without hot rows,
+ * are skipped.  sel_blocks/n_sel: as written by qsa_select_c4_topk (ascending
+ * distinct blocks).  Two launches per call (a plan kernel, one CTA per unit,
+ * and a copy kernel); nothing else may write the same units' slot tables
+ * (qsa_append_token, qsa_slot_table_set) while they run.
+ * Errors: INVALID_ARG, STALE_HANDLE, NO_DEVICE, CUDA; bad blocks and slots
+ * go to the device error word (BAD_BLOCK, BAD_SLOT). */
+qsa_status_t qsa_hot_cache_fetch(qsa_cache* cache, const qsa_batch* batch,
+                                 const int32_t* sel_blocks, const int32_t* n_sel,
+                                 int32_t budget_tokens, void* stream);
+
 /* Step 4.  GQA decode attention of each unit over its selected tokens:
  * for query head h (KV head g = h/4), logits_i = softmax_scale * q[u][h] .
  * K_i[g], out[u][h] = sum_i softmax(logits)_i V_i[g], lse[u][h] =
@@ -363,7 +405,10 @@ qsa_status_t qsa_gather_rows(qsa_cache* cache, const qsa_batch* batch,
  * Rows come from `gathered` ([units][budget_tokens][R], as written by
  * qsa_gather_rows) when it is not NULL, else through the slot table exactly
  * as qsa_gather_rows reads them (pool rows from HBM, cold rows zero-copy
- * from pinned host memory).  Split-K over the tokens with a log-sum-exp merge;
+ * from pinned host memory).  A launch that reads cold rows from host memory
+ * is held to a few dozen CTAs, which saturate the host link without slowing
+ * HBM-bound work beside it; units with hot rows count as reading only HBM
+ * (call qsa_hot_cache_fetch first).  Split-K over the tokens with a log-sum-exp merge;
  * partials live in the workspace, per (request, layer): two calls that
  * overlap on the GPU and share a (request, layer) race.
  * [offload digest: attention reads only the <= 2048 selected rows.]

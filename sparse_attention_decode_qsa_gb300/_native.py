@@ -21,6 +21,7 @@ KV_BF16 = 0
 KV_FP8 = 1
 MAX_UNITS = 256
 MAX_BUDGET_TOKENS = 8192
+MAX_HOT_ROWS = 65536
 STATIC_MAX_UNITS = 16
 STATIC_MAX_ROWS = 2048
 
@@ -44,6 +45,7 @@ class CacheConfig(C.Structure):
         ("kv_format", C.c_int32), ("hbm_pool_rows", C.c_int64),
         ("hbm_pool", C.c_void_p), ("index_keys", C.c_void_p), ("index_scales", C.c_void_p),
         ("slot_table", C.c_void_p), ("workspace", C.c_void_p), ("workspace_bytes", C.c_int64),
+        ("hot_rows", C.c_int32), ("reserved1", C.c_int32),
     ]
 
 
@@ -61,7 +63,8 @@ class RequestDesc(C.Structure):
 
 class RequestInfo(C.Structure):
     _fields_ = [("ctx_len", C.c_int64), ("placement", C.c_int32), ("layer_rows", C.c_int32),
-                ("hbm_row_base", C.c_int64), ("host_rows", C.c_void_p), ("max_ctx", C.c_int64)]
+                ("hbm_row_base", C.c_int64), ("host_rows", C.c_void_p), ("max_ctx", C.c_int64),
+                ("hot_row_base", C.c_int64)]
 
 
 class Stats(C.Structure):
@@ -106,6 +109,8 @@ SIGNATURES = {
                                      C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
     "qsa_gather_rows": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p,
                                   C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "qsa_hot_cache_fetch": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p,
+                                      C.c_int32, C.c_void_p]),
     "qsa_sparse_decode_attn": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p,
                                          C.c_void_p, C.c_int32, C.c_void_p, C.c_float,
                                          C.c_void_p, C.c_void_p, C.c_void_p]),

@@ -46,11 +46,14 @@ class Cache:
       index_scales fp16  [max_requests][n_layers][ctx_capacity]
       slot_table   int32 [max_requests][n_layers][ctx_capacity]
       workspace    uint8 [qsa_workspace_bytes]
+    hot_rows > 0 gives every offloaded request that many hot rows per layer
+    (the cross-step hot cache filled by hot_cache_fetch).
     """
 
     def __init__(self, n_layers: int, max_requests: int, ctx_capacity: int,
                  hbm_pool_rows: int, budget_tokens: int = 2048, ring_tokens: int = 4096,
-                 staging_rows: int = 2048, device="cuda", kv_format: int = N.KV_BF16):
+                 staging_rows: int = 2048, device="cuda", kv_format: int = N.KV_BF16,
+                 hot_rows: int = 0):
         self.L = N.lib()
         cfg = N.CacheConfig()
         cfg.n_layers = n_layers
@@ -61,7 +64,9 @@ class Cache:
         cfg.staging_rows = staging_rows
         cfg.hbm_pool_rows = hbm_pool_rows
         cfg.kv_format = kv_format
+        cfg.hot_rows = hot_rows
         self.kv_format = kv_format
+        self.hot_rows = hot_rows
         self.row_bytes = N.ROW_BYTES_FP8 if kv_format == N.KV_FP8 else N.ROW_BYTES
         self.n_layers, self.max_requests, self.ctx_capacity = n_layers, max_requests, ctx_capacity
         self.budget_tokens, self.ring_tokens, self.staging_rows = budget_tokens, ring_tokens, staging_rows
@@ -183,6 +188,12 @@ class Cache:
         check(self.L.qsa_gather_rows(self.h, C.byref(b), _ptr(sel_blocks), _ptr(n_sel),
                                      budget_tokens, out_ptr, _ptr(n_rows), _stream(stream)),
               "qsa_gather_rows")
+
+    def hot_cache_fetch(self, handles, layer0, n_layers, sel_blocks, n_sel, budget_tokens,
+                        stream=None):
+        b = _batch(handles, layer0, n_layers)
+        check(self.L.qsa_hot_cache_fetch(self.h, C.byref(b), _ptr(sel_blocks), _ptr(n_sel),
+                                         budget_tokens, _stream(stream)), "qsa_hot_cache_fetch")
 
     def sparse_decode_attn(self, handles, layer0, n_layers, q, sel_blocks, n_sel, budget_tokens,
                            gathered, softmax_scale, out, lse=None, stream=None):

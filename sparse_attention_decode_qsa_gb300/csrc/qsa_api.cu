@@ -60,6 +60,7 @@ struct Lease {
   int32_t layer_rows = 0;
   int64_t row_base = 0;
   int64_t rows = 0;
+  int64_t hot_base = -1;               // first hot row, or -1
   const uint8_t* host_rows = nullptr;  // device-usable address
 };
 
@@ -73,7 +74,29 @@ bool config_sizes_ok(const qsa_cache_config* c) {
          c->ctx_capacity <= 0x7FFFFFFFll && c->budget_tokens >= 4 &&
          c->budget_tokens % 4 == 0 && c->budget_tokens <= QSA_MAX_BUDGET_TOKENS &&
          c->ring_tokens > 0 && c->staging_rows >= 0 && c->hbm_pool_rows >= 0 &&
-         c->hbm_pool_rows <= 0x7FFFFFFFll && (c->kv_format == QSA_KV_BF16 || c->kv_format == QSA_KV_FP8);
+         c->hbm_pool_rows <= 0x7FFFFFFFll && (c->kv_format == QSA_KV_BF16 || c->kv_format == QSA_KV_FP8) &&
+         (c->hot_rows == 0 || (c->hot_rows >= c->budget_tokens && c->hot_rows <= QSA_MAX_HOT_ROWS)) &&
+         c->reserved1 == 0;
+}
+
+// Workspace layout: error word, split-K partials, index-score work counters,
+// then (hot_rows > 0) the hot-cache state.  Byte offsets.
+struct WorkspaceLayout {
+  int64_t partials, tickets, hot_fills, hot_nfill, hot_cursor, hot_owner, total;
+};
+
+WorkspaceLayout workspace_layout(const qsa_cache_config& c) {
+  const int64_t units = (int64_t)c.max_requests * c.n_layers;
+  WorkspaceLayout w;
+  w.partials = kErrBytes;
+  w.tickets = w.partials + units * splits_max_of(c) * kPartFloats * (int64_t)sizeof(float);
+  w.hot_fills = w.tickets + units * 2 * (int64_t)sizeof(int32_t);   // 8-byte aligned
+  const bool hot = c.hot_rows > 0;
+  w.hot_nfill = w.hot_fills + (hot ? units * c.budget_tokens * (int64_t)sizeof(int2) : 0);
+  w.hot_cursor = w.hot_nfill + (hot ? units * (int64_t)sizeof(int32_t) : 0);
+  w.hot_owner = w.hot_cursor + (hot ? units * (int64_t)sizeof(int32_t) : 0);
+  w.total = w.hot_owner + (hot ? units * c.hot_rows * (int64_t)sizeof(int32_t) : 0);
+  return w;
 }
 
 }  // namespace
@@ -95,13 +118,12 @@ struct qsa_cache {
 
   ErrorWord* err() const { return reinterpret_cast<ErrorWord*>(cfg.workspace); }
   int64_t row_bytes() const { return cfg.kv_format == QSA_KV_FP8 ? kRowBytesFp8 : kRowBytes; }
-  float* partials() const {
-    return reinterpret_cast<float*>(static_cast<uint8_t*>(cfg.workspace) + kErrBytes);
+  template <class T>
+  T* ws_at(int64_t off) const {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(cfg.workspace) + off);
   }
-  int32_t* tickets() const {
-    return reinterpret_cast<int32_t*>(partials() + (int64_t)cfg.max_requests * cfg.n_layers *
-                                                       splits_max * kPartFloats);
-  }
+  float* partials() const { return ws_at<float>(workspace_layout(cfg).partials); }
+  int32_t* tickets() const { return ws_at<int32_t>(workspace_layout(cfg).tickets); }
 
   bool alloc_rows(int64_t n, int64_t* base) {
     for (auto it = free_rows.begin(); it != free_rows.end(); ++it) {
@@ -168,6 +190,14 @@ struct qsa_cache {
     d->tickets = tickets();
     d->splits_max = (int32_t)splits_max;
     d->row_bytes = (int32_t)row_bytes();
+    const WorkspaceLayout w = workspace_layout(cfg);
+    const bool hot = cfg.hot_rows > 0;
+    d->hot_rows = cfg.hot_rows;
+    d->hot_fill_stride = cfg.budget_tokens;
+    d->hot_fills = hot ? ws_at<int2>(w.hot_fills) : nullptr;
+    d->hot_nfill = hot ? ws_at<int32_t>(w.hot_nfill) : nullptr;
+    d->hot_cursor = hot ? ws_at<int32_t>(w.hot_cursor) : nullptr;
+    d->hot_owner = hot ? ws_at<int32_t>(w.hot_owner) : nullptr;
     for (int i = 0; i < b->n_req; ++i) {
       const Lease* l;
       if (qsa_status_t st = check_handle(b->requests[i], &l)) return st;
@@ -182,6 +212,7 @@ struct qsa_cache {
         u.n = l->ctx_len;
         u.host_rows = l->host_rows ? l->host_rows + (int64_t)u.layer * l->max_ctx * row_bytes()
                                    : nullptr;
+        u.hot_base = l->hot_base >= 0 ? l->hot_base + (int64_t)u.layer * cfg.hot_rows : -1;
       }
     }
     return QSA_OK;
@@ -196,9 +227,7 @@ const char* qsa_last_error_string(void) { return g_last_error.c_str(); }
 
 int64_t qsa_workspace_bytes(const qsa_cache_config* c) {
   if (!config_sizes_ok(c)) return -1;
-  const int64_t units = (int64_t)c->max_requests * c->n_layers;
-  return kErrBytes + units * splits_max_of(*c) * kPartFloats * (int64_t)sizeof(float) +
-         units * 2 * (int64_t)sizeof(int32_t);
+  return workspace_layout(*c).total;
 }
 
 qsa_status_t qsa_cache_create(const qsa_cache_config* c, qsa_cache** out) {
@@ -294,7 +323,9 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
   const int32_t layer_rows = desc->placement == QSA_KV_HBM        ? (int32_t)max_ctx
                              : desc->placement == QSA_KV_HOST_RING ? c->cfg.ring_tokens
                                                                    : 0;
-  const int64_t rows = (int64_t)layer_rows * c->cfg.n_layers;
+  const bool hot = desc->placement != QSA_KV_HBM && c->cfg.hot_rows > 0;
+  const int64_t ring_rows = (int64_t)layer_rows * c->cfg.n_layers;
+  const int64_t rows = ring_rows + (hot ? (int64_t)c->cfg.hot_rows * c->cfg.n_layers : 0);
 
   const uint8_t* host_dev = nullptr;
   if (desc->placement != QSA_KV_HBM) {
@@ -323,6 +354,17 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
     cudaError_t e = launch_slot_fill(st, c->cfg.n_layers, c->cfg.ctx_capacity, desc->ctx_len,
                                      desc->placement, base, layer_rows,
                                      static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess && hot) {
+      // every hot row of the request free, cursors at row 0
+      const WorkspaceLayout w = workspace_layout(c->cfg);
+      const int64_t st0 = (int64_t)slot * c->cfg.n_layers;
+      e = cudaMemsetAsync(c->ws_at<int32_t>(w.hot_owner) + st0 * c->cfg.hot_rows, 0xFF,
+                          (size_t)c->cfg.n_layers * c->cfg.hot_rows * sizeof(int32_t),
+                          static_cast<cudaStream_t>(stream));
+      if (e == cudaSuccess)
+        e = cudaMemsetAsync(c->ws_at<int32_t>(w.hot_cursor) + st0, 0,
+                            (size_t)c->cfg.n_layers * sizeof(int32_t), static_cast<cudaStream_t>(stream));
+    }
     if (e != cudaSuccess) {
       c->release_rows(base, rows);
       return cuda_fail(e, "slot-table fill");
@@ -338,6 +380,7 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
   l.layer_rows = layer_rows;
   l.row_base = base;
   l.rows = rows;
+  l.hot_base = hot ? base + ring_rows : -1;
   l.host_rows = host_dev;
   out->index = (uint32_t)slot;
   out->generation = l.generation;
@@ -354,6 +397,7 @@ qsa_status_t qsa_request_end(qsa_cache* c, qsa_handle h) {
   l.ctx_len = 0;
   l.max_ctx = 0;
   l.rows = 0;
+  l.hot_base = -1;
   l.host_rows = nullptr;
   return ok();
 }
@@ -368,6 +412,7 @@ qsa_status_t qsa_request_info_get(qsa_cache* c, qsa_handle h, qsa_request_info* 
   out->hbm_row_base = l->row_base;
   out->host_rows = l->host_rows;
   out->max_ctx = l->max_ctx;
+  out->hot_row_base = l->hot_base;
   return ok();
 }
 
@@ -526,6 +571,20 @@ qsa_status_t qsa_append_token(qsa_cache* c, const qsa_batch* batch, const float*
   cudaError_t e = launch_append_token(d, tg, k_new, static_cast<const uint8_t*>(kv_new),
                                       static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return ok();
+}
+
+qsa_status_t qsa_hot_cache_fetch(qsa_cache* c, const qsa_batch* batch, const int32_t* sel_blocks,
+                                 const int32_t* n_sel, int32_t budget_tokens, void* stream) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  BatchDesc d;
+  if (qsa_status_t st = c->build_batch(batch, &d)) return st;
+  if (!sel_blocks || !n_sel) return fail(QSA_ERR_INVALID_ARG, "null array");
+  if (budget_tokens < 4 || budget_tokens % 4 || budget_tokens > c->cfg.budget_tokens)
+    return fail(QSA_ERR_INVALID_ARG, "bad budget_tokens %d", budget_tokens);
+  if (c->cfg.hot_rows == 0) return ok();
+  cudaError_t e = launch_hot_fetch(d, sel_blocks, n_sel, budget_tokens, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "hot-cache launch");
   return ok();
 }
 

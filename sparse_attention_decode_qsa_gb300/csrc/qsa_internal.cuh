@@ -46,6 +46,7 @@ enum KernelId : int32_t {
   kKernSlotFill = 5,
   kKernSlotSet = 6,
   kKernAppend = 7,
+  kKernHot = 8,
 };
 
 // One decode unit (request slot, layer) of a call.
@@ -55,6 +56,7 @@ struct UnitDesc {
   int64_t n;                  // cached tokens of the request
   const uint8_t* host_rows;   // device-usable address of host row 0 of this
                               // (request, layer), or nullptr
+  int64_t hot_base;           // first hot row of this (request, layer), or -1
 };
 
 // Everything a kernel needs to find a unit's data.  Passed by value.
@@ -72,10 +74,20 @@ struct BatchDesc {
   int32_t* tickets;           // [req][layer][2]: work counter, finished CTAs
   int32_t splits_max;
   int32_t row_bytes;          // kRowBytes (BF16 rows) or kRowBytesFp8 (FP8 rows)
+  // Hot-cache state per (request, layer) (workspace; null without hot rows)
+  int32_t hot_rows;           // rows per (request, layer); 0: no hot cache
+  int32_t hot_fill_stride;    // entries of a fill list (the config's budget_tokens)
+  int2* hot_fills;            // [req][layer][hot_fill_stride] {token, pool row}
+  int32_t* hot_nfill;         // [req][layer] entries in the fill list
+  int32_t* hot_cursor;        // [req][layer] next row to hand out
+  int32_t* hot_owner;         // [req][layer][hot_rows] token held by a row, or -1
   UnitDesc u[kMaxUnits];
 
   __host__ __device__ int64_t unit_row(int u_) const {
     return ((int64_t)u[u_].req * n_layers + u[u_].layer) * ctx_cap;
+  }
+  __host__ __device__ int64_t unit_state(int u_) const {
+    return (int64_t)u[u_].req * n_layers + u[u_].layer;
   }
 };
 
@@ -158,6 +170,11 @@ struct AppendTargets {
 
 cudaError_t launch_append_token(const BatchDesc& b, const AppendTargets& tg, const float* k_new,
                                 const uint8_t* kv_new, cudaStream_t s);
+
+// Cross-step hot cache: plan (slot, owner and cursor updates, fill lists)
+// then the copy of the listed host rows into their hot rows.
+cudaError_t launch_hot_fetch(const BatchDesc& b, const int32_t* sel_blocks, const int32_t* n_sel,
+                             int32_t budget_tokens, cudaStream_t s);
 
 // Slot-table maintenance.
 cudaError_t launch_slot_fill(int32_t* rows, int32_t n_layers, int64_t ctx_cap, int64_t ctx_len,

@@ -552,9 +552,10 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
   p.scale_log2 = softmax_scale * kLog2e;
   p.out = out;
   p.lse = lse;
+  // units with hot rows read HBM only once qsa_hot_cache_fetch has run
   bool any_host = false;
   if (gathered == nullptr)
-    for (int u = 0; u < b.n_units; ++u) any_host |= b.u[u].host_rows != nullptr;
+    for (int u = 0; u < b.n_units; ++u) any_host |= b.u[u].host_rows != nullptr && b.u[u].hot_base < 0;
   const int splits = (p.k_max + kBlocksPerSplit - 1) / kBlocksPerSplit;
   const bool fp8 = b.row_bytes == kRowBytesFp8;
   const int cap = any_host ? (fp8 ? kMaxCtasHostFp8 : kMaxCtasHost) : sm_count;

@@ -117,6 +117,39 @@ def plant(scales: torch.Tensor, blocks, n: int, factor: float = PLANT_FACTOR):
     return scales
 
 
+
+def unplant(scales: torch.Tensor, blocks, n: int, factor: float = PLANT_FACTOR):
+    """Undo plant() on the given blocks (exact: factor is a power of two)."""
+    blocks = torch.as_tensor(blocks, dtype=torch.int64, device=scales.device)
+    if blocks.numel() == 0:
+        return scales
+    toks = (blocks[:, None] * 4 + torch.arange(4, device=scales.device)[None, :]).reshape(-1)
+    toks = toks[toks < n]
+    scales[toks] = (scales[toks].float() / factor).to(torch.float16)
+    return scales
+
+
+def drift_blocks(planted, lo: int, hi: int, frac: float, seed: int):
+    """Selection drift between decode steps: of the planted blocks in
+    [lo, hi), replace round(frac * count) (drawn at random) by as many
+    unplanted blocks of [lo, hi).  Returns (dropped, added, new planted set)
+    as sorted int64 tensors."""
+    g = _gen(seed, "cpu")
+    planted = torch.as_tensor(planted, dtype=torch.int64)
+    inside = planted[(planted >= lo) & (planted < hi)]
+    k = int(round(frac * inside.numel()))
+    k = min(k, (hi - lo) - inside.numel())
+    if k <= 0:
+        e = torch.empty(0, dtype=torch.int64)
+        return e, e, planted.sort().values
+    dropped = inside[torch.randperm(inside.numel(), generator=g)[:k]].sort().values
+    taken = torch.zeros(hi - lo, dtype=torch.bool)
+    taken[inside - lo] = True
+    free = torch.nonzero(~taken).reshape(-1) + lo
+    added = free[torch.randperm(free.numel(), generator=g)[:k]].sort().values
+    keep = planted[~torch.isin(planted, dropped)]
+    return dropped, added, torch.cat([keep, added]).sort().values
+
 def index_query(seed: int, device="cpu"):
     """Index query q[8][64] ~ N(0,1) fp32 and head weights w[8] ~ U(0,1) fp32."""
     g = _gen(seed, device)

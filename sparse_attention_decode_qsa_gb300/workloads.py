@@ -88,6 +88,27 @@ class Workload:
         _fill_request(self, r, seed, self.planting)
         return self.handles[r]
 
+    def drift(self, frac: float, seed: int):
+        """Move a fraction frac of every offloaded unit's cold planted blocks
+        (blocks wholly before the tail ring) to other cold blocks, so that
+        the next step selects them instead: the selection drift of
+        consecutive decode steps."""
+        c = self.cache
+        for l in range(self.n_layers):
+            for r, h in enumerate(self.handles):
+                p, n = self.placements[r], self.ctxs[r]
+                if p == N.KV_HBM:
+                    continue
+                hi = (n - c.ring_tokens) // 4 if p == N.KV_HOST_RING else (n + 3) // 4
+                if hi <= 0:
+                    continue
+                dropped, added, now = synth.drift_blocks(self.planted[l][r], 0, hi, frac,
+                                                         synth.mix_seed(seed, l, r))
+                sc = c.index_scales[h.index, l]
+                synth.unplant(sc, dropped, n)
+                synth.plant(sc, added, n)
+                self.planted[l][r] = now
+
     def close(self):
         for h in self.host:
             if h is not None:
@@ -102,6 +123,8 @@ class Workload:
         sl = slice(l * R, (l + 1) * R)
         c.index_score(hs, l, 1, self.q_idx[sl], self.w[sl], self.blk[sl], stream)
         c.select_c4_topk(hs, l, 1, self.blk[sl], self.budget, self.sel[sl], self.nsel[sl], stream)
+        if c.hot_rows:
+            c.hot_cache_fetch(hs, l, 1, self.sel[sl], self.nsel[sl], self.budget, stream)
         c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
                              gathered, self.softmax_scale, self.out[sl], self.lse[sl], stream)
 
@@ -122,6 +145,8 @@ class Workload:
         c, R = self.cache, self.n_req
         hs = self.handles[r0:r1]
         sl = slice(l * R + r0, l * R + r1)
+        if c.hot_rows:
+            c.hot_cache_fetch(hs, l, 1, self.sel[sl], self.nsel[sl], self.budget, stream)
         c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
                              None, self.softmax_scale, self.out[sl], self.lse[sl], stream)
 
@@ -215,19 +240,21 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
 def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: int = 4096,
           staging_rows: int = 2048, seed: int = 0, device="cuda", extra_requests: int = 0,
           spare_rows: int = 0, ctx_capacity: int | None = None, grow: int = 0,
-          kv_format: int = N.KV_BF16) -> Workload:
+          kv_format: int = N.KV_BF16, hot_rows: int = 0) -> Workload:
     """planting(l, r, n) -> block ids to plant for unit (l, r).  grow: tokens
-    every request may still append (its max_ctx is ctx + grow)."""
+    every request may still append (its max_ctx is ctx + grow).  hot_rows:
+    cross-step hot-cache rows per offloaded request and layer (0: none)."""
     ctx_capacity = ctx_capacity or (max(ctxs) + grow)
     dev = torch.device(device)
     R = len(ctxs)
     rows_needed = 0
     for n, p in zip(ctxs, placements):
         rows_needed += n_layers * (n + grow if p == N.KV_HBM else ring if p == N.KV_HOST_RING else 0)
+        rows_needed += n_layers * hot_rows if p != N.KV_HBM else 0
     pool_rows = n_layers * staging_rows + rows_needed + spare_rows
     cache = Cache(n_layers=n_layers, max_requests=R + extra_requests, ctx_capacity=ctx_capacity,
                   hbm_pool_rows=pool_rows, budget_tokens=budget, ring_tokens=ring,
-                  staging_rows=staging_rows, device=dev, kv_format=kv_format)
+                  staging_rows=staging_rows, device=dev, kv_format=kv_format, hot_rows=hot_rows)
     handles, host = [], []
     for r, (n, p) in enumerate(zip(ctxs, placements)):
         hrows = None
@@ -253,6 +280,42 @@ def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: i
     wl.seeds = dict(seed=seed)
     return wl
 
+
+
+def with_hot_rows(wl: Workload, hot_rows: int) -> Workload:
+    """The same requests and inputs in a new cache whose offloaded requests
+    get hot_rows hot rows per layer.  Takes over wl's pinned host histories
+    and closes wl's cache (wl is unusable afterwards)."""
+    old = wl.cache
+    dev = old.pool.device
+    n_off = sum(1 for p in wl.placements if p != N.KV_HBM)
+    cache = Cache(n_layers=old.n_layers, max_requests=old.max_requests,
+                  ctx_capacity=old.ctx_capacity,
+                  hbm_pool_rows=old.pool.shape[0] + old.n_layers * hot_rows * n_off,
+                  budget_tokens=old.budget_tokens, ring_tokens=old.ring_tokens,
+                  staging_rows=old.staging_rows, device=dev, kv_format=old.kv_format,
+                  hot_rows=hot_rows)
+    handles = []
+    for r, h in enumerate(wl.handles):
+        info = old.request_info(h)
+        nh = cache.request_begin(wl.ctxs[r], wl.placements[r], host_rows=wl.host[r],
+                                 max_ctx=int(info.max_ctx))
+        ni = cache.request_info(nh)
+        cache.index_keys[nh.index] = old.index_keys[h.index]
+        cache.index_scales[nh.index] = old.index_scales[h.index]
+        rows = info.layer_rows * wl.n_layers
+        if rows:
+            cache.pool[ni.hbm_row_base:ni.hbm_row_base + rows] = \
+                old.pool[info.hbm_row_base:info.hbm_row_base + rows]
+        handles.append(nh)
+    torch.cuda.synchronize(dev)
+    new = Workload(cache, handles, wl.n_layers, list(wl.ctxs), list(wl.placements), wl.host,
+                   wl.q_idx, wl.w, wl.q, wl.planted, wl.budget, blk=wl.blk, sel=wl.sel,
+                   nsel=wl.nsel, out=wl.out, lse=wl.lse, softmax_scale=wl.softmax_scale,
+                   seeds=dict(wl.seeds), planting=wl.planting)
+    wl.host = []
+    old.close()
+    return new
 
 # ------------------------------------------------------------- recipes
 

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol():
     for name in sorted(declared):
         assert hasattr(L, name), f"{name} declared in include/ but not exported"
         assert name in N.SIGNATURES, f"{name} has no Python binding"
-    assert L.qsa_abi_version() == 2
+    assert L.qsa_abi_version() == 3
 
 
 def _host_cache(**kw):
@@ -238,3 +238,45 @@ def test_request_growth_bookkeeping():
         assert c.stats() == s0
     finally:
         c.close()
+
+
+def test_hot_rows_config_workspace_and_leases():
+    """Caches with a cross-step hot cache: hot_rows must be 0 or in
+    [budget_tokens, QSA_MAX_HOT_ROWS]; the workspace grows by the hot-cache
+    state; offloaded requests lease hot_rows rows per layer after their ring
+    rows, HBM requests none; everything returns on request_end."""
+    L = N.lib()
+    cfg = N.CacheConfig(n_layers=12, max_requests=8, ctx_capacity=262144, budget_tokens=2048,
+                        ring_tokens=4096, staging_rows=2048, hbm_pool_rows=1 << 20)
+    base = L.qsa_workspace_bytes(C.byref(cfg))
+    c2 = N.CacheConfig.from_buffer_copy(cfg)
+    c2.hot_rows = 4096
+    units = 8 * 12
+    # fill list {token, row} per budget token, its length, the cursor, one owner per row
+    assert L.qsa_workspace_bytes(C.byref(c2)) == base + units * (2048 * 8 + 4 + 4 + 4096 * 4)
+    h = C.c_void_p()
+    for field, bad in [("hot_rows", 2047), ("hot_rows", N.MAX_HOT_ROWS + 1), ("hot_rows", -4),
+                       ("reserved1", 1)]:
+        c3 = N.CacheConfig.from_buffer_copy(c2)
+        setattr(c3, field, bad)
+        assert L.qsa_workspace_bytes(C.byref(c3)) == -1
+        assert L.qsa_cache_create(C.byref(c3), C.byref(h)) == N.ERR_INVALID_ARG
+
+    c = _host_cache(hot_rows=2048)
+    s0 = c.stats()
+    ring = c.request_begin(262144, Q.KV_HOST_RING, host_rows=1 << 20)
+    host = c.request_begin(262144, Q.KV_HOST, host_rows=1 << 22)
+    hbm = c.request_begin(1000, Q.KV_HBM)
+    ir, ih, ib = c.request_info(ring), c.request_info(host), c.request_info(hbm)
+    assert ir.layer_rows == 4096 and ir.hot_row_base == ir.hbm_row_base + 12 * 4096
+    assert ih.layer_rows == 0 and ih.hot_row_base == ih.hbm_row_base
+    assert ib.hot_row_base == -1
+    s1 = c.stats()
+    assert s1["free_hbm_rows"] == s0["free_hbm_rows"] - 12 * (4096 + 2048) - 12 * 2048 - 12 * 1000
+    assert s1["hbm_kv_bytes_in_use"] == (12 * (4096 + 2048) + 12 * 2048 + 12 * 1000) * 2048
+    for hd in (ring, host, hbm):
+        c.request_end(hd)
+    assert c.stats() == s0
+    with pytest.raises(Q.QsaError) as e:
+        c.hot_cache_fetch([ring], 0, 1, None, None, 2048)
+    assert e.value.status in (Q.ERR_NO_DEVICE, Q.ERR_STALE_HANDLE)
