@@ -282,55 +282,69 @@ def _cold_selected_rows(wl):
     return int((c.slot_table.view(-1)[flat] == -1).sum())
 
 
-def hot_cache_timing(wl, dev, args, churns=(0.0, 0.1, 0.25, 1.0)):
-    """The cross-step hot cache on the benchmark workload: the same requests
-    in a cache with BUDGET hot rows per request and layer, the step (with
-    qsa_hot_cache_fetch before each attention) captured as a CUDA graph, and
-    between steps a fraction `churn` of every unit's cold planted blocks
-    moved elsewhere (the selection drift of consecutive decode steps; 1.0
-    makes every cold block new at every step).  Each step is timed with CUDA
-    events around its replay; the drift runs outside them.  Consumes wl."""
-    from sparse_attention_decode_qsa_gb300 import synth, workloads
+def _drift_levels(wl, graph, dev, args, churns, seed):
+    """Time the captured step `graph` of wl at each selection-drift level:
+    before each step a fraction `churn` of every unit's cold planted blocks
+    moves elsewhere (outside the timed region), then one replay is timed
+    with CUDA events on the launching stream."""
+    from sparse_attention_decode_qsa_gb300 import synth
+    stream = torch.cuda.current_stream(dev)
+    units = wl.n_req * wl.n_layers
+    levels, k = [], 0
+    for f in churns:
+        for _ in range(args.warmup):
+            k += 1
+            if f:
+                wl.drift(f, synth.mix_seed(seed, k))
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        total_ms, cold = 0.0, 0
+        for _ in range(args.steps):
+            k += 1
+            if f:
+                wl.drift(f, synth.mix_seed(seed, k))
+            cold += _cold_selected_rows(wl)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            total_ms += e0.elapsed_time(e1)
+        st, det = wl.cache.poll_error()
+        if st != 0:
+            raise RuntimeError(f"device error word {st} ({det}) in the drift timing")
+        step_s = total_ms / 1e3 / args.steps
+        levels.append({"churn": f, "ms_per_step": round(step_s * 1e3, 4),
+                       "layer_steps_per_s": round(units / step_s, 1),
+                       "host_rows_per_step": round(cold / args.steps, 1),
+                       "host_gbs": round(cold / args.steps * ROW / step_s / 1e9, 1)})
+    return levels
+
+
+def drift_timing(wl, graph, dev, args, churns=(0.0, 0.1, 0.25, 1.0)):
+    """The benchmark step when the selection drifts between steps (churn =
+    fraction of each unit's cold planted blocks moved before each step; 1.0
+    makes every cold block new at every step), in two forms: the measured
+    step as it is (cold rows read zero-copy from pinned host memory every
+    step), and the same requests in a cache with BUDGET hot rows per request
+    and layer, whose step fetches the cold selected rows into them
+    (qsa_hot_cache_fetch) and reads only HBM in attention.  Consumes wl and
+    graph."""
+    from sparse_attention_decode_qsa_gb300 import workloads
+    zero_copy = _drift_levels(wl, graph, dev, args, churns, 77)
+    del graph
     hw = workloads.with_hot_rows(wl, BUDGET)
     try:
-        stream = torch.cuda.current_stream(dev)
-        graph = hw.capture(args.groups)
-        units = hw.n_req * hw.n_layers
-        levels = []
-        k = 0
-        for f in churns:
-            for _ in range(args.warmup):
-                k += 1
-                if f:
-                    hw.drift(f, synth.mix_seed(77, k))
-                graph.replay()
-            torch.cuda.synchronize(dev)
-            total_ms, miss = 0.0, 0
-            for _ in range(args.steps):
-                k += 1
-                if f:
-                    hw.drift(f, synth.mix_seed(77, k))
-                miss += _cold_selected_rows(hw)
-                torch.cuda.synchronize(dev)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                graph.replay()
-                e1.record(stream)
-                torch.cuda.synchronize(dev)
-                total_ms += e0.elapsed_time(e1)
-            st, det = hw.cache.poll_error()
-            if st != 0:
-                raise RuntimeError(f"device error word {st} ({det}) in the hot-cache timing")
-            step_s = total_ms / 1e3 / args.steps
-            levels.append({"churn": f, "ms_per_step": round(step_s * 1e3, 4),
-                           "layer_steps_per_s": round(units / step_s, 1),
-                           "host_rows_per_step": round(miss / args.steps, 1),
-                           "host_gbs": round(miss / args.steps * ROW / step_s / 1e9, 1)})
-        del graph
-        return {"hot_rows": BUDGET, "selection_drift": "churn = fraction of each unit's cold "
-                "planted blocks moved between steps", "levels": levels}
+        g = hw.capture(args.groups)
+        hot = _drift_levels(hw, g, dev, args, churns, 78)
+        del g
     finally:
         hw.close()
+    return {"what": "steps whose selection drifts: churn = fraction of each unit's cold planted "
+                    "blocks moved before each step; host_rows_per_step = selected rows cold at "
+                    "the start of the step",
+            "zero_copy": zero_copy, "hot_cache": {"hot_rows": BUDGET, "levels": hot}}
 
 
 def run_ours(args, rank, world):
@@ -438,8 +452,8 @@ def run_ours(args, rank, world):
     st, det = wl.cache.poll_error()
     if st != 0:
         raise RuntimeError(f"device error word {st} ({det}) after timing")
-    del graph
-    hot = hot_cache_timing(wl, dev, args)        # closes wl
+    drift = drift_timing(wl, graph, dev, args)     # consumes wl and graph
+    del graph, wl
     append_us = append_timing(dev)
     fp8_attn_us = fp8_attention_timing(dev)
     link_copy = host_link_peak(dev)
@@ -511,7 +525,7 @@ def run_ours(args, rank, world):
                                  "zero_copy_gather_gbs": round(link_zc, 1)},
         "host_link_frac": round(host_step / step_s / 1e9 / link_peak, 4),
         "eager_sequential_ms_per_step": round(ms_eager / args.steps, 4),
-        "roofline": dom, "kernels": roofs, "hot_cache": hot,
+        "roofline": dom, "kernels": roofs, "selection_drift": drift,
         "gpu_launches": args.steps * L * args.groups * 4,
         "clocks": clk.summary,
         "e2e": {"value": round(units * world / (ms_e2e_max / 1e3 / args.steps), 1),

@@ -14,9 +14,12 @@
 //                    previous owners, then (after a barrier) writes the slot
 //                    table, the owners, the cursor and a fill list
 //                    {token, pool row} in the workspace.
-//   hot_fill_kernel  copies each listed host row into its hot row: 32 rows
+//   hot_fill_kernel  copies each listed host row into its hot row: 8 rows
 //                    per CTA, every 16-byte load of a thread issued before
-//                    its stores, as in the gather kernel.
+//                    its stores.  Few rows per CTA spread a step's misses
+//                    over many SMs: reads of host pages the GPU has not
+//                    touched lately are slow (a cost per page, not per
+//                    byte), and more SMs keep more of them in flight.
 // Afterwards every selected row of the unit is in HBM.
 #include "qsa_internal.cuh"
 
@@ -27,7 +30,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kMaxTokPerThread = QSA_MAX_BUDGET_TOKENS / kPlanThreads;   // 8
 constexpr int kFillThreads = 256;
-constexpr int kFillRows = 32;
+constexpr int kFillRows = 8;
 // plan kernel shared memory at the limits: bitmask of QSA_MAX_HOT_ROWS rows +
 // one victim per token of the largest budget
 constexpr int kPlanSmemMax = QSA_MAX_HOT_ROWS / 8 + QSA_MAX_BUDGET_TOKENS * 4;
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(kFillThreads) hot_fill_kernel(const HotParams 
   }
   __syncthreads();
   constexpr int kTotal = kFillRows * kChunksPerRow;
-  constexpr int kPer = (kTotal + kFillThreads - 1) / kFillThreads;   // 16 or 9
+  constexpr int kPer = (kTotal + kFillThreads - 1) / kFillThreads;   // 4 or 3
   uint4 v[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
