@@ -495,7 +495,7 @@ def run_ours(args, rank, world):
         # producer side: per launch 8 units (one layer) of key quantisation,
         # row store and slot update; not part of the timed decode step
         "append_token": {"bound": "latency", "avg_launch_us": round(append_us, 2),
-                         "units_per_launch": 8},
+                         "units_per_launch": 8, "traffic": measured_traffic("append_token")},
         # FP8 KV variant (1040-byte rows) of the same attention launch; not
         # part of the timed decode step, whose rows are BF16
         "sparse_attn_fp8": {"bound": "host_link",
@@ -503,6 +503,7 @@ def run_ours(args, rank, world):
                             "peak": round(link_peak, 1), "unit": "GB/s",
                             "frac": round(R * (BUDGET // 2) * 1040 / (fp8_attn_us * 1e-6) / 1e9 / link_peak, 4),
                             "host_bytes_per_launch": R * (BUDGET // 2) * 1040,
+                            "traffic": measured_traffic("sparse_attn_fp8"),
                             "avg_launch_us": round(fp8_attn_us, 2)},
     }
     dom = dict(roofs[dominant])

@@ -224,3 +224,46 @@ def test_hot_cache_rejects_bad_selections():
         assert e.value.status == Q.ERR_INVALID_ARG
     finally:
         wl.close()
+
+
+def test_hot_cache_state_starts_fresh_for_a_reissued_request():
+    """A request that ends hands its hot rows back; the request admitted in
+    its slot starts with every hot row free and the cursor at row 0 (the
+    oracle's fresh state), even when it gets the same pool rows."""
+    budget, H, ring = 512, 512, 256
+    wl = workloads.build(1, [7000, 5000], [Q.KV_HOST_RING] * 2, lambda l, r, n: [], budget=budget,
+                         ring=ring, staging_rows=8, seed=45, hot_rows=H)
+    try:
+        c = wl.cache
+        rng = np.random.default_rng(45)
+        k_max = budget // 4
+
+        def fetch_random(units):
+            sel = torch.zeros(2, k_max, dtype=torch.int32)
+            nsel = torch.zeros(2, dtype=torch.int32)
+            for r in range(2):
+                s = _random_selection(rng, wl.ctxs[r], k_max, [], 0.0)
+                sel[r, :len(s)] = torch.from_numpy(s)
+                nsel[r] = len(s)
+            wl.sel.copy_(sel.cuda())
+            wl.nsel.copy_(nsel.cuda())
+            c.hot_cache_fetch(wl.handles, 0, 1, wl.sel, wl.nsel, budget)
+            torch.cuda.synchronize()
+            _clean(wl)
+            for r in range(2):
+                units[r].step(sel[r, :int(nsel[r])].numpy())
+
+        units = [_OracleUnit(wl, 0, r) for r in range(2)]
+        for _ in range(3):
+            fetch_random(units)
+        old_hot = c.request_info(wl.handles[0]).hot_row_base
+        wl.reissue(0, 6000, Q.KV_HOST_RING, seed=46)
+        assert c.request_info(wl.handles[0]).hot_row_base == old_hot      # same rows reused
+        units[0] = _OracleUnit(wl, 0, 0)
+        for _ in range(3):
+            fetch_random(units)
+            for r in range(2):
+                got = c.slot_table[wl.handles[r].index, 0, :wl.ctxs[r]].cpu().numpy()
+                assert np.array_equal(got, units[r].slot), r
+    finally:
+        wl.close()
