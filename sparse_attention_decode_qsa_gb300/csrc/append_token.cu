@@ -38,6 +38,7 @@ struct AppendParams {
 };
 
 __global__ void __launch_bounds__(kThreads) append_token_kernel(const AppendParams p) {
+  grid_dependency_wait();
   __shared__ float s_amax[2];
   const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const int64_t n = p.b.u[u].n;
@@ -140,8 +141,7 @@ cudaError_t launch_append_token(const BatchDesc& b, const AppendTargets& tg, con
   p.tg = tg;
   p.k_new = k_new;
   p.kv_new = kv_new;
-  append_token_kernel<<<b.n_units, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(append_token_kernel, dim3(b.n_units), dim3(kThreads), 0, s, 0, dim3(1), p);
 }
 
 }  // namespace qsa

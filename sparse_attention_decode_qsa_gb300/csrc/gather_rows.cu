@@ -43,6 +43,7 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint8_t* p) {
 // kChunksPerRow: 16-byte chunks of a row (128 for BF16 rows, 65 for FP8 rows)
 template <int kChunksPerRow>
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const GatherParams p) {
+  grid_dependency_wait();
   __shared__ const uint8_t* src[kGatherRows];
   const int u = blockIdx.y;
   const int j0 = blockIdx.x * kGatherBlocks;
@@ -157,10 +158,9 @@ cudaError_t launch_gather_rows(const BatchDesc& b, const int32_t* sel_blocks,
   }
   dim3 grid((p.k_max + kGatherBlocks - 1) / kGatherBlocks, b.n_units);
   if (b.row_bytes == kRowBytesFp8)
-    gather_rows_kernel<kRowBytesFp8 / 16><<<grid, kGatherThreads, 0, s>>>(p);
-  else
-    gather_rows_kernel<kRowBytes / 16><<<grid, kGatherThreads, 0, s>>>(p);
-  return cudaGetLastError();
+    return launch_kernel(gather_rows_kernel<kRowBytesFp8 / 16>, grid, dim3(kGatherThreads), 0, s, 0,
+                         dim3(1), p);
+  return launch_kernel(gather_rows_kernel<kRowBytes / 16>, grid, dim3(kGatherThreads), 0, s, 0, dim3(1), p);
 }
 
 cudaError_t launch_slot_fill(int32_t* rows, int32_t n_layers, int64_t ctx_cap, int64_t ctx_len,

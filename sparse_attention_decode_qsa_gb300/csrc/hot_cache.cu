@@ -74,6 +74,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_wa
 }
 
 __global__ void __launch_bounds__(kPlanThreads) hot_plan_kernel(const HotParams p) {
+  grid_dependency_wait();
   extern __shared__ uint32_t in_use[];         // [ceil(H / 32)] bitmask, then victim[budget]
   __shared__ int s_warp[kPlanWarps];
   __shared__ int s_bad;
@@ -210,6 +211,7 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint8_t* p) {
 // kChunksPerRow: 16-byte chunks of a row (128 for BF16 rows, 65 for FP8 rows)
 template <int kChunksPerRow>
 __global__ void __launch_bounds__(kFillThreads) hot_fill_kernel(const HotParams p) {
+  grid_dependency_wait();
   __shared__ const uint8_t* src[kFillRows];
   __shared__ uint8_t* dst[kFillRows];
   const int u = blockIdx.y;
@@ -265,15 +267,13 @@ cudaError_t launch_hot_fetch(const BatchDesc& b, const int32_t* sel_blocks, cons
   p.n_sel = n_sel;
   p.k_max = budget_tokens / 4;
   const int smem = ((b.hot_rows + 31) / 32) * 4 + budget_tokens * 4;   // <= kPlanSmemMax
-  hot_plan_kernel<<<b.n_units, kPlanThreads, smem, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(hot_plan_kernel, dim3(b.n_units), dim3(kPlanThreads), smem, s, 0,
+                                dim3(1), p);
   if (e != cudaSuccess) return e;
   dim3 grid((budget_tokens + kFillRows - 1) / kFillRows, b.n_units);
   if (b.row_bytes == kRowBytesFp8)
-    hot_fill_kernel<kRowBytesFp8 / 16><<<grid, kFillThreads, 0, s>>>(p);
-  else
-    hot_fill_kernel<kRowBytes / 16><<<grid, kFillThreads, 0, s>>>(p);
-  return cudaGetLastError();
+    return launch_kernel(hot_fill_kernel<kRowBytesFp8 / 16>, grid, dim3(kFillThreads), 0, s, 0, dim3(1), p);
+  return launch_kernel(hot_fill_kernel<kRowBytes / 16>, grid, dim3(kFillThreads), 0, s, 0, dim3(1), p);
 }
 
 }  // namespace qsa

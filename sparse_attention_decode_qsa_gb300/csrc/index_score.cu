@@ -323,6 +323,7 @@ __device__ __forceinline__ int build_pieces(const IndexScoreParams& p, int u, ui
 
 __global__ void __maxnreg__(QSA_K1_MAXREG)
 index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
+  grid_dependency_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the swizzled stages and B slots need 1024-byte alignment
   uint8_t* smem0 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -653,8 +654,7 @@ cudaError_t launch_index_score(const BatchDesc& b, const CUtensorMap* keys_map,
   const int64_t cap = (int64_t)kCtasPerSm * sm_count;
   const int64_t chunks = (tiles + kChunk - 1) / kChunk;
   const unsigned grid = (unsigned)(chunks < cap ? chunks : cap);
-  index_score_tc_kernel<<<grid, kThreadsTc, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(index_score_tc_kernel, dim3(grid), dim3(kThreadsTc), kSmemBytes, s, 0, dim3(1), p);
 }
 
 }  // namespace qsa

@@ -101,6 +101,19 @@ WorkspaceLayout workspace_layout(const qsa_cache_config& c) {
 
 }  // namespace
 
+int qsa::highest_priority() {
+  static int prio = 1;   // 1: not yet queried (priorities are <= 0)
+  if (prio == 1) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) {
+      cudaGetLastError();
+      greatest = 0;
+    }
+    prio = greatest;
+  }
+  return prio;
+}
+
 qsa_status_t qsa::set_last_error(qsa_status_t status, const char* message) {
   g_last_error = message ? message : "";
   return status;

@@ -39,6 +39,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 __global__ void __launch_bounds__(kThreads) select_topk_kernel(const TopkParams p) {
+  grid_dependency_wait();
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_digit, s_krem;
   __shared__ uint32_t warp_gt[kWarps], warp_eq[kWarps];
@@ -244,6 +245,7 @@ __device__ __forceinline__ void find_digit(const uint32_t* h, uint32_t nbins, ui
 
 // 40 registers x 512 threads: a CTA fits on an SM beside two index-score CTAs.
 __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, int slice_cap) {
+  grid_dependency_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   uint32_t* keys = dyn;                                   // [slice_cap]
   uint32_t* sub = dyn + slice_cap;                        // [kSubHists][kBins], first digit
@@ -470,8 +472,7 @@ cudaError_t launch_select_topk(const BatchDesc& b, const float* blk_scores, int6
     if (nb > nb_max) nb_max = nb;
   }
   if (nb_max > (int64_t)kClusterCtas * kMaxSlice) {  // beyond 1M tokens: one CTA per unit
-    select_topk_kernel<<<b.n_units, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(select_topk_kernel, dim3(b.n_units), dim3(kThreads), 0, s, 0, dim3(1), p);
   }
   constexpr int kMaxDynSmem = kMaxSlice * 4 + kSubHists * kBins * 4;
   static bool attr_set = false;
@@ -482,19 +483,9 @@ cudaError_t launch_select_topk(const BatchDesc& b, const float* blk_scores, int6
   }
   // keys per CTA of the largest unit, rounded up to 16-byte multiples
   const int slice_cap = (int)(((nb_max + kClusterCtas - 1) / kClusterCtas + 3) / 4 * 4);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(b.n_units * kClusterCtas);
-  cfg.blockDim = dim3(kCThreads);
-  cfg.dynamicSmemBytes = (size_t)slice_cap * 4 + kSubHists * kBins * 4;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kClusterCtas;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, select_topk_cluster_kernel, p, slice_cap);
+  return launch_kernel(select_topk_cluster_kernel, dim3(b.n_units * kClusterCtas), dim3(kCThreads),
+                       (size_t)slice_cap * 4 + kSubHists * kBins * 4, s, 0, dim3(kClusterCtas), p,
+                       slice_cap);
 }
 
 }  // namespace qsa

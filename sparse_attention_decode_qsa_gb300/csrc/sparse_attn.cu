@@ -179,6 +179,7 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, int u, int r, 
 }
 
 __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams p) {
+  grid_dependency_wait();
   extern __shared__ __align__(16) uint8_t smem[];  // [warp][stage][8][512]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ uint32_t vmask[kWarps][kAStages];     // tokens present in each stage
@@ -375,6 +376,7 @@ __device__ __forceinline__ uint32_t issue_warp_fp8(const AttnParams& p, int u, i
 }
 
 __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnParams p) {
+  grid_dependency_wait();
   extern __shared__ __align__(16) uint8_t smem[];  // [warp][stage][8][272]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ uint32_t vmask[kWarps][kAStagesFp8];
@@ -499,6 +501,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
 
 // Merge: CTA (head, unit), thread = output dim; reads the cpu partials.
 __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const AttnParams p) {
+  grid_dependency_wait();
   const int h = blockIdx.x, u = blockIdx.y, d = threadIdx.x;
   float Mx = -INFINITY;
   for (int s = 0; s < p.cpu; ++s) Mx = fmaxf(Mx, partial_ptr(p.b, u, s)[h]);
@@ -564,14 +567,13 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
   if (cpu > splits) cpu = splits;
   if (cpu > b.splits_max) cpu = b.splits_max;   // partial slots in the workspace
   p.cpu = cpu;
-  if (fp8)
-    attn_split_fp8_kernel<<<b.n_units * cpu, kThreads, kSmemFp8, s>>>(p);
-  else
-    attn_split_kernel<<<b.n_units * cpu, kThreads, kSmemBytes, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  const int prio = highest_priority();
+  cudaError_t e = fp8 ? launch_kernel(attn_split_fp8_kernel, dim3(b.n_units * cpu), dim3(kThreads), kSmemFp8,
+                                      s, prio, dim3(1), p)
+                      : launch_kernel(attn_split_kernel, dim3(b.n_units * cpu), dim3(kThreads), kSmemBytes,
+                                      s, prio, dim3(1), p);
   if (e != cudaSuccess) return e;
-  attn_merge_kernel<<<dim3(kQHeads, b.n_units), kHeadDim, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(attn_merge_kernel, dim3(kQHeads, b.n_units), dim3(kHeadDim), 0, s, prio, dim3(1), p);
 }
 
 }  // namespace qsa

@@ -171,15 +171,22 @@ class Workload:
                 self.score_group_layer(r0, r1, l, ss)
                 if stagger and G > 1:
                     streams[(g + 1) % G][0].wait_stream(ss)
-                sa.wait_stream(ss)
+                if sa is not ss:
+                    sa.wait_stream(ss)
                 self.attn_group_layer(r0, r1, l, sa)
-                ss.wait_stream(sa)   # the next layer of these requests follows it
+                if sa is not ss:
+                    ss.wait_stream(sa)   # the next layer of these requests follows it
         for ss, sa in streams:
             main.wait_stream(ss)
 
-    def make_streams(self, n_groups: int):
-        """Per group a scoring stream and a higher-priority attention stream,
-        so attention CTAs are dispatched ahead of queued scoring CTAs."""
+    def make_streams(self, n_groups: int, split: bool = True):
+        """Per group a scoring stream and a higher-priority attention stream
+        (split), so attention CTAs are dispatched ahead of queued scoring
+        CTAs; or one stream per group (not split), whose chain of launches
+        the library then links by programmatic dependent launch while the
+        attention launches still carry the highest priority."""
+        if not split:
+            return [(s, s) for s in (torch.cuda.Stream() for _ in range(n_groups))]
         try:
             _, hi = torch.cuda.Stream.priority_range()
         except (AttributeError, RuntimeError):
@@ -187,17 +194,17 @@ class Workload:
         return [(torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=hi))
                 for _ in range(n_groups)]
 
-    def capture(self, n_groups: int):
+    def capture(self, n_groups: int, split: bool = True, stagger: bool = True):
         """Capture step_pipelined into a CUDA graph (after one eager warm-up
         run, which also sets the kernels' launch attributes)."""
-        streams = self.make_streams(n_groups)
-        self.step_pipelined(streams)
+        streams = self.make_streams(n_groups, split)
+        self.step_pipelined(streams, stagger)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream()
         cap.wait_stream(torch.cuda.current_stream())
         with torch.cuda.graph(g, stream=cap):
-            self.step_pipelined(streams)
+            self.step_pipelined(streams, stagger)
         torch.cuda.synchronize()
         self._graph_streams = streams
         return g
