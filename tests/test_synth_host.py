@@ -1,0 +1,51 @@
+"""CPU tests of the seeded input generators' selection-drift helpers (the
+inputs of the benchmark's drift measurement): the drift moves exactly the
+asked share of the planted blocks inside the range to unplanted blocks of
+the same range, keeps the rest, and undoing a plant restores the scales bit
+for bit."""
+import numpy as np
+import torch
+
+from sparse_attention_decode_qsa_gb300 import synth
+
+
+def test_drift_blocks_moves_the_asked_share_inside_the_range():
+    planted = synth.planted_hot_cold(65536, 512, 1024, seed=3)
+    lo, hi = 0, 65536 - 1024
+    inside = planted[(planted >= lo) & (planted < hi)]
+    for frac in (0.0, 0.1, 0.25, 1.0):
+        dropped, added, now = synth.drift_blocks(planted, lo, hi, frac, seed=7)
+        k = int(round(frac * inside.numel()))
+        assert dropped.numel() == k and added.numel() == k
+        assert now.numel() == planted.numel() and torch.equal(now, now.unique())
+        assert bool(torch.isin(dropped, inside).all())
+        assert not bool(torch.isin(added, planted).any())
+        assert bool(((added >= lo) & (added < hi)).all())
+        outside = planted[(planted < lo) | (planted >= hi)]
+        assert bool(torch.isin(outside, now).all())            # blocks outside the range stay
+        keep = planted[~torch.isin(planted, dropped)]
+        assert torch.equal(torch.sort(torch.cat([keep, added])).values, now)
+    d1, a1, _ = synth.drift_blocks(planted, lo, hi, 0.5, seed=9)
+    d2, a2, _ = synth.drift_blocks(planted, lo, hi, 0.5, seed=9)
+    assert torch.equal(d1, d2) and torch.equal(a1, a2)           # seeded
+
+
+def test_drift_blocks_when_the_range_is_nearly_full():
+    planted = torch.arange(0, 10)
+    dropped, added, now = synth.drift_blocks(planted, 0, 12, 1.0, seed=1)
+    assert dropped.numel() == 2 and added.numel() == 2           # only two free blocks
+    assert set(added.tolist()) == {10, 11}
+    assert now.numel() == 10
+
+
+def test_unplant_restores_plant_exactly():
+    g = torch.Generator().manual_seed(5)
+    n = 4099                                                     # ragged last block
+    sc = (torch.rand(n, generator=g) * torch.exp2(torch.randint(-20, 4, (n,), generator=g).float())).half()
+    sc[:8] = torch.tensor([0.0, -0.0, 6.0e-8, 1.0e-5, 0.5, 1.0, 800.0, 1000.0]).half()
+    before = sc.clone()
+    blocks = [0, 1, 5, 17, 1024]                                 # 1024: the partial last block
+    synth.plant(sc, blocks, n)
+    assert not torch.equal(sc.view(torch.int16), before.view(torch.int16))
+    synth.unplant(sc, blocks, n)
+    assert np.array_equal(sc.view(torch.int16).numpy(), before.view(torch.int16).numpy())
