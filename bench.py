@@ -276,6 +276,84 @@ def fp8_timing(dev, args):
         wl.close()
 
 
+def hbm_resident_timing(dev, args):
+    """The HBM-resident configuration: 1 request x 12 layers x 131072 tokens,
+    every KV row in HBM.  Times (CUDA events, captured graphs) the faithful
+    layer-sequential step (12 dependent layers of one request), the upper
+    bound with the 12 layers batched into one call per kernel, and each
+    kernel over the 12 units."""
+    from sparse_attention_decode_qsa_gb300 import workloads
+    wl = workloads.c128k(device=dev)
+    try:
+        c, hs, L = wl.cache, wl.handles, wl.n_layers
+        cur = torch.cuda.current_stream(dev)
+        wl.step(cur)
+        torch.cuda.synchronize(dev)
+
+        def gtime(fn, reps):
+            s = torch.cuda.Stream()
+            s.wait_stream(cur)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(reps):
+                    fn(s)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            for _ in range(args.steps):
+                g.replay()
+            e1.record(cur)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1) * 1e3 / (args.steps * reps)
+
+        def seq(s):
+            for l in range(L):
+                wl.step_layer(l, s)
+
+        def score(s):
+            c.index_score(hs, 0, L, wl.q_idx, wl.w, wl.blk, s)
+
+        def topk(s):
+            c.select_c4_topk(hs, 0, L, wl.blk, BUDGET, wl.sel, wl.nsel, s)
+
+        def attn(s):
+            c.sparse_decode_attn(hs, 0, L, wl.q, wl.sel, wl.nsel, BUDGET, None, wl.softmax_scale,
+                                 wl.out, wl.lse, s)
+
+        def batched(s):
+            score(s)
+            topk(s)
+            attn(s)
+
+        t = {k: gtime(f, r) for k, f, r in [("seq", seq, 1), ("batched", batched, 1), ("score", score, 10),
+                                             ("topk", topk, 10), ("attn", attn, 10)]}
+        st, det = c.poll_error()
+        if st != 0:
+            raise RuntimeError(f"device error word {st} ({det}) in the HBM-resident timing")
+        n = wl.ctxs[0]
+        key_b, row_b = L * IDX_BYTES * n, L * BUDGET * ROW
+        hbm_peak, _ = peaks()
+        gbs = lambda b, us: round(b / (us * 1e-6) / 1e9, 1)
+        return {"workload": f"c128k: 1 request x {L} layers x {n} tokens, KV in HBM",
+                "algorithmic_bytes_per_step": key_b + row_b,
+                "layer_sequential": {"us_per_step": round(t["seq"], 2),
+                                     "layer_steps_per_s": round(L / (t["seq"] * 1e-6), 1),
+                                     "hbm_gbs": gbs(key_b + row_b, t["seq"]),
+                                     "frac": round(gbs(key_b + row_b, t["seq"]) / hbm_peak, 4)},
+                "layers_batched_upper_bound": {"us_per_step": round(t["batched"], 2),
+                                               "hbm_gbs": gbs(key_b + row_b, t["batched"]),
+                                               "frac": round(gbs(key_b + row_b, t["batched"]) / hbm_peak, 4)},
+                "kernels_12_units": {
+                    "index_score": {"us": round(t["score"], 2), "hbm_gbs": gbs(key_b, t["score"]),
+                                    "frac": round(gbs(key_b, t["score"]) / hbm_peak, 4)},
+                    "select_topk": {"us": round(t["topk"], 2)},
+                    "sparse_attn": {"us": round(t["attn"], 2), "hbm_gbs": gbs(row_b, t["attn"]),
+                                    "frac": round(gbs(row_b, t["attn"]) / hbm_peak, 4)}}}
+    finally:
+        wl.close()
+
+
 def _cold_selected_rows(wl):
     """Selected tokens of the offloaded units that are cold (slot -1) before
     the next step: the rows that step fetches from host memory.  The
@@ -468,6 +546,7 @@ def run_ours(args, rank, world):
     del graph, wl
     append_us = append_timing(dev)
     fp8_step_ms, fp8_attn_us = fp8_timing(dev, args)
+    hbm_res = hbm_resident_timing(dev, args)
     link_copy = host_link_peak(dev)
     link_zc = zero_copy_peak(dev)
     link_peak = max(link_copy, link_zc)
@@ -539,7 +618,7 @@ def run_ours(args, rank, world):
                                  "zero_copy_gather_gbs": round(link_zc, 1)},
         "host_link_frac": round(host_step / step_s / 1e9 / link_peak, 4),
         "eager_sequential_ms_per_step": round(ms_eager / args.steps, 4),
-        "roofline": dom, "kernels": roofs, "selection_drift": drift,
+        "roofline": dom, "kernels": roofs, "selection_drift": drift, "hbm_resident": hbm_res,
         "fp8_kv": {"what": "the same step over FP8 KV rows (1040 bytes: E4M3 K and V codes, fp16 "
                            "scales per head); BF16 queries, fp32 outputs",
                    "ms_per_step": round(fp8_step_ms, 4),
