@@ -500,17 +500,20 @@ def run_ours(args, rank, world):
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize(dev)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # an event after every replay gives the per-step spread (no extra syncs)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with Clocks(dev.index) as clk:
-        t0.record(stream)
-        for _ in range(args.steps):
+        ev[0].record(stream)
+        for i in range(args.steps):
             graph.replay()
-        t1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize(dev)
-    ms = t0.elapsed_time(t1)
+    ms = ev[0].elapsed_time(ev[-1])
+    per_step = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
+    pct = lambda q: per_step[min(len(per_step) - 1, int(round(q * (len(per_step) - 1))))]
 
     # ---- end to end: per-step queries from pinned host, outputs back to pinned host
     hq_idx = wl.q_idx.cpu().pin_memory()
@@ -618,6 +621,7 @@ def run_ours(args, rank, world):
                                  "zero_copy_gather_gbs": round(link_zc, 1)},
         "host_link_frac": round(host_step / step_s / 1e9 / link_peak, 4),
         "eager_sequential_ms_per_step": round(ms_eager / args.steps, 4),
+        "step_ms_p10_p50_p90": [round(pct(0.1), 4), round(pct(0.5), 4), round(pct(0.9), 4)],
         "roofline": dom, "kernels": roofs, "selection_drift": drift, "hbm_resident": hbm_res,
         "fp8_kv": {"what": "the same step over FP8 KV rows (1040 bytes: E4M3 K and V codes, fp16 "
                            "scales per head); BF16 queries, fp32 outputs",
