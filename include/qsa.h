@@ -9,6 +9,9 @@
  *   3. qsa_gather_rows      (optional) copy the selected KV rows, found through
  *                           the logical-token -> physical-slot table, into a
  *                           dense buffer;
+ *   3a. qsa_hot_cache_fetch (caches with hot rows) copy the selected cold rows
+ *                           into the request's hot HBM rows, which keep them
+ *                           for later steps, and point their slots there;
  *   4. qsa_sparse_decode_attn  GQA decode attention over the selected rows,
  *                           read through the slot table (HBM rows from the
  *                           pool, cold rows straight from pinned host memory)
@@ -38,7 +41,9 @@
  *   index key   = 64 FP8-e4m3 codes + 1 fp16 scale   (66 B / token / layer)
  *   index query = 8 heads x 64 fp32, head weights 8 fp32
  *   token score = sum_h w_h * relu(sum_d q[h][d] * scale * e4m3(code[d]))
- *   KV row      = K[4][128] bf16 then V[4][128] bf16  (2048 B / token / layer)
+ *   KV row      = K[4][128] bf16 then V[4][128] bf16  (2048 B / token / layer),
+ *                 or in an FP8 cache (qsa_kv_format) E4M3 codes of K and V plus
+ *                 8 fp16 scales (1040 B)
  *   query       = 16 heads x 128 bf16, query head h reads KV head h / 4
  *
  * Conventions for every entry point.
@@ -190,7 +195,7 @@ typedef struct qsa_stats {
   int64_t free_hbm_rows;        /* rows not leased to any request (staging excluded) */
   int64_t largest_free_rows;
   int64_t staging_rows_total;   /* n_layers * staging_rows */
-  int64_t hbm_kv_bytes_in_use;  /* rows leased to requests x 2048 */
+  int64_t hbm_kv_bytes_in_use;  /* pool rows leased to requests (ring, resident and hot rows) x R */
 } qsa_stats;
 
 /* A batch of decode units: n_req requests at layers layer0 .. layer0+n_layers-1.
@@ -253,6 +258,10 @@ qsa_status_t qsa_request_begin(qsa_cache* cache, const qsa_request_desc* desc,
  * capacity and cache slots.] */
 qsa_status_t qsa_request_end(qsa_cache* cache, qsa_handle handle);
 
+/* The lease of a live request: context length, placement, its pool region
+ * (hbm_row_base, layer_rows, hot_row_base), the device-usable address of its
+ * host history and its row stride max_ctx.  Errors: INVALID_ARG (null),
+ * STALE_HANDLE. */
 qsa_status_t qsa_request_info_get(qsa_cache* cache, qsa_handle handle, qsa_request_info* out);
 
 /* Counters of free and leased capacity; equal to their initial values once
