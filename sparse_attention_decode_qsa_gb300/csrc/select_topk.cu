@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const TopkParams 
 // writes its selected ids at their global ascending-id positions.  A CTA
 // takes half an SM's registers, so it can share an SM with other kernels.
 constexpr int kClusterCtas = 8;
+static_assert(kClusterCtas <= 8, "cross-CTA sums reduce over lanes 0..7");
 constexpr int kCThreads = 512;
 constexpr int kCWarps = kCThreads / 32;
 constexpr int kMaxSlice = 32768;  // keys per CTA: 8 x 32768 blocks = 1M tokens
@@ -324,11 +325,14 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     // the select on the low 21 bits (11 + 10) alone.  No CTA changes its
     // histogram before the next cluster barrier, so the offsets read here
     // (earlier CTAs' counts of bin d1) are stable.
-    if (tid == 0) {
-      uint32_t base = 0;
-      for (uint32_t c = 0; c < rank; ++c) base += ld_dsmem(dsmem_addr(&hist[d1], c));
-      s_base = base;
-      s_pos = 0;
+    if (warp == 0) {   // lane c < rank reads CTA c's count of bin d1
+      uint32_t v = (uint32_t)lane < rank ? ld_dsmem(dsmem_addr(&hist[d1], (uint32_t)lane)) : 0u;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      if (lane == 0) {
+        s_base = v;
+        s_pos = 0;
+      }
     }
     __syncthreads();
     for (int i = tid; i < cnt; i += kCThreads) {
@@ -428,11 +432,24 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   }
   __syncthreads();
   cluster_sync();                                          // every CTA's totals are published
-  uint32_t base_gt = 0, base_eq = 0;
-  for (uint32_t c = 0; c < rank; ++c) {
-    base_gt += ld_dsmem(dsmem_addr(&s_cnt[0], c));
-    base_eq += ld_dsmem(dsmem_addr(&s_cnt[1], c));
+  if (warp == 0) {   // lane c < rank reads CTA c's totals; sums go to s_base / s_pos
+    uint32_t vg = 0u, ve = 0u;
+    if ((uint32_t)lane < rank) {
+      vg = ld_dsmem(dsmem_addr(&s_cnt[0], (uint32_t)lane));
+      ve = ld_dsmem(dsmem_addr(&s_cnt[1], (uint32_t)lane));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      vg += __shfl_xor_sync(0xFFFFFFFFu, vg, o);
+      ve += __shfl_xor_sync(0xFFFFFFFFu, ve, o);
+    }
+    if (lane == 0) {
+      s_base = vg;
+      s_pos = ve;
+    }
   }
+  __syncthreads();
+  const uint32_t base_gt = s_base, base_eq = s_pos;
   uint32_t gt_before = base_gt + warp_gt[warp] + ig - g;   // greater keys before mine, globally
   uint32_t eq_before = base_eq + warp_eq[warp] + ie - e;   // T-equal keys before mine, globally
   if (g + e > 0) {
