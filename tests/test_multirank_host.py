@@ -59,3 +59,13 @@ def test_reference_arm_under_torchrun_two_ranks():
     line = lines[0]
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_cpu_baseline_falls_back_to_one_process(monkeypatch):
+    """When the oracle's process pool cannot start, the CPU baseline times one
+    process and reports one core instead of failing the benchmark."""
+    import bench
+    monkeypatch.setattr(bench, "_spawn_oracle_pool", lambda workers: None)
+    r = bench.cpu_baseline(seconds=0.0)
+    assert r["cores"] == 1 and r["kind"] == "oracle" and r["value"] > 0
+    assert "one process" in r["sample"]
