@@ -143,6 +143,40 @@ def test_compute_calls_need_device_storage():
     with pytest.raises(Q.QsaError) as e:
         c.slot_table_ptr(h, 0)
     assert e.value.status == Q.ERR_NO_DEVICE
+    for name, args in [
+        ("qsa_select_c4_topk", (C.byref(b), 16, 100, 2048, 16, 16, None)),
+        ("qsa_gather_rows", (C.byref(b), 16, 16, 2048, 16, None, None)),
+        ("qsa_append_token", (C.byref(b), 16, 16, None)),
+        ("qsa_hot_cache_fetch", (C.byref(b), 16, 16, 2048, None)),
+    ]:
+        assert getattr(L, name)(c.h, *args) == Q.ERR_NO_DEVICE, name
+        assert b"device storage" in L.qsa_last_error_string(), name
+    st = L.qsa_staging_ptr(c.h, 0, C.byref(C.c_void_p()))
+    assert st == Q.ERR_NO_DEVICE
+    st32 = C.c_int32()
+    assert L.qsa_poll_error(c.h, None, C.byref(st32), None) == Q.ERR_NO_DEVICE
+
+
+def test_entry_points_reject_null_and_bad_arguments():
+    """Null caches and outputs, bad layers and stale handles are refused with
+    a status and a message, and change nothing."""
+    L = N.lib()
+    c = _host_cache()
+    s0 = c.stats()
+    h = c.request_begin(100, Q.KV_HBM)
+    assert L.qsa_request_end(None, N.Handle(h.index, h.generation)) == Q.ERR_INVALID_ARG
+    assert L.qsa_request_info_get(c.h, N.Handle(h.index, h.generation), None) == Q.ERR_INVALID_ARG
+    assert L.qsa_cache_stats(c.h, None) == Q.ERR_INVALID_ARG
+    assert L.qsa_request_advance(None, N.Handle(h.index, h.generation), 1) == Q.ERR_INVALID_ARG
+    assert L.qsa_hot_cache_fetch(None, None, None, None, 2048, None) == Q.ERR_INVALID_ARG
+    out = C.c_void_p()
+    assert L.qsa_cache_create(None, C.byref(out)) == Q.ERR_INVALID_ARG
+    assert L.qsa_cache_create(C.byref(c.cfg), None) == Q.ERR_INVALID_ARG
+    stale = N.Handle(h.index, h.generation + 1)
+    assert L.qsa_request_advance(c.h, stale, 1) == Q.ERR_STALE_HANDLE
+    assert b"stale" in L.qsa_last_error_string()
+    c.request_end(h)
+    assert c.stats() == s0
 
 
 def test_free_list_coalesces_after_fragmentation():
