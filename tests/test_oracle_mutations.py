@@ -210,7 +210,22 @@ def _hot_mutant(kind):
     return step
 
 
+
+def _gap_from_top(blk, budget_tokens):
+    s = np.sort(np.asarray(blk, dtype=np.float64))[::-1]
+    k = min(budget_tokens // 4, len(s))
+    return float("inf") if k >= len(s) else float(s[0] - s[k])
+
+
+def _gap_off_by_one(blk, budget_tokens):
+    s = np.sort(np.asarray(blk, dtype=np.float64))[::-1]
+    k = min(budget_tokens // 4, len(s))
+    return float("inf") if k + 1 >= len(s) else float(s[k] - s[k + 1])
+
+
 MUTATIONS = {
+    "boundary gap measured from the top block": {"boundary_gap": _gap_from_top},
+    "boundary gap one place too low": {"boundary_gap": _gap_off_by_one},
     "hot cache: misses take rows in descending token order": {"hot_cache_step": _hot_mutant("misses descending")},
     "hot cache: rows in use by the step handed out": {"hot_cache_step": _hot_mutant("rows in use handed out")},
     "hot cache: evicted token keeps its slot": {"hot_cache_step": _hot_mutant("evicted token keeps its slot")},

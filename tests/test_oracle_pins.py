@@ -566,3 +566,17 @@ def test_hot_cache_invariants_on_drifting_selections():
         assert all(own[slot[t] - base] == t for t in hot)
         assert np.array_equal(O.gather_rows(sel, slot, pool, host, row_bytes=16), host[sel])
         cur = new_cur
+
+
+def test_boundary_gap_hand_worked():
+    """The fp64 gap between the K-th best block score and the (K+1)-th, the
+    quantity the parity tests require to be >= 1e-3 before they compare
+    selections bit for bit; worked out by hand."""
+    blk = [5.0, 1.0, 3.0, 9.0, 7.0, 2.0]                 # sorted: 9 7 5 3 2 1
+    assert O.boundary_gap(blk, 12) == 2.0                 # K = 3: 5 - 3
+    assert O.boundary_gap(blk, 10) == 2.0                 # K = 2 (10 tokens = 2 whole blocks): 7 - 5
+    assert O.boundary_gap(blk, 4) == 2.0                  # K = 1: 9 - 7
+    assert O.boundary_gap(blk, 20) == 1.0                 # K = 5: 2 - 1
+    assert O.boundary_gap([4.0, 4.0, 4.0, 1.0], 8) == 0.0  # a tie at the boundary
+    assert O.boundary_gap([1.0, 2.0], 8) == float("inf")  # every block selected
+    assert O.boundary_gap([-1.0, -5.0, -2.0], 4) == 1.0   # K = 1: -1 - (-2)
