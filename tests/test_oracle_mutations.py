@@ -223,7 +223,22 @@ def _gap_off_by_one(blk, budget_tokens):
     return float("inf") if k + 1 >= len(s) else float(s[k] - s[k + 1])
 
 
+
+def _bf16_kv_swapped(rows_u8):
+    k, v = O._orig_split_kv(rows_u8)
+    return v, k
+
+
+def _bf16_heads_interleaved(rows_u8):
+    # K and V of each head side by side ([4][2][128]) instead of K[4][128] then V[4][128]
+    bits = np.ascontiguousarray(rows_u8, dtype=np.uint8).view(np.uint16).reshape(-1, O.KV_HEADS, 2, O.HEAD_DIM)
+    vals = O.decode_bf16(bits)
+    return vals[:, :, 0, :], vals[:, :, 1, :]
+
+
 MUTATIONS = {
+    "bf16 row with K and V swapped": {"split_kv": _bf16_kv_swapped},
+    "bf16 row with K and V interleaved per head": {"split_kv": _bf16_heads_interleaved},
     "boundary gap measured from the top block": {"boundary_gap": _gap_from_top},
     "boundary gap one place too low": {"boundary_gap": _gap_off_by_one},
     "hot cache: misses take rows in descending token order": {"hot_cache_step": _hot_mutant("misses descending")},
@@ -275,6 +290,7 @@ def test_pins_catch_mutation(name, monkeypatch):
     monkeypatch.setattr(O, "_orig_encode", O.encode_e4m3, raising=False)
     monkeypatch.setattr(O, "_orig_append", O.append_slot_writes, raising=False)
     monkeypatch.setattr(O, "_orig_split_fp8", O.split_kv_fp8, raising=False)
+    monkeypatch.setattr(O, "_orig_split_kv", O.split_kv, raising=False)
     for attr, val in MUTATIONS[name].items():
         monkeypatch.setattr(O, attr, val)
     caught = 0
