@@ -110,18 +110,21 @@ def test_append_host_only_request():
         wl.close()
 
 
-def test_append_ring_request_then_decode_step_matches_the_oracle():
+@pytest.mark.parametrize("hot_rows", [0, 2048])
+def test_append_ring_request_then_decode_step_matches_the_oracle(hot_rows):
     """Two offloaded requests with a 512-token HBM tail ring grow by 260
     tokens at both layers (every append hands a ring row over and makes the
     token it held cold); the slot tables, ring rows and host history follow
     the oracle's layouts, and a decode step over the grown context matches
-    the oracle run on the generator's bytes plus the test's own keys and rows."""
+    the oracle run on the generator's bytes plus the test's own keys and rows
+    (also with a hot cache, whose fetch moves the selected cold rows into
+    HBM before attention)."""
     L, R, n0, G, ring = 2, 2, 3000, 260, 512
     seed = 21
     wl = workloads.build(L, [n0] * R, [Q.KV_HOST_RING] * R,
                          lambda l, r, n: synth.planted_hot_cold(n // 4, 512, ring // 4,
                                                                 synth.mix_seed(seed, 90, l, r)),
-                         ring=ring, staging_rows=64, seed=seed, grow=G)
+                         ring=ring, staging_rows=64, seed=seed, grow=G, hot_rows=hot_rows)
     try:
         c, hs, dev = wl.cache, wl.handles, wl.cache.pool.device
         n = n0 + G

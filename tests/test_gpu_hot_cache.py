@@ -113,16 +113,18 @@ def test_hot_cache_fetch_matches_the_oracle_over_drifting_steps(kv_format):
         wl.close()
 
 
-def test_hot_cache_decode_steps_match_the_oracle():
+@pytest.mark.parametrize("kv_format", [Q.KV_BF16, Q.KV_FP8])
+def test_hot_cache_decode_steps_match_the_oracle(kv_format):
     """Decode steps (score, top-k, fetch, attention) over a host-ring cache
-    with hot rows, the selection drifting between steps: selections and
-    attention match the oracle, which reads every cold row from host memory,
-    and the slot tables follow the oracle's hot-cache state."""
+    with hot rows (BF16 and FP8 rows), the selection drifting between steps:
+    selections and attention match the oracle, which reads every cold row
+    from host memory, and the slot tables follow the oracle's hot-cache
+    state."""
     L, R, n, ring, H, seed = 2, 2, 40000, 2048, 2048, 41
     wl = workloads.build(L, [n] * R, [Q.KV_HOST_RING] * R,
                          lambda l, r, n: synth.planted_hot_cold(n // 4, 512, ring // 4,
                                                                 synth.mix_seed(seed, 90, l, r)),
-                         ring=ring, staging_rows=8, seed=seed, hot_rows=H)
+                         ring=ring, staging_rows=8, seed=seed, hot_rows=H, kv_format=kv_format)
     try:
         units = {(l, r): _OracleUnit(wl, l, r) for l in range(L) for r in range(R)}
         for step, frac in enumerate([0.0, 0.0, 0.25, 1.0, 0.1]):
