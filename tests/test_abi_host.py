@@ -314,3 +314,24 @@ def test_hot_rows_config_workspace_and_leases():
     with pytest.raises(Q.QsaError) as e:
         c.hot_cache_fetch([ring], 0, 1, None, None, 2048)
     assert e.value.status in (Q.ERR_NO_DEVICE, Q.ERR_STALE_HANDLE)
+
+
+def test_header_is_plain_c():
+    """include/qsa.h compiles as C99 (not only C++), with every declared
+    entry point referenced, so C callers can use the ABI as declared."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = sorted(_declared_symbols())
+    src = ("#include <qsa.h>\ntypedef void (*any_fn)(void);\n"
+           + "\n".join(f"any_fn ref_{n} = (any_fn)&{n};" for n in names) + "\n")
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "use_qsa.c")
+        with open(path, "w") as f:
+            f.write(src)
+        r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
+                            "-I", os.path.join(ROOT, "include"), path], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
