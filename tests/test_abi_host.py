@@ -335,3 +335,65 @@ def test_header_is_plain_c():
         r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
                             "-I", os.path.join(ROOT, "include"), path], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+_C_PROGRAM = r"""
+#include <qsa.h>
+#include <stdio.h>
+#include <string.h>
+
+int main(void) {
+  qsa_cache_config cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.n_layers = 12; cfg.max_requests = 4; cfg.ctx_capacity = 262144;
+  cfg.budget_tokens = 2048; cfg.ring_tokens = 4096; cfg.staging_rows = 2048;
+  cfg.kv_format = QSA_KV_BF16; cfg.hbm_pool_rows = 200000; cfg.hot_rows = 2048;
+  if (qsa_abi_version() != QSA_ABI_VERSION) return 10;
+  if (qsa_workspace_bytes(&cfg) <= 0) return 11;
+  qsa_cache* c = NULL;
+  if (qsa_cache_create(&cfg, &c) != QSA_OK || !c) return 12;
+  qsa_stats s0, s1;
+  if (qsa_cache_stats(c, &s0) != QSA_OK) return 13;
+  qsa_request_desc d;
+  memset(&d, 0, sizeof d);
+  d.ctx_len = 262144; d.placement = QSA_KV_HOST_RING; d.host_rows = (const void*)(size_t)(1u << 20);
+  qsa_handle h;
+  if (qsa_request_begin(c, &d, NULL, &h) != QSA_OK) return 14;
+  qsa_request_info info;
+  if (qsa_request_info_get(c, h, &info) != QSA_OK) return 15;
+  if (info.layer_rows != 4096 || info.hot_row_base != info.hbm_row_base + 12 * 4096) return 16;
+  if (qsa_cache_stats(c, &s1) != QSA_OK || s1.free_hbm_rows != s0.free_hbm_rows - 12 * (4096 + 2048)) return 17;
+  qsa_handle stale = h;
+  stale.generation += 1;
+  if (qsa_request_end(c, stale) != QSA_ERR_STALE_HANDLE) return 18;
+  if (strlen(qsa_last_error_string()) == 0) return 19;
+  if (qsa_request_end(c, h) != QSA_OK) return 20;
+  if (qsa_cache_stats(c, &s1) != QSA_OK || memcmp(&s0, &s1, sizeof s0) != 0) return 21;
+  if (qsa_cache_destroy(c) != QSA_OK) return 22;
+  printf("c abi ok\n");
+  return 0;
+}
+"""
+
+
+def test_c_program_drives_the_host_bookkeeping():
+    """A C program linked against libqsa_gb300.so leases, inspects and ends a
+    request on a host-only cache (hot rows included) through the C ABI alone,
+    and capacity returns to its initial value."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(N.LIB_PATH)
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "host_abi.c"), os.path.join(d, "host_abi")
+        with open(src, "w") as f:
+            f.write(_C_PROGRAM)
+        r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src,
+                            "-o", exe, "-L", libdir, "-lqsa_gb300", f"-Wl,-rpath,{libdir}"],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "c abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
