@@ -397,3 +397,102 @@ def test_c_program_drives_the_host_bookkeeping():
         assert r.returncode == 0, r.stderr
         r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and "c abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
+
+
+class _PoolModel:
+    """First-fit row ranges with coalescing, lowest free request slot, and
+    the rows each placement leases: the allocation contract of the cache."""
+
+    def __init__(self, pool_rows, staging, n_layers, ring, hot_rows, max_requests):
+        self.free = [(staging, pool_rows - staging)] if pool_rows > staging else []
+        self.n_layers, self.ring, self.hot = n_layers, ring, hot_rows
+        self.slots = [None] * max_requests
+        self.gen = [0] * max_requests
+
+    def rows(self, n, placement):
+        L = self.n_layers
+        if placement == Q.KV_HBM:
+            return L * n
+        hot = L * self.hot
+        return (L * self.ring if placement == Q.KV_HOST_RING else 0) + hot
+
+    def begin(self, n, placement):
+        """-> (slot, base) or an error status"""
+        try:
+            slot = self.slots.index(None)
+        except ValueError:
+            return Q.ERR_OUT_OF_SLOTS
+        need = self.rows(n, placement)
+        base = 0
+        if need > 0:
+            for i, (s, length) in enumerate(self.free):
+                if length >= need:
+                    base = s
+                    self.free[i] = (s + need, length - need)
+                    if self.free[i][1] == 0:
+                        del self.free[i]
+                    break
+            else:
+                return Q.ERR_CAPACITY
+        self.slots[slot] = (base, need)
+        self.gen[slot] += 1
+        return slot, base
+
+    def end(self, slot):
+        base, n = self.slots[slot]
+        self.slots[slot] = None
+        if n == 0:
+            return
+        self.free.append((base, n))
+        self.free.sort()
+        merged = []
+        for s, length in self.free:
+            if merged and merged[-1][0] + merged[-1][1] == s:
+                merged[-1] = (merged[-1][0], merged[-1][1] + length)
+            else:
+                merged.append((s, length))
+        self.free = merged
+
+
+@pytest.mark.parametrize("hot_rows", [0, 2048])
+def test_pool_allocation_follows_first_fit_model(hot_rows):
+    """Random admissions and finishes (all three placements, sizes up to the
+    pool) on a host-only cache: every lease's pool base, every refusal and
+    the free-capacity counters equal those of a first-fit model with
+    coalescing; generations advance per slot."""
+    rng = random.Random(17 + hot_rows)
+    L, ring, staging, pool, maxr = 4, 512, 256, 60000, 6
+    c = Q.Cache(n_layers=L, max_requests=maxr, ctx_capacity=20000, hbm_pool_rows=pool,
+                budget_tokens=2048, ring_tokens=ring, staging_rows=staging, device=None, hot_rows=hot_rows)
+    m = _PoolModel(pool, L * staging, L, ring, hot_rows, maxr)
+    live = {}
+    for step in range(400):
+        if live and (rng.random() < 0.45 or len(live) == maxr):
+            slot = rng.choice(sorted(live))
+            c.request_end(live.pop(slot))
+            m.end(slot)
+        else:
+            placement = rng.choice([Q.KV_HBM, Q.KV_HBM, Q.KV_HOST_RING, Q.KV_HOST])
+            n = rng.randint(1, 20000) if placement != Q.KV_HBM else rng.randint(1, 6000)
+            host = None if placement == Q.KV_HBM else 1 << 20
+            want = m.begin(n, placement)
+            if isinstance(want, tuple):
+                h = c.request_begin(n, placement, host_rows=host)
+                slot, base = want
+                assert (h.index, h.generation) == (slot, m.gen[slot]), step
+                info = c.request_info(h)
+                if m.slots[slot][1] > 0:
+                    assert info.hbm_row_base == base, step
+                live[slot] = h
+            else:
+                with pytest.raises(Q.QsaError) as e:
+                    c.request_begin(n, placement, host_rows=host)
+                assert e.value.status == want, step
+        st = c.stats()
+        assert st["free_hbm_rows"] == sum(length for _, length in m.free), step
+        assert st["free_ranges"] == len(m.free), step
+        assert st["largest_free_rows"] == max((length for _, length in m.free), default=0), step
+        assert st["active_requests"] == len(live), step
+    for slot in sorted(live):
+        c.request_end(live.pop(slot))
+    assert c.stats()["free_hbm_rows"] == pool - L * staging
