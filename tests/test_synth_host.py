@@ -49,3 +49,36 @@ def test_unplant_restores_plant_exactly():
     assert not torch.equal(sc.view(torch.int16), before.view(torch.int16))
     synth.unplant(sc, blocks, n)
     assert np.array_equal(sc.view(torch.int16).numpy(), before.view(torch.int16).numpy())
+
+
+def test_planting_recipes_match_their_definitions():
+    """The planting recipes of the workloads: uniform distinct blocks; half
+    of the planted blocks inside the tail ring and half before it (the 256K
+    config); sinks 0-3 plus a 50/50 mix of a recency Zipf(1.1) law and a
+    uniform law (the 1M config)."""
+    u = synth.planted_uniform(1000, 300, seed=2)
+    assert u.numel() == 300 and u.unique().numel() == 300 and int(u.min()) >= 0 and int(u.max()) < 1000
+    assert synth.planted_uniform(10, 300, seed=2).numel() == 10
+
+    n_blocks, tail = 65536, 1024
+    hc = synth.planted_hot_cold(n_blocks, 512, tail, seed=3)
+    assert hc.numel() == 512 and hc.unique().numel() == 512
+    assert int((hc >= n_blocks - tail).sum()) == 256 and int((hc < n_blocks - tail).sum()) == 256
+    small = synth.planted_hot_cold(600, 512, 1024, seed=3)           # tail covers every block
+    assert small.numel() == 512 and int(small.max()) < 600
+
+    nb = 262144
+    z = synth.planted_zipf_sinks(nb, 512, seed=4)
+    assert z.numel() == 512 and z.unique().numel() == 512 and int(z.max()) < nb
+    assert set(range(4)) <= set(z.tolist())
+    newest_percent = int((z >= nb - nb // 100).sum())
+    assert 100 <= newest_percent <= 400            # the recency law puts ~200 of 508 there
+    assert int((z < nb // 2).sum()) >= 100          # the uniform half spreads over the context
+
+
+def test_ragged_contexts_are_log_uniform_multiples():
+    ctx = synth.log_uniform_contexts(64, 4096, 262144, seed=5)
+    ctx = [int(c) for c in ctx]
+    assert all(c % 4 == 0 and 4096 <= c <= 262144 for c in ctx)
+    assert min(ctx) < 16384 and max(ctx) > 65536   # spread over the decades, not clustered
+    assert ctx == [int(c) for c in synth.log_uniform_contexts(64, 4096, 262144, seed=5)]
