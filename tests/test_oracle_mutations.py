@@ -236,7 +236,19 @@ def _bf16_heads_interleaved(rows_u8):
     return vals[:, :, 0, :], vals[:, :, 1, :]
 
 
+
+def _resident_ctx_stride(ctx_len, layer, base_row, layer_rows=None):
+    return (base_row + layer * ctx_len + np.arange(ctx_len, dtype=np.int64)).astype(np.int32)
+
+
+def _resident_off_by_one(ctx_len, layer, base_row, layer_rows=None):
+    stride = ctx_len if layer_rows is None else layer_rows
+    return (base_row + layer * stride + 1 + np.arange(ctx_len, dtype=np.int64)).astype(np.int32)
+
+
 MUTATIONS = {
+    "resident slots with the context as layer stride": {"resident_slot_row": _resident_ctx_stride},
+    "resident slots one row off": {"resident_slot_row": _resident_off_by_one},
     "bf16 row with K and V swapped": {"split_kv": _bf16_kv_swapped},
     "bf16 row with K and V interleaved per head": {"split_kv": _bf16_heads_interleaved},
     "boundary gap measured from the top block": {"boundary_gap": _gap_from_top},

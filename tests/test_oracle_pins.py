@@ -580,3 +580,15 @@ def test_boundary_gap_hand_worked():
     assert O.boundary_gap([4.0, 4.0, 4.0, 1.0], 8) == 0.0  # a tie at the boundary
     assert O.boundary_gap([1.0, 2.0], 8) == float("inf")  # every block selected
     assert O.boundary_gap([-1.0, -5.0, -2.0], 4) == 1.0   # K = 1: -1 - (-2)
+
+
+def test_resident_slot_row_hand_worked():
+    """An HBM-resident request's slot row: token t of layer l sits in pool row
+    base + l * layer_rows + t, where layer_rows is the region's rows per
+    layer (the request's capacity), and the context length when none is
+    given; worked out by hand."""
+    assert O.resident_slot_row(5, 2, 100, 8).tolist() == [116, 117, 118, 119, 120]
+    assert O.resident_slot_row(3, 0, 7).tolist() == [7, 8, 9]
+    assert O.resident_slot_row(3, 1, 7).tolist() == [10, 11, 12]
+    assert O.resident_slot_row(4, 3, 0, 10).tolist() == [30, 31, 32, 33]
+    assert O.resident_slot_row(1, 0, 5, 1).tolist() == [5]
