@@ -246,7 +246,15 @@ def _resident_off_by_one(ctx_len, layer, base_row, layer_rows=None):
     return (base_row + layer * stride + 1 + np.arange(ctx_len, dtype=np.int64)).astype(np.int32)
 
 
+
+def _layer_step_host_only(codes, scale_bits, q_idx, w, q_bits, slot_row, hbm_pool_rows, host_rows,
+                          budget_tokens, softmax_scale):
+    return O._orig_layer_step(codes, scale_bits, q_idx, w, q_bits, np.full_like(np.asarray(slot_row), -1),
+                              hbm_pool_rows, host_rows, budget_tokens, softmax_scale)
+
+
 MUTATIONS = {
+    "unit step reads every row from the host history": {"layer_step": _layer_step_host_only},
     "resident slots with the context as layer stride": {"resident_slot_row": _resident_ctx_stride},
     "resident slots one row off": {"resident_slot_row": _resident_off_by_one},
     "bf16 row with K and V swapped": {"split_kv": _bf16_kv_swapped},
@@ -303,6 +311,7 @@ def test_pins_catch_mutation(name, monkeypatch):
     monkeypatch.setattr(O, "_orig_append", O.append_slot_writes, raising=False)
     monkeypatch.setattr(O, "_orig_split_fp8", O.split_kv_fp8, raising=False)
     monkeypatch.setattr(O, "_orig_split_kv", O.split_kv, raising=False)
+    monkeypatch.setattr(O, "_orig_layer_step", O.layer_step, raising=False)
     for attr, val in MUTATIONS[name].items():
         monkeypatch.setattr(O, attr, val)
     caught = 0

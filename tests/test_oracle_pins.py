@@ -592,3 +592,27 @@ def test_resident_slot_row_hand_worked():
     assert O.resident_slot_row(3, 1, 7).tolist() == [10, 11, 12]
     assert O.resident_slot_row(4, 3, 0, 10).tolist() == [30, 31, 32, 33]
     assert O.resident_slot_row(1, 0, 5, 1).tolist() == [5]
+
+
+def test_layer_step_reads_pool_rows_for_slotted_tokens():
+    """The whole unit with pool and host rows that differ: tokens whose slot
+    is a pool row must be read from the pool, the cold ones from the host
+    history.  The reference picks the rows by the slot row itself and runs
+    torch's fp64 scaled_dot_product_attention over them."""
+    n = 12
+    u = synth.unit_inputs(n, seed=31, planted_blocks=[], device="cpu")
+    host = synth.kv_rows(n, seed=32).numpy()
+    pooled = synth.kv_rows(n, seed=33).numpy()
+    slot = np.array([-1, -1, 5, 6, -1, 7, -1, -1, 8, -1, -1, 9], dtype=np.int32)
+    pool = {int(s): pooled[t] for t, s in enumerate(slot) if s >= 0}
+    qb = u.q.view(torch.int16).numpy().view(np.uint16)
+    res = O.layer_step(u.codes.numpy(), u.scales.view(torch.int16).numpy().view(np.uint16),
+                       u.q_idx.numpy(), u.w.numpy(), qb, slot, pool, host, 2048, 1 / math.sqrt(128))
+    assert res["tokens"].tolist() == list(range(n))
+    rows = np.where((slot >= 0)[:, None], pooled, host)
+    rt = torch.from_numpy(np.ascontiguousarray(rows)).view(torch.bfloat16).reshape(n, 2, 4, 128).double()
+    K = rt[:, 0].permute(1, 0, 2).repeat_interleave(4, dim=0)
+    V = rt[:, 1].permute(1, 0, 2).repeat_interleave(4, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(u.q.double().reshape(16, 1, 128), K, V,
+                                                           scale=1 / math.sqrt(128))
+    assert np.allclose(res["out"], ref.reshape(16, 128).numpy(), rtol=0, atol=1e-12)
