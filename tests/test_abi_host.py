@@ -496,3 +496,89 @@ def test_pool_allocation_follows_first_fit_model(hot_rows):
     for slot in sorted(live):
         c.request_end(live.pop(slot))
     assert c.stats()["free_hbm_rows"] == pool - L * staging
+
+
+_C_DECODE_STEP = r"""
+#include <cuda_runtime.h>
+#include <qsa.h>
+#include <stdio.h>
+#include <string.h>
+
+#define CK(x) do { if ((x) != cudaSuccess) return 1; } while (0)
+#define QK(x) do { if ((x) != QSA_OK) { fprintf(stderr, "%s\n", qsa_last_error_string()); return 2; } } while (0)
+
+/* One decode step of one HBM-resident request at one layer, from C with
+   plain device pointers: score, select, attend, check the error word. */
+int main(void) {
+  const int n = 8192, budget = 2048, L = 1;
+  qsa_cache_config cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.n_layers = L; cfg.max_requests = 1; cfg.ctx_capacity = n; cfg.budget_tokens = budget;
+  cfg.ring_tokens = 4096; cfg.staging_rows = 0; cfg.kv_format = QSA_KV_BF16; cfg.hbm_pool_rows = n;
+  CK(cudaMalloc(&cfg.hbm_pool, (size_t)n * QSA_ROW_BYTES));
+  CK(cudaMalloc((void**)&cfg.index_keys, (size_t)n * QSA_INDEX_DIM));
+  CK(cudaMalloc((void**)&cfg.index_scales, (size_t)n * 2));
+  CK(cudaMalloc((void**)&cfg.slot_table, (size_t)n * 4));
+  cfg.workspace_bytes = qsa_workspace_bytes(&cfg);
+  CK(cudaMalloc(&cfg.workspace, (size_t)cfg.workspace_bytes));
+  CK(cudaMemset(cfg.index_keys, 0x38, (size_t)n * QSA_INDEX_DIM));   /* e4m3 1.0 */
+  CK(cudaMemset(cfg.index_scales, 0, (size_t)n * 2));
+  CK(cudaMemset(cfg.hbm_pool, 0, (size_t)n * QSA_ROW_BYTES));
+  qsa_cache* c = NULL;
+  QK(qsa_cache_create(&cfg, &c));
+  qsa_request_desc d;
+  memset(&d, 0, sizeof d);
+  d.ctx_len = n; d.placement = QSA_KV_HBM;
+  qsa_handle h;
+  QK(qsa_request_begin(c, &d, NULL, &h));
+  float *q_idx, *w, *blk, *out, *lse;
+  uint16_t* q;
+  int32_t *sel, *nsel;
+  CK(cudaMalloc((void**)&q_idx, 8 * 64 * 4)); CK(cudaMemset(q_idx, 0, 8 * 64 * 4));
+  CK(cudaMalloc((void**)&w, 8 * 4)); CK(cudaMemset(w, 0, 8 * 4));
+  CK(cudaMalloc((void**)&blk, (size_t)(n / 4) * 4));
+  CK(cudaMalloc((void**)&sel, (size_t)(budget / 4) * 4));
+  CK(cudaMalloc((void**)&nsel, 4));
+  CK(cudaMalloc((void**)&q, 16 * 128 * 2)); CK(cudaMemset(q, 0, 16 * 128 * 2));
+  CK(cudaMalloc((void**)&out, 16 * 128 * 4));
+  CK(cudaMalloc((void**)&lse, 16 * 4));
+  qsa_batch b = {1, 0, 1, 0, &h};
+  QK(qsa_index_score(c, &b, q_idx, w, blk, n / 4, NULL));
+  QK(qsa_select_c4_topk(c, &b, blk, n / 4, budget, sel, nsel, NULL));
+  QK(qsa_sparse_decode_attn(c, &b, q, sel, nsel, budget, NULL, 0.0883883f, out, lse, NULL));
+  int32_t st = -1;
+  QK(qsa_poll_error(c, NULL, &st, NULL));
+  if (st != QSA_OK) return 3;
+  QK(qsa_request_end(c, h));
+  QK(qsa_cache_destroy(c));
+  printf("decode step ok\n");
+  return 0;
+}
+"""
+
+
+def test_c_decode_step_compiles_and_links():
+    """A whole decode step written in C against the CUDA runtime (device
+    buffers from cudaMalloc, no PyTorch) compiles and links against the
+    library as declared."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda = "/usr/local/cuda"
+    if cc is None or not os.path.exists(os.path.join(cuda, "include", "cuda_runtime.h")):
+        pytest.skip("no C compiler or CUDA headers")
+    libdir = os.path.dirname(N.LIB_PATH)
+    cudalib = next((p for p in (os.path.join(cuda, "lib64"), os.path.join(cuda, "lib"))
+                    if os.path.isdir(p)), None)
+    if cudalib is None:
+        pytest.skip("no CUDA runtime library directory")
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "decode_step.c"), os.path.join(d, "decode_step")
+        with open(src, "w") as f:
+            f.write(_C_DECODE_STEP)
+        r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                            "-I", os.path.join(cuda, "include"), src, "-o", exe, "-L", libdir,
+                            "-lqsa_gb300", "-L", cudalib, "-lcudart", f"-Wl,-rpath,{libdir}"],
+                           capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
