@@ -354,6 +354,161 @@ def hbm_resident_timing(dev, args):
         wl.close()
 
 
+def _replay_ms(graph, dev, args):
+    """Per-replay times (ms) of a captured step: args.warmup untimed replays,
+    then args.steps replays with a CUDA event after each on the launching
+    stream."""
+    cur = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(cur)
+    for i in range(args.steps):
+        graph.replay()
+        ev[i + 1].record(cur)
+    torch.cuda.synchronize(dev)
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+
+
+def _attn_launch_us(wl, dev, args, r0=0, r1=None):
+    """Average time (us) of one attention launch over requests r0..r1-1 at
+    layer 0: 12 launches captured as one CUDA graph, replayed args.steps
+    times between CUDA events."""
+    cur = torch.cuda.current_stream(dev)
+    c, R = wl.cache, wl.n_req
+    r1 = R if r1 is None else r1
+    hs = wl.handles[r0:r1]
+    s = torch.cuda.Stream()
+    s.wait_stream(cur)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(N_LAYERS):
+            c.sparse_decode_attn(hs, 0, 1, wl.q[r0:r1], wl.sel[r0:r1], wl.nsel[r0:r1], BUDGET, None,
+                                 wl.softmax_scale, wl.out[r0:r1], wl.lse[r0:r1], s)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) * 1e3 / (args.steps * N_LAYERS)
+
+
+def _pct(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, int(round(q * (len(xs) - 1))))]
+
+
+def host_only_timing(dev, args, link_peak):
+    """The host-only configuration: 4 requests x 12 layers x 1048576 tokens,
+    KV only in pinned host memory (every selected row crosses the host link:
+    2048 rows x 2 KiB per unit, 48 MiB per step of the 12 layers of one
+    request), index keys (66 B per token, 3.32 GB per step) in HBM.  Times
+    the captured two-micro-batch step and one attention launch (4 units)."""
+    from sparse_attention_decode_qsa_gb300 import workloads
+    wl = workloads.c1m_x4(device=dev, n_layers=args.layers)
+    try:
+        R, L, n = wl.n_req, wl.n_layers, wl.ctxs[0]
+        units = R * L
+        graph = wl.capture(args.groups)
+        ms = _replay_ms(graph, dev, args)
+        del graph
+        attn_us = _attn_launch_us(wl, dev, args)
+        st, det = wl.cache.poll_error()
+        if st != 0:
+            raise RuntimeError(f"device error word {st} ({det}) in the host-only timing")
+        step_s = statistics.mean(ms) / 1e3
+        host_b, hbm_b = units * BUDGET * ROW, units * IDX_BYTES * n
+        attn_host = R * BUDGET * ROW
+        hbm_peak, _ = peaks()
+        return {"workload": f"c1m_x4: {R} requests x {L} layers x {n} tokens, KV only in pinned host "
+                            "memory (sinks 0-3 + recency Zipf(1.1)/uniform planting)",
+                "ms_per_step": round(step_s * 1e3, 4),
+                "step_ms_p10_p50_p90": [round(_pct(ms, q), 4) for q in (0.1, 0.5, 0.9)],
+                "layer_steps_per_s": round(units / step_s, 1),
+                "host_bytes_per_step": host_b, "hbm_bytes_per_step": hbm_b,
+                "host_gbs": round(host_b / step_s / 1e9, 1),
+                "host_frac": round(host_b / step_s / 1e9 / link_peak, 4),
+                "hbm_gbs": round(hbm_b / step_s / 1e9, 1),
+                "hbm_frac": round(hbm_b / step_s / 1e9 / hbm_peak, 4),
+                "roofline_ms": round(max(host_b / (link_peak * 1e9), hbm_b / (hbm_peak * 1e9)) * 1e3, 4),
+                "sparse_attn": {"units_per_launch": R, "host_bytes_per_launch": attn_host,
+                                "avg_launch_us": round(attn_us, 2),
+                                "achieved": round(attn_host / (attn_us * 1e-6) / 1e9, 1),
+                                "peak": round(link_peak, 1), "unit": "GB/s",
+                                "frac": round(attn_host / (attn_us * 1e-6) / 1e9 / link_peak, 4)}}
+    finally:
+        wl.close()
+
+
+def ragged_timing(dev, args, link_peak):
+    """The ragged batch: 64 requests with contexts log-uniform in [4096,
+    262144] (multiples of 4) x 12 layers; KV in HBM below 32768 tokens, pinned
+    host history + HBM tail ring above.  Times the captured step (one batch
+    per layer, split into micro-batches); then finishes 16 requests, admits
+    16 new ones in their slots under new generations, times the step again,
+    ends every request and checks that the cache counters are back at their
+    initial values."""
+    import sparse_attention_decode_qsa_gb300 as Q
+    from sparse_attention_decode_qsa_gb300 import synth, workloads
+    L = args.layers
+    new_ctx = synth.log_uniform_contexts(16, 4096, 262144, seed=77)
+    spare = sum(L * (n if n < 32768 else 4096) for n in new_ctx)
+    wl = workloads.ragged(device=dev, n_layers=L, extra_requests=0, spare_rows=spare)
+    try:
+        c, R = wl.cache, wl.n_req
+        units = R * L
+        s0 = dict(c.stats())
+
+        def measure():
+            g = wl.capture(args.groups)
+            ms = _replay_ms(g, dev, args)
+            del g
+            st, det = c.poll_error()
+            if st != 0:
+                raise RuntimeError(f"device error word {st} ({det}) in the ragged timing")
+            ctx = list(wl.ctxs)
+            off = [r for r in range(R) if wl.placements[r] != Q.KV_HBM]
+            host_rows = sum(L * BUDGET // 2 for r in off)      # half of an offloaded unit's rows are cold
+            hbm_b = sum(L * (IDX_BYTES * n + (BUDGET * ROW if wl.placements[r] == Q.KV_HBM else BUDGET * ROW // 2))
+                        for r, n in enumerate(ctx))
+            step_s = statistics.mean(ms) / 1e3
+            return {"ms_per_step": round(step_s * 1e3, 4),
+                    "step_ms_p10_p50_p90": [round(_pct(ms, q), 4) for q in (0.1, 0.5, 0.9)],
+                    "layer_steps_per_s": round(units / step_s, 1),
+                    "requests_hbm": R - len(off), "requests_offloaded": len(off),
+                    "tokens_total": sum(ctx),
+                    "host_gbs": round(host_rows * ROW / step_s / 1e9, 1),
+                    "hbm_gbs": round(hbm_b / step_s / 1e9, 1)}
+
+        before = measure()
+        rng = np.random.default_rng(3)
+        done = [int(x) for x in rng.choice(R, 16, replace=False)]
+        gens = []
+        for j, r in enumerate(done):
+            n = new_ctx[j]
+            h = wl.reissue(r, n, Q.KV_HBM if n < 32768 else Q.KV_HOST_RING, seed=500 + j)
+            gens.append(int(h.generation))
+        after = measure()
+        for h in wl.handles:
+            c.request_end(h)
+        wl.handles = []
+        s_end = dict(c.stats())
+        restored = (s_end["active_requests"] == 0 and s_end["free_request_slots"] == s0["free_request_slots"] + R
+                    and s_end["hbm_kv_bytes_in_use"] == 0 and s_end["free_ranges"] == 1
+                    and s_end["free_hbm_rows"] == s0["hbm_pool_rows"] - s0["staging_rows_total"])
+        return {"workload": f"ragged: {R} requests x {L} layers, contexts log-uniform in [4096, 262144]; "
+                            "KV in HBM below 32768 tokens, pinned host + 4096-token HBM tail ring above",
+                "before_recycling": before, "after_recycling": after,
+                "recycled": {"finished": 16, "admitted": 16, "new_generations": sorted(set(gens))},
+                "counters_restored": bool(restored), "stats_initial": s0, "stats_end": s_end}
+    finally:
+        wl.close()
+
+
 def _cold_selected_rows(wl):
     """Selected tokens of the offloaded units that are cold (slot -1) before
     the next step: the rows that step fetches from host memory.  The
@@ -553,6 +708,8 @@ def run_ours(args, rank, world):
     link_copy = host_link_peak(dev)
     link_zc = zero_copy_peak(dev)
     link_peak = max(link_copy, link_zc)
+    host_only = host_only_timing(dev, args, link_peak)
+    ragged = ragged_timing(dev, args, link_peak)
 
     ms_max, ms_e2e_max = max_over_ranks([ms, ms_e2e], world)
     if rank != 0:
@@ -623,6 +780,7 @@ def run_ours(args, rank, world):
         "eager_sequential_ms_per_step": round(ms_eager / args.steps, 4),
         "step_ms_p10_p50_p90": [round(pct(0.1), 4), round(pct(0.5), 4), round(pct(0.9), 4)],
         "roofline": dom, "kernels": roofs, "selection_drift": drift, "hbm_resident": hbm_res,
+        "host_only_1m": host_only, "ragged_batch": ragged,
         "fp8_kv": {"what": "the same step over FP8 KV rows (1040 bytes: E4M3 K and V codes, fp16 "
                            "scales per head); BF16 queries, fp32 outputs",
                    "ms_per_step": round(fp8_step_ms, 4),

@@ -8,9 +8,11 @@
 // synchronise the device or is forbidden.  They pass the query, the rows and
 // the outputs; the split-K partials live in g_attn_scratch below.
 //
-// It computes what qsa_sparse_decode_attn computes from gathered rows, with
-// the same 32-row splits; the two merge their splits in a different order, so
-// they agree to rounding (far inside the 2e-3 attention tolerance).
+// It computes what qsa_sparse_decode_attn computes from gathered rows, but
+// with its own work layout: one CTA per 32 gathered rows, where the main
+// kernel's CTAs stream 16-row splits and keep a running softmax state.  The
+// two sum and merge in a different order, so they agree to rounding (far
+// inside the 2e-3 attention tolerance).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,7 +29,6 @@ constexpr int kSmemBytes = kSplitTokens * kRowBytes;
 constexpr int kStaticSplits = QSA_STATIC_MAX_ROWS / kSplitTokens;  // 64
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kMaxDevices = 64;
 
 // One (m[16], l[16], acc[16][128]) partial per (unit, split): 8.5 MB.  Every
 // GPU that loads the library holds this array until the process exits.

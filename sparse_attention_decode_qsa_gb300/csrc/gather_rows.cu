@@ -144,8 +144,8 @@ cudaError_t launch_gather_rows(const BatchDesc& b, const int32_t* sel_blocks,
   p.budget_tokens = budget_tokens;
   p.out = rows_out;
   p.n_rows = n_rows;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceOnce setup;
+  cudaError_t e0 = setup.run([] {
     cudaError_t e = cudaFuncSetAttribute(gather_rows_kernel<kRowBytes / 16>,
                                          cudaFuncAttributePreferredSharedMemoryCarveout,
                                          cudaSharedmemCarveoutMaxShared);
@@ -153,9 +153,9 @@ cudaError_t launch_gather_rows(const BatchDesc& b, const int32_t* sel_blocks,
       e = cudaFuncSetAttribute(gather_rows_kernel<kRowBytesFp8 / 16>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  });
+  if (e0 != cudaSuccess) return e0;
   dim3 grid((p.k_max + kGatherBlocks - 1) / kGatherBlocks, b.n_units);
   if (b.row_bytes == kRowBytesFp8)
     return launch_kernel(gather_rows_kernel<kRowBytesFp8 / 16>, grid, dim3(kGatherThreads), 0, s, 0,

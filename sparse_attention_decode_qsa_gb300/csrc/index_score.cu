@@ -19,11 +19,16 @@
 //    bytes under the 64-byte swizzle, which is the tensor core's K-major
 //    SWIZZLE_64B layout, so the codes are never touched by a thread;
 //  * B = the index query as e4m3 "pieces": q * 2^s = sum_p piece_p * 16^-p
-//    (p = 0..4; each piece the round-to-nearest e4m3 of the remaining
-//    residual times 16), one B row per (piece, head).  Five pieces carry
-//    20 bits of every query element, so sum_p 16^-p * D[:, 8p + h] / 2^s
-//    equals the fp32 dot product to about 2^-20 relative.  Every product of
-//    two e4m3 values is exact, and the tensor core accumulates in fp32.
+//    (p = 0..5; each piece the round-to-nearest e4m3 of the remaining
+//    residual times 16), one B row per (piece, head): 6 x 8 = 48 rows, the
+//    MMA's N.  An e4m3 rounding leaves a residual of at most 2^-4 of its
+//    input, so after six pieces an element's remaining error is at most
+//    2^-24 of the element (or, once a residual falls into the e4m3
+//    subnormals, at most 2^-37 of the unit's largest element, which the
+//    common scale puts in [128, 256)): the pieces carry the fp32 query to
+//    fp32's own precision.  Every product of two
+//    e4m3 values is exact, and the tensor core accumulates in fp32, so
+//    sum_p 16^-p * D[:, 8p + h] / 2^s is the dot product to fp32 rounding.
 // Per tile that is two MMAs (K = 32 each); a tensor core spends ~160 cycles
 // on an MMA of this size whatever its N, so the instruction count per token
 // is what bounds the kernel, and fp8 operands halve it against f16 ones.
@@ -64,8 +69,11 @@ constexpr int kPipes = QSA_K1_PIPES;            // independent pipelines per CTA
 #define QSA_K1_STAGES 3
 #endif
 constexpr int kStages = QSA_K1_STAGES;          // code ring depth per pipeline (8 KiB each)
-constexpr int kPieces = 5;                      // e4m3 pieces of the query
-constexpr int kN = 48;                          // B rows: 8 heads x 5 pieces, padded to 16
+#ifndef QSA_K1_PIECES
+#define QSA_K1_PIECES 6
+#endif
+constexpr int kPieces = QSA_K1_PIECES;          // e4m3 pieces of the query (5 or 6)
+constexpr int kN = 48;                          // B rows: 8 heads x 6 pieces (5 pieces: padded)
 constexpr int kDBufs = 2;                       // accumulators per pipeline in tensor memory
 constexpr int kDStride = 64;                    // tensor-memory columns per accumulator
 // Warp roles within a pipeline (6 warps): producer, MMA, 4 workers.
@@ -115,7 +123,8 @@ static_assert(kOffScale % 128 == 0 && kScaleSlot % 128 == 0 && kScaleBox * 2 <= 
                   (kScaleBox * 2) % 16 == 0, "scale boxes: 16-byte multiples in 128-byte slots");
 static_assert(kOffBar % 8 == 0 && kOffStageMeta % 16 == 0,
               "mbarriers need 8-byte, int4 metadata 16-byte alignment");
-static_assert(kPieces * kIndexHeads <= kN && kN % 16 == 0 && kN <= kDStride, "B rows");
+static_assert((kPieces == 5 || kPieces == 6) && kPieces * kIndexHeads <= kN && kN % 16 == 0 &&
+                  kN <= kDStride, "B rows");
 static_assert(kPipeWarps - kRoleWork0 == 4, "four worker warps cover the four lane quarters");
 // kind::f8f6f4 instruction descriptor: D f32 (bit 4), A = B = e4m3 (type 0 at
 // bits 7-9 and 10-12), both K-major, N/8 at bits 17-22, M/16 at bits 24-28.
@@ -236,6 +245,7 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr)
       : "memory");
 }
+#if QSA_K1_PIECES != 6
 __device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
@@ -243,6 +253,7 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                : "r"(taddr)
                : "memory");
 }
+#endif
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void tc_reg_fence(uint32_t (&r)[N]) {
@@ -534,18 +545,32 @@ index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
       const uint32_t dcol = lane_base + (uint32_t)(db * kDStride);
       float y[kIndexHeads];
       {
+        auto f = [](uint32_t x) { return __uint_as_float(x); };
+#if QSA_K1_PIECES == 6
+        uint32_t v45[16], v23[16], v01[16];
+        tc_ld16(dcol + 32, v45);
+#else
         uint32_t v4[8], v23[16], v01[16];
         tc_ld8(dcol + 32, v4);
+#endif
         tc_ld16(dcol + 16, v23);
         tc_ld16(dcol, v01);
         tc_wait_ld();
+#if QSA_K1_PIECES == 6
+        tc_reg_fence(v45);
+#else
         tc_reg_fence(v4);
+#endif
         tc_reg_fence(v23);
         tc_reg_fence(v01);
-        auto f = [](uint32_t x) { return __uint_as_float(x); };
 #pragma unroll
         for (int h = 0; h < kIndexHeads; ++h) {
+#if QSA_K1_PIECES == 6
+          float a = fmaf(f(v45[8 + h]), 0.0625f, f(v45[h]));
+          a = fmaf(a, 0.0625f, f(v23[8 + h]));
+#else
           float a = fmaf(f(v4[h]), 0.0625f, f(v23[8 + h]));
+#endif
           a = fmaf(a, 0.0625f, f(v23[h]));
           a = fmaf(a, 0.0625f, f(v01[8 + h]));
           y[h] = fmaf(a, 0.0625f, f(v01[h]));
@@ -625,16 +650,11 @@ cudaError_t make_index_maps(CUtensorMap* keys_map, const void* keys, CUtensorMap
 cudaError_t launch_index_score(const BatchDesc& b, const CUtensorMap* keys_map,
                                const CUtensorMap* scales_map, const float* q_idx, const float* w,
                                float* blk_scores, int64_t blk_stride, cudaStream_t s) {
-  static bool attr_set = false;
-  static int sm_count = 0;
-  if (!attr_set) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = prefer_max_shared(index_score_tc_kernel, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDeviceOnce setup;
+  cudaError_t e = setup.run([] { return prefer_max_shared(index_score_tc_kernel, kSmemBytes); });
+  int sm_count = 0;
+  if (e == cudaSuccess) e = current_sm_count(&sm_count);
+  if (e != cudaSuccess) return e;
   IndexScoreParams p;
   p.keys_map = *keys_map;
   p.scales_map = *scales_map;

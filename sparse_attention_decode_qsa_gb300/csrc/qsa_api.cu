@@ -102,17 +102,59 @@ WorkspaceLayout workspace_layout(const qsa_cache_config& c) {
 }  // namespace
 
 int qsa::highest_priority() {
-  static int prio = 1;   // 1: not yet queried (priorities are <= 0)
-  if (prio == 1) {
+  static const int prio = [] {   // thread-safe one-time initialisation
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) {
       cudaGetLastError();
       greatest = 0;
     }
-    prio = greatest;
-  }
+    return greatest;
+  }();
   return prio;
 }
+
+cudaError_t qsa::current_sm_count(int* out) {
+  static std::atomic<int> counts[kMaxDevices];   // 0: not yet queried
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int v = counts[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    counts[dev].store(v, std::memory_order_relaxed);
+  }
+  *out = v;
+  return cudaSuccess;
+}
+
+namespace {
+
+// Makes `dev` the calling thread's current device for the lifetime of the
+// guard and restores the previous one afterwards (dev < 0: no change).
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    if (dev < 0) return;
+    status_ = cudaGetDevice(&prev_);
+    if (status_ == cudaSuccess && prev_ != dev) {
+      status_ = cudaSetDevice(dev);
+      switched_ = status_ == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (switched_) cudaSetDevice(prev_);
+  }
+  cudaError_t status() const { return status_; }
+
+ private:
+  int prev_ = 0;
+  bool switched_ = false;
+  cudaError_t status_ = cudaSuccess;
+};
+
+}  // namespace
 
 qsa_status_t qsa::set_last_error(qsa_status_t status, const char* message) {
   g_last_error = message ? message : "";
@@ -124,6 +166,7 @@ struct qsa_cache {
   CUtensorMap scales_map;
   qsa_cache_config cfg;
   bool has_device = false;
+  int device = -1;            // CUDA device of the device storage (-1: host-only cache)
   int64_t staging_total = 0;
   int64_t splits_max = 0;
   std::vector<Lease> leases;
@@ -166,6 +209,29 @@ struct qsa_cache {
       }
     }
     free_rows[base] = n;
+  }
+
+  // Every call that touches device storage runs on the cache's device (a
+  // DeviceGuard makes it current) and refuses a stream of another device:
+  // here when the stream is not being captured (a stream's device cannot be
+  // queried during capture), else through the launch, which fails for a
+  // stream that does not belong to the current device.
+  qsa_status_t check_stream(void* stream, const DeviceGuard& g) const {
+    if (device < 0) return QSA_OK;
+    if (g.status() != cudaSuccess) return cuda_fail(g.status(), "making the cache's device current");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) return QSA_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "querying the stream's capture status");
+    if (cs != cudaStreamCaptureStatusNone) return QSA_OK;
+    int sdev = -1;
+    e = cudaStreamGetDevice(s, &sdev);
+    if (e != cudaSuccess) return cuda_fail(e, "querying the stream's device");
+    if (sdev != device)
+      return fail(QSA_ERR_INVALID_ARG, "stream belongs to device %d, the cache's storage to device %d",
+                  sdev, device);
+    return QSA_OK;
   }
 
   qsa_status_t check_handle(qsa_handle h, const Lease** out) const {
@@ -260,6 +326,23 @@ qsa_status_t qsa_cache_create(const qsa_cache_config* c, qsa_cache** out) {
       if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
         return fail(QSA_ERR_INVALID_ARG, "device buffers must be 16-byte aligned");
   }
+  int device = -1;
+  if (all) {
+    // the device storage must live on one device, which every call then uses
+    const void* ptrs[] = {c->hbm_pool, c->index_keys, c->index_scales, c->slot_table, c->workspace};
+    for (const void* p : ptrs) {
+      cudaPointerAttributes a{};
+      cudaError_t e = cudaPointerGetAttributes(&a, p);
+      if (e != cudaSuccess) return cuda_fail(e, "querying a device buffer");
+      if (a.type != cudaMemoryTypeDevice)
+        return fail(QSA_ERR_INVALID_ARG, "device storage must be device memory");
+      if (device >= 0 && a.device != device)
+        return fail(QSA_ERR_INVALID_ARG, "device storage spans devices %d and %d", device, a.device);
+      device = a.device;
+    }
+  }
+  DeviceGuard guard(device);
+  if (guard.status() != cudaSuccess) return cuda_fail(guard.status(), "making the storage's device current");
   const int64_t staging = (int64_t)c->n_layers * c->staging_rows;
   if (staging > c->hbm_pool_rows)
     return fail(QSA_ERR_CAPACITY, "staging (%lld rows) does not fit the pool (%lld rows)",
@@ -269,6 +352,7 @@ qsa_status_t qsa_cache_create(const qsa_cache_config* c, qsa_cache** out) {
   if (!cache) return fail(QSA_ERR_INVALID_ARG, "out of host memory");
   cache->cfg = *c;
   cache->has_device = all;
+  cache->device = device;
   cache->staging_total = staging;
   cache->splits_max = splits_max_of(*c);
   cache->leases.resize(c->max_requests);
@@ -328,6 +412,8 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
   if (desc->placement == QSA_KV_HBM && desc->host_rows)
     return fail(QSA_ERR_INVALID_ARG, "HBM placement takes no host_rows");
 
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   int slot = -1;
   for (size_t i = 0; i < c->leases.size(); ++i)
     if (!c->leases[i].active) { slot = (int)i; break; }
@@ -475,6 +561,8 @@ qsa_status_t qsa_slot_table_ptr(qsa_cache* c, qsa_handle h, int32_t layer, int32
 qsa_status_t qsa_slot_table_set(qsa_cache* c, qsa_handle h, int32_t layer, const int64_t* tokens,
                                 const int32_t* slots, int32_t n, void* stream) {
   if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   int32_t* row = nullptr;
   if (qsa_status_t st = qsa_slot_table_ptr(c, h, layer, &row)) return st;
   if (n < 0 || (n > 0 && (!tokens || !slots))) return fail(QSA_ERR_INVALID_ARG, "bad token/slot arrays");
@@ -495,6 +583,8 @@ qsa_status_t qsa_staging_ptr(qsa_cache* c, int32_t layer, void** out) {
 qsa_status_t qsa_poll_error(qsa_cache* c, void* stream, int32_t* dev_status, int64_t* detail) {
   if (!c || !dev_status) return fail(QSA_ERR_INVALID_ARG, "null argument");
   if (!c->has_device) return fail(QSA_ERR_NO_DEVICE, "cache has no device storage");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ErrorWord host{};
   cudaError_t e = cudaMemcpyAsync(&host, c->err(), sizeof host, cudaMemcpyDeviceToHost, s);
@@ -509,6 +599,8 @@ qsa_status_t qsa_poll_error(qsa_cache* c, void* stream, int32_t* dev_status, int
 qsa_status_t qsa_index_score(qsa_cache* c, const qsa_batch* batch, const float* q_idx,
                              const float* w, float* blk_scores, int64_t blk_stride, void* stream) {
   if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   BatchDesc d;
   if (qsa_status_t st = c->build_batch(batch, &d)) return st;
   if (!q_idx || !w || !blk_scores) return fail(QSA_ERR_INVALID_ARG, "null q_idx, w or blk_scores");
@@ -526,6 +618,8 @@ qsa_status_t qsa_select_c4_topk(qsa_cache* c, const qsa_batch* batch, const floa
                                 int64_t blk_stride, int32_t budget_tokens, int32_t* sel_blocks,
                                 int32_t* n_sel, void* stream) {
   if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   BatchDesc d;
   if (qsa_status_t st = c->build_batch(batch, &d)) return st;
   if (!blk_scores || !sel_blocks || !n_sel) return fail(QSA_ERR_INVALID_ARG, "null array");
@@ -545,6 +639,8 @@ qsa_status_t qsa_gather_rows(qsa_cache* c, const qsa_batch* batch, const int32_t
                              const int32_t* n_sel, int32_t budget_tokens, void* rows_out,
                              int32_t* n_rows, void* stream) {
   if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   BatchDesc d;
   if (qsa_status_t st = c->build_batch(batch, &d)) return st;
   if (!sel_blocks || !n_sel || !rows_out) return fail(QSA_ERR_INVALID_ARG, "null array");
@@ -562,6 +658,8 @@ qsa_status_t qsa_gather_rows(qsa_cache* c, const qsa_batch* batch, const int32_t
 qsa_status_t qsa_append_token(qsa_cache* c, const qsa_batch* batch, const float* k_new,
                               const void* kv_new, void* stream) {
   if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   BatchDesc d;
   if (qsa_status_t st = c->build_batch(batch, &d)) return st;
   if (!k_new || !kv_new) return fail(QSA_ERR_INVALID_ARG, "null k_new or kv_new");
@@ -590,6 +688,8 @@ qsa_status_t qsa_append_token(qsa_cache* c, const qsa_batch* batch, const float*
 qsa_status_t qsa_hot_cache_fetch(qsa_cache* c, const qsa_batch* batch, const int32_t* sel_blocks,
                                  const int32_t* n_sel, int32_t budget_tokens, void* stream) {
   if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   BatchDesc d;
   if (qsa_status_t st = c->build_batch(batch, &d)) return st;
   if (!sel_blocks || !n_sel) return fail(QSA_ERR_INVALID_ARG, "null array");
@@ -606,6 +706,8 @@ qsa_status_t qsa_sparse_decode_attn(qsa_cache* c, const qsa_batch* batch, const 
                                     int32_t budget_tokens, const void* gathered,
                                     float softmax_scale, float* out, float* lse, void* stream) {
   if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
   BatchDesc d;
   if (qsa_status_t st = c->build_batch(batch, &d)) return st;
   if (!q || !sel_blocks || !n_sel || !out) return fail(QSA_ERR_INVALID_ARG, "null array");

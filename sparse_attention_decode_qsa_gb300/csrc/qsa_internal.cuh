@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "qsa.h"
 
 namespace qsa {
@@ -20,8 +23,10 @@ constexpr int kRowBytes = QSA_ROW_BYTES;      // 2048: BF16 row
 constexpr int kRowBytesFp8 = QSA_ROW_BYTES_FP8;  // 1040: FP8 row
 constexpr int kMaxUnits = QSA_MAX_UNITS;
 
-// Split-K granularity of the attention: one CTA covers this many selected
-// C4 blocks (32 tokens, 64 KiB of rows).
+// Split-K partial slots of the workspace: one per this many selected C4
+// blocks of the budget (32 tokens), which caps the CTAs (partials) the
+// attention gives one unit.  The no-allocation attention splits its rows in
+// pieces of the same 32 tokens.
 constexpr int kAttnBlocksPerSplit = 8;
 constexpr int kAttnTokensPerSplit = kAttnBlocksPerSplit * 4;
 // One split-K partial: running max m[16] and sum l[16] (base-2 logits), then
@@ -155,6 +160,38 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// Device ids the library keeps per-device state for.
+constexpr int kMaxDevices = 64;
+
+// One-time setup per device.  Kernel attributes set with cudaFuncSetAttribute
+// apply to the device current on the calling thread, so every launcher runs
+// its setup once for each device it launches on; the mutex serialises the
+// first calls of concurrent threads.
+class PerDeviceOnce {
+ public:
+  template <class F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices]{};
+};
+
+// SM count of the device current on the calling thread (queried once per
+// device).
+cudaError_t current_sm_count(int* out);
 
 // Highest launch priority of the device (numerically lowest), for the
 // attention launches: their CTAs are dispatched ahead of queued scoring CTAs

@@ -528,22 +528,18 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
                                const int32_t* n_sel, int32_t budget_tokens,
                                const uint8_t* gathered, float softmax_scale, float* out,
                                float* lse, cudaStream_t s) {
-  static bool attr_set = false;
-  static int sm_count = 0;
-  if (!attr_set) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = prefer_max_shared(attn_split_kernel, kSmemBytes);
-    if (e == cudaSuccess)
-      e = prefer_max_shared(attn_split_fp8_kernel, kSmemFp8);
+  static PerDeviceOnce setup;
+  cudaError_t e0 = setup.run([] {
+    cudaError_t e = prefer_max_shared(attn_split_kernel, kSmemBytes);
+    if (e == cudaSuccess) e = prefer_max_shared(attn_split_fp8_kernel, kSmemFp8);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_merge_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  });
+  int sm_count = 0;
+  if (e0 == cudaSuccess) e0 = current_sm_count(&sm_count);
+  if (e0 != cudaSuccess) return e0;
   AttnParams p;
   p.b = b;
   p.q = q;

@@ -158,6 +158,19 @@ def index_query(seed: int, device="cpu"):
     return q, w
 
 
+def index_query_skewed(seed: int, span_log2: float = 12.0, device="cpu"):
+    """Index query with skewed magnitudes: every element is a random sign
+    times 2^(-span_log2 * u), u ~ U(0,1), so the elements spread
+    log-uniformly over [2^-span_log2, 1] of the largest one; head weights
+    U(0,1) fp32 [8] as in index_query."""
+    g = _gen(seed, device)
+    u = torch.rand(INDEX_HEADS, INDEX_DIM, generator=g, device=device, dtype=torch.float64)
+    sgn = torch.randint(0, 2, (INDEX_HEADS, INDEX_DIM), generator=g, device=device) * 2 - 1
+    q = (sgn * torch.exp2(-span_log2 * u)).to(torch.float32)
+    w = torch.rand(INDEX_HEADS, generator=g, device=device, dtype=torch.float32)
+    return q, w
+
+
 def attn_query(seed: int, device="cpu"):
     """Attention query [16][128] bf16 ~ N(0,1)."""
     g = _gen(seed, device)

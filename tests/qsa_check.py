@@ -107,3 +107,94 @@ def check_unit(wl, l, r, ref=None, check_scores=True):
     assert e_out <= ATTN_TOL, f"unit ({l},{r}): attention max abs err {e_out}"
     assert e_lse <= ATTN_TOL, f"unit ({l},{r}): lse max abs err {e_lse}"
     return dict(err_out=e_out, err_lse=e_lse, ref=ref)
+
+
+# ------------------------------------------------ tight boundary gaps
+
+TIGHT_GAP = (1.1e-3, 1.9e-3)   # fp64 boundary-gap window of the tight-gap tests
+_ONE_FP16 = 0x3C00
+
+
+def _fp16_bits(x: np.ndarray) -> np.ndarray:
+    return np.asarray(x, dtype=np.float16).view(np.uint16)
+
+
+def tune_boundary(codes, scale_bits, q_idx, w, budget, cand_codes, window=TIGHT_GAP,
+                  margin=0.05):
+    """Rewrite index keys of unselected blocks of one unit so that the
+    oracle's fp64 boundary gap falls inside `window` (input construction for
+    the tight-gap tests; the arithmetic is the oracle's):
+
+      1. every unselected block within `margin` of the K-th best block score T
+         gets the scales of its four tokens halved (exact for normal fp16)
+         until it is not;
+      2. the best unselected block b gets, in its first token, the codes of
+         the first candidate row of cand_codes for which some fp16 scale puts
+         that token's score in [T - window[1], T - window[0]], and that scale.
+         Its other tokens are already at most T - margin, so the token's
+         score is b's block score, and b is the best unselected block.
+
+    The selected set does not change.  Returns (codes, scale_bits, b, token)
+    as new arrays; raises AssertionError when no candidate fits."""
+    codes = np.array(codes, dtype=np.uint8, copy=True)
+    sb = np.array(scale_bits, dtype=np.uint16, copy=True)
+    q_idx = np.asarray(q_idx, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    n = codes.shape[0]
+    blk = O.c4_block_scores(O.token_scores(codes, sb, q_idx, w))
+    nb = blk.shape[0]
+    K = min(budget // 4, nb)
+    assert K < nb, "every block is selected: there is no boundary"
+    order = np.lexsort((np.arange(nb), -blk))
+    sel0 = np.sort(order[:K])
+    T = blk[order[K - 1]]
+    assert T > margin + window[1], f"K-th best score {T} too small to place a gap below it"
+    unsel = np.ones(nb, dtype=bool)
+    unsel[sel0] = False
+
+    def token_range(b):
+        return np.arange(4 * b, min(n, 4 * b + 4))
+
+    # 1. push every close unselected block below T - margin
+    for _ in range(64):
+        close = np.nonzero(unsel & (blk > T - margin))[0]
+        if close.size == 0:
+            break
+        toks = np.concatenate([token_range(b) for b in close])
+        sb[toks] = _fp16_bits(O.decode_fp16(sb[toks]) / 2.0)
+        S = O.token_scores(codes[toks], sb[toks], q_idx, w)
+        for b in close:
+            m = (toks >= 4 * b) & (toks < 4 * b + 4)
+            blk[b] = S[m].max()
+    else:
+        raise AssertionError("could not push the unselected blocks below the margin")
+
+    # 2. the best unselected block takes a score just below T
+    cand = np.nonzero(unsel)[0]
+    b = int(cand[np.argmax(blk[cand])])
+    t = 4 * b
+    s8 = O.token_scores(cand_codes, np.full(cand_codes.shape[0], _ONE_FP16, dtype=np.uint16),
+                        q_idx, w)
+    lo_s, hi_s = T - window[1], T - window[0]
+    for c in np.nonzero(s8 > 0)[0]:
+        mid = np.float16(0.5 * (lo_s + hi_s) / s8[c]).view(np.uint16).astype(np.int64)
+        hit = None
+        for bits in (mid, mid - 1, mid + 1, mid - 2, mid + 2):
+            if not (0 < bits < 0x7C00):
+                continue
+            s = O.decode_fp16(np.uint16(bits)) * s8[c]
+            if lo_s <= s <= hi_s:
+                hit = np.uint16(bits)
+                break
+        if hit is not None:
+            codes[t] = cand_codes[c]
+            sb[t] = hit
+            break
+    else:
+        raise AssertionError("no candidate key reaches the gap window")
+
+    blk2 = O.c4_block_scores(O.token_scores(codes, sb, q_idx, w))
+    gap = O.boundary_gap(blk2, budget)
+    assert window[0] <= gap <= window[1], gap
+    assert np.array_equal(O.select_blocks(blk2, budget), sel0)
+    return codes, sb, b, t

@@ -286,26 +286,34 @@ def test_c256k_x8_bench_configuration_sampled():
 
 def test_c1m_host_only_sampled():
     """1M-token contexts with KV only in pinned host memory (sinks + Zipf
-    recency planting); 4 requests, 3 of the 12 layers to bound host memory."""
-    wl = workloads.c1m_x4(n_layers=3)
+    recency planting): 4 requests x 12 layers at full size (96 GiB of pinned
+    host history), the captured two-micro-batch step as the benchmark runs
+    it; sampled units from every request checked against the oracle."""
+    wl = workloads.c1m_x4()
     try:
-        wl.step()
+        g = wl.capture(2)
+        g.replay()
         torch.cuda.synchronize()
         _clean(wl)
-        for (l, r) in [(0, 0), (2, 3)]:
+        for (l, r) in [(0, 0), (5, 1), (8, 2), (11, 3)]:
             res = QC.check_unit(wl, l, r)
             assert set(range(4)) <= set(res["ref"]["sel"].tolist())   # sink blocks kept
+            assert (res["ref"]["slot"] == -1).all()                   # every row from host memory
+        del g
     finally:
         wl.close()
 
 
 def test_ragged_batch_recycling_on_gpu():
-    """64 requests with log-uniform contexts in one batch per layer (2 of the
-    12 layers, to bound host memory); 16 of them finish and 16 new requests
-    are admitted in their slots under new generations with new contexts;
-    every unit type is checked against the oracle before and after, and the
-    cache counters return to their initial values at the end."""
-    wl = workloads.ragged(n_layers=2, extra_requests=0, spare_rows=2 * 262144)
+    """64 requests with log-uniform contexts in one batch per layer, all 12
+    layers; 16 of them finish and 16 new requests are admitted in their slots
+    under new generations with new contexts; every unit type is checked
+    against the oracle before and after, and the cache counters return to
+    their initial values at the end."""
+    L = 12
+    new_ctx = synth.log_uniform_contexts(16, 4096, 262144, seed=77)
+    spare = sum(L * (n if n < 32768 else 4096) for n in new_ctx)   # room for the new leases
+    wl = workloads.ragged(n_layers=L, extra_requests=0, spare_rows=spare)
     try:
         s0 = dict(wl.cache.stats())
         wl.step()
@@ -316,11 +324,10 @@ def test_ragged_batch_recycling_on_gpu():
         off = [r for r in range(R) if wl.placements[r] != Q.KV_HBM]
         assert hbm and off
         for r in hbm[:2] + off[:2]:
-            QC.check_unit(wl, 1, r)
+            QC.check_unit(wl, 11, r)
         rng = np.random.default_rng(3)
         done = [int(x) for x in rng.choice(R, 16, replace=False)]
         old = [wl.handles[r] for r in done]
-        new_ctx = synth.log_uniform_contexts(16, 4096, 262144, seed=77)
         for j, r in enumerate(done):
             n = new_ctx[j]
             h = wl.reissue(r, n, Q.KV_HBM if n < 32768 else Q.KV_HOST_RING, seed=500 + j)
@@ -332,8 +339,8 @@ def test_ragged_batch_recycling_on_gpu():
         wl.step()
         torch.cuda.synchronize()
         _clean(wl)
-        for r in done[:4]:
-            QC.check_unit(wl, 0, r)
+        for i, r in enumerate(done[:4]):
+            QC.check_unit(wl, 3 * i, r)
         for h in wl.handles:
             wl.cache.request_end(h)
         s_end = wl.cache.stats()

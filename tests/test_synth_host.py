@@ -82,3 +82,14 @@ def test_ragged_contexts_are_log_uniform_multiples():
     assert all(c % 4 == 0 and 4096 <= c <= 262144 for c in ctx)
     assert min(ctx) < 16384 and max(ctx) > 65536   # spread over the decades, not clustered
     assert ctx == [int(c) for c in synth.log_uniform_contexts(64, 4096, 262144, seed=5)]
+
+
+def test_skewed_index_query_spans_the_stated_range():
+    q, w = synth.index_query_skewed(seed=5)
+    a = q.abs().double()
+    assert q.shape == (8, 64) and w.shape == (8,)
+    assert float(a.max()) <= 1.0 and float(a.min()) >= 2.0 ** -12
+    assert float(a.max()) > 0.5 and float(a.min()) < 2.0 ** -11      # both ends reached
+    assert 0.3 < float((q > 0).double().mean()) < 0.7                 # random signs
+    q2, _ = synth.index_query_skewed(seed=5)
+    assert torch.equal(q, q2)
