@@ -73,7 +73,7 @@
 extern "C" {
 #endif
 
-#define QSA_ABI_VERSION 3
+#define QSA_ABI_VERSION 4
 
 #define QSA_INDEX_HEADS 8
 #define QSA_INDEX_DIM 64
@@ -167,9 +167,11 @@ typedef struct qsa_request_desc {
    * request leases n_layers * M pool rows, and a host history is laid out
    * [n_layers][M][R]. */
   int32_t max_ctx;
-  /* QSA_KV_HOST_RING, QSA_KV_HOST: pinned host memory [n_layers][M][R]
-   * holding the full history (host address; the library maps it for the
-   * device, and qsa_append_token writes the rows of new tokens into it).
+  /* QSA_KV_HOST_RING, QSA_KV_HOST: host memory [n_layers][M][R] holding the
+   * full history: memory from qsa_host_alloc for this cache's device, or
+   * pinned memory registered or allocated with the CUDA runtime's mapped
+   * flag (host address; the library finds the device address, and
+   * qsa_append_token writes the rows of new tokens into it).
    * QSA_KV_HBM: NULL. */
   const void* host_rows;
 } qsa_request_desc;
@@ -428,6 +430,30 @@ qsa_status_t qsa_sparse_decode_attn(qsa_cache* cache, const qsa_batch* batch,
                                     const int32_t* n_sel, int32_t budget_tokens,
                                     const void* gathered, float softmax_scale,
                                     float* out, float* lse, void* stream);
+
+/* -------------------------------------------------- host history memory */
+
+/* Host memory for the history of offloaded requests, laid out for the device
+ * to read selected rows from it: physical pages on host NUMA node numa_node
+ * (-1: the node the driver reports as closest to `device`), created and
+ * mapped with the driver's virtual-memory API in 2 MiB pieces into one
+ * virtual range that the device's own page tables and the host's page
+ * tables both hold, at the same address.  Pages that are only registered
+ * with cudaHostRegister are reached, on an NVLink-C2C system, through the
+ * CPU's page tables one 64 KiB page at a time.  bytes is rounded up to
+ * 2 MiB.  Pass the address as qsa_request_desc.host_rows of a cache whose
+ * storage is on `device`; the host reads and writes the memory like any
+ * other.  Free it with qsa_host_free once no request uses it.
+ * [RTX4090 port, memory-ledger section: the full history stays in pinned
+ * host memory, missing blocks come back to the GPU on demand.]
+ * Errors: INVALID_ARG (null out, bytes <= 0, bad device), CAPACITY (no
+ * room on the node), CUDA (no virtual-memory API or host NUMA memory). */
+qsa_status_t qsa_host_alloc(int32_t device, int32_t numa_node, int64_t bytes, void** out);
+
+/* Unmap and free memory from qsa_host_alloc (NULL: nothing to do).  No
+ * request may still use it and no work reading it may be in flight.
+ * Errors: INVALID_ARG (not an address qsa_host_alloc returned), CUDA. */
+qsa_status_t qsa_host_free(void* ptr);
 
 /* ------------------------------------------- no-allocation variant */
 

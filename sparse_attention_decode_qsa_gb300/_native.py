@@ -114,6 +114,8 @@ SIGNATURES = {
     "qsa_sparse_decode_attn": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p,
                                          C.c_void_p, C.c_int32, C.c_void_p, C.c_float,
                                          C.c_void_p, C.c_void_p, C.c_void_p]),
+    "qsa_host_alloc": (C.c_int, [C.c_int32, C.c_int32, C.c_int64, C.POINTER(C.c_void_p)]),
+    "qsa_host_free": (C.c_int, [C.c_void_p]),
     "qsa_sparse_decode_attn_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32,
                                                  C.c_int32, C.c_float, C.c_void_p, C.c_void_p,
                                                  C.c_void_p]),

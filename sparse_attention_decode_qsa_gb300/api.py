@@ -36,6 +36,57 @@ def _batch(handles, layer0: int, n_layers: int):
     return b
 
 
+class HostMemory:
+    """Host memory from qsa_host_alloc: pages on a host NUMA node, mapped into
+    the device's page tables and the host's at one address.  Pass
+    .cpu(shape) as a request's host_rows; .cuda(shape) is a view of the same
+    bytes for device-side copies.  Freed by free() (or when collected)."""
+
+    def __init__(self, nbytes: int, device: int = 0, numa_node: int = -1):
+        self.L = N.lib()
+        out = C.c_void_p()
+        check(self.L.qsa_host_alloc(int(device), int(numa_node), int(nbytes), C.byref(out)),
+              "qsa_host_alloc")
+        self.ptr, self.nbytes, self.device = out.value, int(nbytes), int(device)
+
+    def cpu(self, shape) -> torch.Tensor:
+        import numpy as np
+        n = 1
+        for x in shape:
+            n *= int(x)
+        if n > self.nbytes:
+            raise ValueError("view larger than the allocation")
+        arr = np.ctypeslib.as_array((C.c_uint8 * n).from_address(self.ptr)).reshape(tuple(shape))
+        t = torch.from_numpy(arr)
+        t._qsa_host_memory = self          # the view keeps the allocation alive
+        return t
+
+    def cuda(self, shape) -> torch.Tensor:
+        n = 1
+        for x in shape:
+            n *= int(x)
+        if n > self.nbytes:
+            raise ValueError("view larger than the allocation")
+
+        class _View:
+            __cuda_array_interface__ = {"shape": tuple(int(x) for x in shape), "typestr": "|u1",
+                                        "data": (self.ptr, False), "version": 3, "strides": None}
+        t = torch.as_tensor(_View(), device=torch.device("cuda", self.device))
+        t._qsa_host_memory = self
+        return t
+
+    def free(self):
+        if getattr(self, "ptr", None):
+            check(self.L.qsa_host_free(self.ptr), "qsa_host_free")
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
 class Cache:
     """A qsa_cache plus the device storage it runs on.
 

@@ -593,6 +593,7 @@ index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
 
   tc_fence_before();
   __syncthreads();
+  trigger_dependents();
   tc_fence_after();
   if (warp == kRoleMma)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot),

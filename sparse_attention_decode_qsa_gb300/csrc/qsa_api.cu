@@ -129,32 +129,6 @@ cudaError_t qsa::current_sm_count(int* out) {
   return cudaSuccess;
 }
 
-namespace {
-
-// Makes `dev` the calling thread's current device for the lifetime of the
-// guard and restores the previous one afterwards (dev < 0: no change).
-class DeviceGuard {
- public:
-  explicit DeviceGuard(int dev) {
-    if (dev < 0) return;
-    status_ = cudaGetDevice(&prev_);
-    if (status_ == cudaSuccess && prev_ != dev) {
-      status_ = cudaSetDevice(dev);
-      switched_ = status_ == cudaSuccess;
-    }
-  }
-  ~DeviceGuard() {
-    if (switched_) cudaSetDevice(prev_);
-  }
-  cudaError_t status() const { return status_; }
-
- private:
-  int prev_ = 0;
-  bool switched_ = false;
-  cudaError_t status_ = cudaSuccess;
-};
-
-}  // namespace
 
 qsa_status_t qsa::set_last_error(qsa_status_t status, const char* message) {
   g_last_error = message ? message : "";
@@ -429,14 +403,20 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
   const uint8_t* host_dev = nullptr;
   if (desc->placement != QSA_KV_HBM) {
     if (c->has_device) {
-      void* dptr = nullptr;
-      cudaError_t e = cudaHostGetDevicePointer(&dptr, const_cast<void*>(desc->host_rows), 0);
-      if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(QSA_ERR_INVALID_ARG, "host_rows is not pinned, mapped host memory: %s",
-                    cudaGetErrorString(e));
+      const int64_t need = (int64_t)c->cfg.n_layers * max_ctx * c->row_bytes();
+      if (host_alloc_covers(desc->host_rows, need, c->device)) {
+        host_dev = static_cast<const uint8_t*>(desc->host_rows);   // same address on the device
+      } else {
+        void* dptr = nullptr;
+        cudaError_t e = cudaHostGetDevicePointer(&dptr, const_cast<void*>(desc->host_rows), 0);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          return fail(QSA_ERR_INVALID_ARG,
+                      "host_rows is neither qsa_host_alloc memory nor pinned, mapped host memory: %s",
+                      cudaGetErrorString(e));
+        }
+        host_dev = static_cast<const uint8_t*>(dptr);
       }
-      host_dev = static_cast<const uint8_t*>(dptr);
     } else {
       host_dev = static_cast<const uint8_t*>(desc->host_rows);
     }

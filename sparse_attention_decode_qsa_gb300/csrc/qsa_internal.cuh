@@ -129,6 +129,16 @@ __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Lets the next kernel on the stream start launching once every CTA of this
+// one has passed this point (its grid_dependency_wait() still waits for this
+// kernel's completion).  Called where a CTA's main work ends, when
+// QSA_PDL_TRIGGER is set.
+__device__ __forceinline__ void trigger_dependents() {
+#if defined(QSA_PDL_TRIGGER) && QSA_PDL_TRIGGER
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
 // Launch `kernel` on stream s with programmatic stream serialization, an
 // optional launch priority (0: the stream's) and optional cluster dims.
 template <class... KArgs, class... Args>
@@ -192,6 +202,35 @@ class PerDeviceOnce {
 // SM count of the device current on the calling thread (queried once per
 // device).
 cudaError_t current_sm_count(int* out);
+
+// Makes `dev` the calling thread's current device for the lifetime of the
+// guard and restores the previous one afterwards (dev < 0: no change).
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    if (dev < 0) return;
+    status_ = cudaGetDevice(&prev_);
+    if (status_ == cudaSuccess && prev_ != dev) {
+      status_ = cudaSetDevice(dev);
+      switched_ = status_ == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (switched_) cudaSetDevice(prev_);
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+  cudaError_t status() const { return status_; }
+
+ private:
+  int prev_ = 0;
+  bool switched_ = false;
+  cudaError_t status_ = cudaSuccess;
+};
+
+// Whether [p, p + bytes) lies inside host memory from qsa_host_alloc mapped
+// for `device` (such memory is used by the device at its host address).
+bool host_alloc_covers(const void* p, int64_t bytes, int device);
 
 // Highest launch priority of the device (numerically lowest), for the
 // attention launches: their CTAs are dispatched ahead of queued scoring CTAs

@@ -7,14 +7,15 @@
 // rows.  Rows are read through the slot table (pool rows from HBM, cold rows
 // zero-copy from mapped pinned host memory) or from a dense gathered buffer.
 //
-// Work layout: `cpu` CTAs per unit; CTA (unit u, slot r) takes the splits
-// r, r + cpu, r + 2*cpu, ... of unit u and visits them alternately from the
-// front and the back of that list.  Selected blocks are in ascending id order,
-// so for a request with an HBM tail ring the early splits are cold (host) and
-// the late ones hot (HBM): the alternation overlaps host transfers with
-// compute.  When some row comes from host memory the grid is capped at
-// kMaxCtasHost CTAs: that many SMs saturate the host link, and the others
-// stay free for HBM-bound work of other requests on other streams.
+// Work layout: unit u gets cpu_u CTAs (cta_start holds their prefix sums);
+// CTA (unit u, slot r) takes the splits r, r + cpu_u, r + 2*cpu_u, ... of
+// unit u and visits them alternately from the front and the back of that
+// list.  Selected blocks are in ascending id order, so for a request with an
+// HBM tail ring the early splits are cold (host) and the late ones hot (HBM):
+// the alternation overlaps host transfers with compute.  The units that read
+// host memory share kMaxCtasHost CTAs: that many SMs saturate the host link,
+// and the others stay free for HBM-bound work of other requests on other
+// streams.  Units that read only HBM share the rest of the SMs.
 //
 // Inside a CTA the 8 warps work independently: warp w serves KV head
 // g = w % 4 (its 4 query heads) for tokens 8*(w/4) .. 8*(w/4)+7 of every
@@ -74,7 +75,7 @@ struct AttnParams {
   const int32_t* n_sel;
   int32_t k_max;
   int32_t budget_tokens;
-  int32_t cpu;              // CTAs (partials) per unit
+  int32_t cta_start[kMaxUnits + 1];  // prefix sums of the CTAs (partials) per unit
   const uint8_t* gathered;  // [units][budget_tokens][2048] or nullptr
   float scale_log2;         // softmax_scale * log2(e)
   float* out;               // [units][16][128]
@@ -98,6 +99,18 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint32_
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Unit u of CTA `cta`, its slot r among the unit's CTAs and their number cpu.
+__device__ __forceinline__ void cta_unit(const AttnParams& p, int cta, int& u, int& r, int& cpu) {
+  int lo = 0, hi = p.b.n_units - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cta_start[mid] <= cta) lo = mid; else hi = mid - 1;
+  }
+  u = lo;
+  r = cta - p.cta_start[lo];
+  cpu = p.cta_start[lo + 1] - p.cta_start[lo];
+}
 
 // The k-th split this CTA visits (0 <= k < count): alternately from the front
 // and the back of its list r, r + cpu, ...
@@ -185,7 +198,8 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   __shared__ uint32_t vmask[kWarps][kAStages];     // tokens present in each stage
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
-  const int u = blockIdx.x / p.cpu, r = blockIdx.x % p.cpu;
+  int u, r, cpu;
+  cta_unit(p, blockIdx.x, u, r, cpu);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = warp & 3, half = warp >> 2;
   uint8_t* wbuf = smem + warp * kAStages * kWarpBufBytes;
@@ -195,7 +209,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
     nsel = 0;
   }
   const int splits = (nsel + kBlocksPerSplit - 1) / kBlocksPerSplit;
-  const int count = r < splits ? (splits - 1 - r) / p.cpu + 1 : 0;
+  const int count = r < splits ? (splits - 1 - r) / cpu + 1 : 0;
 
   // query dims 4l..4l+3 of the 4 heads of KV head g, pre-scaled to base 2
   float qr[kGroup][4];
@@ -220,7 +234,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
 #pragma unroll
   for (int k = 0; k < kAStages - 1; ++k) {
     if (k < count) {
-      const uint32_t v = issue_warp(p, u, visit_split(k, count, r, p.cpu), nsel, g, half,
+      const uint32_t v = issue_warp(p, u, visit_split(k, count, r, cpu), nsel, g, half,
                                     wbuf + k * kWarpBufBytes);
       if (lane == 0) vmask[warp][k] = v;
     }
@@ -229,7 +243,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   for (int k = 0; k < count; ++k) {
     const int kn = k + kAStages - 1;
     if (kn < count) {   // its buffer was last read in iteration k - 1
-      const uint32_t v = issue_warp(p, u, visit_split(kn, count, r, p.cpu), nsel, g, half,
+      const uint32_t v = issue_warp(p, u, visit_split(kn, count, r, cpu), nsel, g, half,
                                     wbuf + (kn % kAStages) * kWarpBufBytes);
       if (lane == 0) vmask[warp][kn % kAStages] = v;
     }
@@ -303,6 +317,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   asm volatile("cp.async.wait_all;" ::: "memory");
 
   finish_split(p, u, r, g, half, lane, hj, m_run, l_run, acc, xm, xl, xacc);
+  trigger_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -382,7 +397,8 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   __shared__ uint32_t vmask[kWarps][kAStagesFp8];
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
-  const int u = blockIdx.x / p.cpu, r = blockIdx.x % p.cpu;
+  int u, r, cpu;
+  cta_unit(p, blockIdx.x, u, r, cpu);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = warp & 3, half = warp >> 2;
   uint8_t* wbuf = smem + warp * kAStagesFp8 * kWarpBufFp8;
@@ -392,7 +408,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
     nsel = 0;
   }
   const int splits = (nsel + kBlocksPerSplit - 1) / kBlocksPerSplit;
-  const int count = r < splits ? (splits - 1 - r) / p.cpu + 1 : 0;
+  const int count = r < splits ? (splits - 1 - r) / cpu + 1 : 0;
 
   float qr[kGroup][4];
   {
@@ -415,7 +431,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
 #pragma unroll
   for (int k = 0; k < kAStagesFp8 - 1; ++k) {
     if (k < count) {
-      const uint32_t v = issue_warp_fp8(p, u, visit_split(k, count, r, p.cpu), nsel, g, half,
+      const uint32_t v = issue_warp_fp8(p, u, visit_split(k, count, r, cpu), nsel, g, half,
                                         wbuf + k * kWarpBufFp8);
       if (lane == 0) vmask[warp][k] = v;
     }
@@ -424,7 +440,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   for (int k = 0; k < count; ++k) {
     const int kn = k + kAStagesFp8 - 1;
     if (kn < count) {
-      const uint32_t v = issue_warp_fp8(p, u, visit_split(kn, count, r, p.cpu), nsel, g, half,
+      const uint32_t v = issue_warp_fp8(p, u, visit_split(kn, count, r, cpu), nsel, g, half,
                                         wbuf + (kn % kAStagesFp8) * kWarpBufFp8);
       if (lane == 0) vmask[warp][kn % kAStagesFp8] = v;
     }
@@ -497,18 +513,21 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   finish_split(p, u, r, g, half, lane, hj, m_run, l_run, acc, xm, xl, xacc);
+  trigger_dependents();
 }
 
 // Merge: CTA (head, unit), thread = output dim; reads the cpu partials.
 __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const AttnParams p) {
   grid_dependency_wait();
+  trigger_dependents();
   const int h = blockIdx.x, u = blockIdx.y, d = threadIdx.x;
+  const int cpu = p.cta_start[u + 1] - p.cta_start[u];
   float Mx = -INFINITY;
-  for (int s = 0; s < p.cpu; ++s) Mx = fmaxf(Mx, partial_ptr(p.b, u, s)[h]);
+  for (int s = 0; s < cpu; ++s) Mx = fmaxf(Mx, partial_ptr(p.b, u, s)[h]);
   float Lt = 0.f, acc = 0.f;
   if (Mx != -INFINITY) {
 #pragma unroll 4
-    for (int s = 0; s < p.cpu; ++s) {
+    for (int s = 0; s < cpu; ++s) {
       const float* part = partial_ptr(p.b, u, s);
       const float ms = part[h], ls = part[kQHeads + h], as = part[2 * kQHeads + h * kHeadDim + d];
       const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - Mx);
@@ -551,22 +570,32 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
   p.scale_log2 = softmax_scale * kLog2e;
   p.out = out;
   p.lse = lse;
-  // units with hot rows read HBM only once qsa_hot_cache_fetch has run
-  bool any_host = false;
-  if (gathered == nullptr)
-    for (int u = 0; u < b.n_units; ++u) any_host |= b.u[u].host_rows != nullptr && b.u[u].hot_base < 0;
+  // Units that read host memory (units with hot rows read HBM only once
+  // qsa_hot_cache_fetch has run) share the host cap; the others share the
+  // remaining SMs.  A unit never gets more CTAs than splits or than the
+  // workspace's partial slots.
   const int splits = (p.k_max + kBlocksPerSplit - 1) / kBlocksPerSplit;
   const bool fp8 = b.row_bytes == kRowBytesFp8;
-  const int cap = any_host ? (fp8 ? kMaxCtasHostFp8 : kMaxCtasHost) : sm_count;
-  int cpu = cap / b.n_units;
-  if (cpu < 1) cpu = 1;
-  if (cpu > splits) cpu = splits;
-  if (cpu > b.splits_max) cpu = b.splits_max;   // partial slots in the workspace
-  p.cpu = cpu;
+  const int host_cap = fp8 ? kMaxCtasHostFp8 : kMaxCtasHost;
+  int n_host = 0;
+  for (int u = 0; u < b.n_units; ++u)
+    n_host += gathered == nullptr && b.u[u].host_rows != nullptr && b.u[u].hot_base < 0;
+  const int n_hbm = b.n_units - n_host;
+  int cpu_max = splits < b.splits_max ? splits : b.splits_max;
+  if (cpu_max < 1) cpu_max = 1;
+  auto clamp = [&](int c) { return c < 1 ? 1 : (c > cpu_max ? cpu_max : c); };
+  const int cpu_host = n_host ? clamp(host_cap / n_host) : 0;
+  const int cpu_hbm = n_hbm ? clamp((sm_count - n_host * cpu_host) / n_hbm) : 0;
+  int total = 0;
+  for (int u = 0; u < b.n_units; ++u) {
+    p.cta_start[u] = total;
+    total += gathered == nullptr && b.u[u].host_rows != nullptr && b.u[u].hot_base < 0 ? cpu_host : cpu_hbm;
+  }
+  p.cta_start[b.n_units] = total;
   const int prio = highest_priority();
-  cudaError_t e = fp8 ? launch_kernel(attn_split_fp8_kernel, dim3(b.n_units * cpu), dim3(kThreads), kSmemFp8,
+  cudaError_t e = fp8 ? launch_kernel(attn_split_fp8_kernel, dim3(total), dim3(kThreads), kSmemFp8,
                                       s, prio, dim3(1), p)
-                      : launch_kernel(attn_split_kernel, dim3(b.n_units * cpu), dim3(kThreads), kSmemBytes,
+                      : launch_kernel(attn_split_kernel, dim3(total), dim3(kThreads), kSmemBytes,
                                       s, prio, dim3(1), p);
   if (e != cudaSuccess) return e;
   return launch_kernel(attn_merge_kernel, dim3(kQHeads, b.n_units), dim3(kHeadDim), 0, s, prio, dim3(1), p);

@@ -25,7 +25,14 @@ import torch
 
 from . import _native as N
 from . import synth
-from .api import Cache
+from .api import Cache, HostMemory
+
+# Host memory for the histories of offloaded requests:
+#   "vmm"         qsa_host_alloc: pages on the GPU's host NUMA node, in the
+#                 GPU's own page tables (2 MiB entries)
+#   "registered"  ordinary pages page-locked with cudaHostRegister
+HOST_MEMORY_KINDS = ("vmm", "registered")
+DEFAULT_HOST_MEMORY = "registered"
 
 
 def register_pinned(t: torch.Tensor):
@@ -38,6 +45,35 @@ def register_pinned(t: torch.Tensor):
 
 def unregister_pinned(t: torch.Tensor):
     torch.cuda.cudart().cudaHostUnregister(t.data_ptr())
+
+
+def alloc_host(shape, device, kind: str = None) -> torch.Tensor:
+    """A uint8 CPU tensor of `shape` in host memory the GPU reads directly."""
+    kind = kind or DEFAULT_HOST_MEMORY
+    if kind not in HOST_MEMORY_KINDS:
+        raise ValueError(f"unknown host memory kind {kind}")
+    if kind == "registered":
+        return register_pinned(torch.empty(tuple(shape), dtype=torch.uint8))
+    n = 1
+    for x in shape:
+        n *= int(x)
+    dev = torch.device(device)
+    return HostMemory(n, device=dev.index if dev.index is not None else torch.cuda.current_device()).cpu(shape)
+
+
+def free_host(t: torch.Tensor):
+    m = getattr(t, "_qsa_host_memory", None)
+    if m is not None:
+        m.free()
+    else:
+        unregister_pinned(t)
+
+
+def device_view(t: torch.Tensor) -> torch.Tensor:
+    """A tensor the GPU's copy kernels can write into: the CUDA view of
+    qsa_host_alloc memory, else the pinned CPU tensor itself."""
+    m = getattr(t, "_qsa_host_memory", None)
+    return m.cuda(t.shape) if m is not None else t
 
 
 @dataclass
@@ -61,6 +97,7 @@ class Workload:
     softmax_scale: float = 1.0 / math.sqrt(128)
     seeds: dict = field(default_factory=dict)
     planting: object = None
+    host_memory: str = None
 
     @property
     def n_req(self):
@@ -78,10 +115,11 @@ class Workload:
         self.cache.request_end(self.handles[r])
         old = self.host[r]
         if old is not None and (placement == N.KV_HBM or old.shape[1] != n):
-            unregister_pinned(old)
+            free_host(old)
             old = None
         if placement != N.KV_HBM and old is None:
-            old = register_pinned(torch.empty(self.n_layers, n, self.cache.row_bytes, dtype=torch.uint8))
+            old = alloc_host((self.n_layers, n, self.cache.row_bytes), self.cache.pool.device,
+                             self.host_memory)
         self.host[r] = old
         self.ctxs[r], self.placements[r] = n, placement
         self.handles[r] = self.cache.request_begin(n, placement, host_rows=old)
@@ -112,7 +150,7 @@ class Workload:
     def close(self):
         for h in self.host:
             if h is not None:
-                unregister_pinned(h)
+                free_host(h)
         self.host = []
         self.cache.close()
 
@@ -236,7 +274,7 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
             b0 = info.hbm_row_base + l * stride
             cache.pool[b0:b0 + n] = rows
         else:
-            wl.host[r][l, :n].copy_(rows)
+            device_view(wl.host[r])[l, :n].copy_(rows)
             if p == N.KV_HOST_RING:
                 t = torch.arange(max(0, n - ring), n, device=dev)
                 cache.pool[info.hbm_row_base + l * ring + (t % ring)] = rows[t]
@@ -247,10 +285,13 @@ def _fill_request(wl: "Workload", r: int, seed: int, planting):
 def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: int = 4096,
           staging_rows: int = 2048, seed: int = 0, device="cuda", extra_requests: int = 0,
           spare_rows: int = 0, ctx_capacity: int | None = None, grow: int = 0,
-          kv_format: int = N.KV_BF16, hot_rows: int = 0) -> Workload:
+          kv_format: int = N.KV_BF16, hot_rows: int = 0, host_memory: str | None = None) -> Workload:
     """planting(l, r, n) -> block ids to plant for unit (l, r).  grow: tokens
     every request may still append (its max_ctx is ctx + grow).  hot_rows:
-    cross-step hot-cache rows per offloaded request and layer (0: none)."""
+    cross-step hot-cache rows per offloaded request and layer (0: none).
+    host_memory: kind of the offloaded histories' host memory (see
+    HOST_MEMORY_KINDS; None: DEFAULT_HOST_MEMORY)."""
+    host_memory = host_memory or DEFAULT_HOST_MEMORY
     ctx_capacity = ctx_capacity or (max(ctxs) + grow)
     dev = torch.device(device)
     R = len(ctxs)
@@ -266,7 +307,7 @@ def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: i
     for r, (n, p) in enumerate(zip(ctxs, placements)):
         hrows = None
         if p != N.KV_HBM:
-            hrows = register_pinned(torch.empty(n_layers, n + grow, cache.row_bytes, dtype=torch.uint8))
+            hrows = alloc_host((n_layers, n + grow, cache.row_bytes), dev, host_memory)
         host.append(hrows)
         handles.append(cache.request_begin(n, p, host_rows=hrows, max_ctx=n + grow if grow else 0))
     U = n_layers * R
@@ -276,6 +317,7 @@ def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: i
                   torch.empty(U, 16, 128, dtype=torch.bfloat16, device=dev),
                   [[None] * R for _ in range(n_layers)], budget)
     wl.planting = planting
+    wl.host_memory = host_memory
     for r in range(R):
         _fill_request(wl, r, seed, planting)
     blk_stride = (ctx_capacity + 3) // 4
@@ -319,7 +361,7 @@ def with_hot_rows(wl: Workload, hot_rows: int) -> Workload:
     new = Workload(cache, handles, wl.n_layers, list(wl.ctxs), list(wl.placements), wl.host,
                    wl.q_idx, wl.w, wl.q, wl.planted, wl.budget, blk=wl.blk, sel=wl.sel,
                    nsel=wl.nsel, out=wl.out, lse=wl.lse, softmax_scale=wl.softmax_scale,
-                   seeds=dict(wl.seeds), planting=wl.planting)
+                   seeds=dict(wl.seeds), planting=wl.planting, host_memory=wl.host_memory)
     wl.host = []
     old.close()
     return new
@@ -340,25 +382,26 @@ def c128k(device="cuda", seed=1, n_layers=12):
                  staging_rows=64, seed=seed, device=device)
 
 
-def c256k_x8(device="cuda", seed=2, n_layers=12, n_req=8, n=262144, kv_format=N.KV_BF16):
+def c256k_x8(device="cuda", seed=2, n_layers=12, n_req=8, n=262144, kv_format=N.KV_BF16,
+             host_memory=None):
     return build(n_layers, [n] * n_req, [N.KV_HOST_RING] * n_req,
                  lambda l, r, n: synth.planted_hot_cold(n // 4, 512, 4096 // 4,
                                                         synth.mix_seed(seed, 90, l, r)),
-                 seed=seed, device=device, kv_format=kv_format)
+                 seed=seed, device=device, kv_format=kv_format, host_memory=host_memory)
 
 
-def c1m_x4(device="cuda", seed=3, n_layers=12, n_req=4, n=1048576):
+def c1m_x4(device="cuda", seed=3, n_layers=12, n_req=4, n=1048576, host_memory=None):
     return build(n_layers, [n] * n_req, [N.KV_HOST] * n_req,
                  lambda l, r, n: synth.planted_zipf_sinks(n // 4, 512, synth.mix_seed(seed, 90, l, r)),
-                 staging_rows=64, seed=seed, device=device)
+                 staging_rows=64, seed=seed, device=device, host_memory=host_memory)
 
 
 def ragged(device="cuda", seed=4, n_layers=12, n_req=64, lo=4096, hi=262144, extra_requests=16,
-           spare_rows=0):
+           spare_rows=0, host_memory=None):
     ctxs = synth.log_uniform_contexts(n_req, lo, hi, synth.mix_seed(seed, 80))
     pl = [N.KV_HBM if n < 32768 else N.KV_HOST_RING for n in ctxs]
     return build(n_layers, ctxs, pl,
                  lambda l, r, n: synth.planted_hot_cold(n // 4, min(512, n // 4), 1024,
                                                         synth.mix_seed(seed, 90, l, r)),
                  seed=seed, device=device, extra_requests=extra_requests, spare_rows=spare_rows,
-                 ctx_capacity=hi)
+                 ctx_capacity=hi, host_memory=host_memory)

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol():
     for name in sorted(declared):
         assert hasattr(L, name), f"{name} declared in include/ but not exported"
         assert name in N.SIGNATURES, f"{name} has no Python binding"
-    assert L.qsa_abi_version() == 3
+    assert L.qsa_abi_version() == 4
 
 
 def _host_cache(**kw):

@@ -112,12 +112,18 @@ def test_topk_bit_exact_on_any_fp32_scores():
             v = np.round(rng.standard_normal(nb) * 4).astype(np.float32) / 8   # coarse ties
         ctxs.append(n)
         rows.append(v)
+    # a call's largest unit sets the keys each cluster CTA holds: once with
+    # the 1M-token unit (32768 keys per CTA), once without it (8192); heavy
+    # ties also push some units onto the general path (boundary bin larger
+    # than the candidate buffer)
+    small = [i for i, n in enumerate(ctxs) if n <= 262144]
     for budget in (4, 2048, 8192):
-        sel, nsel = _run_select(rows, ctxs, budget)
-        for i, v in enumerate(rows):
-            ref = O.select_blocks(v.astype(np.float64), budget)
-            assert int(nsel[i]) == len(ref)
-            assert np.array_equal(sel[i, :len(ref)], ref), (ctxs[i], budget)
+        for pick in (list(range(len(ctxs))), small):
+            sel, nsel = _run_select([rows[i] for i in pick], [ctxs[i] for i in pick], budget)
+            for j, i in enumerate(pick):
+                ref = O.select_blocks(rows[i].astype(np.float64), budget)
+                assert int(nsel[j]) == len(ref)
+                assert np.array_equal(sel[j, :len(ref)], ref), (ctxs[i], budget, len(pick))
 
 
 def _host_ring_workload(n_req=2, n_layers=2, n=20000, seed=5):
@@ -422,3 +428,27 @@ def test_index_score_work_counter_rearms_and_is_per_first_unit():
             QC.check_unit(wl, l, 3)
     finally:
         wl.close()
+
+
+def test_host_ring_on_host_numa_memory():
+    """Host histories in qsa_host_alloc memory (host NUMA pages in the GPU's
+    page tables): the decode step reads its cold rows there and matches the
+    oracle, which reads the same bytes through the host mapping; freeing the
+    memory of an ended request is accepted, a foreign pointer is refused."""
+    wl = workloads.build(2, [20000] * 2, [Q.KV_HOST_RING] * 2,
+                         lambda l, r, n: synth.planted_hot_cold(n // 4, 512, 1024,
+                                                                synth.mix_seed(13, 90, l, r)),
+                         seed=13, host_memory="vmm")
+    try:
+        assert getattr(wl.host[0], "_qsa_host_memory", None) is not None
+        wl.step()
+        torch.cuda.synchronize()
+        _clean(wl)
+        for l in range(2):
+            for r in range(2):
+                res = QC.check_unit(wl, l, r)
+                assert (res["ref"]["slot"][res["ref"]["tokens"]] == -1).any()   # some rows from host
+    finally:
+        wl.close()
+    L = Q.lib()
+    assert L.qsa_host_free(12345 * 4096) == Q.ERR_INVALID_ARG
