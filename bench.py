@@ -269,9 +269,7 @@ def fp8_timing(dev, args):
         torch.cuda.synchronize(dev)
         attn_us = e0.elapsed_time(e1) * 1e3 / (args.steps * N_LAYERS)
         st, det = c.poll_error()
-        if st != 0:
-            raise RuntimeError(f"device error word {st} ({det}) in the FP8 timing")
-        return step_ms, attn_us
+        return step_ms, attn_us, ({"status": st, "detail": det} if st else None)
     finally:
         wl.close()
 
@@ -418,8 +416,6 @@ def host_only_timing(dev, args, link_peak):
         del graph
         attn_us = _attn_launch_us(wl, dev, args)
         st, det = wl.cache.poll_error()
-        if st != 0:
-            raise RuntimeError(f"device error word {st} ({det}) in the host-only timing")
         step_s = statistics.mean(ms) / 1e3
         host_b, hbm_b = units * BUDGET * ROW, units * IDX_BYTES * n
         attn_host = R * BUDGET * ROW
@@ -435,6 +431,7 @@ def host_only_timing(dev, args, link_peak):
                 "hbm_gbs": round(hbm_b / step_s / 1e9, 1),
                 "hbm_frac": round(hbm_b / step_s / 1e9 / hbm_peak, 4),
                 "roofline_ms": round(max(host_b / (link_peak * 1e9), hbm_b / (hbm_peak * 1e9)) * 1e3, 4),
+                "device_error": {"status": st, "detail": det} if st else None,
                 "sparse_attn": {"units_per_launch": R, "host_bytes_per_launch": attn_host,
                                 "avg_launch_us": round(attn_us, 2),
                                 "achieved": round(attn_host / (attn_us * 1e-6) / 1e9, 1),
@@ -468,8 +465,6 @@ def ragged_timing(dev, args, link_peak):
             ms = _replay_ms(g, dev, args)
             del g
             st, det = c.poll_error()
-            if st != 0:
-                raise RuntimeError(f"device error word {st} ({det}) in the ragged timing")
             ctx = list(wl.ctxs)
             off = [r for r in range(R) if wl.placements[r] != Q.KV_HBM]
             host_rows = sum(L * BUDGET // 2 for r in off)      # half of an offloaded unit's rows are cold
@@ -479,6 +474,7 @@ def ragged_timing(dev, args, link_peak):
             return {"ms_per_step": round(step_s * 1e3, 4),
                     "step_ms_p10_p50_p90": [round(_pct(ms, q), 4) for q in (0.1, 0.5, 0.9)],
                     "layer_steps_per_s": round(units / step_s, 1),
+                    "device_error": {"status": st, "detail": det} if st else None,
                     "requests_hbm": R - len(off), "requests_offloaded": len(off),
                     "tokens_total": sum(ctx),
                     "host_gbs": round(host_rows * ROW / step_s / 1e9, 1),
@@ -557,39 +553,66 @@ def _drift_levels(wl, graph, dev, args, churns, seed):
             torch.cuda.synchronize(dev)
             total_ms += e0.elapsed_time(e1)
         st, det = wl.cache.poll_error()
-        if st != 0:
-            raise RuntimeError(f"device error word {st} ({det}) in the drift timing")
         step_s = total_ms / 1e3 / args.steps
-        levels.append({"churn": f, "ms_per_step": round(step_s * 1e3, 4),
-                       "layer_steps_per_s": round(units / step_s, 1),
-                       "host_rows_per_step": round(cold / args.steps, 1),
-                       "host_gbs": round(cold / args.steps * ROW / step_s / 1e9, 1)})
+        lv = {"churn": f, "ms_per_step": round(step_s * 1e3, 4),
+              "layer_steps_per_s": round(units / step_s, 1),
+              "host_rows_per_step": round(cold / args.steps, 1),
+              "host_gbs": round(cold / args.steps * ROW / step_s / 1e9, 1)}
+        if st != 0:       # recorded, not raised: a slow host-memory state can run out a bounded wait
+            lv["device_error"] = {"status": st, "detail": det}
+        levels.append(lv)
     return levels
 
 
 def drift_timing(wl, graph, dev, args, churns=(0.0, 0.1, 0.25, 1.0)):
     """The benchmark step when the selection drifts between steps (churn =
     fraction of each unit's cold planted blocks moved before each step; 1.0
-    makes every cold block new at every step), in two forms: the measured
-    step as it is (cold rows read zero-copy from pinned host memory every
-    step), and the same requests in a cache with BUDGET hot rows per request
-    and layer, whose step fetches the cold selected rows into them
-    (qsa_hot_cache_fetch) and reads only HBM in attention.  Consumes wl and
-    graph."""
+    makes every cold block new at every step), in four forms:
+      - the measured step as it is: cold rows read zero-copy every step from
+        the pinned (registered) host history;
+      - on host histories in host NUMA memory mapped into the GPU's page
+        tables (qsa_host_alloc): zero-copy; and in a cache with BUDGET hot
+        rows per request and layer, whose step copies the cold selected rows
+        into them first (qsa_hot_cache_fetch), or plans them and lets the
+        attention copy them as it reads them (qsa_hot_cache_plan).
+    Consumes wl and graph."""
     from sparse_attention_decode_qsa_gb300 import workloads
+
+    def hot_levels(w, fold, seed):
+        hw = workloads.with_hot_rows(w, BUDGET, fold_fill=fold)
+        try:
+            g = hw.capture(args.groups)
+            lv = _drift_levels(hw, g, dev, args, churns, seed)
+            del g
+        finally:
+            hw.close()
+        return lv
+
     zero_copy = _drift_levels(wl, graph, dev, args, churns, 77)
     del graph
-    hw = workloads.with_hot_rows(wl, BUDGET)
+    wl.close()
+    w3 = workloads.c256k_x8(device=dev, n_layers=args.layers, n_req=args.requests, host_memory="vmm")
     try:
-        g = hw.capture(args.groups)
-        hot = _drift_levels(hw, g, dev, args, churns, 78)
-        del g
-    finally:
-        hw.close()
+        g3 = w3.capture(args.groups)
+        vmm_zero_copy = _drift_levels(w3, g3, dev, args, churns, 80)
+        del g3
+    except Exception:
+        w3.close()
+        raise
+    vmm_fetch = hot_levels(w3, False, 81)           # consumes w3
+    w4 = workloads.c256k_x8(device=dev, n_layers=args.layers, n_req=args.requests, host_memory="vmm")
+    vmm_plan = hot_levels(w4, True, 82)
     return {"what": "steps whose selection drifts: churn = fraction of each unit's cold planted "
                     "blocks moved before each step; host_rows_per_step = selected rows cold at "
                     "the start of the step",
-            "zero_copy": zero_copy, "hot_cache": {"hot_rows": BUDGET, "levels": hot}}
+            "zero_copy": zero_copy,
+            "host_numa_memory": {"what": "host histories from qsa_host_alloc (host NUMA pages in "
+                                         "the GPU's page tables); the hot cache has BUDGET rows per "
+                                         "request and layer",
+                                 "hot_rows": BUDGET,
+                                 "zero_copy": vmm_zero_copy,
+                                 "hot_cache_fetch": vmm_fetch,
+                                 "hot_cache_plan_in_attention": vmm_plan}}
 
 
 def run_ours(args, rank, world):
@@ -703,7 +726,7 @@ def run_ours(args, rank, world):
     drift = drift_timing(wl, graph, dev, args)     # consumes wl and graph
     del graph, wl
     append_us = append_timing(dev)
-    fp8_step_ms, fp8_attn_us = fp8_timing(dev, args)
+    fp8_step_ms, fp8_attn_us, fp8_err = fp8_timing(dev, args)
     hbm_res = hbm_resident_timing(dev, args)
     link_copy = host_link_peak(dev)
     link_zc = zero_copy_peak(dev)
@@ -785,7 +808,8 @@ def run_ours(args, rank, world):
                            "scales per head); BF16 queries, fp32 outputs",
                    "ms_per_step": round(fp8_step_ms, 4),
                    "layer_steps_per_s": round(units / (fp8_step_ms / 1e3), 1),
-                   "host_gbs": round(units * (BUDGET // 2) * 1040 / (fp8_step_ms / 1e3) / 1e9, 1)},
+                   "host_gbs": round(units * (BUDGET // 2) * 1040 / (fp8_step_ms / 1e3) / 1e9, 1),
+                   "device_error": fp8_err},
         "gpu_launches": args.steps * L * args.groups * 4,
         "clocks": clk.summary,
         "e2e": {"value": round(units * world / (ms_e2e_max / 1e3 / args.steps), 1),

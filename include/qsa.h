@@ -221,7 +221,8 @@ const char* qsa_last_error_string(void);
  * split-K partials of every request x layer, two int32 work counters per
  * request x layer for qsa_index_score, and with hot_rows > 0 the hot-cache
  * state of every request x layer: a fill list of budget_tokens entries, its
- * length, the cursor and hot_rows owner entries).  Returns -1 on a bad
+ * length, the cursor, hot_rows owner entries, and the budget_tokens rows and
+ * the flag of qsa_hot_cache_plan's pending map).  Returns -1 on a bad
  * config. */
 int64_t qsa_workspace_bytes(const qsa_cache_config* config);
 
@@ -409,6 +410,23 @@ qsa_status_t qsa_hot_cache_fetch(qsa_cache* cache, const qsa_batch* batch,
                                  const int32_t* sel_blocks, const int32_t* n_sel,
                                  int32_t budget_tokens, void* stream);
 
+/* The plan of qsa_hot_cache_fetch without its copy: the same slot-table,
+ * owner and cursor updates (one launch, one CTA per unit), and a per-unit
+ * map from selected position to the hot row its miss was given.  The next
+ * qsa_sparse_decode_attn of those units (without `gathered`) reads the
+ * misses' rows from host memory, as a zero-copy read would, and writes them
+ * into their hot rows as it goes; afterwards the units are in the state
+ * qsa_hot_cache_fetch leaves.  Until that attention has run, the misses'
+ * hot rows hold stale bytes: no other call may read those units' rows
+ * (qsa_gather_rows, attention with `gathered`), and the pending map is
+ * replaced by the next plan or fetch of the unit.
+ * [RTX4090 port, memory-ledger section: missing blocks moved back on
+ * demand; here the move rides on the attention's own read.]
+ * Errors: as qsa_hot_cache_fetch. */
+qsa_status_t qsa_hot_cache_plan(qsa_cache* cache, const qsa_batch* batch,
+                                const int32_t* sel_blocks, const int32_t* n_sel,
+                                int32_t budget_tokens, void* stream);
+
 /* Step 4.  GQA decode attention of each unit over its selected tokens:
  * for query head h (KV head g = h/4), logits_i = softmax_scale * q[u][h] .
  * K_i[g], out[u][h] = sum_i softmax(logits)_i V_i[g], lse[u][h] =
@@ -419,7 +437,8 @@ qsa_status_t qsa_hot_cache_fetch(qsa_cache* cache, const qsa_batch* batch,
  * from pinned host memory).  A launch that reads cold rows from host memory
  * is held to a few dozen CTAs, which saturate the host link without slowing
  * HBM-bound work beside it; units with hot rows count as reading only HBM
- * (call qsa_hot_cache_fetch first).  Split-K over the tokens with a log-sum-exp merge;
+ * (call qsa_hot_cache_fetch or qsa_hot_cache_plan first; after a plan, this
+ * call also copies the planned misses into their hot rows).  Split-K over the tokens with a log-sum-exp merge;
  * partials live in the workspace, per (request, layer): two calls that
  * overlap on the GPU and share a (request, layer) race.
  * [offload digest: attention reads only the <= 2048 selected rows.]

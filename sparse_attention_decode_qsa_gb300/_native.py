@@ -111,6 +111,8 @@ SIGNATURES = {
                                   C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
     "qsa_hot_cache_fetch": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p,
                                       C.c_int32, C.c_void_p]),
+    "qsa_hot_cache_plan": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p,
+                                     C.c_int32, C.c_void_p]),
     "qsa_sparse_decode_attn": (C.c_int, [C.c_void_p, C.POINTER(Batch), C.c_void_p, C.c_void_p,
                                          C.c_void_p, C.c_int32, C.c_void_p, C.c_float,
                                          C.c_void_p, C.c_void_p, C.c_void_p]),

@@ -246,6 +246,12 @@ class Cache:
         check(self.L.qsa_hot_cache_fetch(self.h, C.byref(b), _ptr(sel_blocks), _ptr(n_sel),
                                          budget_tokens, _stream(stream)), "qsa_hot_cache_fetch")
 
+    def hot_cache_plan(self, handles, layer0, n_layers, sel_blocks, n_sel, budget_tokens,
+                       stream=None):
+        b = _batch(handles, layer0, n_layers)
+        check(self.L.qsa_hot_cache_plan(self.h, C.byref(b), _ptr(sel_blocks), _ptr(n_sel),
+                                        budget_tokens, _stream(stream)), "qsa_hot_cache_plan")
+
     def sparse_decode_attn(self, handles, layer0, n_layers, q, sel_blocks, n_sel, budget_tokens,
                            gathered, softmax_scale, out, lse=None, stream=None):
         b = _batch(handles, layer0, n_layers)

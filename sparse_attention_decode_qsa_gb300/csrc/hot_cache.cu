@@ -21,6 +21,10 @@
 //                    touched lately are slow (a cost per page, not per
 //                    byte), and more SMs keep more of them in flight.
 // Afterwards every selected row of the unit is in HBM.
+// qsa_hot_cache_plan runs the plan alone and also writes, per selected
+// position, the row its miss goes to: the next attention of the unit reads
+// those rows from host memory (once, as a zero-copy read would) and writes
+// them into their hot rows, so a miss costs no separate copy pass.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -42,6 +46,7 @@ struct HotParams {
   const int32_t* sel;
   const int32_t* n_sel;
   int32_t k_max;           // stride of sel (budget_tokens / 4)
+  int32_t plan_only;       // 1: leave the copies to the next attention (pending map)
 };
 
 // Exclusive scan of v over the CTA; *total receives the sum.  Every thread
@@ -92,6 +97,7 @@ __global__ void __launch_bounds__(kPlanThreads) hot_plan_kernel(const HotParams 
     if (tid == 0) {
       report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernHot, nsel);
       p.b.hot_nfill[st] = 0;
+      p.b.hot_pend_on[st] = 0;
     }
     return;
   }
@@ -133,7 +139,10 @@ __global__ void __launch_bounds__(kPlanThreads) hot_plan_kernel(const HotParams 
   int m;
   const int miss_base = block_exclusive_scan(my_miss, &m, s_warp);
   if (s_bad) {                                   // uniform: written before the scan's barriers
-    if (tid == 0) p.b.hot_nfill[st] = 0;
+    if (tid == 0) {
+      p.b.hot_nfill[st] = 0;
+      p.b.hot_pend_on[st] = 0;
+    }
     return;
   }
 
@@ -179,23 +188,32 @@ __global__ void __launch_bounds__(kPlanThreads) hot_plan_kernel(const HotParams 
   }
   __syncthreads();
 
-  // ---- writes: evicted owners go cold, misses take their rows
+  // ---- writes: evicted owners go cold, misses take their rows; with
+  // plan_only, each selected position also records the row its token is
+  // copied into by the attention (-1: none)
   int2* fills = p.b.hot_fills + st * p.b.hot_fill_stride;
+  int32_t* pend = p.b.hot_pend + st * p.b.hot_fill_stride;
   r = miss_base;
 #pragma unroll
   for (int i = 0; i < kMaxTokPerThread; ++i) {
-    if (tok[i] < 0) continue;
-    if (r < mm) {
-      const int v = victim[r];
-      if (evict[i] >= 0) slots[evict[i]] = -1;
-      owner[v] = tok[i];
-      slots[tok[i]] = (int32_t)(hb + v);
-      fills[r] = make_int2(tok[i], (int32_t)(hb + v));
+    const int j = tid * per + i;
+    int32_t row = -1;
+    if (tok[i] >= 0) {
+      if (r < mm) {
+        const int v = victim[r];
+        if (evict[i] >= 0) slots[evict[i]] = -1;
+        owner[v] = tok[i];
+        row = (int32_t)(hb + v);
+        slots[tok[i]] = row;
+        fills[r] = make_int2(tok[i], row);
+      }
+      ++r;
     }
-    ++r;
+    if (p.plan_only && i < per && j < ntok) pend[j] = row;
   }
   if (tid == 0) {
     p.b.hot_nfill[st] = mm;
+    p.b.hot_pend_on[st] = p.plan_only ? 1 : 0;
     if (mm > 0) p.b.hot_cursor[st] = victim[mm - 1] + 1 == H ? 0 : victim[mm - 1] + 1;
   }
 }
@@ -259,17 +277,18 @@ __global__ void __launch_bounds__(kFillThreads) hot_fill_kernel(const HotParams 
 }  // namespace
 
 cudaError_t launch_hot_fetch(const BatchDesc& b, const int32_t* sel_blocks, const int32_t* n_sel,
-                             int32_t budget_tokens, cudaStream_t s) {
+                             int32_t budget_tokens, bool copy_rows, cudaStream_t s) {
   if (b.n_units <= 0 || b.hot_rows <= 0) return cudaSuccess;
   HotParams p;
   p.b = b;
   p.sel = sel_blocks;
   p.n_sel = n_sel;
   p.k_max = budget_tokens / 4;
+  p.plan_only = copy_rows ? 0 : 1;
   const int smem = ((b.hot_rows + 31) / 32) * 4 + budget_tokens * 4;   // <= kPlanSmemMax
   cudaError_t e = launch_kernel(hot_plan_kernel, dim3(b.n_units), dim3(kPlanThreads), smem, s, 0,
                                 dim3(1), p);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !copy_rows) return e;
   dim3 grid((budget_tokens + kFillRows - 1) / kFillRows, b.n_units);
   if (b.row_bytes == kRowBytesFp8)
     return launch_kernel(hot_fill_kernel<kRowBytesFp8 / 16>, grid, dim3(kFillThreads), 0, s, 0, dim3(1), p);

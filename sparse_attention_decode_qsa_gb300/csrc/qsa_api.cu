@@ -82,7 +82,8 @@ bool config_sizes_ok(const qsa_cache_config* c) {
 // Workspace layout: error word, split-K partials, index-score work counters,
 // then (hot_rows > 0) the hot-cache state.  Byte offsets.
 struct WorkspaceLayout {
-  int64_t partials, tickets, hot_fills, hot_nfill, hot_cursor, hot_owner, total;
+  int64_t partials, tickets, hot_fills, hot_nfill, hot_cursor, hot_owner, hot_pend, hot_pend_on,
+      total;
 };
 
 WorkspaceLayout workspace_layout(const qsa_cache_config& c) {
@@ -95,7 +96,9 @@ WorkspaceLayout workspace_layout(const qsa_cache_config& c) {
   w.hot_nfill = w.hot_fills + (hot ? units * c.budget_tokens * (int64_t)sizeof(int2) : 0);
   w.hot_cursor = w.hot_nfill + (hot ? units * (int64_t)sizeof(int32_t) : 0);
   w.hot_owner = w.hot_cursor + (hot ? units * (int64_t)sizeof(int32_t) : 0);
-  w.total = w.hot_owner + (hot ? units * c.hot_rows * (int64_t)sizeof(int32_t) : 0);
+  w.hot_pend = w.hot_owner + (hot ? units * c.hot_rows * (int64_t)sizeof(int32_t) : 0);
+  w.hot_pend_on = w.hot_pend + (hot ? units * c.budget_tokens * (int64_t)sizeof(int32_t) : 0);
+  w.total = w.hot_pend_on + (hot ? units * (int64_t)sizeof(int32_t) : 0);
   return w;
 }
 
@@ -251,6 +254,8 @@ struct qsa_cache {
     d->hot_nfill = hot ? ws_at<int32_t>(w.hot_nfill) : nullptr;
     d->hot_cursor = hot ? ws_at<int32_t>(w.hot_cursor) : nullptr;
     d->hot_owner = hot ? ws_at<int32_t>(w.hot_owner) : nullptr;
+    d->hot_pend = hot ? ws_at<int32_t>(w.hot_pend) : nullptr;
+    d->hot_pend_on = hot ? ws_at<int32_t>(w.hot_pend_on) : nullptr;
     for (int i = 0; i < b->n_req; ++i) {
       const Lease* l;
       if (qsa_status_t st = check_handle(b->requests[i], &l)) return st;
@@ -442,6 +447,9 @@ qsa_status_t qsa_request_begin(qsa_cache* c, const qsa_request_desc* desc, void*
                           static_cast<cudaStream_t>(stream));
       if (e == cudaSuccess)
         e = cudaMemsetAsync(c->ws_at<int32_t>(w.hot_cursor) + st0, 0,
+                            (size_t)c->cfg.n_layers * sizeof(int32_t), static_cast<cudaStream_t>(stream));
+      if (e == cudaSuccess)   // no planned rows pending a copy
+        e = cudaMemsetAsync(c->ws_at<int32_t>(w.hot_pend_on) + st0, 0,
                             (size_t)c->cfg.n_layers * sizeof(int32_t), static_cast<cudaStream_t>(stream));
     }
     if (e != cudaSuccess) {
@@ -676,8 +684,26 @@ qsa_status_t qsa_hot_cache_fetch(qsa_cache* c, const qsa_batch* batch, const int
   if (budget_tokens < 4 || budget_tokens % 4 || budget_tokens > c->cfg.budget_tokens)
     return fail(QSA_ERR_INVALID_ARG, "bad budget_tokens %d", budget_tokens);
   if (c->cfg.hot_rows == 0) return ok();
-  cudaError_t e = launch_hot_fetch(d, sel_blocks, n_sel, budget_tokens, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_hot_fetch(d, sel_blocks, n_sel, budget_tokens, true,
+                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "hot-cache launch");
+  return ok();
+}
+
+qsa_status_t qsa_hot_cache_plan(qsa_cache* c, const qsa_batch* batch, const int32_t* sel_blocks,
+                                const int32_t* n_sel, int32_t budget_tokens, void* stream) {
+  if (!c) return fail(QSA_ERR_INVALID_ARG, "null cache");
+  DeviceGuard guard(c->device);
+  if (qsa_status_t st = c->check_stream(stream, guard)) return st;
+  BatchDesc d;
+  if (qsa_status_t st = c->build_batch(batch, &d)) return st;
+  if (!sel_blocks || !n_sel) return fail(QSA_ERR_INVALID_ARG, "null array");
+  if (budget_tokens < 4 || budget_tokens % 4 || budget_tokens > c->cfg.budget_tokens)
+    return fail(QSA_ERR_INVALID_ARG, "bad budget_tokens %d", budget_tokens);
+  if (c->cfg.hot_rows == 0) return ok();
+  cudaError_t e = launch_hot_fetch(d, sel_blocks, n_sel, budget_tokens, false,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "hot-cache plan launch");
   return ok();
 }
 

@@ -86,6 +86,11 @@ struct BatchDesc {
   int32_t* hot_nfill;         // [req][layer] entries in the fill list
   int32_t* hot_cursor;        // [req][layer] next row to hand out
   int32_t* hot_owner;         // [req][layer][hot_rows] token held by a row, or -1
+  // Misses planned by qsa_hot_cache_plan and not yet copied: per selected
+  // position the pool row the attention fills from host memory (-1: none),
+  // and per (request, layer) whether the map is live.
+  int32_t* hot_pend;          // [req][layer][hot_fill_stride]
+  int32_t* hot_pend_on;       // [req][layer]
   UnitDesc u[kMaxUnits];
 
   __host__ __device__ int64_t unit_row(int u_) const {
@@ -299,8 +304,10 @@ cudaError_t launch_append_token(const BatchDesc& b, const AppendTargets& tg, con
 
 // Cross-step hot cache: plan (slot, owner and cursor updates, fill lists)
 // then the copy of the listed host rows into their hot rows.
+// copy_rows = false: plan only; the next attention of the units reads the
+// misses from host memory and writes them into their hot rows.
 cudaError_t launch_hot_fetch(const BatchDesc& b, const int32_t* sel_blocks, const int32_t* n_sel,
-                             int32_t budget_tokens, cudaStream_t s);
+                             int32_t budget_tokens, bool copy_rows, cudaStream_t s);
 
 // Slot-table maintenance.
 cudaError_t launch_slot_fill(int32_t* rows, int32_t n_layers, int64_t ctx_cap, int64_t ctx_len,

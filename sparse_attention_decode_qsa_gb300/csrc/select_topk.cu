@@ -284,11 +284,25 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   // ---- first digit: bits 31..21, counted into kSubHists copies while the
   // keys are loaded, then folded into hist
   {
+    // kLoadBatch loads in flight per thread before their keys are counted
+    constexpr int kLoadBatch = 8;
     uint32_t* h = sub + (warp % kSubHists) * kBins;
-    for (int i = tid; i < cnt; i += kCThreads) {
-      const uint32_t k = order_key(s[lo + i]);
-      keys[i] = k;
-      atomicAdd(&h[k >> 21], 1u);
+    for (int i0 = tid; i0 < cnt; i0 += kCThreads * kLoadBatch) {
+      float v[kLoadBatch];
+#pragma unroll
+      for (int j = 0; j < kLoadBatch; ++j) {
+        const int i = i0 + j * kCThreads;
+        v[j] = i < cnt ? __ldg(s + lo + i) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kLoadBatch; ++j) {
+        const int i = i0 + j * kCThreads;
+        if (i < cnt) {
+          const uint32_t k = order_key(v[j]);
+          keys[i] = k;
+          atomicAdd(&h[k >> 21], 1u);
+        }
+      }
     }
   }
   __syncthreads();
@@ -468,6 +482,7 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
       }
     }
   }
+  trigger_dependents();
   cluster_sync();                              // keep s_cnt and s_T alive until every CTA read them
 }
 

@@ -122,11 +122,37 @@ __device__ __forceinline__ int visit_split(int k, int count, int r, int cpu) {
 // Copy this warp's 8 token slices (K[g], V[g]) of `split` into buf.  Lane l
 // resolves token l (l < 8); every lane then copies 16 bytes of each slice.
 // Returns a bitmask of the tokens that exist.
+// Source row of selected token t (selected position jpos) of unit u: the
+// dense gathered buffer, else a miss planned by qsa_hot_cache_plan (read from
+// host memory; *dst = the hot row it is copied into), else the slot table.
+__device__ __forceinline__ const uint8_t* attn_source(const AttnParams& p, int u, int64_t t,
+                                                      int jpos, const int32_t* pend, uint8_t** dst) {
+  if (p.gathered) return p.gathered + ((int64_t)u * p.budget_tokens + jpos) * p.b.row_bytes;
+  if (pend) {
+    const int32_t row = pend[jpos];
+    if (row >= 0 && (int64_t)row < p.b.pool_rows && p.b.u[u].host_rows) {
+      *dst = p.b.pool + (int64_t)row * p.b.row_bytes;
+      return p.b.u[u].host_rows + t * p.b.row_bytes;
+    }
+  }
+  return row_source(p.b, u, t, kKernAttn);
+}
+
+// The pending map of unit u when qsa_hot_cache_plan left copies to this
+// launch, else nullptr.
+__device__ __forceinline__ const int32_t* pending_map(const AttnParams& p, int u) {
+  if (p.gathered || !p.b.hot_pend || p.b.u[u].hot_base < 0) return nullptr;
+  const int64_t st = p.b.unit_state(u);
+  return p.b.hot_pend_on[st] ? p.b.hot_pend + st * p.b.hot_fill_stride : nullptr;
+}
+
 __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int split, int nsel,
-                                               int g, int half, uint8_t* buf) {
+                                               int g, int half, uint8_t* buf, const int32_t* pend,
+                                               uint8_t** dsts) {
   const int lane = threadIdx.x & 31;
   const int64_t n = p.b.u[u].n;
   const uint8_t* src = nullptr;
+  uint8_t* dst = nullptr;
   if (lane < kWarpTokens) {
     const int tok = half * kWarpTokens + lane;              // token within the split
     const int j = split * kBlocksPerSplit + tok / 4;        // selected-block index
@@ -136,10 +162,10 @@ __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int s
       if (b < 0 || 4 * b >= n) {
         if ((tok & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
       } else if (t < n) {
-        src = p.gathered ? p.gathered + ((int64_t)u * p.budget_tokens + 4 * j + (tok & 3)) * kRowBytes
-                         : row_source(p.b, u, t, kKernAttn);
+        src = attn_source(p, u, t, 4 * j + (tok & 3), pend, &dst);
       }
     }
+    dsts[lane] = dst;
   }
   const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & ((1u << kWarpTokens) - 1u);
   // lanes 0..15 copy K[g] (chunks of 16 B), lanes 16..31 copy V[g]
@@ -152,6 +178,18 @@ __device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int s
     cp_async16(buf + i * kSliceBytes + lane * 16, s ? s + off : p.b.pool, s ? 16u : 0u);
   }
   return valid;
+}
+
+// Copy this warp's slices of the stage's planned misses (K[g], V[g]: 16
+// bytes per lane and token) from shared memory into their hot rows.
+__device__ __forceinline__ void write_back(uint8_t* const* dsts, const uint8_t* R, int g, int lane) {
+  const int off = (lane < 16) ? g * kHeadDim * 2 + lane * 16
+                              : kKvHeads * kHeadDim * 2 + g * kHeadDim * 2 + (lane - 16) * 16;
+#pragma unroll
+  for (int i = 0; i < kWarpTokens; ++i) {
+    uint8_t* d = dsts[i];
+    if (d) *reinterpret_cast<uint4*>(d + off) = *reinterpret_cast<const uint4*>(R + i * kSliceBytes + lane * 16);
+  }
 }
 
 // End of a split CTA: merge the two token halves of each KV head through
@@ -196,6 +234,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   extern __shared__ __align__(16) uint8_t smem[];  // [warp][stage][8][512]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ uint32_t vmask[kWarps][kAStages];     // tokens present in each stage
+  __shared__ uint8_t* pdst[kWarps][kAStages][kWarpTokens];   // hot rows of planned misses
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
   int u, r, cpu;
@@ -231,11 +270,12 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   for (int j = 0; j < kGroup; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
   // splits k + 1 .. k + kAStages - 1 are in flight while split k is computed
+  const int32_t* pend = pending_map(p, u);
 #pragma unroll
   for (int k = 0; k < kAStages - 1; ++k) {
     if (k < count) {
       const uint32_t v = issue_warp(p, u, visit_split(k, count, r, cpu), nsel, g, half,
-                                    wbuf + k * kWarpBufBytes);
+                                    wbuf + k * kWarpBufBytes, pend, pdst[warp][k]);
       if (lane == 0) vmask[warp][k] = v;
     }
     cp_async_commit();
@@ -244,7 +284,8 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
     const int kn = k + kAStages - 1;
     if (kn < count) {   // its buffer was last read in iteration k - 1
       const uint32_t v = issue_warp(p, u, visit_split(kn, count, r, cpu), nsel, g, half,
-                                    wbuf + (kn % kAStages) * kWarpBufBytes);
+                                    wbuf + (kn % kAStages) * kWarpBufBytes, pend,
+                                    pdst[warp][kn % kAStages]);
       if (lane == 0) vmask[warp][kn % kAStages] = v;
     }
     cp_async_commit();
@@ -252,6 +293,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
     __syncwarp();
     const uint32_t valid_cur = vmask[warp][k % kAStages];
     const uint8_t* R = wbuf + (k % kAStages) * kWarpBufBytes;
+    if (pend) write_back(pdst[warp][k % kAStages], R, g, lane);
 
     // logits: lane 8j+kk ends with token kk of head j
     float x0 = -INFINITY;
@@ -352,11 +394,20 @@ __device__ __forceinline__ void e4m3x4_to_float4(uint32_t w, float& a, float& b,
   a = f0.x; b = f0.y; c = f1.x; d = f1.y;
 }
 
+// Byte offset in an FP8 row of 16-byte chunk c of KV head g's slice:
+// c < 8 K codes, 8..15 V codes, 16 the row's scales.
+__device__ __forceinline__ int fp8_chunk_offset(int g, int c) {
+  return c < 8 ? g * kHeadDim + c * 16
+               : (c < 16 ? kKvHeads * kHeadDim + g * kHeadDim + (c - 8) * 16 : 2 * kKvHeads * kHeadDim);
+}
+
 __device__ __forceinline__ uint32_t issue_warp_fp8(const AttnParams& p, int u, int split, int nsel,
-                                                   int g, int half, uint8_t* buf) {
+                                                   int g, int half, uint8_t* buf,
+                                                   const int32_t* pend, uint8_t** dsts) {
   const int lane = threadIdx.x & 31;
   const int64_t n = p.b.u[u].n;
   const uint8_t* src = nullptr;
+  uint8_t* dst = nullptr;
   if (lane < kWarpTokens) {
     const int tok = half * kWarpTokens + lane;              // token within the split
     const int j = split * kBlocksPerSplit + tok / 4;        // selected-block index
@@ -366,10 +417,10 @@ __device__ __forceinline__ uint32_t issue_warp_fp8(const AttnParams& p, int u, i
       if (b < 0 || 4 * b >= n) {
         if ((tok & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
       } else if (t < n) {
-        src = p.gathered ? p.gathered + ((int64_t)u * p.budget_tokens + 4 * j + (tok & 3)) * kRowBytesFp8
-                         : row_source(p.b, u, t, kKernAttn);
+        src = attn_source(p, u, t, 4 * j + (tok & 3), pend, &dst);
       }
     }
+    dsts[lane] = dst;
   }
   const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & ((1u << kWarpTokens) - 1u);
   // 8 tokens x 17 chunks: chunk c < 8 of K[g], 8..15 of V[g], 16 = scales
@@ -381,13 +432,27 @@ __device__ __forceinline__ uint32_t issue_warp_fp8(const AttnParams& p, int u, i
         __shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(src), tok));
     if (idx < kWarpTokens * kChunksFp8) {
       const int c = idx - tok * kChunksFp8;
-      const int off = c < 8 ? g * kHeadDim + c * 16
-                            : (c < 16 ? kKvHeads * kHeadDim + g * kHeadDim + (c - 8) * 16
-                                      : 2 * kKvHeads * kHeadDim);
-      cp_async16(buf + tok * kSliceFp8 + c * 16, s ? s + off : p.b.pool, s ? 16u : 0u);
+      cp_async16(buf + tok * kSliceFp8 + c * 16, s ? s + fp8_chunk_offset(g, c) : p.b.pool, s ? 16u : 0u);
     }
   }
   return valid;
+}
+
+// FP8 rows: copy this warp's slices of the stage's planned misses (K[g] and
+// V[g] codes, and the row's scales, which every head's warp holds) into their
+// hot rows.
+__device__ __forceinline__ void write_back_fp8(uint8_t* const* dsts, const uint8_t* R, int g, int lane) {
+#pragma unroll
+  for (int it = 0; it < (kWarpTokens * kChunksFp8 + 31) / 32; ++it) {
+    const int idx = it * 32 + lane;
+    if (idx < kWarpTokens * kChunksFp8) {
+      const int tok = idx / kChunksFp8, c = idx - tok * kChunksFp8;
+      uint8_t* d = dsts[tok];
+      if (d && (c < 16 || g == 0))
+        *reinterpret_cast<uint4*>(d + fp8_chunk_offset(g, c)) =
+            *reinterpret_cast<const uint4*>(R + tok * kSliceFp8 + c * 16);
+    }
+  }
 }
 
 __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnParams p) {
@@ -395,6 +460,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   extern __shared__ __align__(16) uint8_t smem[];  // [warp][stage][8][272]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ uint32_t vmask[kWarps][kAStagesFp8];
+  __shared__ uint8_t* pdst[kWarps][kAStagesFp8][kWarpTokens];
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
   int u, r, cpu;
@@ -428,11 +494,12 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
 #pragma unroll
   for (int j = 0; j < kGroup; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
+  const int32_t* pend = pending_map(p, u);
 #pragma unroll
   for (int k = 0; k < kAStagesFp8 - 1; ++k) {
     if (k < count) {
       const uint32_t v = issue_warp_fp8(p, u, visit_split(k, count, r, cpu), nsel, g, half,
-                                        wbuf + k * kWarpBufFp8);
+                                        wbuf + k * kWarpBufFp8, pend, pdst[warp][k]);
       if (lane == 0) vmask[warp][k] = v;
     }
     cp_async_commit();
@@ -441,7 +508,8 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
     const int kn = k + kAStagesFp8 - 1;
     if (kn < count) {
       const uint32_t v = issue_warp_fp8(p, u, visit_split(kn, count, r, cpu), nsel, g, half,
-                                        wbuf + (kn % kAStagesFp8) * kWarpBufFp8);
+                                        wbuf + (kn % kAStagesFp8) * kWarpBufFp8, pend,
+                                        pdst[warp][kn % kAStagesFp8]);
       if (lane == 0) vmask[warp][kn % kAStagesFp8] = v;
     }
     cp_async_commit();
@@ -449,6 +517,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
     __syncwarp();
     const uint32_t valid_cur = vmask[warp][k % kAStagesFp8];
     const uint8_t* R = wbuf + (k % kAStagesFp8) * kWarpBufFp8;
+    if (pend) write_back_fp8(pdst[warp][k % kAStagesFp8], R, g, lane);
 
     float x0 = -INFINITY;
 #pragma unroll
@@ -537,6 +606,9 @@ __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const AttnParams p
   }
   float* o = p.out + ((int64_t)u * kQHeads + h) * kHeadDim;
   o[d] = Lt > 0.f ? acc / Lt : 0.f;
+  // the planned misses of the unit are in their hot rows now
+  if (h == 0 && d == 0 && !p.gathered && p.b.hot_pend_on && p.b.u[u].hot_base >= 0)
+    p.b.hot_pend_on[p.b.unit_state(u)] = 0;
   if (p.lse && d == 0)
     p.lse[(int64_t)u * kQHeads + h] = Lt > 0.f ? (Mx + log2f(Lt)) * kLn2 : -INFINITY;
 }

@@ -98,6 +98,9 @@ class Workload:
     seeds: dict = field(default_factory=dict)
     planting: object = None
     host_memory: str = None
+    # with hot rows: plan the hot rows before attention and let the attention
+    # copy the misses (qsa_hot_cache_plan), instead of a separate fetch
+    fold_fill: bool = False
 
     @property
     def n_req(self):
@@ -161,10 +164,18 @@ class Workload:
         sl = slice(l * R, (l + 1) * R)
         c.index_score(hs, l, 1, self.q_idx[sl], self.w[sl], self.blk[sl], stream)
         c.select_c4_topk(hs, l, 1, self.blk[sl], self.budget, self.sel[sl], self.nsel[sl], stream)
-        if c.hot_rows:
-            c.hot_cache_fetch(hs, l, 1, self.sel[sl], self.nsel[sl], self.budget, stream)
+        self._hot(hs, l, sl, stream)
         c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
                              gathered, self.softmax_scale, self.out[sl], self.lse[sl], stream)
+
+    def _hot(self, hs, l, sl, stream):
+        c = self.cache
+        if not c.hot_rows:
+            return
+        if self.fold_fill:
+            c.hot_cache_plan(hs, l, 1, self.sel[sl], self.nsel[sl], self.budget, stream)
+        else:
+            c.hot_cache_fetch(hs, l, 1, self.sel[sl], self.nsel[sl], self.budget, stream)
 
     def step(self, stream=None):
         for l in range(self.n_layers):
@@ -183,8 +194,7 @@ class Workload:
         c, R = self.cache, self.n_req
         hs = self.handles[r0:r1]
         sl = slice(l * R + r0, l * R + r1)
-        if c.hot_rows:
-            c.hot_cache_fetch(hs, l, 1, self.sel[sl], self.nsel[sl], self.budget, stream)
+        self._hot(hs, l, sl, stream)
         c.sparse_decode_attn(hs, l, 1, self.q[sl], self.sel[sl], self.nsel[sl], self.budget,
                              None, self.softmax_scale, self.out[sl], self.lse[sl], stream)
 
@@ -331,7 +341,7 @@ def build(n_layers: int, ctxs, placements, planting, budget: int = 2048, ring: i
 
 
 
-def with_hot_rows(wl: Workload, hot_rows: int) -> Workload:
+def with_hot_rows(wl: Workload, hot_rows: int, fold_fill: bool = False) -> Workload:
     """The same requests and inputs in a new cache whose offloaded requests
     get hot_rows hot rows per layer.  Takes over wl's pinned host histories
     and closes wl's cache (wl is unusable afterwards)."""
@@ -361,7 +371,8 @@ def with_hot_rows(wl: Workload, hot_rows: int) -> Workload:
     new = Workload(cache, handles, wl.n_layers, list(wl.ctxs), list(wl.placements), wl.host,
                    wl.q_idx, wl.w, wl.q, wl.planted, wl.budget, blk=wl.blk, sel=wl.sel,
                    nsel=wl.nsel, out=wl.out, lse=wl.lse, softmax_scale=wl.softmax_scale,
-                   seeds=dict(wl.seeds), planting=wl.planting, host_memory=wl.host_memory)
+                   seeds=dict(wl.seeds), planting=wl.planting, host_memory=wl.host_memory,
+                   fold_fill=fold_fill)
     wl.host = []
     old.close()
     return new

@@ -286,8 +286,9 @@ def test_hot_rows_config_workspace_and_leases():
     c2 = N.CacheConfig.from_buffer_copy(cfg)
     c2.hot_rows = 4096
     units = 8 * 12
-    # fill list {token, row} per budget token, its length, the cursor, one owner per row
-    assert L.qsa_workspace_bytes(C.byref(c2)) == base + units * (2048 * 8 + 4 + 4 + 4096 * 4)
+    # fill list {token, row} per budget token, its length, the cursor, one owner per row,
+    # the plan's pending row per budget token and its flag
+    assert L.qsa_workspace_bytes(C.byref(c2)) == base + units * (2048 * 8 + 4 + 4 + 4096 * 4 + 2048 * 4 + 4)
     h = C.c_void_p()
     for field, bad in [("hot_rows", 2047), ("hot_rows", N.MAX_HOT_ROWS + 1), ("hot_rows", -4),
                        ("reserved1", 1)]:

@@ -113,18 +113,21 @@ def test_hot_cache_fetch_matches_the_oracle_over_drifting_steps(kv_format):
         wl.close()
 
 
+@pytest.mark.parametrize("fold", [False, True])
 @pytest.mark.parametrize("kv_format", [Q.KV_BF16, Q.KV_FP8])
-def test_hot_cache_decode_steps_match_the_oracle(kv_format):
+def test_hot_cache_decode_steps_match_the_oracle(kv_format, fold):
     """Decode steps (score, top-k, fetch, attention) over a host-ring cache
     with hot rows (BF16 and FP8 rows), the selection drifting between steps:
     selections and attention match the oracle, which reads every cold row
     from host memory, and the slot tables follow the oracle's hot-cache
-    state."""
+    state.  With fold, the step plans the hot rows (qsa_hot_cache_plan) and
+    the attention copies the misses into them."""
     L, R, n, ring, H, seed = 2, 2, 40000, 2048, 2048, 41
     wl = workloads.build(L, [n] * R, [Q.KV_HOST_RING] * R,
                          lambda l, r, n: synth.planted_hot_cold(n // 4, 512, ring // 4,
                                                                 synth.mix_seed(seed, 90, l, r)),
                          ring=ring, staging_rows=8, seed=seed, hot_rows=H, kv_format=kv_format)
+    wl.fold_fill = fold
     try:
         units = {(l, r): _OracleUnit(wl, l, r) for l in range(L) for r in range(R)}
         for step, frac in enumerate([0.0, 0.0, 0.25, 1.0, 0.1]):
@@ -153,10 +156,12 @@ def _same(wl, out_lse, slots, step):
     assert torch.equal(wl.cache.slot_table, slots), step
 
 
-def test_hot_cache_pipelined_graph_step_matches_sequential_steps():
-    """The captured two-micro-batch step with fetches gives the same outputs
-    and slot tables as eager sequential steps on an identical workload, over
-    steps whose selection drifts."""
+@pytest.mark.parametrize("fold", [False, True])
+def test_hot_cache_pipelined_graph_step_matches_sequential_steps(fold):
+    """The captured two-micro-batch step with fetches (or, with fold, plans
+    whose copies ride on the attention) gives the same outputs and slot
+    tables as eager sequential steps with fetches on an identical workload,
+    over steps whose selection drifts."""
     L, R, n, ring, H, seed = 2, 4, 30000, 1024, 2048, 43
 
     def make():
@@ -178,6 +183,7 @@ def test_hot_cache_pipelined_graph_step_matches_sequential_steps():
     finally:
         a.close()
     b = make()
+    b.fold_fill = fold
     try:
         streams = b.make_streams(2)
         b.step_pipelined(streams)                 # step 0 (eager, sets kernel attributes)
@@ -267,5 +273,75 @@ def test_hot_cache_state_starts_fresh_for_a_reissued_request():
             for r in range(2):
                 got = c.slot_table[wl.handles[r].index, 0, :wl.ctxs[r]].cpu().numpy()
                 assert np.array_equal(got, units[r].slot), r
+    finally:
+        wl.close()
+
+
+@pytest.mark.parametrize("kv_format", [Q.KV_BF16, Q.KV_FP8])
+def test_hot_cache_plan_then_attention_matches_the_oracle(kv_format):
+    """qsa_hot_cache_plan followed by qsa_sparse_decode_attn, over drifting
+    random selections: after each attention the slot tables equal the
+    oracle's hot_cache_step state and every row the oracle fills holds its
+    host row, byte for byte (the attention wrote it); the attention equals
+    the oracle's attention over the selected tokens' host rows; a second
+    attention without a new plan reads the filled rows from HBM and gives
+    the same result bit for bit."""
+    budget, H, ring = 512, 600, 256
+    ctxs = [6001, 9000, 3000]
+    placements = [Q.KV_HOST_RING, Q.KV_HOST, Q.KV_HOST_RING]
+    L = 2
+    wl = workloads.build(L, ctxs, placements, lambda l, r, n: [], budget=budget, ring=ring,
+                         staging_rows=8, seed=47, hot_rows=H, kv_format=kv_format)
+    try:
+        c, R = wl.cache, len(ctxs)
+        fp8 = kv_format == Q.KV_FP8
+        rng = np.random.default_rng(47)
+        units = {(l, r): _OracleUnit(wl, l, r) for l in range(L) for r in range(R)}
+        prev = {key: [] for key in units}
+        k_max = budget // 4
+        host_np = [h.numpy() for h in wl.host]
+        for step in range(8):
+            keep = [1.0, 0.9, 0.5, 0.0][step % 4]
+            sel = torch.zeros(L * R, k_max, dtype=torch.int32)
+            nsel = torch.zeros(L * R, dtype=torch.int32)
+            for (l, r), ou in units.items():
+                s_ = _random_selection(rng, ctxs[r], k_max, prev[(l, r)], keep)
+                prev[(l, r)] = list(s_)
+                sel[wl.unit(l, r), :len(s_)] = torch.from_numpy(s_)
+                nsel[wl.unit(l, r)] = len(s_)
+            wl.sel.copy_(sel.cuda())
+            wl.nsel.copy_(nsel.cuda())
+            for l in range(L):
+                sl = slice(l * R, (l + 1) * R)
+                c.hot_cache_plan(wl.handles, l, 1, wl.sel[sl], wl.nsel[sl], budget)
+                c.sparse_decode_attn(wl.handles, l, 1, wl.q[sl], wl.sel[sl], wl.nsel[sl], budget,
+                                     None, wl.softmax_scale, wl.out[sl], wl.lse[sl])
+            torch.cuda.synchronize()
+            _clean(wl)
+            out1, lse1 = wl.out.clone(), wl.lse.clone()
+            for l in range(L):
+                sl = slice(l * R, (l + 1) * R)
+                c.sparse_decode_attn(wl.handles, l, 1, wl.q[sl], wl.sel[sl], wl.nsel[sl], budget,
+                                     None, wl.softmax_scale, wl.out[sl], wl.lse[sl])
+            torch.cuda.synchronize()
+            _clean(wl)
+            assert torch.equal(out1, wl.out) and torch.equal(lse1, wl.lse), step
+            for (l, r), ou in units.items():
+                u = wl.unit(l, r)
+                blocks = sel[u, :int(nsel[u])].numpy()
+                fills = ou.step(blocks)
+                h = wl.handles[r]
+                got = c.slot_table[h.index, l, :ctxs[r]].cpu().numpy()
+                assert np.array_equal(got, ou.slot), (step, l, r)
+                if fills:
+                    rows = torch.tensor([row for _, row in fills], dtype=torch.int64, device="cuda")
+                    got_rows = c.pool[rows].cpu().numpy()
+                    want = np.stack([host_np[r][l, t] for t, _ in fills])
+                    assert np.array_equal(got_rows, want), (step, l, r)
+                toks = O.selected_tokens(blocks, ctxs[r])
+                o_ref, lse_ref = O.decode_attention(QC.bits16(wl.q[u]), host_np[r][l][toks],
+                                                    wl.softmax_scale, "fp8" if fp8 else "bf16")
+                assert np.abs(out1[u].cpu().double().numpy() - o_ref).max() <= QC.ATTN_TOL, (step, l, r)
+                assert np.abs(lse1[u].cpu().double().numpy() - lse_ref).max() <= QC.ATTN_TOL, (step, l, r)
     finally:
         wl.close()
