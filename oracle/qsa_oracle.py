@@ -50,7 +50,7 @@ HEAD_DIM = 128
 Q_HEADS = 16
 GQA_GROUP = Q_HEADS // KV_HEADS
 ROW_BYTES = 2048
-ROW_BYTES_FP8 = 1056
+ROW_BYTES_FP8 = 1040
 
 
 # ------------------------------------------------------------------ formats
@@ -187,7 +187,7 @@ def gather_rows(tokens, slot_row, hbm_pool_rows, host_rows, row_bytes: int = ROW
     """Bytes of the rows of the given logical tokens: pool row slot_row[t]
     when it is >= 0, else host row t (step 4 above).  Returns uint8
     [m][row_bytes].  hbm_pool_rows / host_rows: anything indexable by row
-    giving row_bytes bytes (2048 for bf16 rows, 1056 for FP8 rows)."""
+    giving row_bytes bytes (2048 for bf16 rows, 1040 for FP8 rows)."""
     out = np.empty((len(tokens), row_bytes), dtype=np.uint8)
     for i, t in enumerate(tokens):
         s = int(slot_row[int(t)])
@@ -258,11 +258,9 @@ def split_kv(rows_u8) -> tuple[np.ndarray, np.ndarray]:
 
 
 def split_kv_fp8(rows_u8) -> tuple[np.ndarray, np.ndarray]:
-    """A 1056-byte FP8 row holds K codes [4][128] E4M3, V codes [4][128]
-    E4M3, fp16 scales for K heads 0-3 and V heads 0-3, then 16 zero bytes
-    (a row is a whole number of 32-byte sectors, so every 128-byte piece of
-    codes starts on a sector); an element's value is its head's scale times
-    e4m3(code).  This is the library's
+    """A 1040-byte FP8 row holds K codes [4][128] E4M3, V codes [4][128]
+    E4M3, then fp16 scales for K heads 0-3 and V heads 0-3; an element's
+    value is its head's scale times e4m3(code).  This is the library's
     reading of an FP8 KV cache: the RTX 5090 page runs one (FP8 KV), and the
     RTX4090 port's per-card memory figure fits about 1 KiB per token and
     layer.  The per-head absmax scale is the same reading as the index
@@ -279,7 +277,7 @@ def decode_attention(q_bits, rows_u8, softmax_scale: float, kv_format: str = "bf
     """GQA decode attention over the gathered rows (step 5 above; sparse
     attention over the selected rows only, offload digest section
     "Механизм гибридного разреженного оффлоадинга").  kv_format "bf16":
-    2048-byte rows (split_kv); "fp8": 1056-byte rows (split_kv_fp8).
+    2048-byte rows (split_kv); "fp8": 1040-byte rows (split_kv_fp8).
 
     q_bits: uint16 [16][128] bf16 bits.  Returns (out float64 [16][128],
     lse float64 [16]); with no rows, out = 0 and lse = -inf.
@@ -410,12 +408,11 @@ def append_slot_writes(t: int, placement: str, base_row: int, layer: int, layer_
 
 
 def quantize_kv_row_fp8(row_u8) -> np.ndarray:
-    """FP8 row (1056 bytes, layout of split_kv_fp8) of a bf16 KV row (2048
+    """FP8 row (1040 bytes, layout of split_kv_fp8) of a bf16 KV row (2048
     bytes, layout of split_kv): each of the 8 vectors K[h], V[h] (128 values,
     exact in fp32) is quantised under the index key's rule - fp16 scale =
     round-to-nearest-even of absmax/448 in fp32, E4M3 codes of clamp(x/scale,
-    +-448) - and stored as codes K[4][128], V[4][128], scales K[4], V[4],
-    then 16 zero bytes."""
+    +-448) - and stored as codes K[4][128], V[4][128], scales K[4], V[4]."""
     bits = np.ascontiguousarray(row_u8, dtype=np.uint8).view(np.uint16).reshape(2, KV_HEADS, HEAD_DIM)
     vals = decode_bf16(bits).astype(np.float32)
     out = np.zeros(ROW_BYTES_FP8, dtype=np.uint8)
