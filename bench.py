@@ -37,6 +37,7 @@ METRIC = "QSA decode layer-steps/sec at 256K ctx; achieved HBM & PCIe GB/s vs pe
 WORKLOAD = "c256k_x8"
 N_LAYERS, N_REQ, CTX, BUDGET, RING = 12, 8, 262144, 2048, 4096
 ROW = 2048
+ROW_FP8 = 1040
 IDX_BYTES = 66
 
 
@@ -564,7 +565,7 @@ def _drift_levels(wl, graph, dev, args, churns, seed):
     return levels
 
 
-def drift_timing(wl, graph, dev, args, churns=(0.0, 0.1, 0.25, 1.0)):
+def drift_timing(dev, args, churns=(0.0, 0.1, 0.25, 1.0)):
     """The benchmark step when the selection drifts between steps (churn =
     fraction of each unit's cold planted blocks moved before each step; 1.0
     makes every cold block new at every step), in four forms:
@@ -575,7 +576,7 @@ def drift_timing(wl, graph, dev, args, churns=(0.0, 0.1, 0.25, 1.0)):
         rows per request and layer, whose step copies the cold selected rows
         into them first (qsa_hot_cache_fetch), or plans them and lets the
         attention copy them as it reads them (qsa_hot_cache_plan).
-    Consumes wl and graph."""
+    Runs after the other legs: drift on registered pages leaves them slow."""
     from sparse_attention_decode_qsa_gb300 import workloads
 
     def hot_levels(w, fold, seed):
@@ -588,9 +589,13 @@ def drift_timing(wl, graph, dev, args, churns=(0.0, 0.1, 0.25, 1.0)):
             hw.close()
         return lv
 
-    zero_copy = _drift_levels(wl, graph, dev, args, churns, 77)
-    del graph
-    wl.close()
+    wl = workloads.c256k_x8(device=dev, n_layers=args.layers, n_req=args.requests)
+    try:
+        graph = wl.capture(args.groups)
+        zero_copy = _drift_levels(wl, graph, dev, args, churns, 77)
+        del graph
+    finally:
+        wl.close()
     w3 = workloads.c256k_x8(device=dev, n_layers=args.layers, n_req=args.requests, host_memory="vmm")
     try:
         g3 = w3.capture(args.groups)
@@ -723,16 +728,19 @@ def run_ours(args, rank, world):
     st, det = wl.cache.poll_error()
     if st != 0:
         raise RuntimeError(f"device error word {st} ({det}) after timing")
-    drift = drift_timing(wl, graph, dev, args)     # consumes wl and graph
-    del graph, wl
-    append_us = append_timing(dev)
-    fp8_step_ms, fp8_attn_us, fp8_err = fp8_timing(dev, args)
-    hbm_res = hbm_resident_timing(dev, args)
+    del graph
+    wl.close()
+    del wl
+    all_legs = args.legs == "all"
+    append_us = append_timing(dev) if all_legs else None
+    fp8_step_ms, fp8_attn_us, fp8_err = fp8_timing(dev, args) if all_legs else (None, None, None)
+    hbm_res = hbm_resident_timing(dev, args) if all_legs else None
     link_copy = host_link_peak(dev)
     link_zc = zero_copy_peak(dev)
     link_peak = max(link_copy, link_zc)
-    host_only = host_only_timing(dev, args, link_peak)
-    ragged = ragged_timing(dev, args, link_peak)
+    host_only = host_only_timing(dev, args, link_peak) if all_legs else None
+    ragged = ragged_timing(dev, args, link_peak) if all_legs else None
+    drift = drift_timing(dev, args) if all_legs else None
 
     ms_max, ms_e2e_max = max_over_ranks([ms, ms_e2e], world)
     if rank != 0:
@@ -769,17 +777,19 @@ def run_ours(args, rank, world):
         # producer side: per launch 8 units (one layer) of key quantisation,
         # row store and slot update; not part of the timed decode step
         "append_token": {"bound": "latency", "avg_launch_us": round(append_us, 2),
-                         "units_per_launch": 8, "traffic": measured_traffic("append_token")},
+                         "units_per_launch": 8, "traffic": measured_traffic("append_token")}
+        if append_us is not None else None,
         # FP8 KV variant (1040-byte rows) of the same attention launch; not
         # part of the timed decode step, whose rows are BF16 (the whole FP8
         # step is reported under "fp8_kv")
         "sparse_attn_fp8": {"bound": "host_link",
-                            "achieved": round(R * (BUDGET // 2) * 1040 / (fp8_attn_us * 1e-6) / 1e9, 1),
+                            "achieved": round(R * (BUDGET // 2) * ROW_FP8 / (fp8_attn_us * 1e-6) / 1e9, 1),
                             "peak": round(link_peak, 1), "unit": "GB/s",
-                            "frac": round(R * (BUDGET // 2) * 1040 / (fp8_attn_us * 1e-6) / 1e9 / link_peak, 4),
-                            "host_bytes_per_launch": R * (BUDGET // 2) * 1040,
+                            "frac": round(R * (BUDGET // 2) * ROW_FP8 / (fp8_attn_us * 1e-6) / 1e9 / link_peak, 4),
+                            "host_bytes_per_launch": R * (BUDGET // 2) * ROW_FP8,
                             "traffic": measured_traffic("sparse_attn_fp8"),
-                            "avg_launch_us": round(fp8_attn_us, 2)},
+                            "avg_launch_us": round(fp8_attn_us, 2)}
+        if fp8_attn_us is not None else None,
     }
     dom = dict(roofs[dominant])
     dom["kernel"] = dominant
@@ -804,11 +814,11 @@ def run_ours(args, rank, world):
         "step_ms_p10_p50_p90": [round(pct(0.1), 4), round(pct(0.5), 4), round(pct(0.9), 4)],
         "roofline": dom, "kernels": roofs, "selection_drift": drift, "hbm_resident": hbm_res,
         "host_only_1m": host_only, "ragged_batch": ragged,
-        "fp8_kv": {"what": "the same step over FP8 KV rows (1040 bytes: E4M3 K and V codes, fp16 "
+        "fp8_kv": None if fp8_step_ms is None else {"what": "the same step over FP8 KV rows (1040 bytes: E4M3 K and V codes, fp16 "
                            "scales per head); BF16 queries, fp32 outputs",
                    "ms_per_step": round(fp8_step_ms, 4),
                    "layer_steps_per_s": round(units / (fp8_step_ms / 1e3), 1),
-                   "host_gbs": round(units * (BUDGET // 2) * 1040 / (fp8_step_ms / 1e3) / 1e9, 1),
+                   "host_gbs": round(units * (BUDGET // 2) * ROW_FP8 / (fp8_step_ms / 1e3) / 1e9, 1),
                    "device_error": fp8_err},
         "gpu_launches": args.steps * L * args.groups * 4,
         "clocks": clk.summary,
@@ -963,6 +973,53 @@ def run_reference(args, rank, world):
     }
 
 
+PROFILE_CASES = ("hbm_attn", "step_1layer", "fp8_1layer", "hot_plan_1layer", "c1m_1layer")
+
+
+def run_profile_case(name, args):
+    """One small run of a named case, for ncu captures of single kernels
+    (each case's last launches are the ones to capture):
+      hbm_attn         1 request x 12 layers x 131072 tokens in HBM: one
+                       decode step, then one attention launch over the 12
+                       units (HBM rows only)
+      step_1layer      8 requests x 1 layer x 262144 tokens, host history +
+                       tail ring: warm-up steps, then one step
+      fp8_1layer       the same with FP8 KV rows
+      hot_plan_1layer  the same requests on host NUMA memory with a 2048-row
+                       hot cache planned before attention: warm-up steps,
+                       then one step
+      c1m_1layer       4 requests x 1 layer x 1048576 tokens, every row in
+                       host memory: warm-up steps, then one step"""
+    from sparse_attention_decode_qsa_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if name == "hbm_attn":
+        wl = workloads.c128k(device=dev)
+        wl.step()
+        torch.cuda.synchronize(dev)
+        wl.cache.sparse_decode_attn(wl.handles, 0, wl.n_layers, wl.q, wl.sel, wl.nsel, BUDGET, None,
+                                    wl.softmax_scale, wl.out, wl.lse)
+    else:
+        if name == "step_1layer":
+            wl = workloads.c256k_x8(device=dev, n_layers=1)
+        elif name == "fp8_1layer":
+            import sparse_attention_decode_qsa_gb300 as Q
+            wl = workloads.c256k_x8(device=dev, n_layers=1, kv_format=Q.KV_FP8)
+        elif name == "hot_plan_1layer":
+            wl = workloads.with_hot_rows(workloads.c256k_x8(device=dev, n_layers=1, host_memory="vmm"),
+                                         BUDGET, fold_fill=True)
+        else:
+            wl = workloads.c1m_x4(device=dev, n_layers=1)
+        for _ in range(args.warmup + 1):
+            wl.step()
+    torch.cuda.synchronize(dev)
+    st, det = wl.cache.poll_error()
+    wl.close()
+    print(json.dumps({"profile_case": name, "device_error": st, "detail": det}), flush=True)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} ({det}) in profile case {name}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -975,7 +1032,14 @@ def main():
     ap.add_argument("--requests", type=int, default=N_REQ)
     ap.add_argument("--groups", type=int, default=2,
                     help="request micro-batches, each on its own stream")
+    ap.add_argument("--legs", choices=["all", "headline"], default="all",
+                    help="headline: only the measured 256K step (for quick runs and launch lists)")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES, default=None,
+                    help="run one small named case once (for ncu captures) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:

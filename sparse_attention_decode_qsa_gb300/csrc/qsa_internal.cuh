@@ -125,21 +125,26 @@ __device__ __forceinline__ const uint8_t* row_source(const BatchDesc& b, int u, 
 // launched with programmatic stream serialization (launch_kernel below), and
 // its first statement is grid_dependency_wait(), which returns once the
 // kernel before it on the stream has completed and its memory operations are
-// visible (at once when there is none).  No kernel triggers its dependents
-// early, so a dependent is scheduled when its predecessor completes, with
-// part of the launch work already done: measured on the 8 x 262144-token
-// step, 1.191 -> 1.175 ms.  An early trigger at kernel start made dependents
-// occupy SMs while they waited and slowed the same step to 1.23 ms.
+// visible (at once when there is none): measured on the 8 x 262144-token
+// step, 1.191 -> 1.175 ms.  The main kernels also trigger their dependents
+// where their CTAs' main work ends (trigger_dependents below).
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Lets the next kernel on the stream start launching once every CTA of this
 // one has passed this point (its grid_dependency_wait() still waits for this
-// kernel's completion).  Called where a CTA's main work ends, when
-// QSA_PDL_TRIGGER is set.
+// kernel's completion and memory).  Called where a CTA's main work ends:
+// the dependent's launch then overlaps this kernel's tail.  Measured on the
+// HBM-resident chain (score, top-k, attention, merge per layer, one unit):
+// 39.5 -> 37.5 us per layer; the two-micro-batch 256K step is unchanged
+// (1.176 -> 1.172 ms).  A trigger at kernel start slowed that step (its
+// dependents held SMs while they waited).  QSA_PDL_TRIGGER=0 removes it.
+#ifndef QSA_PDL_TRIGGER
+#define QSA_PDL_TRIGGER 1
+#endif
 __device__ __forceinline__ void trigger_dependents() {
-#if defined(QSA_PDL_TRIGGER) && QSA_PDL_TRIGGER
+#if QSA_PDL_TRIGGER
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #endif
 }

@@ -45,6 +45,10 @@
 namespace qsa {
 namespace {
 
+#ifndef QSA_PDL_TRIGGER_MERGE
+#define QSA_PDL_TRIGGER_MERGE 1
+#endif
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBlocksPerSplit = 4;                    // selected C4 blocks per split
@@ -60,6 +64,11 @@ constexpr int kSmemBytes = kWarps * kAStages * kWarpBufBytes;  // 64 KiB at 2 st
 #define QSA_ATTN_HOST_CTAS 32
 #endif
 constexpr int kMaxCtasHost = QSA_ATTN_HOST_CTAS;
+// CTAs per SM that units reading only HBM share
+#ifndef QSA_ATTN_HBM_CTAS_PER_SM
+#define QSA_ATTN_HBM_CTAS_PER_SM 1
+#endif
+constexpr int kHbmCtasPerSm = QSA_ATTN_HBM_CTAS_PER_SM;
 // Register budget per thread: at 80 one CTA (20 K registers) fits on an SM
 // beside two index-score CTAs.
 #ifndef QSA_ATTN_MAXREG
@@ -119,23 +128,44 @@ __device__ __forceinline__ int visit_split(int k, int count, int r, int cpu) {
   return r + idx * cpu;
 }
 
-// Copy this warp's 8 token slices (K[g], V[g]) of `split` into buf.  Lane l
-// resolves token l (l < 8); every lane then copies 16 bytes of each slice.
-// Returns a bitmask of the tokens that exist.
-// Source row of selected token t (selected position jpos) of unit u: the
-// dense gathered buffer, else a miss planned by qsa_hot_cache_plan (read from
-// host memory; *dst = the hot row it is copied into), else the slot table.
-__device__ __forceinline__ const uint8_t* attn_source(const AttnParams& p, int u, int64_t t,
-                                                      int jpos, const int32_t* pend, uint8_t** dst) {
-  if (p.gathered) return p.gathered + ((int64_t)u * p.budget_tokens + jpos) * p.b.row_bytes;
+// Row code of token `tok` (0..15) of a split: >= 0 a pool row (with gathered
+// rows, a row of that buffer), -1 no row (past the selection or the
+// context, or invalid), <= -2 the host row of token -code - 2 (a cold token,
+// or a miss planned by qsa_hot_cache_plan, whose hot row goes to *dst_row).
+// Reads the selection, the pending map and the slot table.
+__device__ __forceinline__ int32_t resolve_row(const AttnParams& p, int u, int split, int tok, int nsel,
+                                               const int32_t* pend, int32_t* dst_row) {
+  *dst_row = -1;
+  const int j = split * kBlocksPerSplit + tok / 4;        // selected-block index
+  if (j >= nsel) return -1;
+  const int64_t n = p.b.u[u].n;
+  const int64_t b = p.sel[(int64_t)u * p.k_max + j];
+  const int64_t t = 4 * b + (tok & 3);
+  if (b < 0 || 4 * b >= n) {
+    if ((tok & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
+    return -1;
+  }
+  if (t >= n) return -1;
+  const int jpos = 4 * j + (tok & 3);
+  if (p.gathered) return (int32_t)((int64_t)u * p.budget_tokens + jpos);
   if (pend) {
     const int32_t row = pend[jpos];
     if (row >= 0 && (int64_t)row < p.b.pool_rows && p.b.u[u].host_rows) {
-      *dst = p.b.pool + (int64_t)row * p.b.row_bytes;
-      return p.b.u[u].host_rows + t * p.b.row_bytes;
+      *dst_row = row;
+      return (int32_t)(-2 - t);
     }
   }
-  return row_source(p.b, u, t, kKernAttn);
+  const int32_t slot = p.b.slot_table[p.b.unit_row(u) + t];
+  if (slot >= 0 && (int64_t)slot < p.b.pool_rows) return slot;
+  if (slot == -1 && p.b.u[u].host_rows) return (int32_t)(-2 - t);
+  report_error(p.b.err, QSA_ERR_BAD_SLOT, kKernAttn, ((int64_t)u << 40) | (t & 0xFFFFFFFFFFll));
+  return -1;
+}
+
+__device__ __forceinline__ const uint8_t* row_ptr(const AttnParams& p, int u, int32_t code) {
+  if (code == -1) return nullptr;
+  if (code >= 0) return (p.gathered ? p.gathered : p.b.pool) + (int64_t)code * p.b.row_bytes;
+  return p.b.u[u].host_rows + (-2 - (int64_t)code) * p.b.row_bytes;
 }
 
 // The pending map of unit u when qsa_hot_cache_plan left copies to this
@@ -146,25 +176,61 @@ __device__ __forceinline__ const int32_t* pending_map(const AttnParams& p, int u
   return p.b.hot_pend_on[st] ? p.b.hot_pend + st * p.b.hot_fill_stride : nullptr;
 }
 
-__device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int split, int nsel,
+// Row sources resolved up front: a CTA's first kPreSplits splits (16 rows
+// each, in visit order) are resolved by all its threads at once, so that
+// the streaming loop issues each split's row copies without first waiting
+// for the selection and the slot table (two dependent global loads that
+// otherwise sat in front of every split).  Later splits, if any, are
+// resolved when they are issued.
+#ifndef QSA_ATTN_PRESPLITS
+#define QSA_ATTN_PRESPLITS 32
+#endif
+constexpr int kPreSplits = QSA_ATTN_PRESPLITS;
+constexpr int kPreRows = (kPreSplits > 0 ? kPreSplits : 1) * kBlocksPerSplit * 4;   // 512
+
+__device__ __forceinline__ void preload_rows(const AttnParams& p, int u, int r, int cpu, int count,
+                                             int nsel, const int32_t* pend, int32_t* code,
+                                             int32_t* dst) {
+  const int npre = (count < kPreSplits ? count : kPreSplits) * kBlocksPerSplit * 4;
+  for (int idx = threadIdx.x; idx < npre; idx += kThreads) {
+    const int k = idx >> 4, tok = idx & 15;
+    int32_t d;
+    code[idx] = resolve_row(p, u, visit_split(k, count, r, cpu), tok, nsel, pend, &d);
+    dst[idx] = d;
+  }
+  __syncthreads();
+}
+
+// Lane l < 8 of the warp: the source (and, for a planned miss, the hot row)
+// of token half*8 + l of the k-th split the CTA visits.
+__device__ __forceinline__ const uint8_t* lane_source(const AttnParams& p, int u, int k, int split,
+                                                      int nsel, int half, const int32_t* pend,
+                                                      const int32_t* pcode, const int32_t* pdst,
+                                                      uint8_t** dst) {
+  const int tok = half * kWarpTokens + (threadIdx.x & 31);
+  int32_t code, drow;
+  if (k < kPreSplits) {
+    code = pcode[k * 16 + tok];
+    drow = pdst[k * 16 + tok];
+  } else {
+    code = resolve_row(p, u, split, tok, nsel, pend, &drow);
+  }
+  *dst = drow >= 0 ? p.b.pool + (int64_t)drow * p.b.row_bytes : nullptr;
+  return row_ptr(p, u, code);
+}
+
+// Copy this warp's 8 token slices (K[g], V[g]) of the k-th split it visits
+// into buf.  Lane l resolves token l (l < 8); every lane then copies 16
+// bytes of each slice.  Returns a bitmask of the tokens that exist.
+__device__ __forceinline__ uint32_t issue_warp(const AttnParams& p, int u, int k, int split, int nsel,
                                                int g, int half, uint8_t* buf, const int32_t* pend,
+                                               const int32_t* pcode, const int32_t* pdst,
                                                uint8_t** dsts) {
   const int lane = threadIdx.x & 31;
-  const int64_t n = p.b.u[u].n;
   const uint8_t* src = nullptr;
-  uint8_t* dst = nullptr;
   if (lane < kWarpTokens) {
-    const int tok = half * kWarpTokens + lane;              // token within the split
-    const int j = split * kBlocksPerSplit + tok / 4;        // selected-block index
-    if (j < nsel) {
-      const int64_t b = p.sel[(int64_t)u * p.k_max + j];
-      const int64_t t = 4 * b + (tok & 3);
-      if (b < 0 || 4 * b >= n) {
-        if ((tok & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
-      } else if (t < n) {
-        src = attn_source(p, u, t, 4 * j + (tok & 3), pend, &dst);
-      }
-    }
+    uint8_t* dst;
+    src = lane_source(p, u, k, split, nsel, half, pend, pcode, pdst, &dst);
     dsts[lane] = dst;
   }
   const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & ((1u << kWarpTokens) - 1u);
@@ -235,6 +301,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ uint32_t vmask[kWarps][kAStages];     // tokens present in each stage
   __shared__ uint8_t* pdst[kWarps][kAStages][kWarpTokens];   // hot rows of planned misses
+  __shared__ int32_t pre_code[kPreRows], pre_dst[kPreRows];     // resolved row sources
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
   int u, r, cpu;
@@ -271,11 +338,12 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
 
   // splits k + 1 .. k + kAStages - 1 are in flight while split k is computed
   const int32_t* pend = pending_map(p, u);
+  preload_rows(p, u, r, cpu, count, nsel, pend, pre_code, pre_dst);
 #pragma unroll
   for (int k = 0; k < kAStages - 1; ++k) {
     if (k < count) {
-      const uint32_t v = issue_warp(p, u, visit_split(k, count, r, cpu), nsel, g, half,
-                                    wbuf + k * kWarpBufBytes, pend, pdst[warp][k]);
+      const uint32_t v = issue_warp(p, u, k, visit_split(k, count, r, cpu), nsel, g, half,
+                                    wbuf + k * kWarpBufBytes, pend, pre_code, pre_dst, pdst[warp][k]);
       if (lane == 0) vmask[warp][k] = v;
     }
     cp_async_commit();
@@ -283,8 +351,8 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   for (int k = 0; k < count; ++k) {
     const int kn = k + kAStages - 1;
     if (kn < count) {   // its buffer was last read in iteration k - 1
-      const uint32_t v = issue_warp(p, u, visit_split(kn, count, r, cpu), nsel, g, half,
-                                    wbuf + (kn % kAStages) * kWarpBufBytes, pend,
+      const uint32_t v = issue_warp(p, u, kn, visit_split(kn, count, r, cpu), nsel, g, half,
+                                    wbuf + (kn % kAStages) * kWarpBufBytes, pend, pre_code, pre_dst,
                                     pdst[warp][kn % kAStages]);
       if (lane == 0) vmask[warp][kn % kAStages] = v;
     }
@@ -401,25 +469,15 @@ __device__ __forceinline__ int fp8_chunk_offset(int g, int c) {
                : (c < 16 ? kKvHeads * kHeadDim + g * kHeadDim + (c - 8) * 16 : 2 * kKvHeads * kHeadDim);
 }
 
-__device__ __forceinline__ uint32_t issue_warp_fp8(const AttnParams& p, int u, int split, int nsel,
+__device__ __forceinline__ uint32_t issue_warp_fp8(const AttnParams& p, int u, int k, int split, int nsel,
                                                    int g, int half, uint8_t* buf,
-                                                   const int32_t* pend, uint8_t** dsts) {
+                                                   const int32_t* pend, const int32_t* pcode,
+                                                   const int32_t* pdst, uint8_t** dsts) {
   const int lane = threadIdx.x & 31;
-  const int64_t n = p.b.u[u].n;
   const uint8_t* src = nullptr;
-  uint8_t* dst = nullptr;
   if (lane < kWarpTokens) {
-    const int tok = half * kWarpTokens + lane;              // token within the split
-    const int j = split * kBlocksPerSplit + tok / 4;        // selected-block index
-    if (j < nsel) {
-      const int64_t b = p.sel[(int64_t)u * p.k_max + j];
-      const int64_t t = 4 * b + (tok & 3);
-      if (b < 0 || 4 * b >= n) {
-        if ((tok & 3) == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, b);
-      } else if (t < n) {
-        src = attn_source(p, u, t, 4 * j + (tok & 3), pend, &dst);
-      }
-    }
+    uint8_t* dst;
+    src = lane_source(p, u, k, split, nsel, half, pend, pcode, pdst, &dst);
     dsts[lane] = dst;
   }
   const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & ((1u << kWarpTokens) - 1u);
@@ -461,6 +519,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ uint32_t vmask[kWarps][kAStagesFp8];
   __shared__ uint8_t* pdst[kWarps][kAStagesFp8][kWarpTokens];
+  __shared__ int32_t pre_code[kPreRows], pre_dst[kPreRows];
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
   int u, r, cpu;
@@ -495,11 +554,12 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   for (int j = 0; j < kGroup; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
   const int32_t* pend = pending_map(p, u);
+  preload_rows(p, u, r, cpu, count, nsel, pend, pre_code, pre_dst);
 #pragma unroll
   for (int k = 0; k < kAStagesFp8 - 1; ++k) {
     if (k < count) {
-      const uint32_t v = issue_warp_fp8(p, u, visit_split(k, count, r, cpu), nsel, g, half,
-                                        wbuf + k * kWarpBufFp8, pend, pdst[warp][k]);
+      const uint32_t v = issue_warp_fp8(p, u, k, visit_split(k, count, r, cpu), nsel, g, half,
+                                        wbuf + k * kWarpBufFp8, pend, pre_code, pre_dst, pdst[warp][k]);
       if (lane == 0) vmask[warp][k] = v;
     }
     cp_async_commit();
@@ -507,9 +567,9 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   for (int k = 0; k < count; ++k) {
     const int kn = k + kAStagesFp8 - 1;
     if (kn < count) {
-      const uint32_t v = issue_warp_fp8(p, u, visit_split(kn, count, r, cpu), nsel, g, half,
-                                        wbuf + (kn % kAStagesFp8) * kWarpBufFp8, pend,
-                                        pdst[warp][kn % kAStagesFp8]);
+      const uint32_t v = issue_warp_fp8(p, u, kn, visit_split(kn, count, r, cpu), nsel, g, half,
+                                        wbuf + (kn % kAStagesFp8) * kWarpBufFp8, pend, pre_code,
+                                        pre_dst, pdst[warp][kn % kAStagesFp8]);
       if (lane == 0) vmask[warp][kn % kAStagesFp8] = v;
     }
     cp_async_commit();
@@ -588,7 +648,9 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
 // Merge: CTA (head, unit), thread = output dim; reads the cpu partials.
 __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const AttnParams p) {
   grid_dependency_wait();
+#if QSA_PDL_TRIGGER_MERGE
   trigger_dependents();
+#endif
   const int h = blockIdx.x, u = blockIdx.y, d = threadIdx.x;
   const int cpu = p.cta_start[u + 1] - p.cta_start[u];
   float Mx = -INFINITY;
@@ -657,7 +719,7 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
   if (cpu_max < 1) cpu_max = 1;
   auto clamp = [&](int c) { return c < 1 ? 1 : (c > cpu_max ? cpu_max : c); };
   const int cpu_host = n_host ? clamp(host_cap / n_host) : 0;
-  const int cpu_hbm = n_hbm ? clamp((sm_count - n_host * cpu_host) / n_hbm) : 0;
+  const int cpu_hbm = n_hbm ? clamp((kHbmCtasPerSm * sm_count - n_host * cpu_host) / n_hbm) : 0;
   int total = 0;
   for (int u = 0; u < b.n_units; ++u) {
     p.cta_start[u] = total;
