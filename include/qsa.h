@@ -413,10 +413,10 @@ qsa_status_t qsa_hot_cache_fetch(qsa_cache* cache, const qsa_batch* batch,
 /* The plan of qsa_hot_cache_fetch without its copy: the same slot-table,
  * owner and cursor updates (one launch, one CTA per unit), and a per-unit
  * map from selected position to the hot row its miss was given.  The next
- * qsa_sparse_decode_attn of those units (without `gathered`) reads the
- * misses' rows from host memory, as a zero-copy read would, and writes them
- * into their hot rows as it goes; afterwards the units are in the state
- * qsa_hot_cache_fetch leaves.  Until that attention has run, the misses'
+ * qsa_sparse_decode_attn of those units (without `gathered`, and with the
+ * same sel_blocks and n_sel) reads the misses' rows from host memory, as a
+ * zero-copy read would, and writes them into their hot rows as it goes;
+ * afterwards the units are in the state qsa_hot_cache_fetch leaves.  Until that attention has run, the misses'
  * hot rows hold stale bytes: no other call may read those units' rows
  * (qsa_gather_rows, attention with `gathered`), and the pending map is
  * replaced by the next plan or fetch of the unit.

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kPlanThreads) hot_plan_kernel(const HotParams 
     }
     return;
   }
+  const int c0 = p.b.hot_cursor[st];   // read early: it overlaps the classification
   const int words = (H + 31) / 32;
   int32_t* victim = reinterpret_cast<int32_t*>(in_use + words);
   int32_t* slots = p.b.slot_table + p.b.unit_row(u);
@@ -147,7 +148,6 @@ __global__ void __launch_bounds__(kPlanThreads) hot_plan_kernel(const HotParams 
   }
 
   // ---- rows not in use, in circular order from the cursor
-  const int c0 = p.b.hot_cursor[st];
   const int cursor = (c0 >= 0 && c0 < H) ? c0 : 0;
   const int hper = (H + kPlanThreads - 1) / kPlanThreads;
   int my_free = 0;

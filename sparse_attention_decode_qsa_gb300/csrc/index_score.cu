@@ -523,6 +523,9 @@ index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
     int eu = -1;                       // unit of the scoring cursor
     int64_t en = 0;
     float* out = nullptr;
+    float wr[kIndexHeads];             // the unit's head weights
+#pragma unroll
+    for (int h = 0; h < kIndexHeads; ++h) wr[h] = 0.f;
     for (int i = 0;; ++i) {
       const int st = i % kStages, db = i % kDBufs;
       if (!mbar_wait(full(st), (uint32_t)(i / kStages) & 1u, p.b.err, i)) break;
@@ -537,8 +540,9 @@ index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
         eu = m.x;
         en = p.b.u[eu].n;
         out = p.blk + (int64_t)eu * p.blk_stride;
+#pragma unroll
+        for (int h = 0; h < kIndexHeads; ++h) wr[h] = __ldg(p.w + (int64_t)eu * kIndexHeads + h);
       }
-      const float* wu = p.w + (int64_t)eu * kIndexHeads;
       if (!mbar_wait(d_full(db), (uint32_t)(i / kDBufs) & 1u, p.b.err, i)) break;
       tc_fence_after();
       // columns 8p + h: piece p of head h; y_h = sum_p 16^-p * D[8p + h] (Horner)
@@ -583,7 +587,7 @@ index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
       if (tok < en) {
         s = 0.f;
 #pragma unroll
-        for (int h = 0; h < kIndexHeads; ++h) s = fmaf(__ldg(wu + h), fmaxf(y[h] * sc, 0.f), s);
+        for (int h = 0; h < kIndexHeads; ++h) s = fmaf(wr[h], fmaxf(y[h] * sc, 0.f), s);
       }
       s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 1));
       s = fmaxf(s, __shfl_xor_sync(0xFFFFFFFFu, s, 2));

@@ -138,8 +138,10 @@ __device__ __forceinline__ void grid_dependency_wait() {
 // the dependent's launch then overlaps this kernel's tail.  Measured on the
 // HBM-resident chain (score, top-k, attention, merge per layer, one unit):
 // 39.5 -> 37.5 us per layer; the two-micro-batch 256K step is unchanged
-// (1.176 -> 1.172 ms).  A trigger at kernel start slowed that step (its
-// dependents held SMs while they waited).  QSA_PDL_TRIGGER=0 removes it.
+// (1.176 -> 1.172 ms).  A trigger at kernel start was slower everywhere (the
+// chain 42.0 us per layer, the 256K step 1.239 against 1.215 ms, the 12-unit
+// HBM attention 26 against 20 us): dependents held SMs while they waited.
+// QSA_PDL_TRIGGER=0 removes the trigger.
 #ifndef QSA_PDL_TRIGGER
 #define QSA_PDL_TRIGGER 1
 #endif

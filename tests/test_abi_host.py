@@ -583,3 +583,25 @@ def test_c_decode_step_compiles_and_links():
                             "-lqsa_gb300", "-L", cudalib, "-lcudart", f"-Wl,-rpath,{libdir}"],
                            capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_host_memory_entry_points_check_their_arguments():
+    """qsa_host_alloc refuses a null output and a non-positive size before it
+    touches the driver; qsa_host_free accepts NULL and refuses an address it
+    did not return (both without a GPU)."""
+    L = N.lib()
+    out = C.c_void_p()
+    assert L.qsa_host_alloc(0, -1, 4096, None) == N.ERR_INVALID_ARG
+    assert L.qsa_host_alloc(0, -1, 0, C.byref(out)) == N.ERR_INVALID_ARG
+    assert L.qsa_host_alloc(0, -1, -5, C.byref(out)) == N.ERR_INVALID_ARG
+    assert out.value is None
+    assert L.qsa_host_free(None) == N.OK
+    assert L.qsa_host_free(0x10000) == N.ERR_INVALID_ARG
+    assert b"qsa_host_alloc" in L.qsa_last_error_string()
+
+
+def test_workloads_refuse_an_unknown_host_memory_kind():
+    from sparse_attention_decode_qsa_gb300 import workloads
+    with pytest.raises(ValueError):
+        workloads.alloc_host((1, 4, 2048), "cpu", "paged")
+    assert set(workloads.HOST_MEMORY_KINDS) == {"vmm", "registered"}
