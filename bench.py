@@ -279,8 +279,9 @@ def hbm_resident_timing(dev, args):
     """The HBM-resident configuration: 1 request x 12 layers x 131072 tokens,
     every KV row in HBM.  Times (CUDA events, captured graphs) the faithful
     layer-sequential step (12 dependent layers of one request), the upper
-    bound with the 12 layers batched into one call per kernel, and each
-    kernel over the 12 units."""
+    bound with the 12 layers batched into one call per kernel, each kernel
+    over the 12 units, and each kernel over one unit (the launches of the
+    layer-sequential chain)."""
     from sparse_attention_decode_qsa_gb300 import workloads
     wl = workloads.c128k(device=dev)
     try:
@@ -325,8 +326,21 @@ def hbm_resident_timing(dev, args):
             topk(s)
             attn(s)
 
+        # one unit (layer 0 of the request), the launches of the sequential chain
+        def score1(s):
+            c.index_score(hs, 0, 1, wl.q_idx[:1], wl.w[:1], wl.blk[:1], s)
+
+        def topk1(s):
+            c.select_c4_topk(hs, 0, 1, wl.blk[:1], BUDGET, wl.sel[:1], wl.nsel[:1], s)
+
+        def attn1(s):
+            c.sparse_decode_attn(hs, 0, 1, wl.q[:1], wl.sel[:1], wl.nsel[:1], BUDGET, None,
+                                 wl.softmax_scale, wl.out[:1], wl.lse[:1], s)
+
         t = {k: gtime(f, r) for k, f, r in [("seq", seq, 1), ("batched", batched, 1), ("score", score, 10),
-                                             ("topk", topk, 10), ("attn", attn, 10)]}
+                                             ("topk", topk, 10), ("attn", attn, 10),
+                                             ("score1", score1, 10), ("topk1", topk1, 10),
+                                             ("attn1", attn1, 10)]}
         st, det = c.poll_error()
         if st != 0:
             raise RuntimeError(f"device error word {st} ({det}) in the HBM-resident timing")
@@ -348,7 +362,10 @@ def hbm_resident_timing(dev, args):
                                     "frac": round(gbs(key_b, t["score"]) / hbm_peak, 4)},
                     "select_topk": {"us": round(t["topk"], 2)},
                     "sparse_attn": {"us": round(t["attn"], 2), "hbm_gbs": gbs(row_b, t["attn"]),
-                                    "frac": round(gbs(row_b, t["attn"]) / hbm_peak, 4)}}}
+                                    "frac": round(gbs(row_b, t["attn"]) / hbm_peak, 4)}},
+                "kernels_1_unit": {"index_score_us": round(t["score1"], 2),
+                                   "select_topk_us": round(t["topk1"], 2),
+                                   "sparse_attn_us": round(t["attn1"], 2)}}
     finally:
         wl.close()
 

@@ -624,16 +624,15 @@ cudaError_t make_index_maps(CUtensorMap* keys_map, const void* keys, CUtensorMap
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                               CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                               CUtensorMapFloatOOBfill);
-  static Encode encode = nullptr;
-  if (!encode) {
+  static const Encode encode = [] {   // resolved once, thread-safe
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q{};
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                     cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-    encode = reinterpret_cast<Encode>(fn);
-  }
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                           cudaEnableDefault, &q);
+    return (e == cudaSuccess && q == cudaDriverEntryPointSuccess) ? reinterpret_cast<Encode>(fn)
+                                                                   : nullptr;
+  }();
+  if (!encode) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)kIndexDim, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kIndexDim};
   const cuuint32_t box[2] = {(cuuint32_t)kIndexDim, (cuuint32_t)kTile};

@@ -513,12 +513,10 @@ cudaError_t launch_select_topk(const BatchDesc& b, const float* blk_scores, int6
     return launch_kernel(select_topk_kernel, dim3(b.n_units), dim3(kThreads), 0, s, 0, dim3(1), p);
   }
   constexpr int kMaxDynSmem = kMaxSlice * 4 + kSubHists * kBins * 4;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = prefer_max_shared(select_topk_cluster_kernel, kMaxDynSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDeviceOnce setup;
+  const cudaError_t e =
+      setup.run([] { return prefer_max_shared(select_topk_cluster_kernel, kMaxDynSmem); });
+  if (e != cudaSuccess) return e;
   // keys per CTA of the largest unit, rounded up to 16-byte multiples
   const int slice_cap = (int)(((nb_max + kClusterCtas - 1) / kClusterCtas + 3) / 4 * 4);
   return launch_kernel(select_topk_cluster_kernel, dim3(b.n_units * kClusterCtas), dim3(kCThreads),

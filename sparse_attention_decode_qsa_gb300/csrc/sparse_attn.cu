@@ -645,34 +645,78 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   trigger_dependents();
 }
 
-// Merge: CTA (head, unit), thread = output dim; reads the cpu partials.
-__global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const AttnParams p) {
+// Merge: CTA (head, unit) of kMergeThreads threads.  The unit has cpu
+// partials (up to QSA_MAX_BUDGET_TOKENS / 16 = 512).  Thread s reads the
+// statistics of partial s; block reductions give the maximum M and the
+// total L = sum_s 2^(m_s - M) l_s, and the weights 2^(m_s - M) go to shared
+// memory.  Then kMergeGroups groups of 128 threads (one per output dim)
+// each sum every kMergeGroups-th partial, and the groups' sums are added.
+// A unit read from HBM alone can have 128 or more partials; one thread per
+// dim walking all of them one dependent load after another took several
+// microseconds.
+constexpr int kMergeGroups = 4;
+constexpr int kMergeThreads = kHeadDim * kMergeGroups;   // 512
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMaxPartials = QSA_MAX_BUDGET_TOKENS / (4 * kBlocksPerSplit);
+static_assert(kMaxPartials <= kMergeThreads, "one partial per thread in the statistics pass");
+
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p) {
   grid_dependency_wait();
 #if QSA_PDL_TRIGGER_MERGE
   trigger_dependents();
 #endif
-  const int h = blockIdx.x, u = blockIdx.y, d = threadIdx.x;
-  const int cpu = p.cta_start[u + 1] - p.cta_start[u];
-  float Mx = -INFINITY;
-  for (int s = 0; s < cpu; ++s) Mx = fmaxf(Mx, partial_ptr(p.b, u, s)[h]);
-  float Lt = 0.f, acc = 0.f;
+  __shared__ float wgt[kMaxPartials];
+  __shared__ float red[kMergeWarps];
+  __shared__ __align__(16) float part_acc[kMergeGroups][kHeadDim];
+  const int h = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int cpu = p.cta_start[u + 1] - p.cta_start[u];
+  if (cpu > kMaxPartials) cpu = kMaxPartials;   // the launcher never grants more
+
+  const float* ps = tid < cpu ? partial_ptr(p.b, u, tid) : nullptr;
+  const float ms = ps ? ps[h] : -INFINITY;
+  const float ls = ps ? ps[kQHeads + h] : 0.f;
+  float v = ms;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float Mx = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeWarps; ++w) Mx = fmaxf(Mx, red[w]);
+  const float ws = (ms == -INFINITY) ? 0.f : exp2f(ms - Mx);
+  if (tid < cpu) wgt[tid] = ws;
+  float lt = ws * ls;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xFFFFFFFFu, lt, o);
+  __syncthreads();   // every warp has read red[] as maxima
+  if (lane == 0) red[warp] = lt;
+  __syncthreads();
+  float Lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) Lt += red[w];
+
+  const int d = tid % kHeadDim, grp = tid / kHeadDim;
+  float acc = 0.f;
   if (Mx != -INFINITY) {
-#pragma unroll 4
-    for (int s = 0; s < cpu; ++s) {
-      const float* part = partial_ptr(p.b, u, s);
-      const float ms = part[h], ls = part[kQHeads + h], as = part[2 * kQHeads + h * kHeadDim + d];
-      const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - Mx);
-      Lt = fmaf(wgt, ls, Lt);
-      acc = fmaf(wgt, as, acc);
-    }
+#pragma unroll 8
+    for (int s = grp; s < cpu; s += kMergeGroups)
+      acc = fmaf(wgt[s], partial_ptr(p.b, u, s)[2 * kQHeads + h * kHeadDim + d], acc);
   }
-  float* o = p.out + ((int64_t)u * kQHeads + h) * kHeadDim;
-  o[d] = Lt > 0.f ? acc / Lt : 0.f;
-  // the planned misses of the unit are in their hot rows now
-  if (h == 0 && d == 0 && !p.gathered && p.b.hot_pend_on && p.b.u[u].hot_base >= 0)
-    p.b.hot_pend_on[p.b.unit_state(u)] = 0;
-  if (p.lse && d == 0)
-    p.lse[(int64_t)u * kQHeads + h] = Lt > 0.f ? (Mx + log2f(Lt)) * kLn2 : -INFINITY;
+  part_acc[grp][d] = acc;
+  __syncthreads();
+  if (grp == 0) {
+    float a = part_acc[0][d];
+#pragma unroll
+    for (int g2 = 1; g2 < kMergeGroups; ++g2) a += part_acc[g2][d];
+    float* o = p.out + ((int64_t)u * kQHeads + h) * kHeadDim;
+    o[d] = Lt > 0.f ? a / Lt : 0.f;
+    // the planned misses of the unit are in their hot rows now
+    if (h == 0 && d == 0 && !p.gathered && p.b.hot_pend_on && p.b.u[u].hot_base >= 0)
+      p.b.hot_pend_on[p.b.unit_state(u)] = 0;
+    if (p.lse && d == 0)
+      p.lse[(int64_t)u * kQHeads + h] = Lt > 0.f ? (Mx + log2f(Lt)) * kLn2 : -INFINITY;
+  }
 }
 
 }  // namespace
@@ -732,7 +776,8 @@ cudaError_t launch_sparse_attn(const BatchDesc& b, const uint16_t* q, const int3
                       : launch_kernel(attn_split_kernel, dim3(total), dim3(kThreads), kSmemBytes,
                                       s, prio, dim3(1), p);
   if (e != cudaSuccess) return e;
-  return launch_kernel(attn_merge_kernel, dim3(kQHeads, b.n_units), dim3(kHeadDim), 0, s, prio, dim3(1), p);
+  return launch_kernel(attn_merge_kernel, dim3(kQHeads, b.n_units), dim3(kMergeThreads), 0, s, prio,
+                       dim3(1), p);
 }
 
 }  // namespace qsa
