@@ -245,19 +245,26 @@ __device__ __forceinline__ void find_digit(const uint32_t* h, uint32_t nbins, ui
 }
 
 // 40 registers x 512 threads: a CTA fits on an SM beside two index-score CTAs.
+// red.shared::cluster: add v to a shared variable of another CTA of the cluster.
+__device__ __forceinline__ void red_dsmem(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// 40 registers x 512 threads: a CTA fits on an SM beside two index-score CTAs.
 __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, int slice_cap) {
   grid_dependency_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   uint32_t* keys = dyn;                                   // [slice_cap]
   uint32_t* sub = dyn + slice_cap;                        // [kSubHists][kBins], first digit
-  // later, in CTA 0, the same space holds the boundary-bin candidates
+  // later the same space holds the unit's boundary-bin candidates (all CTAs')
   uint32_t* cand_key = sub;                               // [kCandMax]: low 21 bits
-  uint32_t* cand_id = sub + kCandMax;                     // [kCandMax]: block ids
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t tot[kBins];
+  __shared__ uint32_t hist[kBins];                        // this CTA's first-digit histogram
+  __shared__ uint32_t tot[kBins];                         // the unit's, summed over the cluster
   __shared__ uint32_t warp_sum[kCWarps];
-  __shared__ uint32_t s_digit, s_krem, s_T, s_base, s_pos;
+  __shared__ uint32_t s_digit, s_krem, s_base, s_pos, s_above;
   __shared__ uint32_t s_cnt[2];
+  __shared__ uint32_t c_bin[kClusterCtas], c_above[kClusterCtas];   // per CTA: keys in / above bin d1
+  __shared__ uint32_t c_gt[kClusterCtas], c_eq[kClusterCtas];       // per CTA: keys above / equal to T
   __shared__ uint32_t warp_gt[kCWarps], warp_eq[kCWarps];
 
   const uint32_t rank = cluster_rank();
@@ -278,8 +285,10 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     return;       // uniform across the cluster: no DSMEM access follows
   }
 
+  for (int i = tid; i < kBins; i += kCThreads) tot[i] = 0;
   for (int i = tid; i < kSubHists * kBins; i += kCThreads) sub[i] = 0;
   __syncthreads();
+  cluster_arrive();   // my tot is zeroed (waited for once the keys are in)
 
   // ---- first digit: bits 31..21, counted into kSubHists copies while the
   // keys are loaded, then folded into hist
@@ -316,81 +325,95 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     hist[b] = t;
   }
   __syncthreads();
-  cluster_sync();                              // all histograms complete
-  {
-    constexpr int kPer = kBins / kCThreads;    // 4 bins per thread, all loads in flight at once
-    uint32_t v[kPer][kClusterCtas];
+  // The cluster's histogram: every CTA adds its non-zero bins into every
+  // CTA's tot (remote atomic adds, fire and forget; block scores crowd into
+  // few bins), so each CTA then holds the sum locally.
+  cluster_wait();                              // every CTA's tot is zeroed
+  for (int b = tid; b < kBins; b += kCThreads) {
+    const uint32_t v = hist[b];
+    if (v) {
 #pragma unroll
-    for (int j = 0; j < kPer; ++j)
-#pragma unroll
-      for (int c = 0; c < kClusterCtas; ++c) v[j][c] = ld_dsmem(dsmem_addr(&hist[tid + j * kCThreads], c));
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      uint32_t t = 0;
-#pragma unroll
-      for (int c = 0; c < kClusterCtas; ++c) t += v[j][c];
-      tot[tid + j * kCThreads] = t;
+      for (int c = 0; c < kClusterCtas; ++c) red_dsmem(dsmem_addr(&tot[b], (uint32_t)c), v);
     }
   }
-  __syncthreads();
+  cluster_sync();                              // every tot holds the unit's histogram
   find_digit(tot, kBins, (uint32_t)K, warp_sum, &s_digit, &s_krem);
   const uint32_t d1 = s_digit;
   uint32_t krem = s_krem;
   uint32_t T;
-  if (tot[d1] <= (uint32_t)kCandMax) {
-    // ---- fast path: the boundary bin's keys go to CTA 0, which finishes
-    // the select on the low 21 bits (11 + 10) alone.  No CTA changes its
-    // histogram before the next cluster barrier, so the offsets read here
-    // (earlier CTAs' counts of bin d1) are stable.
-    if (warp == 0) {   // lane c < rank reads CTA c's count of bin d1
-      uint32_t v = (uint32_t)lane < rank ? ld_dsmem(dsmem_addr(&hist[d1], (uint32_t)lane)) : 0u;
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-      if (lane == 0) {
-        s_base = v;
-        s_pos = 0;
-      }
-    }
+  const bool fast = tot[d1] <= (uint32_t)kCandMax;
+  if (fast) {
+    // ---- usual path: every CTA sends its keys in bin d1 (low 21 bits) and
+    // its count of keys above the bin to every CTA; each CTA then finishes
+    // the select on the candidates alone, and knows every CTA's counts of
+    // keys above and equal to T, so no further cluster barrier is needed.
+    // A CTA's hist stays as it is until the barrier below, so the counts of
+    // bin d1 read here are stable.
+    if (warp == 0 && lane < kClusterCtas) c_bin[lane] = ld_dsmem(dsmem_addr(&hist[d1], (uint32_t)lane));
+    if (tid == 0) { s_pos = 0; s_above = 0; }
     __syncthreads();
+    uint32_t base = 0;
+    for (uint32_t c = 0; c < rank; ++c) base += c_bin[c];
+    uint32_t above = 0;
     for (int i0 = 0; i0 < cnt; i0 += kCThreads) {   // CTA-uniform trip count
       const int i = i0 + tid;
       const uint32_t k = i < cnt ? keys[i] : 0u;
       const bool hit = i < cnt && (k >> 21) == d1;
-      const uint32_t hb = __ballot_sync(0xFFFFFFFFu, hit);   // one atomic per warp
-      uint32_t base = 0;
-      if (hb && lane == 0) base = atomicAdd(&s_pos, (uint32_t)__popc(hb));
-      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      above += (i < cnt && (k >> 21) > d1) ? 1u : 0u;
+      const uint32_t hb = __ballot_sync(0xFFFFFFFFu, hit);   // one slot reservation per warp
+      uint32_t wb = 0;
+      if (hb && lane == 0) wb = atomicAdd(&s_pos, (uint32_t)__popc(hb));
+      wb = __shfl_sync(0xFFFFFFFFu, wb, 0);
       if (hit) {
-        const uint32_t pos = s_base + base + __popc(hb & ((1u << lane) - 1u));
-        st_dsmem(dsmem_addr(&cand_key[pos], 0), k & 0x1FFFFFu);
-        st_dsmem(dsmem_addr(&cand_id[pos], 0), (uint32_t)(lo + i));
+        const uint32_t pos = base + wb + __popc(hb & ((1u << lane) - 1u));
+#pragma unroll
+        for (int c = 0; c < kClusterCtas; ++c)
+          st_dsmem(dsmem_addr(&cand_key[pos], (uint32_t)c), k & 0x1FFFFFu);
       }
     }
-    cluster_sync();                            // candidates complete in CTA 0
-    if (rank == 0) {
-      const uint32_t ncand = tot[d1];
-      uint32_t prefix = 0, mask = 0;
-      for (int pass = 0; pass < 2; ++pass) {
-        const int shift = pass == 0 ? 10 : 0;
-        const uint32_t nbins = pass == 0 ? 2048u : 1024u;
-        for (int i = tid; i < (int)nbins; i += kCThreads) hist[i] = 0;
-        __syncthreads();
-        for (int j = tid; j < (int)ncand; j += kCThreads) {
-          const uint32_t k = cand_key[j];
-          if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
-        }
-        __syncthreads();
-        find_digit(hist, nbins, krem, warp_sum, &s_digit, &s_krem);
-        prefix |= s_digit << shift;
-        mask |= (nbins - 1) << shift;
-        krem = s_krem;
-        __syncthreads();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
+    if (lane == 0 && above) atomicAdd(&s_above, above);
+    __syncthreads();
+    if (warp == 0 && lane < kClusterCtas) st_dsmem(dsmem_addr(&c_above[rank], (uint32_t)lane), s_above);
+    cluster_sync();                            // every CTA holds all candidates and counts
+    const uint32_t ncand = tot[d1];
+    uint32_t prefix = 0, mask = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      const int shift = pass == 0 ? 10 : 0;
+      const uint32_t nbins = pass == 0 ? 2048u : 1024u;
+      for (int i = tid; i < (int)nbins; i += kCThreads) hist[i] = 0;
+      __syncthreads();
+      for (int j = tid; j < (int)ncand; j += kCThreads) {
+        const uint32_t k = cand_key[j];
+        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
       }
-      if (tid == 0) s_T = (d1 << 21) | prefix;   // s_krem already holds the ties to keep
+      __syncthreads();
+      find_digit(hist, nbins, krem, warp_sum, &s_digit, &s_krem);
+      prefix |= s_digit << shift;
+      mask |= (nbins - 1) << shift;
+      krem = s_krem;
+      __syncthreads();
     }
-    cluster_sync();                            // CTA 0 published T and the ties
-    T = ld_dsmem(dsmem_addr(&s_T, 0));
-    krem = ld_dsmem(dsmem_addr(&s_krem, 0));
+    T = (d1 << 21) | prefix;
+    // warp c: CTA c's keys above T (above bin d1, or candidates above) and equal to T
+    if (warp < kClusterCtas) {
+      uint32_t b0 = 0;
+      for (int c = 0; c < warp; ++c) b0 += c_bin[c];
+      uint32_t g = 0, e = 0;
+      for (uint32_t j = b0 + lane; j < b0 + c_bin[warp]; j += 32) {
+        const uint32_t k = cand_key[j];
+        g += k > prefix ? 1u : 0u;
+        e += k == prefix ? 1u : 0u;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
+        e += __shfl_xor_sync(0xFFFFFFFFu, e, o);
+      }
+      if (lane == 0) { c_gt[warp] = c_above[warp] + g; c_eq[warp] = e; }
+    }
+    __syncthreads();
   } else {
     // ---- general path: two more cluster-wide passes over every key
     uint32_t prefix = d1 << 21, mask = 0x7FFu << 21;
@@ -425,8 +448,9 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   // counts those above / equal to T 32 at a time (ballots; lanes read
   // consecutive keys, so no bank conflicts - a contiguous run per thread
   // put up to 32 lanes on one bank), a scan of the warp totals gives the
-  // offsets within the CTA, the CTAs exchange their totals through DSMEM,
-  // and a second walk over the range writes the selected ids in id order.
+  // offsets within the CTA, and a second walk over the range writes the
+  // selected ids in id order, after the keys of the lower-rank CTAs (known
+  // locally on the usual path, exchanged through DSMEM otherwise).
   const int R = ((cnt + kCWarps - 1) / kCWarps + 31) / 32 * 32;
   const int w0 = warp * R, w1 = w0 + R < cnt ? w0 + R : cnt;
   const uint32_t lt_mask = (1u << lane) - 1u;
@@ -452,21 +476,30 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     if (lane == 31) { s_cnt[0] = sg; s_cnt[1] = se; }
   }
   __syncthreads();
-  cluster_sync();                                          // every CTA's totals are published
-  if (warp == 0) {   // lane c < rank reads CTA c's totals; sums go to s_base / s_pos
-    uint32_t vg = 0u, ve = 0u;
-    if ((uint32_t)lane < rank) {
-      vg = ld_dsmem(dsmem_addr(&s_cnt[0], (uint32_t)lane));
-      ve = ld_dsmem(dsmem_addr(&s_cnt[1], (uint32_t)lane));
-    }
-#pragma unroll
-    for (int o = 4; o > 0; o >>= 1) {
-      vg += __shfl_xor_sync(0xFFFFFFFFu, vg, o);
-      ve += __shfl_xor_sync(0xFFFFFFFFu, ve, o);
-    }
-    if (lane == 0) {
+  if (fast) {
+    if (tid == 0) {
+      uint32_t vg = 0, ve = 0;
+      for (uint32_t c = 0; c < rank; ++c) { vg += c_gt[c]; ve += c_eq[c]; }
       s_base = vg;
       s_pos = ve;
+    }
+  } else {
+    cluster_sync();                                        // every CTA's totals are published
+    if (warp == 0) {   // lane c < rank reads CTA c's totals; sums go to s_base / s_pos
+      uint32_t vg = 0u, ve = 0u;
+      if ((uint32_t)lane < rank) {
+        vg = ld_dsmem(dsmem_addr(&s_cnt[0], (uint32_t)lane));
+        ve = ld_dsmem(dsmem_addr(&s_cnt[1], (uint32_t)lane));
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {
+        vg += __shfl_xor_sync(0xFFFFFFFFu, vg, o);
+        ve += __shfl_xor_sync(0xFFFFFFFFu, ve, o);
+      }
+      if (lane == 0) {
+        s_base = vg;
+        s_pos = ve;
+      }
     }
   }
   __syncthreads();
@@ -489,7 +522,7 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     eq_run += __popc(be);
   }
   trigger_dependents();
-  cluster_sync();                              // keep s_cnt and s_T alive until every CTA read them
+  if (!fast) cluster_sync();   // keep s_cnt alive until every CTA read it
 }
 
 }  // namespace
