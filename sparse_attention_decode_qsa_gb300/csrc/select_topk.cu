@@ -192,59 +192,52 @@ __device__ __forceinline__ void st_dsmem(uint32_t addr, uint32_t v) {
 }
 
 // Digit of the krem-th largest key from a histogram of nbins bins (counted
-// from the top): *digit, and *krem_out = its rank within that bin.  Called by
-// the whole CTA; the results are valid after the closing __syncthreads().
+// from the top; nbins 1024 or 2048): *digit, and *krem_out = its rank within
+// that bin.  Thread t owns the bins nbins-1-per*t .. nbins-per*(t+1) (per =
+// nbins / kCThreads, one vector load); a scan over the threads finds the one
+// thread whose bins hold rank krem.  Called by the whole CTA; the results are
+// valid after the closing __syncthreads().
+static_assert(kCThreads * 4 == kBins && kCThreads * 2 == 1024, "find_digit: 4 or 2 bins per thread");
 __device__ __forceinline__ void find_digit(const uint32_t* h, uint32_t nbins, uint32_t krem,
                                            uint32_t* warp_sum, uint32_t* digit,
                                            uint32_t* krem_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (int)nbins / kCWarps;  // bins per warp, from the top: 128 or 64
-  {
-    uint32_t sum = 0;
-    for (int j = lane; j < per; j += 32) sum += h[nbins - 1 - (warp * per + j)];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (lane == 0) warp_sum[warp] = sum;
+  uint32_t c[4];   // c[j]: bin nbins-1-(per*t+j)
+  int per;
+  if (nbins == 2048u) {
+    per = 4;
+    const uint4 v = *reinterpret_cast<const uint4*>(h + 2048 - 4 * (tid + 1));
+    c[0] = v.w; c[1] = v.z; c[2] = v.y; c[3] = v.x;
+  } else {
+    per = 2;
+    const uint2 v = *reinterpret_cast<const uint2*>(h + 1024 - 2 * (tid + 1));
+    c[0] = v.y; c[1] = v.x; c[2] = 0u; c[3] = 0u;
   }
+  const uint32_t sum = c[0] + c[1] + c[2] + c[3];
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t ws = lane < kCWarps ? warp_sum[lane] : 0u;
-    uint32_t incl = ws;
+  uint32_t cum = incl - sum;
+  for (int w = 0; w < warp; ++w) cum += warp_sum[w];
+  if (cum < krem && krem <= cum + sum) {   // exactly one thread when krem is in range
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const uint32_t excl = incl - ws;
-    const bool mine = lane < kCWarps && excl < krem && krem <= incl;
-    const uint32_t owners = __ballot_sync(0xFFFFFFFFu, mine);
-    const uint32_t owner = owners ? (uint32_t)(__ffs(owners) - 1) : 0u;  // always one by construction
-    uint32_t cum = __shfl_sync(0xFFFFFFFFu, excl, owner);
-    for (int j0 = 0; j0 < per; j0 += 32) {
-      const uint32_t c = h[nbins - 1 - (owner * per + j0 + lane)];
-      uint32_t ic = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, ic, o);
-        if (lane >= o) ic += v;
-      }
-      const uint32_t ex = cum + ic - c;
-      const uint32_t hb = __ballot_sync(0xFFFFFFFFu, ex < krem && krem <= cum + ic);
-      if (hb) {
-        const int hl = __ffs(hb) - 1;
-        if (lane == hl) {
-          *digit = nbins - 1 - (owner * per + j0 + hl);
-          *krem_out = krem - ex;
-        }
+    for (int j = 0; j < 4; ++j) {
+      if (j < per && cum + c[j] >= krem) {
+        *digit = nbins - 1u - (uint32_t)(per * tid + j);
+        *krem_out = krem - cum;
         break;
       }
-      cum += __shfl_sync(0xFFFFFFFFu, ic, 31);
+      cum += c[j];
     }
   }
   __syncthreads();
 }
 
-// 40 registers x 512 threads: a CTA fits on an SM beside two index-score CTAs.
 // red.shared::cluster: add v to a shared variable of another CTA of the cluster.
 __device__ __forceinline__ void red_dsmem(uint32_t addr, uint32_t v) {
   asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -258,8 +251,8 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   uint32_t* sub = dyn + slice_cap;                        // [kSubHists][kBins], first digit
   // later the same space holds the unit's boundary-bin candidates (all CTAs')
   uint32_t* cand_key = sub;                               // [kCandMax]: low 21 bits
-  __shared__ uint32_t hist[kBins];                        // this CTA's first-digit histogram
-  __shared__ uint32_t tot[kBins];                         // the unit's, summed over the cluster
+  __shared__ __align__(16) uint32_t hist[kBins];         // this CTA's first-digit histogram
+  __shared__ __align__(16) uint32_t tot[kBins];          // the unit's, summed over the cluster
   __shared__ uint32_t warp_sum[kCWarps];
   __shared__ uint32_t s_digit, s_krem, s_base, s_pos, s_above;
   __shared__ uint32_t s_cnt[2];
