@@ -157,7 +157,8 @@ constexpr int kCThreads = 512;
 constexpr int kCWarps = kCThreads / 32;
 constexpr int kMaxSlice = 32768;  // keys per CTA: 8 x 32768 blocks = 1M tokens
 constexpr int kBins = 2048;
-constexpr int kCandMax = 2048;    // boundary-bin keys finished by CTA 0
+constexpr int kCandMax = 2048;    // boundary-bin keys the CTAs finish the select on
+constexpr int kRegion = kCandMax / kClusterCtas;   // slots per source CTA in the candidate list
 constexpr int kSubHists = 4;      // first-digit histogram copies (warps w % 4), less contention
 static_assert(kCandMax * 8 <= kSubHists * kBins * 4, "candidates reuse the sub-histograms");
 
@@ -254,7 +255,7 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   __shared__ __align__(16) uint32_t hist[kBins];         // this CTA's first-digit histogram
   __shared__ __align__(16) uint32_t tot[kBins];          // the unit's, summed over the cluster
   __shared__ uint32_t warp_sum[kCWarps];
-  __shared__ uint32_t s_digit, s_krem, s_base, s_pos, s_above;
+  __shared__ uint32_t s_digit, s_krem, s_pos, s_above;
   __shared__ uint32_t s_cnt[2];
   __shared__ uint32_t c_bin[kClusterCtas], c_above[kClusterCtas];   // per CTA: keys in / above bin d1
   __shared__ uint32_t c_gt[kClusterCtas], c_eq[kClusterCtas];       // per CTA: keys above / equal to T
@@ -280,6 +281,7 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
 
   for (int i = tid; i < kBins; i += kCThreads) tot[i] = 0;
   for (int i = tid; i < kSubHists * kBins; i += kCThreads) sub[i] = 0;
+  if (tid == 0) { s_pos = 0; s_above = 0; }
   __syncthreads();
   cluster_arrive();   // my tot is zeroed (waited for once the keys are in)
 
@@ -334,19 +336,15 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   const uint32_t d1 = s_digit;
   uint32_t krem = s_krem;
   uint32_t T;
-  const bool fast = tot[d1] <= (uint32_t)kCandMax;
+  bool fast = tot[d1] <= (uint32_t)kCandMax;
   if (fast) {
-    // ---- usual path: every CTA sends its keys in bin d1 (low 21 bits) and
-    // its count of keys above the bin to every CTA; each CTA then finishes
-    // the select on the candidates alone, and knows every CTA's counts of
-    // keys above and equal to T, so no further cluster barrier is needed.
-    // A CTA's hist stays as it is until the barrier below, so the counts of
-    // bin d1 read here are stable.
-    if (warp == 0 && lane < kClusterCtas) c_bin[lane] = ld_dsmem(dsmem_addr(&hist[d1], (uint32_t)lane));
-    if (tid == 0) { s_pos = 0; s_above = 0; }
-    __syncthreads();
-    uint32_t base = 0;
-    for (uint32_t c = 0; c < rank; ++c) base += c_bin[c];
+    // ---- usual path: every CTA sends its keys in bin d1 (low 21 bits) to
+    // its own region of kRegion slots in every CTA's candidate list, and its
+    // counts of keys in and above the bin to every CTA; each CTA then
+    // finishes the select on the candidates alone and knows every CTA's
+    // counts of keys above and equal to T, so no further cluster barrier is
+    // needed.  A CTA with more than kRegion keys in the bin sends the first
+    // kRegion; all CTAs see its count and take the general path below.
     uint32_t above = 0;
     for (int i0 = 0; i0 < cnt; i0 += kCThreads) {   // CTA-uniform trip count
       const int i = i0 + tid;
@@ -357,29 +355,35 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
       uint32_t wb = 0;
       if (hb && lane == 0) wb = atomicAdd(&s_pos, (uint32_t)__popc(hb));
       wb = __shfl_sync(0xFFFFFFFFu, wb, 0);
-      if (hit) {
-        const uint32_t pos = base + wb + __popc(hb & ((1u << lane) - 1u));
+      const uint32_t pos = wb + __popc(hb & ((1u << lane) - 1u));
+      if (hit && pos < (uint32_t)kRegion) {
 #pragma unroll
         for (int c = 0; c < kClusterCtas; ++c)
-          st_dsmem(dsmem_addr(&cand_key[pos], (uint32_t)c), k & 0x1FFFFFu);
+          st_dsmem(dsmem_addr(&cand_key[rank * kRegion + pos], (uint32_t)c), k & 0x1FFFFFu);
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
     if (lane == 0 && above) atomicAdd(&s_above, above);
     __syncthreads();
-    if (warp == 0 && lane < kClusterCtas) st_dsmem(dsmem_addr(&c_above[rank], (uint32_t)lane), s_above);
+    if (warp == 0 && lane < kClusterCtas) {
+      st_dsmem(dsmem_addr(&c_above[rank], (uint32_t)lane), s_above);
+      st_dsmem(dsmem_addr(&c_bin[rank], (uint32_t)lane), s_pos);
+    }
     cluster_sync();                            // every CTA holds all candidates and counts
-    const uint32_t ncand = tot[d1];
+    for (int c = 0; c < kClusterCtas; ++c) fast = fast && c_bin[c] <= (uint32_t)kRegion;
+  }
+  if (fast) {
     uint32_t prefix = 0, mask = 0;
     for (int pass = 0; pass < 2; ++pass) {
       const int shift = pass == 0 ? 10 : 0;
       const uint32_t nbins = pass == 0 ? 2048u : 1024u;
       for (int i = tid; i < (int)nbins; i += kCThreads) hist[i] = 0;
       __syncthreads();
-      for (int j = tid; j < (int)ncand; j += kCThreads) {
+      for (int j = tid; j < kCandMax; j += kCThreads) {
         const uint32_t k = cand_key[j];
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
+        if ((uint32_t)(j % kRegion) < c_bin[j / kRegion] && (k & mask) == prefix)
+          atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
       }
       __syncthreads();
       find_digit(hist, nbins, krem, warp_sum, &s_digit, &s_krem);
@@ -391,11 +395,9 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     T = (d1 << 21) | prefix;
     // warp c: CTA c's keys above T (above bin d1, or candidates above) and equal to T
     if (warp < kClusterCtas) {
-      uint32_t b0 = 0;
-      for (int c = 0; c < warp; ++c) b0 += c_bin[c];
       uint32_t g = 0, e = 0;
-      for (uint32_t j = b0 + lane; j < b0 + c_bin[warp]; j += 32) {
-        const uint32_t k = cand_key[j];
+      for (uint32_t j = lane; j < c_bin[warp]; j += 32) {
+        const uint32_t k = cand_key[warp * kRegion + j];
         g += k > prefix ? 1u : 0u;
         e += k == prefix ? 1u : 0u;
       }
@@ -456,48 +458,31 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   }
   if (lane == 0) { warp_gt[warp] = g; warp_eq[warp] = e; }
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t wg = lane < kCWarps ? warp_gt[lane] : 0u, we = lane < kCWarps ? warp_eq[lane] : 0u;
-    uint32_t sg = wg, se = we;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, sg, o);
-      const uint32_t ve = __shfl_up_sync(0xFFFFFFFFu, se, o);
-      if (lane >= o) { sg += vg; se += ve; }
-    }
-    if (lane < kCWarps) { warp_gt[lane] = sg - wg; warp_eq[lane] = se - we; }
-    if (lane == 31) { s_cnt[0] = sg; s_cnt[1] = se; }
-  }
-  __syncthreads();
+  uint32_t gt_run = 0, eq_run = 0;   // keys above / equal to T before the warp's range, globally
+  for (int w = 0; w < warp; ++w) { gt_run += warp_gt[w]; eq_run += warp_eq[w]; }
   if (fast) {
-    if (tid == 0) {
-      uint32_t vg = 0, ve = 0;
-      for (uint32_t c = 0; c < rank; ++c) { vg += c_gt[c]; ve += c_eq[c]; }
-      s_base = vg;
-      s_pos = ve;
-    }
+    for (uint32_t c = 0; c < rank; ++c) { gt_run += c_gt[c]; eq_run += c_eq[c]; }
   } else {
-    cluster_sync();                                        // every CTA's totals are published
-    if (warp == 0) {   // lane c < rank reads CTA c's totals; sums go to s_base / s_pos
-      uint32_t vg = 0u, ve = 0u;
-      if ((uint32_t)lane < rank) {
-        vg = ld_dsmem(dsmem_addr(&s_cnt[0], (uint32_t)lane));
-        ve = ld_dsmem(dsmem_addr(&s_cnt[1], (uint32_t)lane));
-      }
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1) {
-        vg += __shfl_xor_sync(0xFFFFFFFFu, vg, o);
-        ve += __shfl_xor_sync(0xFFFFFFFFu, ve, o);
-      }
-      if (lane == 0) {
-        s_base = vg;
-        s_pos = ve;
-      }
+    if (tid == 0) {
+      uint32_t sg = 0, se = 0;
+      for (int w = 0; w < kCWarps; ++w) { sg += warp_gt[w]; se += warp_eq[w]; }
+      s_cnt[0] = sg;
+      s_cnt[1] = se;
     }
+    cluster_sync();                                        // every CTA's totals are published
+    uint32_t vg = 0u, ve = 0u;   // lane c < rank reads CTA c's totals
+    if ((uint32_t)lane < rank) {
+      vg = ld_dsmem(dsmem_addr(&s_cnt[0], (uint32_t)lane));
+      ve = ld_dsmem(dsmem_addr(&s_cnt[1], (uint32_t)lane));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      vg += __shfl_xor_sync(0xFFFFFFFFu, vg, o);
+      ve += __shfl_xor_sync(0xFFFFFFFFu, ve, o);
+    }
+    gt_run += __shfl_sync(0xFFFFFFFFu, vg, 0);   // lanes 0..7 hold the sums
+    eq_run += __shfl_sync(0xFFFFFFFFu, ve, 0);
   }
-  __syncthreads();
-  uint32_t gt_run = s_base + warp_gt[warp];   // keys above T before the warp's range, globally
-  uint32_t eq_run = s_pos + warp_eq[warp];    // T-equal keys before it, globally
   for (int i0 = w0; i0 < w1; i0 += 32) {
     const int i = i0 + lane;
     const uint32_t k = i < w1 ? keys[i] : 0u;
