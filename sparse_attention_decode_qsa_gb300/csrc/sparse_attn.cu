@@ -431,24 +431,32 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
 }
 
 // ---------------------------------------------------------------------------
-// FP8 rows (QSA_ROW_BYTES_FP8: E4M3 codes of K and V, then fp16 scales per
-// KV head).  Same work layout as the BF16 kernel; per token and KV head a
-// warp copies 272 bytes - the 128 K codes and 128 V codes of head g and the
-// row's 16 bytes of scales - half the host-link bytes of a BF16 row.  A
-// token's K scale multiplies its logit after the dot product, its V scale
-// its probability in P.V.
-constexpr int kSliceFp8 = 272;                        // K[g] codes | V[g] codes | scales
-constexpr int kChunksFp8 = kSliceFp8 / 16;            // 17
-constexpr int kWarpBufFp8 = kWarpTokens * kSliceFp8;  // 2176 B
+// FP8 rows (QSA_ROW_BYTES_FP8: E4M3 codes of K [4][128] and V [4][128], then
+// fp16 scales K[4], V[4]).  Same work layout as the BF16 kernel, except
+// that the four warps of a token half (one per KV head) share their rows:
+// per split they copy the half's 8 rows whole (8 x 1040 bytes, 16-byte
+// pieces; thread t of the half takes pieces t, t + 128, ...) into a stage
+// buffer, meet at a named barrier, and each warp then reads its head's
+// codes and scales from the staged rows.  A warp instruction so covers 512
+// contiguous bytes of a row, as in the BF16 kernel; fetching each head's
+// 128-byte code pieces and the 16 scale bytes separately (four times, once
+// per head) gave 2.5 times the requests per byte and 21 % more host-memory
+// sectors than the rows hold.  A token's K scale multiplies its logit after
+// the dot product, its V scale its probability in P.V.
+constexpr int kChunksRowFp8 = kRowBytesFp8 / 16;          // 65
+constexpr int kHalfRowsFp8 = kWarpTokens * kRowBytesFp8;  // 8320 B: a token half's rows
+constexpr int kHalfThreads = kThreads / 2;                // 128
 #ifndef QSA_ATTN_STAGES_FP8
 #define QSA_ATTN_STAGES_FP8 2
 #endif
 #ifndef QSA_ATTN_HOST_CTAS_FP8
 #define QSA_ATTN_HOST_CTAS_FP8 64
 #endif
-constexpr int kAStagesFp8 = QSA_ATTN_STAGES_FP8;      // splits in flight per warp
+constexpr int kAStagesFp8 = QSA_ATTN_STAGES_FP8;          // splits in flight per half
 constexpr int kMaxCtasHostFp8 = QSA_ATTN_HOST_CTAS_FP8;
-constexpr int kSmemFp8 = kWarps * kAStagesFp8 * kWarpBufFp8;
+constexpr int kSmemFp8 = 2 * kAStagesFp8 * kHalfRowsFp8;  // [half][stage][8][1040]
+static_assert(kRowBytesFp8 % 16 == 0, "FP8 rows are whole 16-byte pieces");
+static_assert(kAStagesFp8 >= 2, "a split is copied while the one before is computed");
 
 // Four E4M3 codes (bytes of w, low first) -> four floats (exact).
 __device__ __forceinline__ void e4m3x4_to_float4(uint32_t w, float& a, float& b, float& c, float& d) {
@@ -462,63 +470,65 @@ __device__ __forceinline__ void e4m3x4_to_float4(uint32_t w, float& a, float& b,
   a = f0.x; b = f0.y; c = f1.x; d = f1.y;
 }
 
-// Byte offset in an FP8 row of 16-byte chunk c of KV head g's slice:
-// c < 8 K codes, 8..15 V codes, 16 the row's scales.
-__device__ __forceinline__ int fp8_chunk_offset(int g, int c) {
-  return c < 8 ? g * kHeadDim + c * 16
-               : (c < 16 ? kKvHeads * kHeadDim + g * kHeadDim + (c - 8) * 16 : 2 * kKvHeads * kHeadDim);
+// Row code (resolve_row) of token `tok` of the k-th split the CTA visits,
+// and for a planned miss the hot row it goes to (else -1).
+__device__ __forceinline__ int32_t row_code_fp8(const AttnParams& p, int u, int k, int split, int tok,
+                                                int nsel, const int32_t* pend,
+                                                const int32_t* pcode, const int32_t* pdst,
+                                                int32_t* drow) {
+  if (k < kPreSplits) {
+    *drow = pdst[k * 16 + tok];
+    return pcode[k * 16 + tok];
+  }
+  return resolve_row(p, u, split, tok, nsel, pend, drow);
 }
 
-__device__ __forceinline__ uint32_t issue_warp_fp8(const AttnParams& p, int u, int k, int split, int nsel,
-                                                   int g, int half, uint8_t* buf,
-                                                   const int32_t* pend, const int32_t* pcode,
-                                                   const int32_t* pdst, uint8_t** dsts) {
-  const int lane = threadIdx.x & 31;
-  const uint8_t* src = nullptr;
-  if (lane < kWarpTokens) {
-    uint8_t* dst;
-    src = lane_source(p, u, k, split, nsel, half, pend, pcode, pdst, &dst);
-    dsts[lane] = dst;
+// The 128 threads of token half `half` copy its 8 rows of the k-th split
+// into rows ([8][1040]); absent rows are filled with zeros.
+__device__ __forceinline__ void issue_rows_fp8(const AttnParams& p, int u, int k, int split, int nsel,
+                                               int half, uint8_t* rows,
+                                               const int32_t* pend, const int32_t* pcode,
+                                               const int32_t* pdst) {
+  const int t = threadIdx.x & (kHalfThreads - 1);
+  for (int c = t; c < kWarpTokens * kChunksRowFp8; c += kHalfThreads) {
+    const int i = c / kChunksRowFp8, off = c - i * kChunksRowFp8;
+    int32_t drow;
+    const int32_t code = row_code_fp8(p, u, k, split, half * kWarpTokens + i, nsel, pend, pcode, pdst,
+                                      &drow);
+    const uint8_t* src = row_ptr(p, u, code);
+    cp_async16(rows + i * kRowBytesFp8 + off * 16, src ? src + off * 16 : p.b.pool, src ? 16u : 0u);
   }
-  const uint32_t valid = __ballot_sync(0xFFFFFFFFu, src != nullptr) & ((1u << kWarpTokens) - 1u);
-  // 8 tokens x 17 chunks: chunk c < 8 of K[g], 8..15 of V[g], 16 = scales
-#pragma unroll
-  for (int it = 0; it < (kWarpTokens * kChunksFp8 + 31) / 32; ++it) {
-    const int idx = it * 32 + lane;
-    const int tok = idx < kWarpTokens * kChunksFp8 ? idx / kChunksFp8 : 0;
-    const uint8_t* s = reinterpret_cast<const uint8_t*>(
-        __shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(src), tok));
-    if (idx < kWarpTokens * kChunksFp8) {
-      const int c = idx - tok * kChunksFp8;
-      cp_async16(buf + tok * kSliceFp8 + c * 16, s ? s + fp8_chunk_offset(g, c) : p.b.pool, s ? 16u : 0u);
-    }
-  }
-  return valid;
 }
 
-// FP8 rows: copy this warp's slices of the stage's planned misses (K[g] and
-// V[g] codes, and the row's scales, which every head's warp holds) into their
-// hot rows.
-__device__ __forceinline__ void write_back_fp8(uint8_t* const* dsts, const uint8_t* R, int g, int lane) {
-#pragma unroll
-  for (int it = 0; it < (kWarpTokens * kChunksFp8 + 31) / 32; ++it) {
-    const int idx = it * 32 + lane;
-    if (idx < kWarpTokens * kChunksFp8) {
-      const int tok = idx / kChunksFp8, c = idx - tok * kChunksFp8;
-      uint8_t* d = dsts[tok];
-      if (d && (c < 16 || g == 0))
-        *reinterpret_cast<uint4*>(d + fp8_chunk_offset(g, c)) =
-            *reinterpret_cast<const uint4*>(R + tok * kSliceFp8 + c * 16);
-    }
+// Planned misses of the k-th split: the half's threads copy the staged
+// pieces they fetched into the misses' hot rows.
+__device__ __forceinline__ void write_back_rows_fp8(const AttnParams& p, int u, int k, int split,
+                                                    int nsel, int half,
+                                                    const uint8_t* rows, const int32_t* pend,
+                                                    const int32_t* pcode, const int32_t* pdst) {
+  const int t = threadIdx.x & (kHalfThreads - 1);
+  for (int c = t; c < kWarpTokens * kChunksRowFp8; c += kHalfThreads) {
+    const int i = c / kChunksRowFp8, off = c - i * kChunksRowFp8;
+    int32_t drow;
+    row_code_fp8(p, u, k, split, half * kWarpTokens + i, nsel, pend, pcode, pdst, &drow);
+    if (drow >= 0)
+      *reinterpret_cast<uint4*>(p.b.pool + (int64_t)drow * p.b.row_bytes + off * 16) =
+          *reinterpret_cast<const uint4*>(rows + i * kRowBytesFp8 + off * 16);
   }
+}
+
+// Barrier of the 128 threads of one token half (named barriers 1 and 2).
+__device__ __forceinline__ void half_barrier(int half) {
+  if (half == 0)
+    asm volatile("bar.sync 1, %0;" ::"n"(kHalfThreads) : "memory");
+  else
+    asm volatile("bar.sync 2, %0;" ::"n"(kHalfThreads) : "memory");
 }
 
 __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnParams p) {
   grid_dependency_wait();
-  extern __shared__ __align__(16) uint8_t smem[];  // [warp][stage][8][272]
+  extern __shared__ __align__(16) uint8_t smem[];  // [half][stage][8][1040]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
-  __shared__ uint32_t vmask[kWarps][kAStagesFp8];
-  __shared__ uint8_t* pdst[kWarps][kAStagesFp8][kWarpTokens];
   __shared__ int32_t pre_code[kPreRows], pre_dst[kPreRows];
   __shared__ __align__(16) float xacc[kKvHeads][kGroup][kHeadDim];
 
@@ -526,7 +536,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   cta_unit(p, blockIdx.x, u, r, cpu);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = warp & 3, half = warp >> 2;
-  uint8_t* wbuf = smem + warp * kAStagesFp8 * kWarpBufFp8;
+  uint8_t* hbuf = smem + half * kAStagesFp8 * kHalfRowsFp8;
   int nsel = p.n_sel[u];
   if (nsel < 0 || nsel > p.k_max) {
     if (r == 0 && threadIdx.x == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
@@ -555,35 +565,41 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
 
   const int32_t* pend = pending_map(p, u);
   preload_rows(p, u, r, cpu, count, nsel, pend, pre_code, pre_dst);
+  // splits k + 1 .. k + kAStagesFp8 - 1 are in flight while split k is computed
 #pragma unroll
   for (int k = 0; k < kAStagesFp8 - 1; ++k) {
-    if (k < count) {
-      const uint32_t v = issue_warp_fp8(p, u, k, visit_split(k, count, r, cpu), nsel, g, half,
-                                        wbuf + k * kWarpBufFp8, pend, pre_code, pre_dst, pdst[warp][k]);
-      if (lane == 0) vmask[warp][k] = v;
-    }
+    if (k < count)
+      issue_rows_fp8(p, u, k, visit_split(k, count, r, cpu), nsel, half,
+                     hbuf + k * kHalfRowsFp8, pend, pre_code, pre_dst);
     cp_async_commit();
   }
   for (int k = 0; k < count; ++k) {
+    const int split = visit_split(k, count, r, cpu);
+    cp_async_wait<kAStagesFp8 - 2>();   // this thread's pieces of split k have landed
+    half_barrier(half);                 // everyone's have; split k - 1's stage is free
     const int kn = k + kAStagesFp8 - 1;
-    if (kn < count) {
-      const uint32_t v = issue_warp_fp8(p, u, kn, visit_split(kn, count, r, cpu), nsel, g, half,
-                                        wbuf + (kn % kAStagesFp8) * kWarpBufFp8, pend, pre_code,
-                                        pre_dst, pdst[warp][kn % kAStagesFp8]);
-      if (lane == 0) vmask[warp][kn % kAStagesFp8] = v;
-    }
+    if (kn < count)
+      issue_rows_fp8(p, u, kn, visit_split(kn, count, r, cpu), nsel, half,
+                     hbuf + (kn % kAStagesFp8) * kHalfRowsFp8, pend, pre_code, pre_dst);
     cp_async_commit();
-    cp_async_wait<kAStagesFp8 - 1>();
-    __syncwarp();
-    const uint32_t valid_cur = vmask[warp][k % kAStagesFp8];
-    const uint8_t* R = wbuf + (k % kAStagesFp8) * kWarpBufFp8;
-    if (pend) write_back_fp8(pdst[warp][k % kAStagesFp8], R, g, lane);
+    const uint8_t* R = hbuf + (k % kAStagesFp8) * kHalfRowsFp8;
+    if (pend) write_back_rows_fp8(p, u, k, split, nsel, half, R, pend, pre_code, pre_dst);
+    uint32_t valid_cur;
+    {
+      int32_t drow;
+      const int32_t code = lane < kWarpTokens
+                               ? row_code_fp8(p, u, k, split, half * kWarpTokens + lane, nsel, pend,
+                                              pre_code, pre_dst, &drow)
+                               : -1;
+      valid_cur = __ballot_sync(0xFFFFFFFFu, code != -1) & ((1u << kWarpTokens) - 1u);
+    }
 
     float x0 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kWarpTokens; ++i) {
+      const uint8_t* row = R + i * kRowBytesFp8;
       float k0, k1, k2, k3;
-      e4m3x4_to_float4(*reinterpret_cast<const uint32_t*>(R + i * kSliceFp8 + 4 * lane), k0, k1, k2, k3);
+      e4m3x4_to_float4(*reinterpret_cast<const uint32_t*>(row + g * kHeadDim + 4 * lane), k0, k1, k2, k3);
       float d[kGroup];
 #pragma unroll
       for (int j = 0; j < kGroup; ++j)
@@ -600,7 +616,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
       v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-      const float ks = __half2float(*reinterpret_cast<const __half*>(R + i * kSliceFp8 + 256 + 2 * g));
+      const float ks = __half2float(*reinterpret_cast<const __half*>(row + 2 * kKvHeads * kHeadDim + 2 * g));
       if ((lane & 7) == i) x0 = ((valid_cur >> i) & 1u) ? v * ks : -INFINITY;
     }
 
@@ -625,10 +641,12 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
     }
 #pragma unroll
     for (int i = 0; i < kWarpTokens; ++i) {
+      const uint8_t* row = R + i * kRowBytesFp8;
       float v0, v1, v2, v3;
-      e4m3x4_to_float4(*reinterpret_cast<const uint32_t*>(R + i * kSliceFp8 + kHeadDim + 4 * lane),
+      e4m3x4_to_float4(*reinterpret_cast<const uint32_t*>(row + kKvHeads * kHeadDim + g * kHeadDim + 4 * lane),
                        v0, v1, v2, v3);
-      const float vs = __half2float(*reinterpret_cast<const __half*>(R + i * kSliceFp8 + 256 + 8 + 2 * g));
+      const float vs = __half2float(
+          *reinterpret_cast<const __half*>(row + 2 * kKvHeads * kHeadDim + 2 * (kKvHeads + g)));
 #pragma unroll
       for (int j = 0; j < kGroup; ++j) {
         const float pj = __shfl_sync(0xFFFFFFFFu, p0, 8 * j + i) * vs;
@@ -638,7 +656,6 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
         acc[j][3] = fmaf(pj, v3, acc[j][3]);
       }
     }
-    __syncwarp();
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   finish_split(p, u, r, g, half, lane, hj, m_run, l_run, acc, xm, xl, xacc);
