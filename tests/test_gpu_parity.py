@@ -126,6 +126,34 @@ def test_topk_bit_exact_on_any_fp32_scores():
                 assert np.array_equal(sel[j, :len(ref)], ref), (ctxs[i], budget, len(pick))
 
 
+def test_topk_boundary_bin_crowded_into_one_cta():
+    """The boundary bin of the first 11-bit digit holds few keys overall (600,
+    within the 2048 the CTAs finish the select on) but all in one CTA's slice,
+    more than that CTA's 256 candidate slots: the call must take the general
+    path.  Also the same keys spread over every slice (the usual path), and
+    crowded into the last CTA.  Each equals the oracle's selection."""
+    rng = np.random.default_rng(5)
+    nb = 8192                       # 8 CTA slices of 1024 blocks
+    S = nb // 8
+    rows = []
+    for where in ("first", "spread", "last"):
+        v = np.full(nb, 0.001, np.float32)
+        lo, hi = {"first": (0, S), "spread": (0, nb), "last": (nb - S, nb)}[where]
+        inbin = rng.choice(np.arange(lo, hi), 600, replace=False)
+        rest = np.setdiff1d(np.arange(nb), inbin)
+        above = rng.choice(rest[rest >= S] if where != "last" else rest[rest < nb - S], 300,
+                           replace=False)
+        v[above] = 100.0 + rng.random(300).astype(np.float32)   # far above the bin
+        # 600 distinct keys sharing their top 11 bits (1.0 .. 1.0006)
+        v[inbin] = np.float32(1.0) + rng.permutation(600).astype(np.float32) * np.float32(2 ** -20)
+        rows.append(v)
+    sel, nsel = _run_select(rows, [4 * nb] * 3, 2048)
+    for j, v in enumerate(rows):
+        ref = O.select_blocks(v.astype(np.float64), 2048)
+        assert int(nsel[j]) == len(ref) == 512
+        assert np.array_equal(sel[j, :len(ref)], ref), j
+
+
 def _host_ring_workload(n_req=2, n_layers=2, n=20000, seed=5):
     return workloads.build(n_layers, [n] * n_req, [Q.KV_HOST_RING] * n_req,
                            lambda l, r, n: synth.planted_hot_cold(n // 4, 512, 1024,
