@@ -294,7 +294,37 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     // launch of 262144 tokens.)
     constexpr int kLoadBatch = 8;
     uint32_t* h = sub + (warp % kSubHists) * kBins;
-    for (int i0 = tid; i0 < cnt; i0 += kCThreads * kLoadBatch) {
+    const float* src = s + lo;
+    int done = 0;   // keys loaded by the vector path below
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      // four keys per 16-byte load, kLoadBatch / 2 loads in flight per thread
+      constexpr int kVec = kLoadBatch / 2;
+      const int n4 = cnt / 4;
+      const float4* src4 = reinterpret_cast<const float4*>(src);
+      for (int j0 = tid; j0 < n4; j0 += kCThreads * kVec) {
+        float4 v[kVec];
+#pragma unroll
+        for (int b = 0; b < kVec; ++b) {
+          const int j = j0 + b * kCThreads;
+          v[b] = j < n4 ? __ldg(src4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int b = 0; b < kVec; ++b) {
+          const int j = j0 + b * kCThreads;
+          if (j < n4) {
+            const uint4 k = make_uint4(order_key(v[b].x), order_key(v[b].y), order_key(v[b].z),
+                                       order_key(v[b].w));
+            *reinterpret_cast<uint4*>(keys + 4 * j) = k;
+            atomicAdd(&h[k.x >> 21], 1u);
+            atomicAdd(&h[k.y >> 21], 1u);
+            atomicAdd(&h[k.z >> 21], 1u);
+            atomicAdd(&h[k.w >> 21], 1u);
+          }
+        }
+      }
+      done = 4 * n4;
+    }
+    for (int i0 = done + tid; i0 < cnt; i0 += kCThreads * kLoadBatch) {
       float v[kLoadBatch];
 #pragma unroll
       for (int j = 0; j < kLoadBatch; ++j) {
@@ -345,21 +375,32 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     // counts of keys above and equal to T, so no further cluster barrier is
     // needed.  A CTA with more than kRegion keys in the bin sends the first
     // kRegion; all CTAs see its count and take the general path below.
+    // thread t takes the keys 4t .. 4t+3, then the next 4 x kCThreads (one
+    // 16-byte load); a thread with keys in the bin reserves their slots
+    // itself (they are few: one atomic per such thread and step)
     uint32_t above = 0;
-    for (int i0 = 0; i0 < cnt; i0 += kCThreads) {   // CTA-uniform trip count
-      const int i = i0 + tid;
-      const uint32_t k = i < cnt ? keys[i] : 0u;
-      const bool hit = i < cnt && (k >> 21) == d1;
-      above += (i < cnt && (k >> 21) > d1) ? 1u : 0u;
-      const uint32_t hb = __ballot_sync(0xFFFFFFFFu, hit);   // one slot reservation per warp
-      uint32_t wb = 0;
-      if (hb && lane == 0) wb = atomicAdd(&s_pos, (uint32_t)__popc(hb));
-      wb = __shfl_sync(0xFFFFFFFFu, wb, 0);
-      const uint32_t pos = wb + __popc(hb & ((1u << lane) - 1u));
-      if (hit && pos < (uint32_t)kRegion) {
+    const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // slice_cap is a multiple of 4
+    for (int j = tid; 4 * j < cnt; j += kCThreads) {
+      const uint4 q = k4[j];
+      const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+      uint32_t hits = 0;
 #pragma unroll
-        for (int c = 0; c < kClusterCtas; ++c)
-          st_dsmem(dsmem_addr(&cand_key[rank * kRegion + pos], (uint32_t)c), k & 0x1FFFFFu);
+      for (int e = 0; e < 4; ++e) {
+        const bool in = 4 * j + e < cnt;
+        hits |= (in && (kq[e] >> 21) == d1) ? (1u << e) : 0u;
+        above += (in && (kq[e] >> 21) > d1) ? 1u : 0u;
+      }
+      if (hits) {
+        uint32_t pos = atomicAdd(&s_pos, (uint32_t)__popc(hits));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (((hits >> e) & 1u) && pos < (uint32_t)kRegion) {
+#pragma unroll
+            for (int c = 0; c < kClusterCtas; ++c)
+              st_dsmem(dsmem_addr(&cand_key[rank * kRegion + pos], (uint32_t)c), kq[e] & 0x1FFFFFu);
+          }
+          pos += (hits >> e) & 1u;
+        }
       }
     }
 #pragma unroll
@@ -439,22 +480,32 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     T = prefix;
   }
 
-  // ---- warp w owns the contiguous keys [w*R, (w+1)*R) of the slice: it
-  // counts those above / equal to T 32 at a time (ballots; lanes read
-  // consecutive keys, so no bank conflicts - a contiguous run per thread
-  // put up to 32 lanes on one bank), a scan of the warp totals gives the
-  // offsets within the CTA, and a second walk over the range writes the
-  // selected ids in id order, after the keys of the lower-rank CTAs (known
-  // locally on the usual path, exchanged through DSMEM otherwise).
-  const int R = ((cnt + kCWarps - 1) / kCWarps + 31) / 32 * 32;
+  // ---- warp w owns the contiguous keys [w*R, (w+1)*R) of the slice (R a
+  // multiple of 128) and walks them 128 at a time, lane l taking keys 4l ..
+  // 4l+3 of each step (one 16-byte load).  A first walk counts the keys
+  // above / equal to T, a scan of the warp totals gives the offsets within
+  // the CTA, and a second walk writes the selected ids in id order (warp
+  // scans of the lanes' counts, only in steps that select a key), after the
+  // keys of the lower-rank CTAs (known locally on the usual path, exchanged
+  // through DSMEM otherwise).
+  const int R = ((cnt + kCWarps - 1) / kCWarps + 127) / 128 * 128;
   const int w0 = warp * R, w1 = w0 + R < cnt ? w0 + R : cnt;
-  const uint32_t lt_mask = (1u << lane) - 1u;
+  const uint4* kw = reinterpret_cast<const uint4*>(keys);
   uint32_t g = 0, e = 0;
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    const uint32_t k = i < w1 ? keys[i] : 0u;
-    g += __popc(__ballot_sync(0xFFFFFFFFu, i < w1 && k > T));
-    e += __popc(__ballot_sync(0xFFFFFFFFu, i < w1 && k == T));
+  for (int i0 = w0; i0 < w1; i0 += 128) {
+    const int i = i0 + 4 * lane;
+    const uint4 q = i < w1 ? kw[i / 4] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      g += (i + x < w1 && kq[x] > T) ? 1u : 0u;
+      e += (i + x < w1 && kq[x] == T) ? 1u : 0u;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
+    e += __shfl_xor_sync(0xFFFFFFFFu, e, o);
   }
   if (lane == 0) { warp_gt[warp] = g; warp_eq[warp] = e; }
   __syncthreads();
@@ -483,21 +534,39 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     gt_run += __shfl_sync(0xFFFFFFFFu, vg, 0);   // lanes 0..7 hold the sums
     eq_run += __shfl_sync(0xFFFFFFFFu, ve, 0);
   }
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    const uint32_t k = i < w1 ? keys[i] : 0u;
-    const bool gt = i < w1 && k > T, eq = i < w1 && k == T;
-    const uint32_t bg = __ballot_sync(0xFFFFFFFFu, gt), be = __ballot_sync(0xFFFFFFFFu, eq);
-    const uint32_t gb = gt_run + __popc(bg & lt_mask), eb = eq_run + __popc(be & lt_mask);
-    if (gt) {
-      const uint32_t pos = gb + min(eb, krem);
-      if (pos < (uint32_t)K) sel[pos] = (int32_t)(lo + i);
-    } else if (eq && eb < krem) {
-      const uint32_t pos = gb + eb;
-      if (pos < (uint32_t)K) sel[pos] = (int32_t)(lo + i);
+  for (int i0 = w0; i0 < w1; i0 += 128) {
+    const int i = i0 + 4 * lane;
+    const uint4 q = i < w1 ? kw[i / 4] : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+    uint32_t mg = 0, me = 0;   // this lane's keys above / equal to T
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      mg |= (i + x < w1 && kq[x] > T) ? (1u << x) : 0u;
+      me |= (i + x < w1 && kq[x] == T) ? (1u << x) : 0u;
     }
-    gt_run += __popc(bg);
-    eq_run += __popc(be);
+    if (!__any_sync(0xFFFFFFFFu, (mg | me) != 0u)) continue;   // warp-uniform
+    const uint32_t cg = __popc(mg), ce = __popc(me);
+    uint32_t ig = cg, ie = ce;   // inclusive scans over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, ig, o);
+      const uint32_t ve = __shfl_up_sync(0xFFFFFFFFu, ie, o);
+      if (lane >= o) { ig += vg; ie += ve; }
+    }
+    uint32_t gb = gt_run + ig - cg, eb = eq_run + ie - ce;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      if ((mg >> x) & 1u) {
+        const uint32_t pos = gb + min(eb, krem);
+        if (pos < (uint32_t)K) sel[pos] = (int32_t)(lo + i + x);
+        ++gb;
+      } else if ((me >> x) & 1u) {
+        if (eb < krem && gb + eb < (uint32_t)K) sel[gb + eb] = (int32_t)(lo + i + x);
+        ++eb;
+      }
+    }
+    gt_run += __shfl_sync(0xFFFFFFFFu, ig, 31);
+    eq_run += __shfl_sync(0xFFFFFFFFu, ie, 31);
   }
   trigger_dependents();
   if (!fast) cluster_sync();   // keep s_cnt alive until every CTA read it
