@@ -122,3 +122,35 @@ def test_fp8_append_stores_quantised_rows_like_the_oracle():
             assert int(c.slot_table[hs[1].index, 0, t]) == ring_row
     finally:
         wl.close()
+
+
+def test_fp8_many_host_units_in_one_launch():
+    """32 host-ring units in one attention launch share the 64 host-reading
+    CTAs: each CTA visits 64 splits, past the 32 whose row sources it
+    resolves up front, so the later ones resolve as they are copied.  Plain,
+    and with a hot cache planned into the attention over two steps (the
+    second reads rows the first wrote back); every selected token's HBM row
+    must hold its host row byte for byte, and the attention must match the
+    oracle."""
+    R, n = 32, 8200
+    plant = lambda l, r, n: synth.planted_hot_cold(n // 4, 512, 1024, synth.mix_seed(9, 90, l, r))
+    for hot in (0, 2048):
+        wl = workloads.build(1, [n] * R, [Q.KV_HOST_RING] * R, plant, staging_rows=8, seed=9,
+                             kv_format=Q.KV_FP8, hot_rows=hot)
+        wl.fold_fill = hot > 0
+        try:
+            for _ in range(2 if hot else 1):
+                wl.step()
+                torch.cuda.synchronize()
+                _clean(wl)
+                for r in (0, 13, 31):
+                    ref = QC.check_unit(wl, 0, r)["ref"]
+                    toks = ref["tokens"]
+                    h = wl.handles[r]
+                    slots = wl.cache.slot_table[h.index, 0, :n].cpu().numpy()[toks]   # ring or hot rows
+                    resident = slots >= 0
+                    pool_rows = wl.cache.pool[torch.from_numpy(slots[resident].astype(np.int64)).cuda()]
+                    host_rows = wl.host[r][0, torch.from_numpy(toks[resident].astype(np.int64))]
+                    assert torch.equal(pool_rows.cpu(), host_rows), (hot, r)
+        finally:
+            wl.close()
