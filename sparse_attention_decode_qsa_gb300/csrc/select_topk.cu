@@ -141,16 +141,18 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const TopkParams 
 // ---------------------------------------------------------------------------
 // Cluster version: a cluster of kClusterCtas CTAs of 512 threads per unit.
 // CTA r keeps the keys of its slice [r*S, (r+1)*S) of the unit's blocks in
-// shared memory.  The first digit (the top 11 bits of the key) is found from
-// a histogram that every CTA sums over all CTAs through distributed shared
-// memory (warp-aggregated atomics: block scores crowd into a few exponent
-// bins).  If the boundary bin holds at most kCandMax keys - the usual case -
-// the CTAs send those keys to CTA 0, which finishes the radix select alone
-// and publishes the threshold key T and the number of T-ties to keep; else
-// two more cluster-wide passes (11 and 10 bits) do it.  The compaction
-// exchanges per-CTA counts of blocks above and equal to T, so every CTA
-// writes its selected ids at their global ascending-id positions.  A CTA
-// takes half an SM's registers, so it can share an SM with other kernels.
+// shared memory.  The first digit (the top 11 bits of the key) comes from a
+// histogram that every CTA adds into every CTA's total with remote atomic
+// adds (block scores crowd into a few exponent bins, so few bins are
+// non-zero).  If the boundary bin holds at most kCandMax keys and no CTA
+// more than kRegion of them - the usual case - every CTA sends its keys in
+// that bin, and its counts of keys in and above it, to every CTA; each CTA
+// then finishes the radix select on the candidates (11 and 10 bits) and
+// knows every CTA's counts of keys above and equal to the threshold T, so it
+// writes its selected ids at their global ascending-id positions with no
+// further exchange.  Otherwise two more cluster-wide passes over every key
+// find T and the CTAs exchange their counts.  A CTA takes half an SM's
+// registers, so it can share an SM with other kernels.
 constexpr int kClusterCtas = 8;
 static_assert(kClusterCtas <= 8, "cross-CTA sums reduce over lanes 0..7");
 constexpr int kCThreads = 512;
