@@ -19,6 +19,8 @@ maximum over ranks.
 from __future__ import annotations
 
 import argparse
+import contextlib
+import gc
 import json
 import math
 import os
@@ -71,14 +73,39 @@ def config_block():
             "layer_order": "sequential", "l2": "inputs larger than L2 (1.66 GB index keys per step)"}
 
 
+@contextlib.contextmanager
+def quiet_host():
+    """No Python garbage collection inside a timed region.  On this Grace machine
+    the GPU reads the registered host histories through the CPU's page
+    tables (ATS): a host munmap anywhere in the process (the collector or an
+    allocator returning memory) invalidates the GPU's translations of those
+    pages, and the next step pays ~4 ms to take them again (measured: a 64 MiB
+    allocate-and-free between replays put a 5 ms step after each).  The
+    harness should not add that to the workload's steps."""
+    was = gc.isenabled()
+    gc.disable()
+    try:
+        yield
+    finally:
+        if was:
+            gc.enable()
+
+
 class Clocks:
-    """Sample SM clocks and throttle reasons with nvidia-smi during a region."""
+    """Sample SM clocks and throttle reasons with nvidia-smi during a region.
+    busy(), if given, keeps the GPU at work while the sampler starts (it
+    replays the measured step): the samples are then taken under load, and
+    the step's host-page translations are warm again when the timed region
+    begins (an idle GPU lets them go stale: measured, a 1 s pause left 9-15
+    of the next 40 steps 0.5-2 ms slower)."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, busy=None, dev=None):
         self.index = index
+        self.busy = busy
+        self.dev = dev
         self.proc = None
 
     def __enter__(self):
@@ -89,7 +116,13 @@ class Clocks:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        t_end = time.monotonic() + 0.3
+        if self.busy is None:
+            time.sleep(0.3)
+        while self.busy is not None and time.monotonic() < t_end:
+            for _ in range(8):
+                self.busy()
+            torch.cuda.synchronize(self.dev)
         return self
 
     def __exit__(self, *a):
@@ -375,15 +408,16 @@ def _replay_ms(graph, dev, args):
     then args.steps replays with a CUDA event after each on the launching
     stream."""
     cur = torch.cuda.current_stream(dev)
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize(dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(cur)
-    for i in range(args.steps):
-        graph.replay()
-        ev[i + 1].record(cur)
-    torch.cuda.synchronize(dev)
+    with quiet_host():
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        ev[0].record(cur)
+        for i in range(args.steps):
+            graph.replay()
+            ev[i + 1].record(cur)
+        torch.cuda.synchronize(dev)
     return [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
 
 
@@ -697,15 +731,15 @@ def run_ours(args, rank, world):
     # ---- the measured step: request groups on their own streams, captured
     # once as a CUDA graph and replayed
     graph = wl.capture(args.groups)
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize(dev)
     # an event after every replay gives the per-step spread (no extra syncs)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    with Clocks(dev.index) as clk:
+    with quiet_host(), Clocks(dev.index, busy=graph.replay, dev=dev) as clk:
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
         ev[0].record(stream)
         for i in range(args.steps):
             graph.replay()
@@ -732,15 +766,16 @@ def run_ours(args, rank, world):
         hout.copy_(wl.out, non_blocking=True)
         hlse.copy_(wl.lse, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    with quiet_host():
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
     ms_e2e = e0.elapsed_time(e1)
     st, det = wl.cache.poll_error()
     if st != 0:
