@@ -403,13 +403,19 @@ def hbm_resident_timing(dev, args):
         wl.close()
 
 
-def _replay_ms(graph, dev, args):
-    """Per-replay times (ms) of a captured step: args.warmup untimed replays,
-    then args.steps replays with a CUDA event after each on the launching
-    stream."""
+def _replay_ms(graph, dev, args, settle_s=0.3):
+    """Per-replay times (ms) of a captured step: untimed replays for settle_s
+    seconds (the step's host-page translations are taken again after the
+    workload's set-up), args.warmup untimed replays, then args.steps replays
+    with a CUDA event after each on the launching stream."""
     cur = torch.cuda.current_stream(dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with quiet_host():
+        t_end = time.monotonic() + settle_s
+        while time.monotonic() < t_end:
+            for _ in range(8):
+                graph.replay()
+            torch.cuda.synchronize(dev)
         for _ in range(args.warmup):
             graph.replay()
         torch.cuda.synchronize(dev)

@@ -459,8 +459,13 @@ qsa_status_t qsa_sparse_decode_attn(qsa_cache* cache, const qsa_batch* batch,
  * virtual range that the device's own page tables and the host's page
  * tables both hold, at the same address.  Pages that are only registered
  * with cudaHostRegister are reached, on an NVLink-C2C system, through the
- * CPU's page tables one 64 KiB page at a time.  bytes is rounded up to
- * 2 MiB.  Pass the address as qsa_request_desc.host_rows of a cache whose
+ * CPU's page tables one 64 KiB page at a time: read faster while the GPU's
+ * cached translations of them are warm, but any munmap in the process (an
+ * allocator returning memory) drops those translations, an idle GPU lets
+ * them go stale, and a step that touches new pages pays for each; memory
+ * from this call reads slower (~70 GB/s of random rows on a GB300 against
+ * up to ~186 GB/s) but at the same rate whatever the process does.  bytes
+ * is rounded up to 2 MiB.  Pass the address as qsa_request_desc.host_rows of a cache whose
  * storage is on `device`; the host reads and writes the memory like any
  * other.  Free it with qsa_host_free once no request uses it.
  * [RTX4090 port, memory-ledger section: the full history stays in pinned
