@@ -91,7 +91,7 @@ constexpr int kCtasPerSm = QSA_K1_CTAS_PER_SM;
 #define QSA_K1_MAXREG 56
 #endif
 #ifndef QSA_K1_CHUNK
-#define QSA_K1_CHUNK 4
+#define QSA_K1_CHUNK 2   // measured against 1, 4, 8, 16 (8 x 262144 tokens: 30.6 / 26.9 / 27.4 / 28.8 / 29.0 us)
 #endif
 constexpr int kChunk = QSA_K1_CHUNK;            // tiles per grab from a unit's work counter
 constexpr int kRawBytes = kTile * kIndexDim;    // 8 KiB of codes per tile
