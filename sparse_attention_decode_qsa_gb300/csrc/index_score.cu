@@ -334,7 +334,6 @@ __device__ __forceinline__ int build_pieces(const IndexScoreParams& p, int u, ui
 
 __global__ void __maxnreg__(QSA_K1_MAXREG)
 index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
-  grid_dependency_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the swizzled stages and B slots need 1024-byte alignment
   uint8_t* smem0 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -376,6 +375,10 @@ index_score_tc_kernel(const __grid_constant__ IndexScoreParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot + (uint32_t)pl * kPipeCols;   // this pipeline's columns
+  // Everything above touches only shared and tensor memory and the
+  // parameters, so it overlaps the tail of the kernel before this one;
+  // the work counters, the query and the keys are read only after it.
+  grid_dependency_wait();
 
   if (role == kRoleProd) {
     // ---- producer (whole warp; lane 0 does the atomics, waits and copies).

@@ -123,10 +123,11 @@ __device__ __forceinline__ const uint8_t* row_source(const BatchDesc& b, int u, 
 
 // Programmatic dependent launch.  Every hot-path kernel of the library is
 // launched with programmatic stream serialization (launch_kernel below), and
-// its first statement is grid_dependency_wait(), which returns once the
-// kernel before it on the stream has completed and its memory operations are
-// visible (at once when there is none): measured on the 8 x 262144-token
-// step, 1.191 -> 1.175 ms.  The main kernels also trigger their dependents
+// calls grid_dependency_wait() before its first global-memory access (set-up
+// that touches only shared or tensor memory and the parameters comes first);
+// it returns once the kernel before it on the stream has completed and its
+// memory operations are visible (at once when there is none): measured on
+// the 8 x 262144-token step, 1.191 -> 1.175 ms.  The main kernels also trigger their dependents
 // where their CTAs' main work ends (trigger_dependents below).
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -248,7 +248,6 @@ __device__ __forceinline__ void red_dsmem(uint32_t addr, uint32_t v) {
 
 // 40 registers x 512 threads: a CTA fits on an SM beside two index-score CTAs.
 __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, int slice_cap) {
-  grid_dependency_wait();
   extern __shared__ __align__(16) uint32_t dyn[];
   uint32_t* keys = dyn;                                   // [slice_cap]
   uint32_t* sub = dyn + slice_cap;                        // [kSubHists][kBins], first digit
@@ -274,17 +273,22 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   const int64_t lo = (int64_t)rank * S;
   const int64_t hi = lo + S < nb ? lo + S : nb;
   const int cnt = hi > lo ? (int)(hi - lo) : 0;
+
+  // the histograms are zeroed before the wait for the kernel before this
+  // one (shared memory only), so that work overlaps its tail
+  if (K != nb) {
+    for (int i = tid; i < kBins; i += kCThreads) tot[i] = 0;
+    for (int i = tid; i < kSubHists * kBins; i += kCThreads) sub[i] = 0;
+    if (tid == 0) { s_pos = 0; s_above = 0; }
+  }
+  __syncthreads();
+  grid_dependency_wait();
   if (rank == 0 && tid == 0) p.n_sel[u] = K;
 
   if (K == nb) {  // dense path: every block, in order
     for (int i = tid; i < cnt; i += kCThreads) sel[lo + i] = (int32_t)(lo + i);
     return;       // uniform across the cluster: no DSMEM access follows
   }
-
-  for (int i = tid; i < kBins; i += kCThreads) tot[i] = 0;
-  for (int i = tid; i < kSubHists * kBins; i += kCThreads) sub[i] = 0;
-  if (tid == 0) { s_pos = 0; s_above = 0; }
-  __syncthreads();
   cluster_arrive();   // my tot is zeroed (waited for once the keys are in)
 
   // ---- first digit: bits 31..21, counted into kSubHists copies while the

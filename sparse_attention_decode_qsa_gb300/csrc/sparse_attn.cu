@@ -296,7 +296,6 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, int u, int r, 
 }
 
 __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams p) {
-  grid_dependency_wait();
   extern __shared__ __align__(16) uint8_t smem[];  // [warp][stage][8][512]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ uint32_t vmask[kWarps][kAStages];     // tokens present in each stage
@@ -309,6 +308,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = warp & 3, half = warp >> 2;
   uint8_t* wbuf = smem + warp * kAStages * kWarpBufBytes;
+  grid_dependency_wait();   // the selection is read from here on
   int nsel = p.n_sel[u];
   if (nsel < 0 || nsel > p.k_max) {
     if (r == 0 && threadIdx.x == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
@@ -526,7 +526,6 @@ __device__ __forceinline__ void half_barrier(int half) {
 }
 
 __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnParams p) {
-  grid_dependency_wait();
   extern __shared__ __align__(16) uint8_t smem[];  // [half][stage][8][1040]
   __shared__ float xm[kKvHeads][kGroup], xl[kKvHeads][kGroup];
   __shared__ int32_t pre_code[kPreRows], pre_dst[kPreRows];
@@ -537,6 +536,7 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_fp8_kernel(const AttnPar
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = warp & 3, half = warp >> 2;
   uint8_t* hbuf = smem + half * kAStagesFp8 * kHalfRowsFp8;
+  grid_dependency_wait();   // the selection is read from here on
   int nsel = p.n_sel[u];
   if (nsel < 0 || nsel > p.k_max) {
     if (r == 0 && threadIdx.x == 0) report_error(p.b.err, QSA_ERR_BAD_BLOCK, kKernAttn, nsel);
