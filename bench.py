@@ -311,10 +311,11 @@ def fp8_timing(dev, args):
 def hbm_resident_timing(dev, args):
     """The HBM-resident configuration: 1 request x 12 layers x 131072 tokens,
     every KV row in HBM.  Times (CUDA events, captured graphs) the faithful
-    layer-sequential step (12 dependent layers of one request), the upper
-    bound with the 12 layers batched into one call per kernel, each kernel
-    over the 12 units, and each kernel over one unit (the launches of the
-    layer-sequential chain)."""
+    layer-sequential step (12 dependent layers of one request) and the upper
+    bound with the 12 layers batched into one call per kernel, each step by
+    its own events after warm-up (mean, p10, median, p90), then each kernel
+    over the 12 units and over one unit (the launches of the
+    layer-sequential chain), averaged over repeated launches."""
     from sparse_attention_decode_qsa_gb300 import workloads
     wl = workloads.c128k(device=dev)
     try:
@@ -370,10 +371,23 @@ def hbm_resident_timing(dev, args):
             c.sparse_decode_attn(hs, 0, 1, wl.q[:1], wl.sel[:1], wl.nsel[:1], BUDGET, None,
                                  wl.softmax_scale, wl.out[:1], wl.lse[:1], s)
 
-        t = {k: gtime(f, r) for k, f, r in [("seq", seq, 1), ("batched", batched, 1), ("score", score, 10),
-                                             ("topk", topk, 10), ("attn", attn, 10),
-                                             ("score1", score1, 10), ("topk1", topk1, 10),
-                                             ("attn1", attn1, 10)]}
+        def capture(fn):
+            s = torch.cuda.Stream()
+            s.wait_stream(cur)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                fn(s)
+            g.replay()
+            torch.cuda.synchronize(dev)
+            return g
+
+        # the two steps: per-step CUDA events after warm-up (median, p10, p90)
+        steps_ms = {k: _replay_ms(capture(f), dev, args) for k, f in [("seq", seq), ("batched", batched)]}
+        t = {k: 1e3 * sum(v) / len(v) for k, v in steps_ms.items()}
+        pcts = {k: [round(1e3 * _pct(v, q), 2) for q in (0.1, 0.5, 0.9)] for k, v in steps_ms.items()}
+        t.update({k: gtime(f, r) for k, f, r in [("score", score, 10), ("topk", topk, 10), ("attn", attn, 10),
+                                                  ("score1", score1, 10), ("topk1", topk1, 10),
+                                                  ("attn1", attn1, 10)]})
         st, det = c.poll_error()
         if st != 0:
             raise RuntimeError(f"device error word {st} ({det}) in the HBM-resident timing")
@@ -384,10 +398,12 @@ def hbm_resident_timing(dev, args):
         return {"workload": f"c128k: 1 request x {L} layers x {n} tokens, KV in HBM",
                 "algorithmic_bytes_per_step": key_b + row_b,
                 "layer_sequential": {"us_per_step": round(t["seq"], 2),
+                                     "step_us_p10_p50_p90": pcts["seq"],
                                      "layer_steps_per_s": round(L / (t["seq"] * 1e-6), 1),
                                      "hbm_gbs": gbs(key_b + row_b, t["seq"]),
                                      "frac": round(gbs(key_b + row_b, t["seq"]) / hbm_peak, 4)},
                 "layers_batched_upper_bound": {"us_per_step": round(t["batched"], 2),
+                                               "step_us_p10_p50_p90": pcts["batched"],
                                                "hbm_gbs": gbs(key_b + row_b, t["batched"]),
                                                "frac": round(gbs(key_b + row_b, t["batched"]) / hbm_peak, 4)},
                 "kernels_12_units": {

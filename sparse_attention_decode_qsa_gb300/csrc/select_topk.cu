@@ -147,8 +147,10 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const TopkParams 
 // non-zero).  If the boundary bin holds at most kCandMax keys and no CTA
 // more than kRegion of them - the usual case - every CTA sends its keys in
 // that bin, and its counts of keys in and above it, to every CTA; each CTA
-// then finishes the radix select on the candidates (11 and 10 bits) and
-// knows every CTA's counts of keys above and equal to the threshold T, so it
+// then finds the threshold T among the candidates (one warp ranks them
+// directly when they are at most 32, as for planted workloads, where the
+// K-th score stands alone in its bin; else a radix select of 11 and 10
+// bits) and knows every CTA's counts of keys above and equal to T, so it
 // writes its selected ids at their global ascending-id positions with no
 // further exchange.  Otherwise two more cluster-wide passes over every key
 // find T and the CTAs exchange their counts.  A CTA takes half an SM's
@@ -421,23 +423,60 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     for (int c = 0; c < kClusterCtas; ++c) fast = fast && c_bin[c] <= (uint32_t)kRegion;
   }
   if (fast) {
-    uint32_t prefix = 0, mask = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-      const int shift = pass == 0 ? 10 : 0;
-      const uint32_t nbins = pass == 0 ? 2048u : 1024u;
-      for (int i = tid; i < (int)nbins; i += kCThreads) hist[i] = 0;
-      __syncthreads();
-      for (int j = tid; j < kCandMax; j += kCThreads) {
-        const uint32_t k = cand_key[j];
-        if ((uint32_t)(j % kRegion) < c_bin[j / kRegion] && (k & mask) == prefix)
-          atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
+    uint32_t prefix = 0;
+    if (tot[d1] <= 32u) {
+      // At most 32 keys in the bin (the usual case: the K-th block score
+      // stands alone in its first-digit bin): warp 0 ranks them directly.
+      // Lane i holds candidate i; its value is the krem-th largest when
+      // fewer than krem candidates are greater and at least krem are
+      // greater or equal.  krem then becomes the number of keys equal to T
+      // that are taken (krem minus the candidates above T), as after the
+      // radix passes.
+      if (warp == 0) {
+        const uint32_t C = tot[d1];
+        const bool valid = (uint32_t)lane < C;
+        uint32_t v = 0;
+        if (valid) {
+          uint32_t i = (uint32_t)lane, c = 0;
+          while (c + 1 < (uint32_t)kClusterCtas && i >= c_bin[c]) { i -= c_bin[c]; ++c; }
+          v = cand_key[c * kRegion + i];
+        }
+        uint32_t gt = 0, eq = 0;
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t vj = __shfl_sync(0xFFFFFFFFu, v, j);
+          const bool in = (uint32_t)j < C;
+          gt += (in && vj > v) ? 1u : 0u;
+          eq += (in && vj == v) ? 1u : 0u;
+        }
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, valid && gt < krem && krem <= gt + eq);
+        const int src = hit ? __ffs(hit) - 1 : 0;
+        const uint32_t t = __shfl_sync(0xFFFFFFFFu, v, src);
+        const uint32_t g_hit = __shfl_sync(0xFFFFFFFFu, gt, src);
+        if (lane == 0) { s_digit = t; s_krem = krem - g_hit; }
       }
       __syncthreads();
-      find_digit(hist, nbins, krem, warp_sum, &s_digit, &s_krem);
-      prefix |= s_digit << shift;
-      mask |= (nbins - 1) << shift;
+      prefix = s_digit;
       krem = s_krem;
-      __syncthreads();
+    } else {
+      // two radix passes over the candidates (11 and 10 bits)
+      uint32_t mask = 0;
+      for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const uint32_t nbins = pass == 0 ? 2048u : 1024u;
+        for (int i = tid; i < (int)nbins; i += kCThreads) hist[i] = 0;
+        __syncthreads();
+        for (int j = tid; j < kCandMax; j += kCThreads) {
+          const uint32_t k = cand_key[j];
+          if ((uint32_t)(j % kRegion) < c_bin[j / kRegion] && (k & mask) == prefix)
+            atomicAdd(&hist[(k >> shift) & (nbins - 1)], 1u);
+        }
+        __syncthreads();
+        find_digit(hist, nbins, krem, warp_sum, &s_digit, &s_krem);
+        prefix |= s_digit << shift;
+        mask |= (nbins - 1) << shift;
+        krem = s_krem;
+        __syncthreads();
+      }
     }
     T = (d1 << 21) | prefix;
     // warp c: CTA c's keys above T (above bin d1, or candidates above) and equal to T

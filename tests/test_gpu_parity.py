@@ -126,6 +126,40 @@ def test_topk_bit_exact_on_any_fp32_scores():
                 assert np.array_equal(sel[j, :len(ref)], ref), (ctxs[i], budget, len(pick))
 
 
+def test_topk_small_boundary_bin_with_ties():
+    """At most 32 keys in the bin of the first 11-bit digit that holds the
+    K-th largest score, the case the planted workloads meet (there the K-th
+    score is alone in its bin), which the top-k settles by ranking the few
+    candidates directly: ties at the threshold, distinct values above it in
+    the same bin, and bins of 32 and 33 keys (both sides of that switch).
+    131072 tokens (8 CTAs of 4096 blocks), K = 512, bin keys spread over
+    the CTAs; compared with the oracle's selection."""
+    rng = np.random.default_rng(29)
+    n, budget = 131072, 2048
+    nb, K = n // 4, budget // 4
+
+    def digit(x):   # first 11 bits of the order-preserving key of a positive float
+        return int((np.float32(x).view(np.uint32) | np.uint32(0x80000000)) >> np.uint32(21))
+
+    assert len({digit(x) for x in (2.0, 2.125, 2.25, 2.375)}) == 1
+    assert digit(2.5) != digit(2.0) and digit(0.001) != digit(2.0)
+    for n_top, n_eq, n_other in [(500, 20, 8), (511, 1, 0), (492, 24, 8), (492, 25, 8), (480, 32, 0),
+                                 (510, 3, 29), (505, 10, 10)]:
+        v = np.full(nb, 0.001, np.float32)
+        top = rng.choice(nb, n_top, replace=False)
+        v[top] = 1000 + np.arange(n_top, dtype=np.float32)
+        rest = np.setdiff1d(np.arange(nb), top)
+        pos = rng.choice(rest, n_eq + n_other, replace=False)
+        v[pos[:n_eq]] = 2.0
+        v[pos[n_eq:]] = rng.choice(np.array([2.125, 2.25, 2.375], np.float32), n_other)
+        # the K-th largest lies in the bin of 2.0, which holds n_eq + n_other keys
+        assert n_top < K <= n_top + n_eq + n_other
+        sel, nsel = _run_select([v], [n], budget)
+        ref = O.select_blocks(v.astype(np.float64), budget)
+        assert int(nsel[0]) == len(ref) == K
+        assert np.array_equal(sel[0, :K], ref), (n_top, n_eq, n_other)
+
+
 def test_topk_boundary_bin_crowded_into_one_cta():
     """The boundary bin of the first 11-bit digit holds few keys overall (600,
     within the 2048 the CTAs finish the select on) but all in one CTA's slice,
