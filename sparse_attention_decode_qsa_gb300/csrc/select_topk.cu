@@ -159,6 +159,7 @@ constexpr int kClusterCtas = 8;
 static_assert(kClusterCtas <= 8, "cross-CTA sums reduce over lanes 0..7");
 constexpr int kCThreads = 512;
 constexpr int kCWarps = kCThreads / 32;
+static_assert(kCWarps <= 32 && kClusterCtas <= 32, "per-warp and per-CTA counts are summed by one warp");
 constexpr int kMaxSlice = 32768;  // keys per CTA: 8 x 32768 blocks = 1M tokens
 constexpr int kBins = 2048;
 constexpr int kCandMax = 2048;    // boundary-bin keys the CTAs finish the select on
@@ -351,19 +352,16 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     }
   }
   __syncthreads();
-  for (int b = tid; b < kBins; b += kCThreads) {
-    uint32_t t = 0;
-#pragma unroll
-    for (int c = 0; c < kSubHists; ++c) t += sub[c * kBins + b];
-    hist[b] = t;
-  }
-  __syncthreads();
-  // The cluster's histogram: every CTA adds its non-zero bins into every
-  // CTA's tot (remote atomic adds, fire and forget; block scores crowd into
-  // few bins), so each CTA then holds the sum locally.
+  // The cluster's histogram: every CTA adds its non-zero bins (the sums of
+  // its sub-histograms) into every CTA's tot (remote atomic adds, fire and
+  // forget; block scores crowd into few bins), so each CTA then holds the
+  // sum locally.  The sub-histograms are read here for the last time: the
+  // candidates that later land in the same space come after the barrier.
   cluster_wait();                              // every CTA's tot is zeroed
   for (int b = tid; b < kBins; b += kCThreads) {
-    const uint32_t v = hist[b];
+    uint32_t v = 0;
+#pragma unroll
+    for (int c = 0; c < kSubHists; ++c) v += sub[c * kBins + b];
     if (v) {
 #pragma unroll
       for (int c = 0; c < kClusterCtas; ++c) red_dsmem(dsmem_addr(&tot[b], (uint32_t)c), v);
@@ -528,11 +526,11 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   // ---- warp w owns the contiguous keys [w*R, (w+1)*R) of the slice (R a
   // multiple of 128) and walks them 128 at a time, lane l taking keys 4l ..
   // 4l+3 of each step (one 16-byte load).  A first walk counts the keys
-  // above / equal to T, a scan of the warp totals gives the offsets within
-  // the CTA, and a second walk writes the selected ids in id order (warp
-  // scans of the lanes' counts, only in steps that select a key), after the
-  // keys of the lower-rank CTAs (known locally on the usual path, exchanged
-  // through DSMEM otherwise).
+  // above / equal to T, one warp sum of the lower warps' totals gives the
+  // offsets within the CTA, and a second walk writes the selected ids in id
+  // order (ballots per key position count the lower lanes' keys, only in
+  // steps that select a key), after the keys of the lower-rank CTAs (known
+  // locally on the usual path, exchanged through DSMEM otherwise).
   const int R = ((cnt + kCWarps - 1) / kCWarps + 127) / 128 * 128;
   const int w0 = warp * R, w1 = w0 + R < cnt ? w0 + R : cnt;
   const uint4* kw = reinterpret_cast<const uint4*>(keys);
@@ -554,11 +552,18 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   }
   if (lane == 0) { warp_gt[warp] = g; warp_eq[warp] = e; }
   __syncthreads();
-  uint32_t gt_run = 0, eq_run = 0;   // keys above / equal to T before the warp's range, globally
-  for (int w = 0; w < warp; ++w) { gt_run += warp_gt[w]; eq_run += warp_eq[w]; }
-  if (fast) {
-    for (uint32_t c = 0; c < rank; ++c) { gt_run += c_gt[c]; eq_run += c_eq[c]; }
-  } else {
+  // keys above / equal to T before the warp's range, globally: lane i adds
+  // the counts of warp i < warp (and, on the usual path, of CTA i < rank),
+  // then the warp sums them
+  uint32_t gt_run = 0, eq_run = 0;
+  if (lane < warp) { gt_run = warp_gt[lane]; eq_run = warp_eq[lane]; }
+  if (fast && (uint32_t)lane < rank) { gt_run += c_gt[lane]; eq_run += c_eq[lane]; }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gt_run += __shfl_xor_sync(0xFFFFFFFFu, gt_run, o);
+    eq_run += __shfl_xor_sync(0xFFFFFFFFu, eq_run, o);
+  }
+  if (!fast) {
     if (tid == 0) {
       uint32_t sg = 0, se = 0;
       for (int w = 0; w < kCWarps; ++w) { sg += warp_gt[w]; se += warp_eq[w]; }
@@ -590,15 +595,19 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
       me |= (i + x < w1 && kq[x] == T) ? (1u << x) : 0u;
     }
     if (!__any_sync(0xFFFFFFFFu, (mg | me) != 0u)) continue;   // warp-uniform
-    const uint32_t cg = __popc(mg), ce = __popc(me);
-    uint32_t ig = cg, ie = ce;   // inclusive scans over the lanes
+    // keys of the lower lanes come first in id order: one ballot per key
+    // position counts them, with no chain of dependent shuffles
+    const uint32_t below = (1u << lane) - 1u;
+    uint32_t gb = gt_run, eb = eq_run, tg = 0, te = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, ig, o);
-      const uint32_t ve = __shfl_up_sync(0xFFFFFFFFu, ie, o);
-      if (lane >= o) { ig += vg; ie += ve; }
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t bg = __ballot_sync(0xFFFFFFFFu, (mg >> x) & 1u);
+      const uint32_t be = __ballot_sync(0xFFFFFFFFu, (me >> x) & 1u);
+      gb += __popc(bg & below);
+      eb += __popc(be & below);
+      tg += __popc(bg);
+      te += __popc(be);
     }
-    uint32_t gb = gt_run + ig - cg, eb = eq_run + ie - ce;
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       if ((mg >> x) & 1u) {
@@ -610,8 +619,8 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
         ++eb;
       }
     }
-    gt_run += __shfl_sync(0xFFFFFFFFu, ig, 31);
-    eq_run += __shfl_sync(0xFFFFFFFFu, ie, 31);
+    gt_run += tg;
+    eq_run += te;
   }
   trigger_dependents();
   if (!fast) cluster_sync();   // keep s_cnt alive until every CTA read it
