@@ -160,6 +160,7 @@ static_assert(kClusterCtas <= 8, "cross-CTA sums reduce over lanes 0..7");
 constexpr int kCThreads = 512;
 constexpr int kCWarps = kCThreads / 32;
 static_assert(kCWarps <= 32 && kClusterCtas <= 32, "per-warp and per-CTA counts are summed by one warp");
+static_assert(kCThreads > kClusterCtas * 32, "warps beyond the first kClusterCtas credit the candidates");
 constexpr int kMaxSlice = 32768;  // keys per CTA: 8 x 32768 blocks = 1M tokens
 constexpr int kBins = 2048;
 constexpr int kCandMax = 2048;    // boundary-bin keys the CTAs finish the select on
@@ -264,6 +265,7 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   __shared__ uint32_t c_bin[kClusterCtas], c_above[kClusterCtas];   // per CTA: keys in / above bin d1
   __shared__ uint32_t c_gt[kClusterCtas], c_eq[kClusterCtas];       // per CTA: keys above / equal to T
   __shared__ uint32_t warp_gt[kCWarps], warp_eq[kCWarps];
+  __shared__ uint32_t cand_idx[kRegion];                            // slice index of my candidates
 
   const uint32_t rank = cluster_rank();
   const int u = blockIdx.x / kClusterCtas;
@@ -372,6 +374,12 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
   const uint32_t d1 = s_digit;
   uint32_t krem = s_krem;
   uint32_t T;
+  // warp w owns the contiguous keys [w*R, (w+1)*R) of the slice (R a multiple
+  // of 128) in the walks below, lane l taking keys 4l .. 4l+3 of each step of
+  // 128 (one 16-byte load)
+  const int R = ((cnt + kCWarps - 1) / kCWarps + 127) / 128 * 128;
+  const int w0 = warp * R, w1 = w0 + R < cnt ? w0 + R : cnt;
+  const uint4* kw = reinterpret_cast<const uint4*>(keys);   // slice_cap is a multiple of 4
   bool fast = tot[d1] <= (uint32_t)kCandMax;
   if (fast) {
     // ---- usual path: every CTA sends its keys in bin d1 (low 21 bits) to
@@ -381,18 +389,21 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     // counts of keys above and equal to T, so no further cluster barrier is
     // needed.  A CTA with more than kRegion keys in the bin sends the first
     // kRegion; all CTAs see its count and take the general path below.
-    // thread t takes the keys 4t .. 4t+3, then the next 4 x kCThreads (one
-    // 16-byte load); a thread with keys in the bin reserves their slots
-    // itself (they are few: one atomic per such thread and step)
+    // The walk is the compaction's (warp ranges), so each warp's count of
+    // keys above the bin (all above T) comes with it, and the slice index
+    // of each candidate is kept to credit it to its warp once T is known:
+    // the usual path needs no separate counting walk.  A lane with keys in
+    // the bin reserves their slots itself (they are few: one atomic per such
+    // lane and step).
     uint32_t above = 0;
-    const uint4* k4 = reinterpret_cast<const uint4*>(keys);   // slice_cap is a multiple of 4
-    for (int j = tid; 4 * j < cnt; j += kCThreads) {
-      const uint4 q = k4[j];
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+      const int i = i0 + 4 * lane;
+      const uint4 q = i < w1 ? kw[i / 4] : make_uint4(0u, 0u, 0u, 0u);
       const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
       uint32_t hits = 0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const bool in = 4 * j + e < cnt;
+        const bool in = i + e < w1;
         hits |= (in && (kq[e] >> 21) == d1) ? (1u << e) : 0u;
         above += (in && (kq[e] >> 21) > d1) ? 1u : 0u;
       }
@@ -404,6 +415,7 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
 #pragma unroll
             for (int c = 0; c < kClusterCtas; ++c)
               st_dsmem(dsmem_addr(&cand_key[rank * kRegion + pos], (uint32_t)c), kq[e] & 0x1FFFFFu);
+            cand_idx[pos] = (uint32_t)(i + e);
           }
           pos += (hits >> e) & 1u;
         }
@@ -411,7 +423,11 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
-    if (lane == 0 && above) atomicAdd(&s_above, above);
+    if (lane == 0) {
+      warp_gt[warp] = above;
+      warp_eq[warp] = 0;
+      if (above) atomicAdd(&s_above, above);
+    }
     __syncthreads();
     if (warp == 0 && lane < kClusterCtas) {
       st_dsmem(dsmem_addr(&c_above[rank], (uint32_t)lane), s_above);
@@ -491,6 +507,16 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
         e += __shfl_xor_sync(0xFFFFFFFFu, e, o);
       }
       if (lane == 0) { c_gt[warp] = c_above[warp] + g; c_eq[warp] = e; }
+    } else {
+      // the other warps credit this CTA's candidates above / equal to T to
+      // the warps whose ranges hold them
+      constexpr uint32_t kFirst = kClusterCtas * 32, kStride = kCThreads - kClusterCtas * 32;
+      for (uint32_t j = (uint32_t)tid - kFirst; j < c_bin[rank]; j += kStride) {
+        const uint32_t k = cand_key[rank * kRegion + j];
+        const int w = (int)cand_idx[j] / R;
+        if (k > prefix) atomicAdd(&warp_gt[w], 1u);
+        else if (k == prefix) atomicAdd(&warp_eq[w], 1u);
+      }
     }
     __syncthreads();
   } else {
@@ -523,35 +549,33 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     T = prefix;
   }
 
-  // ---- warp w owns the contiguous keys [w*R, (w+1)*R) of the slice (R a
-  // multiple of 128) and walks them 128 at a time, lane l taking keys 4l ..
-  // 4l+3 of each step (one 16-byte load).  A first walk counts the keys
-  // above / equal to T, one warp sum of the lower warps' totals gives the
+  // ---- compaction over the warp ranges.  Each warp's counts of keys above
+  // / equal to T (from the candidate walk on the usual path, from a counting
+  // walk otherwise), one warp sum of the lower warps' totals gives the
   // offsets within the CTA, and a second walk writes the selected ids in id
   // order (ballots per key position count the lower lanes' keys, only in
   // steps that select a key), after the keys of the lower-rank CTAs (known
   // locally on the usual path, exchanged through DSMEM otherwise).
-  const int R = ((cnt + kCWarps - 1) / kCWarps + 127) / 128 * 128;
-  const int w0 = warp * R, w1 = w0 + R < cnt ? w0 + R : cnt;
-  const uint4* kw = reinterpret_cast<const uint4*>(keys);
-  uint32_t g = 0, e = 0;
-  for (int i0 = w0; i0 < w1; i0 += 128) {
-    const int i = i0 + 4 * lane;
-    const uint4 q = i < w1 ? kw[i / 4] : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
+  if (!fast) {
+    uint32_t g = 0, e = 0;
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+      const int i = i0 + 4 * lane;
+      const uint4 q = i < w1 ? kw[i / 4] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t kq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      g += (i + x < w1 && kq[x] > T) ? 1u : 0u;
-      e += (i + x < w1 && kq[x] == T) ? 1u : 0u;
+      for (int x = 0; x < 4; ++x) {
+        g += (i + x < w1 && kq[x] > T) ? 1u : 0u;
+        e += (i + x < w1 && kq[x] == T) ? 1u : 0u;
+      }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
-    e += __shfl_xor_sync(0xFFFFFFFFu, e, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xFFFFFFFFu, g, o);
+      e += __shfl_xor_sync(0xFFFFFFFFu, e, o);
+    }
+    if (lane == 0) { warp_gt[warp] = g; warp_eq[warp] = e; }
+    __syncthreads();
   }
-  if (lane == 0) { warp_gt[warp] = g; warp_eq[warp] = e; }
-  __syncthreads();
   // keys above / equal to T before the warp's range, globally: lane i adds
   // the counts of warp i < warp (and, on the usual path, of CTA i < rank),
   // then the warp sums them
