@@ -440,37 +440,36 @@ __global__ void __maxnreg__(40) select_topk_cluster_kernel(const TopkParams p, i
     uint32_t prefix = 0;
     if (tot[d1] <= 32u) {
       // At most 32 keys in the bin (the usual case: the K-th block score
-      // stands alone in its first-digit bin): warp 0 ranks them directly.
-      // Lane i holds candidate i; its value is the krem-th largest when
-      // fewer than krem candidates are greater and at least krem are
-      // greater or equal.  krem then becomes the number of keys equal to T
-      // that are taken (krem minus the candidates above T), as after the
-      // radix passes.
-      if (warp == 0) {
-        const uint32_t C = tot[d1];
-        const bool valid = (uint32_t)lane < C;
-        uint32_t v = 0;
-        if (valid) {
-          uint32_t i = (uint32_t)lane, c = 0;
-          while (c + 1 < (uint32_t)kClusterCtas && i >= c_bin[c]) { i -= c_bin[c]; ++c; }
-          v = cand_key[c * kRegion + i];
+      // stands alone in its first-digit bin): every warp ranks them itself,
+      // so no barrier is needed.  Lane i holds candidate i; its value is the
+      // krem-th largest when fewer than krem candidates are greater and at
+      // least krem are greater or equal.  krem then becomes the number of
+      // keys equal to T that are taken (krem minus the candidates above T),
+      // as after the radix passes.
+      const uint32_t C = tot[d1];
+      uint32_t cb[kClusterCtas];   // candidates per source CTA
+#pragma unroll
+      for (int c = 0; c < kClusterCtas; ++c) cb[c] = c_bin[c];
+      const bool valid = (uint32_t)lane < C;
+      uint32_t v = 0;
+      if (valid) {
+        uint32_t i = (uint32_t)lane, c = 0;
+#pragma unroll
+        for (int k = 0; k + 1 < kClusterCtas; ++k) {
+          if (c == (uint32_t)k && i >= cb[k]) { i -= cb[k]; c = (uint32_t)k + 1; }
         }
-        uint32_t gt = 0, eq = 0;
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t vj = __shfl_sync(0xFFFFFFFFu, v, j);
-          const bool in = (uint32_t)j < C;
-          gt += (in && vj > v) ? 1u : 0u;
-          eq += (in && vj == v) ? 1u : 0u;
-        }
-        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, valid && gt < krem && krem <= gt + eq);
-        const int src = hit ? __ffs(hit) - 1 : 0;
-        const uint32_t t = __shfl_sync(0xFFFFFFFFu, v, src);
-        const uint32_t g_hit = __shfl_sync(0xFFFFFFFFu, gt, src);
-        if (lane == 0) { s_digit = t; s_krem = krem - g_hit; }
+        v = cand_key[c * kRegion + i];
       }
-      __syncthreads();
-      prefix = s_digit;
-      krem = s_krem;
+      uint32_t gt = 0, eq = 0;
+      for (uint32_t j = 0; j < C; ++j) {
+        const uint32_t vj = __shfl_sync(0xFFFFFFFFu, v, (int)j);
+        gt += vj > v ? 1u : 0u;
+        eq += vj == v ? 1u : 0u;
+      }
+      const uint32_t hit = __ballot_sync(0xFFFFFFFFu, valid && gt < krem && krem <= gt + eq);
+      const int src = hit ? __ffs(hit) - 1 : 0;
+      prefix = __shfl_sync(0xFFFFFFFFu, v, src);
+      krem -= __shfl_sync(0xFFFFFFFFu, gt, src);
     } else {
       // two radix passes over the candidates (11 and 10 bits)
       uint32_t mask = 0;
