@@ -160,6 +160,39 @@ def test_topk_small_boundary_bin_with_ties():
         assert np.array_equal(sel[0, :K], ref), (n_top, n_eq, n_other)
 
 
+def test_topk_units_on_different_paths_in_one_launch():
+    """One launch whose clusters take different paths: a boundary bin of one
+    key and one of 28 keys with ties (ranked directly), one of 40 keys (the
+    radix passes over the candidates), heavy ties (the general path), and a
+    1M-token unit with a one-key bin (a slice of 32768 keys, so warp ranges
+    of 2048 in the candidate walk).  Each unit against the oracle."""
+    rng = np.random.default_rng(31)
+    budget = 2048
+    K = budget // 4
+
+    def planted(nb, n_top, n_eq, n_other):
+        v = np.full(nb, 0.001, np.float32)
+        top = rng.choice(nb, n_top, replace=False)
+        v[top] = 1000 + np.arange(n_top, dtype=np.float32)
+        rest = np.setdiff1d(np.arange(nb), top)
+        pos = rng.choice(rest, n_eq + n_other, replace=False)
+        v[pos[:n_eq]] = 2.0
+        v[pos[n_eq:]] = rng.choice(np.array([2.125, 2.25, 2.375], np.float32), n_other)
+        return v
+
+    ctxs = [131072, 262144, 131072, 65536, 1048576]
+    rows = [planted(ctxs[0] // 4, 511, 1, 0),
+            planted(ctxs[1] // 4, 500, 20, 8),
+            planted(ctxs[2] // 4, 490, 30, 10),
+            rng.integers(-3, 4, size=ctxs[3] // 4).astype(np.float32),
+            planted(ctxs[4] // 4, 511, 1, 0)]
+    sel, nsel = _run_select(rows, ctxs, budget)
+    for j, v in enumerate(rows):
+        ref = O.select_blocks(v.astype(np.float64), budget)
+        assert int(nsel[j]) == len(ref) == K
+        assert np.array_equal(sel[j, :K], ref), ctxs[j]
+
+
 def test_topk_boundary_bin_crowded_into_one_cta():
     """The boundary bin of the first 11-bit digit holds few keys overall (600,
     within the 2048 the CTAs finish the select on) but all in one CTA's slice,
