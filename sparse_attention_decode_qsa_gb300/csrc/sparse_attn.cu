@@ -446,8 +446,11 @@ __global__ void __maxnreg__(QSA_ATTN_MAXREG) attn_split_kernel(const AttnParams 
 constexpr int kChunksRowFp8 = kRowBytesFp8 / 16;          // 65
 constexpr int kHalfRowsFp8 = kWarpTokens * kRowBytesFp8;  // 8320 B: a token half's rows
 constexpr int kHalfThreads = kThreads / 2;                // 128
+// Three splits in flight per token half: against two, the 8-unit launch at
+// 256K 54.2 -> 51.3-52.5 us and the 12-layer FP8 step 0.835 -> 0.798 ms
+// (same box); four measured no faster launch and a slower step.
 #ifndef QSA_ATTN_STAGES_FP8
-#define QSA_ATTN_STAGES_FP8 2
+#define QSA_ATTN_STAGES_FP8 3
 #endif
 #ifndef QSA_ATTN_HOST_CTAS_FP8
 #define QSA_ATTN_HOST_CTAS_FP8 64
